@@ -1,0 +1,109 @@
+"""Brute-force pin of the oracle GEMV: exact rational arithmetic over a blob decoded
+bit by bit (header parsed independently with struct), on tiny shapes, with and
+without outlier columns, M = 1 and M > 1."""
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import lbq_oracle as O
+
+
+def _f16_value(bits: int) -> Fraction:
+    sign = -1 if bits & 0x8000 else 1
+    e = (bits >> 10) & 0x1F
+    m = bits & 0x3FF
+    assert e != 31
+    if e == 0:
+        return sign * Fraction(m, 1 << 24)
+    return sign * Fraction(1024 + m, 1024) * (Fraction(2) ** (e - 15))
+
+
+def _decode(blob):
+    b = bytes(blob)
+    magic = b[:8]
+    N, K = struct.unpack_from("<qq", b, 16)
+    n_out = struct.unpack_from("<i", b, 32)[0]
+    secs = [struct.unpack_from("<QQ", b, 48 + 16 * i) for i in range(5)]
+    W = [[Fraction(0)] * K for _ in range(N)]
+    for n in range(N):
+        for g in range(K // 32):
+            if magic == b"LBQW4G32":
+                so, sl = secs[1]
+                s = _f16_value(struct.unpack_from("<H", b, so + n * sl + 2 * g)[0])
+                zo, zl = secs[2]
+                zb = b[zo + n * zl + g // 2]
+                z = (zb >> 4) if g % 2 else (zb & 15)
+                qo, ql = secs[0]
+                for k in range(32):
+                    byte = b[qo + n * ql + g * 16 + (k % 16)]
+                    q = (byte >> 4) if k >= 16 else (byte & 15)
+                    W[n][g * 32 + k] = (q - z) * s
+            else:
+                so, sl = secs[1]
+                S = _f16_value(struct.unpack_from("<H", b, so + n * sl + 2 * g)[0])
+                Z = _f16_value(struct.unpack_from("<H", b, secs[2][0] + n * secs[2][1] + 2 * g)[0])
+                for k in range(32):
+                    kk = g * 32 + k
+                    byte = b[secs[0][0] + n * secs[0][1] + kk // 4]
+                    q = (byte >> (2 * (kk % 4))) & 3
+                    C = [-Fraction(389, 256), -Fraction(1843, 4096), Fraction(1843, 4096), Fraction(389, 256)][q]
+                    W[n][kk] = S * C + Z
+    idx = list(struct.unpack_from("<%di" % n_out, b, secs[3][0])) if n_out else []
+    vals = [[_f16_value(struct.unpack_from("<H", b, secs[4][0] + n * secs[4][1] + 2 * j)[0])
+             for j in range(n_out)] for n in range(N)]
+    return W, idx, vals
+
+
+def _exact_gemm(blob, X16):
+    W, idx, vals = _decode(blob)
+    N = len(W)
+    K = len(W[0])
+    out = []
+    for x in X16:
+        xf = [_f16_value(int(v)) for v in x.view("<u2")]
+        y = []
+        for n in range(N):
+            acc = sum(W[n][k] * xf[k] for k in range(K) if k not in idx)
+            acc += sum(vals[n][j] * xf[idx[j]] for j in range(len(idx)))
+            y.append(acc)
+        out.append(y)
+    return out
+
+
+@pytest.mark.parametrize("kind,N,K,idx", [
+    ("w4", 8, 64, []),
+    ("w4", 3, 128, [0, 33, 127]),
+    ("w2", 8, 64, []),
+    ("w2", 3, 128, [2, 64, 100, 101]),
+])
+def test_gemv_exact_rational(kind, N, K, idx):
+    rng = np.random.default_rng(N * 1000 + K + len(idx))
+    W = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    X = rng.standard_normal((2, K)).astype(np.float16)
+    X[:, 5] *= 100
+    idx = np.array(idx, np.int32)
+    blob = O.pack_w4(W, idx) if kind == "w4" else O.pack_w2cb(W, idx)
+    exact = _exact_gemm(blob, X)
+    Y = O.gemm(blob, X)
+    for m in range(2):
+        for n in range(N):
+            e = float(exact[m][n])
+            assert abs(Y[m, n] - e) <= 1e-13 * (abs(e) + 1e-3)
+    y0 = O.gemv(blob, X[0])
+    assert np.array_equal(y0, Y[0])
+    # row subset agrees with the full product
+    assert np.array_equal(O.gemm(blob, X, rows=[1, N - 1]), Y[:, [1, N - 1]])
+
+
+def test_tolerance_function():
+    y = np.array([1.0, -2.0, 100.0, 0.0])
+    rms = np.sqrt(np.mean(y * y))
+    ok = O.within_tolerance(y + 2e-3 * rms * 0.99, y)
+    assert ok.all()
+    bad = O.within_tolerance(y + (2e-3 * rms + 1e-3 * np.abs(y)) * 1.01, y)
+    assert not bad.any()
+    assert O.fp16_ulp(np.array([1.0, 1024.0, 2.0 ** -20]))[0] == 2.0 ** -10
+    assert O.fp16_ulp(np.array([1024.0]))[0] == 1.0
+    assert O.fp16_ulp(np.array([2.0 ** -20]))[0] == 2.0 ** -24
