@@ -1,0 +1,499 @@
+"""Throughput benchmark of the low-bit decode GEMV hot path on GB300.
+
+One step = one decode pass over a Llama-3-8B-shaped layer through every row of
+the hot path:
+  * the 7 linears in Group-32 asymmetric 4-bit (q, k, v, o, gate, up, down), M = 1;
+  * the same 7 linears in 2-bit Lloyd-Max codebook with the top 3.5 % profile-
+    guided FP16 outlier columns, M = 1;
+  * the 4-bit gate and down projections as a small-M batch (M = 4).
+Inputs are seeded synthetic data with the shapes and distributions of the
+decode configurations (see bit_weight_only_lbq_gb300/synth.py).  The packed
+weights of a step (291 MB) are held in 3 rotating replicas, so consecutive steps
+never find their weights in the 126 MB L2.
+
+The step is captured once per replica as a CUDA graph of the 16 launches
+chained with programmatic dependent launch, and timed with CUDA events around
+K replays.  The dominant kernel (4-bit GEMV on the gate/up/down shapes) is
+then timed launch by launch with CUDA events for the roofline figure.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 run under torch.distributed.run: every rank runs an independent
+replica (the path has no exchange step) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_weight_only_lbq_gb300 import synth  # noqa: E402
+
+REPLICAS = 3
+SMALL_M = 4
+SAMPLE_ROWS_MAX = 1024
+L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)      # rows of each matrix kept on the host for the oracle's timed sample
+METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
+W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
+W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
+
+
+def algorithmic_bytes(kind: str, N: int, K: int, n_out: int, M: int = 1) -> int:
+    """Bytes a launch must move at minimum: packed weights, group metadata,
+    outlier indices and values, the activations read and the outputs written."""
+    per_w = W4_BYTES_PER_WEIGHT if kind == "w4" else W2_BYTES_PER_WEIGHT
+    return int(per_w * N * K + n_out * (4 + 2 * N) + 2 * K * M + 2 * N * M)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the benchmark runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.gpu = gpu_index
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        used = inside if inside else [s for _, s in self.samples[-3:]]
+        sm = [float(s[1]) for s in used if len(s) > 8 and s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in used if len(s) > 8 and s[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for s in used:
+            if len(s) > 8:
+                for i, n in enumerate(names):
+                    if s[5 + i].lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples_in_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def make_workload(lbq, rank: int):
+    """Pack the step's 16 matrices on the host (C++ packers) and return host data."""
+    layer = []
+    for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
+        W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li + 100 * rank)
+        x = synth.activations(1, K, config_id=2, layer_id=li)[0]
+        layer.append(dict(kind="w4", name=name, N=N, K=K, n_out=0, M=1, blob=lbq.pack_w4(W), x=x,
+                          W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=np.zeros(0, np.int32)))
+    for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
+        W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li + 100 * rank)
+        prof = synth.profile_vectors(K, config_id=3, layer_id=li)
+        idx = lbq.select_outliers_impact(W, prof, 0.035)
+        x = synth.activations(1, K, config_id=3, layer_id=li)[0]
+        layer.append(dict(kind="w2", name=name, N=N, K=K, n_out=len(idx), M=1, blob=lbq.pack_w2cb(W, idx), x=x,
+                          W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=idx))
+    for li in (4, 6):
+        name, N, K = synth.LLAMA3_8B_LINEARS[li]
+        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li + 100 * rank)
+        X = synth.activations(SMALL_M, K, config_id=4, layer_id=li)
+        layer.append(dict(kind="w4m", name=name, N=N, K=K, n_out=0, M=SMALL_M, blob=lbq.pack_w4(W), x=X,
+                          W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=np.zeros(0, np.int32)))
+    for e in layer:
+        e["bytes"] = algorithmic_bytes("w4" if e["kind"] != "w2" else "w2", e["N"], e["K"], e["n_out"], e["M"])
+    return layer
+
+
+def reps_i(reps, i):
+    return [reps[r][i] for r in range(len(reps))]
+
+
+def launch(lbq, e, blob, x, y, pdl):
+    if e["kind"] == "w4":
+        lbq.gemv_w4a16(blob, e["N"], e["K"], e["n_out"], x, y, pdl=pdl)
+    elif e["kind"] == "w2":
+        lbq.gemv_w2cb_outlier(blob, e["N"], e["K"], e["n_out"], x, y, pdl=pdl)
+    else:
+        lbq.gemm_w4a16_smallM(blob, e["M"], e["N"], e["K"], e["n_out"], x, e["K"], y, e["N"], pdl=pdl)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the FP64 CPU oracle
+# ---------------------------------------------------------------------------
+
+def oracle_sample(layer, rows_per_matrix: int):
+    """A step of the oracle over the first rows of every matrix of the step.  The
+    oracle packs its own blob of those rows (untimed); the returned step times
+    its FP64 dequantise-from-bytes + matvec and returns the algorithmic bytes."""
+    from oracle import lbq_oracle as O
+    prepared = []
+    for e in layer:
+        R = min(rows_per_matrix, e["N"], len(e["W_head"]))
+        pack = O.pack_w2cb if e["kind"] == "w2" else O.pack_w4
+        prepared.append((e, R, pack(e["W_head"][:R], e["idx"])))
+
+    def step():
+        nbytes = 0
+        for e, R, blob in prepared:
+            O.gemm(blob, e["x"])
+            nbytes += algorithmic_bytes("w4" if e["kind"] != "w2" else "w2", R, e["K"], e["n_out"], e["M"])
+        return nbytes
+    return step
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from bit_weight_only_lbq_gb300 import lbq
+    layer = make_workload(lbq, 0)
+    budget_s = 120.0
+    rows = 64
+    step = oracle_sample(layer, rows)
+    t = time.perf_counter()
+    step()
+    one = time.perf_counter() - t
+    per_step_budget = budget_s / max(1, args.steps + args.warmup)
+    while rows > 1 and one > per_step_budget:
+        rows //= 2
+        step = oracle_sample(layer, rows)
+        t = time.perf_counter()
+        step()
+        one = time.perf_counter() - t
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += step()
+    dt = time.perf_counter() - t0
+    value = nbytes / dt / 1e9
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(),
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "first %d rows of each of the step's 16 matrices per step (FP64 NumPy "
+                                   "dequantise-from-bytes + matvec)" % rows},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict():
+    return {"workload": "llama3_8b_layer_decode: 7 linears W4A16 G32 (cfg2) + 7 linears W2 Lloyd-Max G32 with "
+                        "top-3.5% FP16 outliers (cfg3) + W4 gate/down small-M M=4 (cfg4), one token",
+            "linears": [list(x) for x in synth.LLAMA3_8B_LINEARS], "small_m": SMALL_M,
+            "l2": "inputs larger than L2: 3 rotating replicas of the 291 MB step",
+            "parallelism": "replicas (one independent layer per GPU)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="lbq", choices=["lbq", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", default=None,
+                    help="kind:N:K:n_out:M - time one kernel configuration alone (profiling aid), "
+                         "kind in w4, w2, w4m")
+    args = ap.parse_args()
+    if args.single:
+        return run_single(args)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    from bit_weight_only_lbq_gb300 import lbq
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    layer = make_workload(lbq, rank)
+    dev = torch.device("cuda", local_rank)
+    step_bytes = sum(e["bytes"] for e in layer)
+
+    # device buffers: REPLICAS copies of every blob, activations, outputs
+    reps = []
+    for r in range(REPLICAS):
+        reps.append([torch.from_numpy(e["blob"]).to(dev) for e in layer])
+    xs = [torch.from_numpy(np.ascontiguousarray(e["x"])).to(dev) for e in layer]
+    ys = [torch.empty((e["M"], e["N"]), dtype=torch.float16, device=dev) for e in layer]
+
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(REPLICAS):                      # eager warm-up (sets kernel attributes)
+            for i, e in enumerate(layer):
+                launch(lbq, e, reps[r][i], xs[i], ys[i], pdl=True)
+        stream.synchronize()
+        assert lbq.device_error(stream) == 0
+        for r in range(REPLICAS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i, e in enumerate(layer):
+                    launch(lbq, e, reps[r][i], xs[i], ys[i], pdl=True)
+            graphs.append(g)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for s in range(max(3, args.warmup)):
+            graphs[s % REPLICAS].replay()
+        stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        ev0.record(stream)
+        for s in range(args.steps):
+            graphs[s % REPLICAS].replay()
+        ev1.record(stream)
+        ev1.synchronize()
+        t_wall1 = time.time()
+        torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+    clk = clocks.summary(t_wall0, t_wall1)
+
+    # per-kernel timing: each kernel launched back to back over the rotating
+    # replicas inside a CUDA graph (chained with programmatic dependent launch,
+    # as in the step), CUDA events around every replay; also the dominant
+    # kernel (4-bit gate/up/down) chained on its own for the roofline figure
+    def time_graph(g, launches, replays):
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(replays)]
+            for a_, b_ in evs:
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+            stream.synchronize()
+        per_launch = [a_.elapsed_time(b_) / launches for a_, b_ in evs]
+        return per_launch
+
+    # enough distinct copies of every blob that one pass over them streams >= 512 MB
+    # (4x the L2), so no launch finds its weights in L2
+    copies = []
+    for i, e in enumerate(layer):
+        n = max(REPLICAS, -(-L2_ROTATION_BYTES // len(e["blob"])))
+        copies.append(reps_i(reps, i) + [reps[0][i].clone() for _ in range(n - REPLICAS)])
+
+    def graph_of(seq, pdl=True):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for (i, r) in seq:
+                launch(lbq, layer[i], copies[i][r], xs[i], ys[i], pdl=pdl)
+        return g
+
+    replays = max(5, min(50, args.steps // 400))
+    per = []
+    for i in range(len(layer)):
+        seq = [(i, r) for r in range(len(copies[i]))]
+        per.append(time_graph(graph_of(seq), len(seq), replays))
+    dominant = [i for i, e in enumerate(layer) if e["kind"] == "w4" and e["name"] in ("gate_proj", "up_proj", "down_proj")]
+    ndom = min(len(copies[i]) for i in dominant)
+    dom_seq = [(i, r) for r in range(ndom) for i in dominant]
+    dom_ms = time_graph(graph_of(dom_seq), len(dom_seq), replays)
+    dom_ms_serial = time_graph(graph_of(dom_seq, pdl=False), len(dom_seq), replays)
+    clocks.stop()
+    assert lbq.device_error(stream) == 0
+
+    # e2e: host (pinned) activations in, outputs back to host, through the same graph
+    h_x = [torch.from_numpy(np.ascontiguousarray(e["x"])).pin_memory() for e in layer]
+    h_y = [torch.empty((e["M"], e["N"]), dtype=torch.float16).pin_memory() for e in layer]
+    h2d = sum(t.numel() * 2 for t in h_x)
+    d2h = sum(t.numel() * 2 for t in h_y)
+    e2e_steps = max(10, min(2000, args.steps // 10))
+    with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
+        for s in range(e2e_steps):
+            for i in range(len(layer)):
+                xs[i].copy_(h_x[i], non_blocking=True)
+            graphs[s % REPLICAS].replay()
+            for i in range(len(layer)):
+                h_y[i].copy_(ys[i], non_blocking=True)
+            stream.synchronize()
+        e2e_s = time.perf_counter() - t0
+    e2e_value = step_bytes * e2e_steps / e2e_s / 1e9 * world
+
+    peak, peak_kind = load_peaks()
+    ms_step = ms_total / args.steps
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    dom_bytes = sum(layer[i]["bytes"] for i in dominant) / len(dominant)
+    dom_avg_ms = statistics.mean(dom_ms)
+    achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9
+    detail = []
+    for i, e in enumerate(layer):
+        us = statistics.median(per[i]) * 1e3
+        gbs = e["bytes"] / (us * 1e-6) / 1e9
+        detail.append({"kernel": e["kind"], "linear": e["name"], "N": e["N"], "K": e["K"], "n_out": e["n_out"],
+                       "M": e["M"], "us_per_call": round(us, 3), "GB_s": round(gbs, 1),
+                       "frac_of_peak": round(gbs / peak, 4)})
+    w4_bytes = sum(e["bytes"] for e in layer if e["kind"] == "w4")
+    w2_bytes = sum(e["bytes"] for e in layer if e["kind"] == "w2")
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16 activations, fp32 accumulate (w4 / w2 weights)",
+        "data": "synthetic (seeded; shapes and distributions of the decode configs)",
+        "config": config_dict(),
+        "gpu_launches": len(layer) * args.steps,
+        "step_bytes": step_bytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "lbq_gemv_kernel<W4,MB=1> on gate/up/down: chained launches in a CUDA graph, "
+                               "CUDA events around each replay, average per launch",
+                     "serialized_launch_GB_s": round(dom_bytes / (statistics.mean(dom_ms_serial) * 1e-3) / 1e9, 1),
+                     "peak_source": peak_kind},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "detail": {"per_kernel": detail,
+                   "implied_tokens_per_s": {
+                       "llama3_8b_w4_32_layers_from_per_call": round(
+                           1.0 / (32 * sum(statistics.median(per[i]) for i, e in enumerate(layer)
+                                           if e["kind"] == "w4") * 1e-3), 1),
+                       "llama3_8b_w2_32_layers_from_per_call": round(
+                           1.0 / (32 * sum(statistics.median(per[i]) for i, e in enumerate(layer)
+                                           if e["kind"] == "w2") * 1e-3), 1)},
+                   "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layer)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_single(args):
+    """One kernel configuration, launched steps times after warmup (for ncu captures)."""
+    import torch
+    from bit_weight_only_lbq_gb300 import lbq
+    kind, N, K, n_out, M = args.single.split(":")
+    N, K, n_out, M = int(N), int(K), int(n_out), int(M)
+    rng = np.random.default_rng(0)
+    W = (rng.standard_normal((N, K), dtype=np.float32) * 0.02)
+    idx = np.sort(rng.choice(K, size=n_out, replace=False)).astype(np.int32)
+    blob = lbq.pack_w2cb(W, idx) if kind == "w2" else lbq.pack_w4(W, idx)
+    del W
+    e = dict(kind=kind, N=N, K=K, n_out=n_out, M=M)
+    dev = torch.device("cuda", 0)
+    d_blob = torch.from_numpy(blob).to(dev)
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float16)).to(dev)
+    y = torch.empty((M, N), dtype=torch.float16, device=dev)
+    for _ in range(max(1, args.warmup)):
+        launch(lbq, e, d_blob, x, y, pdl=False)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch(lbq, e, d_blob, x, y, pdl=False)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in ts]
+    nbytes = algorithmic_bytes("w2" if kind == "w2" else "w4", N, K, n_out, M)
+    assert lbq.device_error() == 0
+    print(json.dumps({"single": args.single, "bytes": nbytes, "us_median": statistics.median(us),
+                      "GB_s": nbytes / (statistics.median(us) * 1e-6) / 1e9}), flush=True)
+    return 0
+
+
+def cpu_baseline(layer):
+    """The oracle as it stands on the host cores: FP64 dequantise-from-bytes + matvec
+    over a row sample of every matrix of the step, scaled to the step's bytes."""
+    step = None
+    rows = 256
+    t_budget = 15.0
+    while True:
+        step = oracle_sample(layer, rows)
+        t = time.perf_counter()
+        nbytes = step()
+        dt = time.perf_counter() - t
+        if dt > 0.5 or rows >= 4096:
+            break
+        rows *= 2
+    reps = max(1, int(t_budget / max(dt, 1e-3)))
+    reps = min(reps, 20)
+    t = time.perf_counter()
+    for _ in range(reps):
+        step()
+    dt = (time.perf_counter() - t) / reps
+    return {"value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": "first %d rows of each of the step's 16 matrices, %d repetitions (FP64 NumPy "
+                      "dequantise-from-bytes + matvec)" % (rows, reps)}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,77 @@
+"""Build liblbq.so in-tree for sm_103a (no CMake): g++ for the host half,
+nvcc for the CUDA half, compiled in parallel, linked with nvcc."""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(PKG, "_lib")
+LIB = os.path.join(OUT_DIR, "liblbq.so")
+ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+
+
+def _nvcc() -> str:
+    for c in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if c and os.path.exists(c):
+            return c
+    raise RuntimeError("nvcc not found: liblbq needs the CUDA 13 toolkit to build")
+
+
+def sources():
+    cu = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    cpp = sorted(f for f in os.listdir(CSRC) if f.endswith(".cpp"))
+    return cu, cpp
+
+
+def build(verbose: bool = False, debug: bool = False) -> str:
+    nvcc = _nvcc()
+    os.makedirs(OUT_DIR, exist_ok=True)
+    obj_dir = os.path.join(OUT_DIR, "obj")
+    os.makedirs(obj_dir, exist_ok=True)
+    cu, cpp = sources()
+    inc = ["-I" + INCLUDE, "-I" + CSRC]
+    jobs = []
+    for f in cpp:
+        o = os.path.join(obj_dir, f + ".o")
+        # exact FP64 recipe for the packers: no contraction, no fast-math
+        cmd = ["g++", "-std=c++17", "-O2", "-fPIC", "-ffp-contract=off", "-fno-fast-math", "-Wall",
+               "-pthread", *inc, "-c", os.path.join(CSRC, f), "-o", o]
+        jobs.append((cmd, o))
+    for f in cu:
+        o = os.path.join(obj_dir, f + ".o")
+        cmd = [nvcc, ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+               *inc, "-c", os.path.join(CSRC, f), "-o", o]
+        if debug:
+            cmd.insert(1, "-DLBQ_DEBUG=1")
+        jobs.append((cmd, o))
+
+    def run(job):
+        cmd, o = job
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("compile failed: %s\n%s\n%s" % (" ".join(cmd), r.stdout, r.stderr))
+        return r.stderr
+
+    with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
+        logs = list(ex.map(run, jobs))
+    if verbose:
+        for l in logs:
+            sys.stderr.write(l)
+    tmp = LIB + ".tmp"
+    link = [nvcc, ARCH, "-shared", "-o", tmp, *[o for _, o in jobs], "-lpthread"]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed: %s\n%s" % (" ".join(link), r.stderr))
+    os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose="-v" in sys.argv))

@@ -1,0 +1,20 @@
+// Internal constants shared by the host (.cpp) and device (.cu) halves of liblbq.
+#pragma once
+
+#include <cstdint>
+
+#define LBQ_VERSION_NUM 100          // 0.1.0
+#define LBQ_FORMAT_VERSION_NUM 1
+
+namespace lbq {
+
+constexpr int64_t kMaxK = 65536;          // x of one row block must fit in shared memory
+constexpr int32_t kMaxOutliers = 8192;    // gathered outlier activations live in shared memory
+constexpr uint64_t kSectionAlign = 256;   // every blob section starts on this boundary
+constexpr uint64_t kRowAlign = 16;        // rows of 2-D sections are padded to this
+constexpr int kMaxM = 64;                 // largest batch of the small-M entry point
+
+uint16_t host_f64_to_f16(double v);
+double host_f16_to_f64(uint16_t h);
+
+}  // namespace lbq

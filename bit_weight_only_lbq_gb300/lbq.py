@@ -1,0 +1,228 @@
+"""Thin ctypes binding of liblbq.so (include/lbq.h).
+
+Argument marshalling only: every step of the computation runs in the C++/CUDA
+library.  Host entry points take and return numpy arrays; device entry points
+take torch CUDA tensors (or raw device addresses) and the current torch
+stream.  If the library has not been built this module raises on first use;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "liblbq.so")
+
+LBQ_F16 = 0
+LBQ_F32 = 1
+LBQ_KIND_W4 = 0
+LBQ_KIND_W2CB = 1
+LBQ_FLAG_PDL = 1
+
+STATUS = {
+    0: "LBQ_OK", 1: "LBQ_ERR_NULL", 2: "LBQ_ERR_SHAPE", 3: "LBQ_ERR_ALIGN", 4: "LBQ_ERR_OUTLIER_IDX",
+    5: "LBQ_ERR_BUFFER_TOO_SMALL", 6: "LBQ_ERR_FORMAT", 7: "LBQ_ERR_CUDA", 8: "LBQ_ERR_TIMEOUT",
+    9: "LBQ_ERR_VALUE", 10: "LBQ_ERR_UNSUPPORTED",
+}
+
+# every symbol include/lbq.h declares
+EXPORTS = (
+    "lbq_version", "lbq_format_version", "lbq_status_string", "lbq_blob_layout",
+    "lbq_w4_packed_bytes", "lbq_w2cb_packed_bytes", "lbq_select_outliers_w4",
+    "lbq_select_outliers_impact", "lbq_pack_w4", "lbq_pack_w2cb", "lbq_gemv_w4a16",
+    "lbq_gemv_w2cb_outlier", "lbq_gemm_w4a16_smallM", "lbq_gemv_w4a16_ex",
+    "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_device_error",
+)
+
+
+class LbqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (where, STATUS.get(status, "status %d" % status)))
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [("offset", ctypes.c_uint64 * 5), ("row_stride", ctypes.c_uint64 * 5),
+                ("total_bytes", ctypes.c_uint64)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+c_i64, c_i32, c_u32, c_vp, c_sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p, ctypes.c_size_t
+
+
+def lib():
+    """Load liblbq.so (once).  Raises ImportError when it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("liblbq.so is not built (%s); run `python -c \"import __graft_entry__ as g; "
+                              "g.build()\"`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        sig = {
+            "lbq_version": (ctypes.c_int, []),
+            "lbq_format_version": (ctypes.c_int, []),
+            "lbq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "lbq_blob_layout": (ctypes.c_int, [ctypes.c_int, c_i64, c_i64, c_i32, ctypes.POINTER(Layout)]),
+            "lbq_w4_packed_bytes": (c_sz, [c_i64, c_i64, c_i32]),
+            "lbq_w2cb_packed_bytes": (c_sz, [c_i64, c_i64, c_i32]),
+            "lbq_select_outliers_w4": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_i32, ctypes.POINTER(c_i32)]),
+            "lbq_select_outliers_impact": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_i32, ctypes.c_double,
+                                                          c_vp, c_i32, ctypes.POINTER(c_i32)]),
+            "lbq_pack_w4": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_i32, c_vp, c_sz]),
+            "lbq_pack_w2cb": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_i32, c_vp, c_sz]),
+            "lbq_gemv_w4a16": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int, c_vp]),
+            "lbq_gemv_w2cb_outlier": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int, c_vp]),
+            "lbq_gemm_w4a16_smallM": (ctypes.c_int, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp, c_i64,
+                                                     ctypes.c_int, c_vp]),
+            "lbq_gemv_w4a16_ex": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int, c_vp, c_u32]),
+            "lbq_gemv_w2cb_outlier_ex": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int,
+                                                        c_vp, c_u32]),
+            "lbq_gemm_w4a16_smallM_ex": (ctypes.c_int, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp,
+                                                        c_i64, ctypes.c_int, c_vp, c_u32]),
+            "lbq_device_error": (ctypes.c_int, [c_vp]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise LbqError(st, where)
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+# ------------------------------------------------------------------ host side
+
+def blob_layout(kind: int, N: int, K: int, n_out: int) -> dict:
+    L = Layout()
+    _check(lib().lbq_blob_layout(kind, N, K, n_out, ctypes.byref(L)), "lbq_blob_layout")
+    return {"offsets": list(L.offset), "strides": list(L.row_stride), "total": int(L.total_bytes)}
+
+
+def _as_f32(W) -> np.ndarray:
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    assert W.ndim == 2
+    return W
+
+
+def _as_idx(idx) -> np.ndarray:
+    if idx is None:
+        return np.zeros(0, np.int32)
+    return np.ascontiguousarray(idx, dtype=np.int32).reshape(-1)
+
+
+def select_outliers_w4(W) -> np.ndarray:
+    W = _as_f32(W)
+    N, K = W.shape
+    cap = K
+    idx = np.zeros(cap, np.int32)
+    n = c_i32(0)
+    _check(lib().lbq_select_outliers_w4(_ptr(W), N, K, _ptr(idx), cap, ctypes.byref(n)), "lbq_select_outliers_w4")
+    return idx[:n.value].copy()
+
+
+def select_outliers_impact(W, Xprof, frac: float = 0.035) -> np.ndarray:
+    W = _as_f32(W)
+    N, K = W.shape
+    X = np.ascontiguousarray(Xprof, dtype=np.float16).reshape(-1, K)
+    idx = np.zeros(K, np.int32)
+    n = c_i32(0)
+    _check(lib().lbq_select_outliers_impact(_ptr(W), N, K, _ptr(X), X.shape[0], float(frac), _ptr(idx), K,
+                                            ctypes.byref(n)), "lbq_select_outliers_impact")
+    return idx[:n.value].copy()
+
+
+def pack_w4(W, idx=None) -> np.ndarray:
+    W = _as_f32(W)
+    idx = _as_idx(idx)
+    N, K = W.shape
+    nb = lib().lbq_w4_packed_bytes(N, K, idx.size)
+    if nb == 0:
+        raise LbqError(2, "lbq_w4_packed_bytes")
+    out = np.empty(nb, np.uint8)
+    _check(lib().lbq_pack_w4(_ptr(W), N, K, _ptr(idx) if idx.size else None, idx.size, _ptr(out), nb), "lbq_pack_w4")
+    return out
+
+
+def pack_w2cb(W, idx=None) -> np.ndarray:
+    W = _as_f32(W)
+    idx = _as_idx(idx)
+    N, K = W.shape
+    nb = lib().lbq_w2cb_packed_bytes(N, K, idx.size)
+    if nb == 0:
+        raise LbqError(2, "lbq_w2cb_packed_bytes")
+    out = np.empty(nb, np.uint8)
+    _check(lib().lbq_pack_w2cb(_ptr(W), N, K, _ptr(idx) if idx.size else None, idx.size, _ptr(out), nb),
+           "lbq_pack_w2cb")
+    return out
+
+
+# ---------------------------------------------------------------- device side
+
+def _dev_ptr(t) -> int:
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("device entry points take CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ydtype(y) -> int:
+    import torch
+    if y.dtype == torch.float16:
+        return LBQ_F16
+    if y.dtype == torch.float32:
+        return LBQ_F32
+    raise ValueError("y must be float16 or float32")
+
+
+def gemv_w4a16(packed, N: int, K: int, n_out: int, x, y, stream=None, pdl: bool = False, y_dtype: int | None = None):
+    yd = _ydtype(y) if y_dtype is None else y_dtype
+    _check(lib().lbq_gemv_w4a16_ex(_dev_ptr(packed), N, K, n_out, _dev_ptr(x), _dev_ptr(y), yd, _stream(stream),
+                                   LBQ_FLAG_PDL if pdl else 0), "lbq_gemv_w4a16")
+
+
+def gemv_w2cb_outlier(packed, N: int, K: int, n_out: int, x, y, stream=None, pdl: bool = False,
+                      y_dtype: int | None = None):
+    yd = _ydtype(y) if y_dtype is None else y_dtype
+    _check(lib().lbq_gemv_w2cb_outlier_ex(_dev_ptr(packed), N, K, n_out, _dev_ptr(x), _dev_ptr(y), yd,
+                                          _stream(stream), LBQ_FLAG_PDL if pdl else 0), "lbq_gemv_w2cb_outlier")
+
+
+def gemm_w4a16_smallM(packed, M: int, N: int, K: int, n_out: int, X, ldx: int, Y, ldy: int, stream=None,
+                      pdl: bool = False, y_dtype: int | None = None):
+    yd = _ydtype(Y) if y_dtype is None else y_dtype
+    _check(lib().lbq_gemm_w4a16_smallM_ex(_dev_ptr(packed), M, N, K, n_out, _dev_ptr(X), ldx, _dev_ptr(Y), ldy, yd,
+                                          _stream(stream), LBQ_FLAG_PDL if pdl else 0), "lbq_gemm_w4a16_smallM")
+
+
+def device_error(stream=None) -> int:
+    return int(lib().lbq_device_error(_stream(stream)))

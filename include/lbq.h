@@ -1,0 +1,209 @@
+/*
+ * lbq.h - C ABI of the Group-32 low-bit weight-only decode GEMV library
+ * (liblbq.so, built for sm_103a).
+ *
+ * The library computes  y = W_hat x~ + W_out x[idx]  for one FP16 activation
+ * vector (M = 1) or a few (small M), where W_hat is a Group-32 quantised weight
+ * matrix held in a packed blob:
+ *
+ *   4-bit asymmetric  : w_hat = s_g (q - z_g),  q, z in 0..15, s_g FP16
+ *                       (SPECTRA article, "Compress any LLM 3x in one click",
+ *                        section 3.4 and Appendix A, Proposition 2)
+ *   2-bit codebook    : w_hat = S_g C[q] + Z_g, C = FP16{-1.52,-0.45,0.45,1.52},
+ *                       S_g, Z_g FP16 from a per-group least-squares fit
+ *                       (otf-llm 4.0.0, sections 2, 3 and 5)
+ *
+ * and W_out holds exact FP16 outlier input columns idx (SPECTRA sections 3.3
+ * and 4.1; otf-llm section 4 and its architecture diagram).  x~ is x with the
+ * outlier channels set to zero; W_hat is N x K, one output per row, groups of
+ * 32 consecutive k.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Ownership: the caller allocates and owns every buffer, host and device.
+ *    The library keeps no handles and calls no allocator.
+ *  - Shapes: 1 <= N <= 2^31-1, 64 <= K <= 65536, K % 64 == 0,
+ *    0 <= n_out <= min(K, 8192).  Outlier indices are strictly ascending
+ *    int32 in [0, K).
+ *  - Host entry points (layout, outlier selection, packing) are pure CPU
+ *    code; they touch no GPU and are thread-safe.
+ *  - Device entry points take device pointers (16-byte aligned where stated)
+ *    and a stream (a cudaStream_t passed as void*, NULL = legacy default
+ *    stream).  They validate arguments on the host, enqueue one kernel and
+ *    return without synchronising.  They never allocate.
+ *  - Errors: every entry point returns an lbq_status; nothing crosses the ABI
+ *    as an exception.  A kernel never traps: a bounded wait that gives up, or
+ *    a blob whose header does not match the call, records a code in a
+ *    device-side error word that lbq_device_error() reports and clears.
+ *
+ * Packed blob (format version 1; all integers little-endian)
+ * ----------------------------------------------------------
+ *   [0:8)    magic "LBQW4G32" (4-bit) or "LBQW2C32" (2-bit codebook)
+ *   [8:12)   u32 version = 1            [12:16)  u32 header bytes = 128
+ *   [16:24)  i64 N                      [24:32)  i64 K
+ *   [32:36)  i32 n_out                  [36:40)  u32 group size = 32
+ *   [40:48)  u64 total blob bytes
+ *   [48:128) five (u64 offset, u64 row stride) pairs, one per section:
+ *     4-bit : 0 qweight  N x K/2 bytes, byte k of a group = q_k | q_{k+16} << 4
+ *             1 scales   N x K/32 FP16
+ *             2 zeros    N x K/64 bytes, z_{2m} | z_{2m+1} << 4
+ *             3 idx      n_out int32 (1-D, stride 0)
+ *             4 vals     N x n_out FP16 (row n = W[n, idx])
+ *     2-bit : 0 codes    N x K/4 bytes, byte = q0 | q1<<2 | q2<<4 | q3<<6 (k = 4i+j)
+ *             1 S        N x K/32 FP16
+ *             2 Z        N x K/32 FP16
+ *             3 idx, 4 vals as above
+ *   Sections start on 256-byte boundaries (the first at offset 256); each row
+ *   of a 2-D section is zero-padded to a multiple of 16 bytes.  The byte
+ *   layout inside a row is the one the pages print; the padding and section
+ *   alignment let the kernels fetch tiles with the Tensor Memory Accelerator.
+ */
+#ifndef LBQ_H
+#define LBQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LBQ_OK = 0,
+    LBQ_ERR_NULL = 1,              /* a required pointer is NULL */
+    LBQ_ERR_SHAPE = 2,             /* N, K, M, n_out or a leading dimension out of range */
+    LBQ_ERR_ALIGN = 3,             /* a device pointer or leading dimension misaligned */
+    LBQ_ERR_OUTLIER_IDX = 4,       /* indices not strictly ascending or outside [0, K) */
+    LBQ_ERR_BUFFER_TOO_SMALL = 5,  /* destination or cap smaller than needed */
+    LBQ_ERR_FORMAT = 6,            /* blob header does not match the call (device-side check) */
+    LBQ_ERR_CUDA = 7,              /* a CUDA runtime call or kernel launch failed */
+    LBQ_ERR_TIMEOUT = 8,           /* a bounded in-kernel wait gave up (device-side) */
+    LBQ_ERR_VALUE = 9,             /* non-finite input value, or frac outside [0, 1] */
+    LBQ_ERR_UNSUPPORTED = 10       /* no sm_103a device, or a kind/dtype not provided */
+} lbq_status;
+
+typedef enum { LBQ_F16 = 0, LBQ_F32 = 1 } lbq_dtype;
+typedef enum { LBQ_KIND_W4 = 0, LBQ_KIND_W2CB = 1 } lbq_kind;
+
+typedef struct {
+    uint64_t offset[5];       /* byte offset of each section from the blob start */
+    uint64_t row_stride[5];   /* bytes between rows (0 for the 1-D idx section) */
+    uint64_t total_bytes;     /* size of the whole blob */
+} lbq_layout;
+
+/* Library version (major * 10000 + minor * 100 + patch) and blob format version. */
+int lbq_version(void);
+int lbq_format_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* lbq_status_string(lbq_status s);
+
+/* ---------------------------------------------------------------- host side */
+
+/* Section offsets and strides of a blob of the given kind and shape (the layout
+ * above).  Errors: LBQ_ERR_NULL (out), LBQ_ERR_SHAPE. */
+lbq_status lbq_blob_layout(lbq_kind kind, int64_t N, int64_t K, int32_t n_out, lbq_layout* out);
+
+/* Total blob bytes, or 0 when the shape is invalid. */
+size_t lbq_w4_packed_bytes(int64_t N, int64_t K, int32_t n_out);
+size_t lbq_w2cb_packed_bytes(int64_t N, int64_t K, int32_t n_out);
+
+/* Outlier channels for the 4-bit format (SPECTRA sections 3.2-3.3): saliency
+ * S_j = ||W[:,j]||_2 (gain gamma = 1, no preceding normalisation), population
+ * kurtosis kappa of S, ratio r = clamp(0.01 (1 + 0.15 ln(1 + max(0, kappa-3))),
+ * 0.005, 0.03), and the floor(r K) columns of largest saliency (ties to the
+ * lower index), written ascending to idx[0 .. *n_out).
+ * W: host FP32, N x K row-major.  cap: capacity of idx.
+ * Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE, LBQ_ERR_VALUE (non-finite W),
+ * LBQ_ERR_BUFFER_TOO_SMALL (cap < required count; *n_out still set). */
+lbq_status lbq_select_outliers_w4(const float* W, int64_t N, int64_t K,
+                                  int32_t* idx, int32_t cap, int32_t* n_out);
+
+/* Profile-guided outlier channels for the 2-bit format (otf-llm section 4):
+ * I_c = ||W[:,c]||_2 * mean_p |Xprof[p, c]| over P FP16 profile vectors
+ * (Xprof: host, P x K row-major, FP16 bit patterns); the floor(frac K) largest
+ * scores, ties to the lower index, ascending.  Errors as above, plus
+ * LBQ_ERR_VALUE for frac outside [0, 1]. */
+lbq_status lbq_select_outliers_impact(const float* W, int64_t N, int64_t K,
+                                      const uint16_t* Xprof_f16, int32_t P, double frac,
+                                      int32_t* idx, int32_t cap, int32_t* n_out);
+
+/* Quantise and pack W (host FP32, N x K row-major) into a caller-allocated host
+ * buffer dst of dst_bytes >= lbq_w4_packed_bytes(N, K, n_out).  Columns idx
+ * are copied to the FP16 outlier section and set to zero in the dense matrix
+ * before grouping.  Every statistic is computed in FP64 with sequential sums,
+ * round-half-to-even, and rounded to FP16 once; the bytes are deterministic.
+ *   4-bit (SPECTRA 3.4, App. A Prop. 2): per group s = max((wmax-wmin)/15, 1e-8),
+ *     z = clamp(rint(-wmin/s), 0, 15), q = clamp(rint(w/s + z), 0, 15), FP16 s.
+ *   2-bit (otf-llm 2, 3, 5): per group standardise by mean and population std,
+ *     nearest FP16 centroid (ties to the lower code), then
+ *     S = sum(w-wbar)(c-cbar) / (sum(c-cbar)^2 + 1e-8), Z = wbar - S cbar.
+ * Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE, LBQ_ERR_OUTLIER_IDX, LBQ_ERR_VALUE,
+ * LBQ_ERR_BUFFER_TOO_SMALL.  The caller copies dst to the device. */
+lbq_status lbq_pack_w4(const float* W, int64_t N, int64_t K, const int32_t* idx, int32_t n_out,
+                       void* dst, size_t dst_bytes);
+lbq_status lbq_pack_w2cb(const float* W, int64_t N, int64_t K, const int32_t* idx, int32_t n_out,
+                         void* dst, size_t dst_bytes);
+
+/* -------------------------------------------------------------- device side */
+
+/* Fused 4-bit GEMV (SPECTRA section 4.1, "In-Register Fused W4A16 GEMV with
+ * Outlier Channel Accumulation"):
+ *     y[n] = sum_g s_{n,g} sum_{k in g} (q_{n,k} - z_{n,g}) x~_k + sum_j vals[n,j] x[idx_j]
+ * packed : device, 16-byte aligned, a 4-bit blob of exactly (N, K, n_out).
+ * x_f16  : device, 16-byte aligned, K FP16.
+ * y      : device, N values of y_dtype (FP16 rounded once from the FP32
+ *          accumulator, or the FP32 accumulator itself), 4-byte aligned.
+ * The weights are streamed once from HBM; products are accumulated in FP32.
+ * Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE, LBQ_ERR_ALIGN, LBQ_ERR_CUDA,
+ * LBQ_ERR_UNSUPPORTED; LBQ_ERR_FORMAT / LBQ_ERR_TIMEOUT via lbq_device_error. */
+lbq_status lbq_gemv_w4a16(const void* packed, int64_t N, int64_t K, int32_t n_out,
+                          const void* x_f16, void* y, lbq_dtype y_dtype, void* stream);
+
+/* Fused 2-bit codebook GEMV with exact FP16 outlier columns (otf-llm section 5
+ * kernel description and "Architecture & Key Innovations"):
+ *     y[n] = sum_g [ S_{n,g} sum_{k in g} C[q_{n,k}] x~_k + Z_{n,g} sum_{k in g} x~_k ]
+ *            + sum_j vals[n,j] x[idx_j]
+ * Arguments, alignment and errors as lbq_gemv_w4a16, with a 2-bit blob. */
+lbq_status lbq_gemv_w2cb_outlier(const void* packed, int64_t N, int64_t K, int32_t n_out,
+                                 const void* x_f16, void* y, lbq_dtype y_dtype, void* stream);
+
+/* Batched 4-bit GEMM for small M (SPECTRA section 4.2, "Batched Tensor Core
+ * W4A16 GEMM with In-Kernel Outlier Fusion"; M is a runtime argument):
+ *     Y[m, n] = sum_k w_hat[n,k] X~[m,k] + sum_j vals[n,j] X[m, idx_j],  0 <= m < M
+ * X_f16 : device, M rows of K FP16 with leading dimension ldx (elements),
+ *         16-byte aligned base, ldx % 8 == 0, ldx >= K.
+ * Y     : device, M rows of N values of y_dtype with leading dimension ldy >= N.
+ * 1 <= M <= 64.  Errors as lbq_gemv_w4a16. */
+lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
+                                 const void* X_f16, int64_t ldx, void* Y, int64_t ldy,
+                                 lbq_dtype y_dtype, void* stream);
+
+/* Variants with launch flags.  LBQ_FLAG_PDL launches the kernel with
+ * programmatic stream serialisation: it may start while the previous kernel
+ * on the stream is still running, fetch its weights at once, and read x /
+ * write y only after that kernel has completed (griddepcontrol.wait).  Use it
+ * only when the previous kernel on the stream does not write the packed
+ * blob; it removes the launch gap between back-to-back GEMVs of a layer.
+ * flags = 0 is exactly the plain entry point. */
+#define LBQ_FLAG_PDL 1u
+lbq_status lbq_gemv_w4a16_ex(const void* packed, int64_t N, int64_t K, int32_t n_out,
+                             const void* x_f16, void* y, lbq_dtype y_dtype, void* stream,
+                             uint32_t flags);
+lbq_status lbq_gemv_w2cb_outlier_ex(const void* packed, int64_t N, int64_t K, int32_t n_out,
+                                    const void* x_f16, void* y, lbq_dtype y_dtype, void* stream,
+                                    uint32_t flags);
+lbq_status lbq_gemm_w4a16_smallM_ex(const void* packed, int32_t M, int64_t N, int64_t K,
+                                    int32_t n_out, const void* X_f16, int64_t ldx, void* Y,
+                                    int64_t ldy, lbq_dtype y_dtype, void* stream, uint32_t flags);
+
+/* Synchronise the stream, then return and clear the device-side error word of
+ * the current device (LBQ_OK when no kernel recorded an error).  Errors from
+ * the synchronisation itself are reported as LBQ_ERR_CUDA. */
+lbq_status lbq_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LBQ_H */

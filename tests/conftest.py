@@ -28,3 +28,23 @@ def load_golden(name):
 @pytest.fixture
 def golden():
     return load_golden
+
+
+def _lib_stale() -> bool:
+    from bit_weight_only_lbq_gb300 import build as B
+    if not os.path.exists(B.LIB):
+        return True
+    t = os.path.getmtime(B.LIB)
+    srcs = [os.path.join(B.CSRC, f) for f in os.listdir(B.CSRC)] + [os.path.join(B.INCLUDE, "lbq.h")]
+    return any(os.path.getmtime(s) > t for s in srcs)
+
+
+@pytest.fixture(scope="session")
+def lbq():
+    """The binding, with liblbq.so built in-tree if missing or older than its sources."""
+    if _lib_stale():
+        from bit_weight_only_lbq_gb300 import build as B
+        B.build()
+    from bit_weight_only_lbq_gb300 import lbq as L
+    L.lib()
+    return L

@@ -1,0 +1,73 @@
+"""The C ABI: every symbol include/lbq.h declares is exported by liblbq.so, and
+host-side validation rejects bad arguments before anything touches a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "lbq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lbq_\w+)\s*\(", src)))
+
+
+def test_header_declarations_are_exported(lbq):
+    from bit_weight_only_lbq_gb300 import build as B
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True, text=True, check=True).stdout
+    exported = set(l.split()[-1] for l in out.splitlines() if l.strip())
+    declared = _declared()
+    assert len(declared) >= 17
+    missing = [d for d in declared if d not in exported]
+    assert not missing, missing
+    assert sorted(lbq.EXPORTS) == declared
+
+
+def test_status_strings(lbq):
+    L = lbq.lib()
+    for code, name in lbq.STATUS.items():
+        assert L.lbq_status_string(code).decode().startswith(name)
+    assert L.lbq_format_version() == 1
+
+
+def test_host_argument_errors(lbq):
+    L = lbq.lib()
+    W = np.zeros((4, 64), np.float32)
+    buf = np.zeros(1 << 16, np.uint8)
+    p = W.ctypes.data
+    assert L.lbq_pack_w4(None, 4, 64, None, 0, buf.ctypes.data, buf.size) == 1          # NULL
+    assert L.lbq_pack_w4(p, 4, 96, None, 0, buf.ctypes.data, buf.size) == 2             # K % 64
+    assert L.lbq_pack_w4(p, 0, 64, None, 0, buf.ctypes.data, buf.size) == 2             # N
+    assert L.lbq_pack_w4(p, 4, 64, None, 0, buf.ctypes.data, 10) == 5                   # too small
+    bad = np.array([3, 3], np.int32)
+    assert L.lbq_pack_w4(p, 4, 64, bad.ctypes.data, 2, buf.ctypes.data, buf.size) == 4  # not ascending
+    oob = np.array([64], np.int32)
+    assert L.lbq_pack_w2cb(p, 4, 64, oob.ctypes.data, 1, buf.ctypes.data, buf.size) == 4
+    Wn = W.copy()
+    Wn[1, 2] = np.nan
+    assert L.lbq_pack_w4(Wn.ctypes.data, 4, 64, None, 0, buf.ctypes.data, buf.size) == 9
+    assert L.lbq_w4_packed_bytes(4, 96, 0) == 0
+    idx = np.zeros(1, np.int32)
+    n = ctypes.c_int32(0)
+    Wh = np.random.default_rng(0).standard_normal((8, 1536)).astype(np.float32)
+    st = L.lbq_select_outliers_w4(Wh.ctypes.data, 8, 1536, idx.ctypes.data, 1, ctypes.byref(n))
+    assert st == 5 and n.value > 1
+
+
+def test_device_entry_points_reject_bad_args_without_gpu(lbq):
+    """Host validation runs before any CUDA call, so these return on a CPU machine too."""
+    L = lbq.lib()
+    assert L.lbq_gemv_w4a16(None, 8, 64, 0, 16, 16, 0, None) == 1
+    assert L.lbq_gemv_w4a16(16, 8, 96, 0, 16, 16, 0, None) == 2
+    assert L.lbq_gemv_w2cb_outlier(16, 8, 64, 65, 16, 16, 0, None) == 2
+    assert L.lbq_gemv_w4a16(8, 8, 64, 0, 16, 16, 0, None) == 3          # packed not 16-aligned
+    assert L.lbq_gemv_w4a16(16, 8, 64, 0, 16, 16, 7, None) == 10        # bad dtype
+    assert L.lbq_gemm_w4a16_smallM(16, 0, 8, 64, 0, 16, 64, 16, 8, 0, None) == 2
+    assert L.lbq_gemm_w4a16_smallM(16, 65, 8, 64, 0, 16, 64, 16, 8, 0, None) == 2
+    assert L.lbq_gemm_w4a16_smallM(16, 2, 8, 64, 0, 16, 60, 16, 8, 0, None) == 2   # ldx < K
+    assert L.lbq_gemm_w4a16_smallM(16, 2, 8, 64, 0, 16, 68, 16, 8, 0, None) == 3   # ldx % 8

@@ -1,0 +1,64 @@
+"""The C++ packers and outlier selectors against the oracle, byte for byte (CPU)."""
+import numpy as np
+import pytest
+
+from bit_weight_only_lbq_gb300 import synth
+from oracle import lbq_oracle as O
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (3, 128), (17, 192), (64, 1024), (33, 4160)])
+def test_w4_pack_bitexact(lbq, N, K):
+    W = synth.random_matrix(N, K, seed=N * 7 + K, scale=0.02)
+    assert np.array_equal(lbq.pack_w4(W), O.pack_w4(W))
+
+
+@pytest.mark.parametrize("N,K", [(1, 64), (3, 128), (17, 192), (64, 1024), (33, 4160)])
+def test_w2_pack_bitexact(lbq, N, K):
+    W = synth.random_matrix(N, K, seed=N * 5 + K, scale=0.02)
+    assert np.array_equal(lbq.pack_w2cb(W), O.pack_w2cb(W))
+
+
+def test_pack_with_outliers_bitexact(lbq):
+    W = synth.weights_heavy_cols(40, 1024, config_id=2, layer_id=99)
+    idx = O.select_outliers_w4(W)
+    assert np.array_equal(lbq.select_outliers_w4(W), idx)
+    assert np.array_equal(lbq.pack_w4(W, idx), O.pack_w4(W, idx))
+    X = synth.profile_vectors(1024, config_id=3, layer_id=99)
+    idx2 = O.select_outliers_impact(W, X)
+    assert np.array_equal(lbq.select_outliers_impact(W, X), idx2)
+    assert len(idx2) == int(0.035 * 1024)
+    assert np.array_equal(lbq.pack_w2cb(W, idx2), O.pack_w2cb(W, idx2))
+
+
+def test_golden_groups_through_cpp(lbq, golden):
+    g = golden("w4_worked_example.txt")
+    w = np.array([float(v) for v in g["w_group0"] + g["w_group1"]], dtype=np.float32)[None, :]
+    blob = lbq.pack_w4(w)
+    L = lbq.blob_layout(lbq.LBQ_KIND_W4, 1, 64, 0)
+    assert blob[L["offsets"][0]:L["offsets"][0] + 32].tolist() == [int(v, 16) for v in g["qweight_bytes"]]
+    assert blob[L["offsets"][2]] == int(g["zero_bytes"][0], 16)
+    g2 = golden("w2_worked_example.txt")
+    w = np.empty((1, 64), np.float32)
+    w[0, :32] = [O.C16[int(c)] / 16 + 0.125 for c in g2["codes_group0"]]
+    w[0, 32:] = 0.25
+    blob = lbq.pack_w2cb(w)
+    L = lbq.blob_layout(lbq.LBQ_KIND_W2CB, 1, 64, 0)
+    assert blob[L["offsets"][0]:L["offsets"][0] + 16].tolist() == [int(v, 16) for v in g2["code_bytes"]]
+    assert blob[L["offsets"][1]:L["offsets"][1] + 4].view("<u2").tolist() == [int(v, 16) for v in g2["S_f16_bits"]]
+    assert blob[L["offsets"][2]:L["offsets"][2] + 4].view("<u2").tolist() == [int(v, 16) for v in g2["Z_f16_bits"]]
+
+
+def test_layouts_match_oracle(lbq):
+    for kind, name in ((lbq.LBQ_KIND_W4, "w4"), (lbq.LBQ_KIND_W2CB, "w2")):
+        for N, K, n in ((1, 64, 0), (3, 64, 2), (1000, 4160, 143), (7, 65536, 8192)):
+            a = lbq.blob_layout(kind, N, K, n)
+            b = O.layout(name, N, K, n)
+            assert a["offsets"] == b["offsets"] and a["strides"] == b["strides"] and a["total"] == b["total"]
+
+
+def test_llama8b_qproj_rows_bitexact(lbq):
+    """A slice of the config-2 q_proj (full K = 4096) with the W4 outlier variant."""
+    W = synth.weights_heavy_cols(4096, 4096, config_id=2, layer_id=0)[:256]
+    idx = lbq.select_outliers_w4(W)
+    assert np.array_equal(idx, O.select_outliers_w4(W))
+    assert np.array_equal(lbq.pack_w4(W, idx), O.pack_w4(W, idx))
