@@ -42,7 +42,11 @@ from bit_weight_only_lbq_gb300 import synth  # noqa: E402
 REPLICAS = 3
 SMALL_M = 4
 SAMPLE_ROWS_MAX = 1024
-L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)      # rows of each matrix kept on the host for the oracle's timed sample
+L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)
+# DRAM bytes per launch of the dominant kernel from the ncu capture in
+# profiles/w4_gemv_57344x4096.md (135.857664 MB read + 3.044864 MB written for 57344 rows,
+# scaled to the 14336-row gate/up launch); valid only for the kernel source it was taken on.
+TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "8460985e64cf94b3", "bytes_per_launch": (135857664 + 3044864) / 4}      # rows of each matrix kept on the host for the oracle's timed sample
 METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
 W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
 W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
@@ -53,6 +57,13 @@ def algorithmic_bytes(kind: str, N: int, K: int, n_out: int, M: int = 1) -> int:
     outlier indices and values, the activations read and the outputs written."""
     per_w = W4_BYTES_PER_WEIGHT if kind == "w4" else W2_BYTES_PER_WEIGHT
     return int(per_w * N * K + n_out * (4 + 2 * N) + 2 * K * M + 2 * N * M)
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    src = os.path.join(ROOT, "bit_weight_only_lbq_gb300", "csrc", "lbq_gemv.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
 def load_peaks():
@@ -408,7 +419,9 @@ def main():
         "gpu_launches": len(layer) * args.steps,
         "step_bytes": step_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": (TRAFFIC_CAPTURE["bytes_per_launch"]
+                                 if kernel_source_hash() == TRAFFIC_CAPTURE["kernel_sha256_prefix"] else None),
                      "kernel": "lbq_gemv_kernel<W4,MB=1> on gate/up/down: chained launches in a CUDA graph, "
                                "CUDA events around each replay, average per launch",
                      "serialized_launch_GB_s": round(dom_bytes / (statistics.mean(dom_ms_serial) * 1e-3) / 1e9, 1),

@@ -10,10 +10,14 @@
 // accumulated into the same registers.
 //
 // GB300 design (the pages' kernels are Triton code for Ampere laptops):
+//  * the blob stores each (4-row block x 32-group block) as one contiguous
+//    record (packed codes, then scales/S, then zeros/Z), so a tile of GPL
+//    records is one contiguous range of HBM;
 //  * one persistent CTA per SM; each warp owns a private ring of shared-memory
-//    stages that its lane 0 refills with 2-D Tensor Memory Accelerator copies
-//    (cp.async.bulk.tensor) completing on mbarriers, so each SM keeps tens of
-//    KB of weights in flight with no per-thread address arithmetic;
+//    stages that its lane 0 refills with one bulk copy per tile
+//    (cp.async.bulk, the Tensor Memory Accelerator's 1-D mode) completing on
+//    an mbarrier, so each SM keeps tens of KB in flight with no per-thread
+//    address arithmetic;
 //  * a tile is 4 output rows x (32 * GPL) groups; a lane owns GPL groups and
 //    keeps their activations in registers for the tile's 4 rows; the CTA's
 //    tiles are cut into contiguous per-warp ranges (split-K inside the CTA
@@ -29,8 +33,6 @@
 //  * every wait is bounded (2 s of %globaltimer); a timeout records
 //    LBQ_ERR_TIMEOUT in a device error word and the warp drains its copies.
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -54,40 +56,37 @@ enum Kind { kW4 = 0, kW2 = 1 };
 
 constexpr int round128(int b) { return (b + 127) / 128 * 128; }
 
-// Tile geometry: kTR rows x (GPL * 1024) k; a lane owns GPL groups of 32.
+// Dense record (one row block x 32 groups, the blob's unit) and tile geometry:
+// a tile is GPL consecutive records of one row block; a lane owns one group of
+// each record.
 template <int KIND, int GPL>
 struct Geo {
-    static constexpr int kGroups = 32 * GPL;                          // groups per tile
-    static constexpr int kRow0 = KIND == kW4 ? 16 * kGroups : 8 * kGroups;   // packed bytes per row
-    static constexpr int kRow1 = 2 * kGroups;                         // scales / S per row
-    static constexpr int kRow2 = KIND == kW4 ? kGroups / 2 : 2 * kGroups;    // zeros / Z per row
-    static constexpr int kOff1 = kTR * kRow0;
-    static constexpr int kOff2 = kOff1 + kTR * kRow1;
-    static constexpr int kDense = kOff2 + kTR * kRow2;                // bytes of a dense tile
+    static constexpr int kPacked = KIND == kW4 ? 16 : 8;               // packed bytes per (row, group)
+    static constexpr int kOff1 = kTR * 32 * kPacked;                   // scales / S
+    static constexpr int kOff2 = kOff1 + kTR * 32 * 2;                 // zeros / Z
+    static constexpr int kRec = kOff2 + (KIND == kW4 ? kTR * 16 : kTR * 32 * 2);   // 2368 / 1536
+    static constexpr int kDense = GPL * kRec;
     static constexpr int kStage = round128(kDense > kOutTileBytes ? kDense : kOutTileBytes);
-    // TMA boxes (inner elements): packed as u32, scales/S as u16, zeros as u8 / Z as u16
-    static constexpr int kBox0 = kRow0 / 4, kBox1 = kGroups, kBox2 = KIND == kW4 ? kGroups / 2 : kGroups;
     static constexpr uint32_t kMagicLo = 0x5751424Cu;                            // "LBQW"
     static constexpr uint32_t kMagicHi = KIND == kW4 ? 0x32334734u : 0x32334332u;  // "4G32" / "2C32"
 };
 
 struct GemvArgs {
-    CUtensorMap tm0;       // qweight (u32) / codes (u32)
-    CUtensorMap tm1;       // scales / S (u16)
-    CUtensorMap tm2;       // zeros (u8) / Z (u16)
-    CUtensorMap tmv;       // outlier vals (u16), valid when n_out > 0
     const uint8_t* blob;
+    const uint8_t* area;   // first row block
     const __half* x;       // activation rows, leading dimension ldx (elements)
     const int32_t* idx;
     void* y;               // output rows, leading dimension ldy (elements)
     long long N, K;
     long long ldx, ldy;
+    long long rb_bytes;    // bytes per row block
+    int recs;              // dense records per row block
     int mrows;             // activation rows in this launch (<= MB of the kernel)
     int n_out;
     int y_f32;
     int n_rb;              // row blocks of kTR rows
-    int KT;                // dense k tiles
-    int OT;                // outlier tiles
+    int KT;                // dense tiles per row block (records / GPL, rounded up)
+    int OT;                // outlier records per row block
     int SPW;               // stages per warp
     int rb_cap;            // most row blocks any CTA owns
     uint32_t lut_lo, lut_hi;   // 2-bit codebook: low / high bytes of the FP16 centroids
@@ -143,12 +142,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return mbar_wait_bounded(bar, parity, kWaitLimitNs);
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
-                                            uint64_t policy) {
+// One contiguous global -> shared bulk copy (bytes % 16 == 0, both ends 16-byte
+// aligned) completing on an mbarrier, with an L2 eviction-priority hint.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -253,23 +254,26 @@ __device__ __forceinline__ int x_half_index(int k) {
 // 2^-24 sum_k q_k x_k and w.x = s (sum_k q_k x_k - z X_g) = 2^24 s (dot - z X_g 2^-24);
 // the final 2^24 is applied once per output.
 template <int MB, int GPL>
-__device__ __forceinline__ void w4_dense_tile(const uint8_t* st, const uint4* xq, int xq_plane, const float* xs24,
-                                              int xs_plane, int mrows, int lane, float (&acc)[MB][kTR]) {
+__device__ __forceinline__ void w4_dense_tile(const uint8_t* st, int nrec, const uint4* xq, int xq_plane,
+                                              const float* xs24, int xs_plane, int mrows, int lane,
+                                              float (&acc)[MB][kTR]) {
     using G = Geo<kW4, GPL>;
-    const uint4* qw = reinterpret_cast<const uint4*>(st);
-    const __half* sc = reinterpret_cast<const __half*>(st + G::kOff1);
-    const uint8_t* zp = st + G::kOff2;
 #pragma unroll
     for (int h = 0; h < GPL; ++h) {
-        const int gl = h * 32 + lane;                  // group within the tile
+        if (h >= nrec) break;                          // short last tile
+        const uint8_t* rec = st + h * G::kRec;
+        const uint4* qw = reinterpret_cast<const uint4*>(rec);
+        const __half* sc = reinterpret_cast<const __half*>(rec + G::kOff1);
+        const uint8_t* zp = rec + G::kOff2;
+        const int gl = lane;                           // group within the record
         if constexpr (MB == 1) {
             const uint4 xr[4] = {xq[h * 128], xq[h * 128 + 32], xq[h * 128 + 64], xq[h * 128 + 96]};
             const float xsz = xs24[h * 32];
 #pragma unroll
             for (int r = 0; r < kTR; ++r) {
-                const uint4 q = qw[r * G::kGroups + gl];
-                const float s = __half2float(sc[r * G::kGroups + gl]);
-                const uint32_t zb = zp[r * (G::kGroups / 2) + (gl >> 1)];
+                const uint4 q = qw[r * 32 + gl];
+                const float s = __half2float(sc[r * 32 + gl]);
+                const uint32_t zb = zp[r * 16 + (gl >> 1)];
                 const float zf = static_cast<float>((zb >> ((lane & 1) * 4)) & 15u);
                 float l0 = 0.f, l1 = 0.f, h0 = 0.f, h1 = 0.f;
 #pragma unroll
@@ -288,9 +292,9 @@ __device__ __forceinline__ void w4_dense_tile(const uint8_t* st, const uint4* xq
             float s[kTR], zf[kTR];
 #pragma unroll
             for (int r = 0; r < kTR; ++r) {
-                const uint4 q = qw[r * G::kGroups + gl];
-                s[r] = __half2float(sc[r * G::kGroups + gl]);
-                const uint32_t zb = zp[r * (G::kGroups / 2) + (gl >> 1)];
+                const uint4 q = qw[r * 32 + gl];
+                s[r] = __half2float(sc[r * 32 + gl]);
+                const uint32_t zb = zp[r * 16 + (gl >> 1)];
                 zf[r] = static_cast<float>((zb >> ((lane & 1) * 4)) & 15u);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -329,22 +333,24 @@ __device__ __forceinline__ void w4_dense_tile(const uint8_t* st, const uint4* xq
 // 2-bit dense tile: four codes -> PRMT selector (c, c+4 per code) -> two FP16
 // codebook pairs; w.x = S sum_k C[q_k] x_k + Z X_g.
 template <int GPL>
-__device__ __forceinline__ void w2_dense_tile(const uint8_t* st, const uint4* xq, const float* xsum, int lane,
-                                              uint32_t lut_lo, uint32_t lut_hi, float (&acc)[kTR]) {
+__device__ __forceinline__ void w2_dense_tile(const uint8_t* st, int nrec, const uint4* xq, const float* xsum,
+                                              int lane, uint32_t lut_lo, uint32_t lut_hi, float (&acc)[kTR]) {
     using G = Geo<kW2, GPL>;
-    const uint2* cw = reinterpret_cast<const uint2*>(st);
-    const __half* Sg = reinterpret_cast<const __half*>(st + G::kOff1);
-    const __half* Zg = reinterpret_cast<const __half*>(st + G::kOff2);
 #pragma unroll
     for (int h = 0; h < GPL; ++h) {
-        const int gl = h * 32 + lane;
+        if (h >= nrec) break;                          // short last tile
+        const uint8_t* rec = st + h * G::kRec;
+        const uint2* cw = reinterpret_cast<const uint2*>(rec);
+        const __half* Sg = reinterpret_cast<const __half*>(rec + G::kOff1);
+        const __half* Zg = reinterpret_cast<const __half*>(rec + G::kOff2);
+        const int gl = lane;
         const uint4 xr[4] = {xq[h * 128], xq[h * 128 + 32], xq[h * 128 + 64], xq[h * 128 + 96]};
         const float xs = xsum[h * 32];
 #pragma unroll
         for (int r = 0; r < kTR; ++r) {
-            const uint2 c = cw[r * G::kGroups + gl];
-            const float S = __half2float(Sg[r * G::kGroups + gl]);
-            const float Z = __half2float(Zg[r * G::kGroups + gl]);
+            const uint2 c = cw[r * 32 + gl];
+            const float S = __half2float(Sg[r * 32 + gl]);
+            const float Z = __half2float(Zg[r * 32 + gl]);
             float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int v = 0; v < 2; ++v) {
@@ -412,7 +418,7 @@ __device__ __forceinline__ float reduce_rows4(const float (&acc)[4], int lane) {
 // ------------------------------------------------------------------ kernel
 
 struct SmemPlan {
-    int ring, xs, xsum, xo, omask, yacc, part, bars, total;
+    int ring, xs, xsum, xo, omask, yacc, part, seg, bars, total;
 };
 
 // NW warps, rb_cap: most row blocks a CTA owns; MB: activation planes.
@@ -434,6 +440,8 @@ __host__ __device__ inline SmemPlan smem_plan(int NW, int stage, int KTg, int OT
     off += rb_cap * kTR * MB * 4;
     p.part = off;
     off += NW * 2 * kTR * MB * 4;
+    p.seg = off;
+    off += NW * 2 * 4;                     // per warp: first and last row block it touched
     off = (off + 7) / 8 * 8;
     p.bars = off;
     off += NW * SPW * 8;
@@ -446,8 +454,10 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     using G = Geo<KIND, GPL>;
     constexpr int kThreads = NW * 32;
     constexpr float kUnit = KIND == kW4 ? 5.9604644775390625e-8f : 1.f;   // 2^-24 for the 4-bit products
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // align by offsetting the shared array itself, so the compiler keeps the
+    // shared address space (LDS with immediate offsets, no generic addressing)
+    uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const int KTg = a.KT * GPL;
     const SmemPlan P = smem_plan(NW, G::kStage, KTg, a.OT, a.SPW, MB, a.rb_cap);
     uint8_t* ring = smem + P.ring;
@@ -457,6 +467,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     uint32_t* omask = reinterpret_cast<uint32_t*>(smem + P.omask);
     float* yacc = reinterpret_cast<float*>(smem + P.yacc);
     float* part = reinterpret_cast<float*>(smem + P.part);
+    int* seg = reinterpret_cast<int*>(smem + P.seg);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -483,15 +494,18 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     auto issue_next = [&]() {
         uint8_t* dst = my_ring + i_slot * G::kStage;
         uint64_t* bar = my_bars + i_slot;
-        const int row0 = (rb_begin + i_rb) * kTR;
+        const uint8_t* rb_src = a.area + static_cast<long long>(rb_begin + i_rb) * a.rb_bytes;
         if (i_kk < a.KT) {
-            mbar_arrive_expect_tx(bar, G::kDense);
-            tma_load_2d(dst, &a.tm0, i_kk * G::kBox0, row0, bar, policy);
-            tma_load_2d(dst + G::kOff1, &a.tm1, i_kk * G::kBox1, row0, bar, policy);
-            tma_load_2d(dst + G::kOff2, &a.tm2, i_kk * G::kBox2, row0, bar, policy);
+            const int r0 = i_kk * GPL;
+            const int nrec = a.recs - r0 < GPL ? a.recs - r0 : GPL;
+            const uint32_t bytes = static_cast<uint32_t>(nrec * G::kRec);
+            mbar_arrive_expect_tx(bar, bytes);
+            bulk_load(dst, rb_src + static_cast<long long>(r0) * G::kRec, bytes, bar, policy);
         } else {
             mbar_arrive_expect_tx(bar, kOutTileBytes);
-            tma_load_2d(dst, &a.tmv, (i_kk - a.KT) * kOutCols, row0, bar, policy);
+            bulk_load(dst, rb_src + static_cast<long long>(a.recs) * G::kRec +
+                               static_cast<long long>(i_kk - a.KT) * kOutTileBytes,
+                      kOutTileBytes, bar, policy);
         }
         if (++i_kk == TPR) {
             i_kk = 0;
@@ -507,13 +521,14 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         const int pre = my_tiles < SPW ? my_tiles : SPW;
         for (int t = 0; t < pre; ++t) issue_next();
     }
+    // blob header: loaded now (three 16-byte loads in flight), compared after the main loop,
+    // so the check never delays this CTA's prologue
+    uint4 hdr0 = make_uint4(0u, 0u, 0u, 0u), hdr1 = hdr0, hdr2 = hdr0;
     if (blockIdx.x == 0 && tid == 0) {
-        const uint32_t* h = reinterpret_cast<const uint32_t*>(a.blob);
-        const long long* hl = reinterpret_cast<const long long*>(a.blob + 16);
-        const int* hn = reinterpret_cast<const int*>(a.blob + 32);
-        if (h[0] != G::kMagicLo || h[1] != G::kMagicHi || h[2] != LBQ_FORMAT_VERSION_NUM || hl[0] != a.N ||
-            hl[1] != a.K || hn[0] != a.n_out)
-            record_error(LBQ_ERR_FORMAT);
+        const uint4* h = reinterpret_cast<const uint4*>(a.blob);
+        hdr0 = h[0];
+        hdr1 = h[1];
+        hdr2 = h[2];
     }
     // outlier-channel bitmask and the row accumulators (no dependence on the previous grid)
     for (int i = tid; i < ngroups; i += kThreads) omask[i] = 0u;
@@ -598,7 +613,11 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     bool ok = true;
     int c_rb = w_begin / TPR, c_kk = w_begin - (w_begin / TPR) * TPR, c_slot = 0;
     uint32_t c_phase = 0;
-    const int first_rb = c_rb, last_rb = my_tiles > 0 ? (w_end - 1) / TPR : -1;
+    const int first_rb = my_tiles > 0 ? c_rb : -1, last_rb = my_tiles > 0 ? (w_end - 1) / TPR : -1;
+    if (lane == 0) {
+        seg[2 * warp] = first_rb;
+        seg[2 * warp + 1] = last_rb != first_rb ? last_rb : -1;
+    }
     float acc[MB][kTR];
 #pragma unroll
     for (int m = 0; m < MB; ++m)
@@ -615,10 +634,11 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         if (c_kk < a.KT) {
             const uint4* xq = xs + c_kk * GPL * 128 + lane;
             const float* xsg = xsum + c_kk * GPL * 32 + lane;
+            const int nrec = a.recs - c_kk * GPL;            // records in this tile (>= GPL except at the end)
             if constexpr (KIND == kW4)
-                w4_dense_tile<MB, GPL>(st, xq, xq_plane, xsg, ngroups, mrows, lane, acc);
+                w4_dense_tile<MB, GPL>(st, nrec, xq, xq_plane, xsg, ngroups, mrows, lane, acc);
             else
-                w2_dense_tile<GPL>(st, xq, xsg, lane, a.lut_lo, a.lut_hi, acc[0]);
+                w2_dense_tile<GPL>(st, nrec, xq, xsg, lane, a.lut_lo, a.lut_hi, acc[0]);
         } else {
             outlier_tile<MB>(st, xo + (c_kk - a.KT) * kOutCols, xo_plane, mrows, lane, kUnit, acc);
         }
@@ -668,19 +688,23 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     }
     __syncthreads();
 
+    if (blockIdx.x == 0 && tid == 0) {
+        const long long n_hdr = (static_cast<long long>(hdr1.y) << 32) | hdr1.x;
+        const long long k_hdr = (static_cast<long long>(hdr1.w) << 32) | hdr1.z;
+        if (hdr0.x != G::kMagicLo || hdr0.y != G::kMagicHi || hdr0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != a.N ||
+            k_hdr != a.K || static_cast<int>(hdr2.x) != a.n_out)
+            record_error(LBQ_ERR_FORMAT);
+    }
     // combine: owned row blocks are already in yacc; shared ones add the parked
     // partials of their warps in warp order (deterministic)
     for (int i = tid; i < R * kTR * MB; i += kThreads) {
         const int m = i % MB, rr = i / MB;
         const int rbl = rr / kTR, r = rr - rbl * kTR;
         float y = yacc[i];
-#pragma unroll 1
+#pragma unroll 4
         for (int w = 0; w < NW; ++w) {
-            const int wb = (w * n_tiles) / NW, we = ((w + 1) * n_tiles) / NW;
-            if (we <= wb) continue;
-            const int fr = wb / TPR, lr = (we - 1) / TPR;
-            if (fr == rbl) y += part[((w * 2 + 0) * kTR + r) * MB + m];
-            if (lr == rbl && lr != fr) y += part[((w * 2 + 1) * kTR + r) * MB + m];
+            if (seg[2 * w] == rbl) y += part[((w * 2 + 0) * kTR + r) * MB + m];
+            if (seg[2 * w + 1] == rbl) y += part[((w * 2 + 1) * kTR + r) * MB + m];
         }
         const long long n = static_cast<long long>(rb_begin + rbl) * kTR + r;
         if (n < a.N && m < mrows) {
@@ -701,26 +725,14 @@ struct DeviceInfo {
     bool init = false;
     bool ok = false;
     int sms = 0;
-    int max_smem = 0;
+    int max_smem = 0;          // opt-in maximum per CTA
+    int smem_per_sm = 0;
+    int smem_reserved = 0;     // per CTA, reserved by the system
     bool attr_set[kNumVariantsMax] = {};
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
 
 lbq_status device_info(DeviceInfo** out) {
     int dev = 0;
@@ -733,7 +745,9 @@ lbq_status device_info(DeviceInfo** out) {
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
             return LBQ_ERR_CUDA;
         d.ok = (major == 10 && minor == 3);
         d.init = true;
@@ -741,20 +755,6 @@ lbq_status device_info(DeviceInfo** out) {
     if (!d.ok) return LBQ_ERR_UNSUPPORTED;
     *out = &d;
     return LBQ_OK;
-}
-
-bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-               uint64_t rows, uint64_t row_stride, uint32_t box_inner, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {row_stride};
-    cuuint32_t box[2] = {box_inner, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    (void)elem_bytes;
-    return fn(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -784,35 +784,22 @@ const Variant& variant(int v) {
 }
 
 lbq_status prepare_args(const Variant& V, const void* packed, int64_t N, int64_t K, int32_t n_out, GemvArgs* a) {
-    const int kind = V.kind;
     lbq_layout L;
-    lbq_status st = lbq_blob_layout(kind == kW4 ? LBQ_KIND_W4 : LBQ_KIND_W2CB, N, K, n_out, &L);
+    lbq_status st = lbq_blob_layout(V.kind == kW4 ? LBQ_KIND_W4 : LBQ_KIND_W2CB, N, K, n_out, &L);
     if (st != LBQ_OK) return st;
     std::memset(a, 0, sizeof(*a));
     const uint8_t* b = static_cast<const uint8_t*>(packed);
-    const uint32_t g = 32 * V.GPL;        // groups per tile
-    bool enc = true;
-    if (kind == kW4) {
-        enc &= encode_2d(&a->tm0, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, b + L.offset[0], K / 8, N, L.row_stride[0], 4 * g, kTR);
-        enc &= encode_2d(&a->tm1, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b + L.offset[1], K / 32, N, L.row_stride[1], g, kTR);
-        enc &= encode_2d(&a->tm2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b + L.offset[2], K / 64, N, L.row_stride[2], g / 2, kTR);
-    } else {
-        enc &= encode_2d(&a->tm0, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, b + L.offset[0], K / 16, N, L.row_stride[0], 2 * g, kTR);
-        enc &= encode_2d(&a->tm1, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b + L.offset[1], K / 32, N, L.row_stride[1], g, kTR);
-        enc &= encode_2d(&a->tm2, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b + L.offset[2], K / 32, N, L.row_stride[2], g, kTR);
-    }
-    if (n_out > 0)
-        enc &= encode_2d(&a->tmv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, b + L.offset[4], n_out, N, L.row_stride[4],
-                         kOutCols, kTR);
-    if (!enc) return LBQ_ERR_CUDA;
     a->blob = b;
-    a->idx = reinterpret_cast<const int32_t*>(b + L.offset[3]);
+    a->area = b + L.area_offset;
+    a->idx = reinterpret_cast<const int32_t*>(b + L.idx_offset);
+    a->rb_bytes = static_cast<long long>(L.row_block_bytes);
+    a->recs = static_cast<int>(L.records);
     a->N = N;
     a->K = K;
     a->n_out = n_out;
     a->n_rb = static_cast<int>((N + kTR - 1) / kTR);
-    a->KT = static_cast<int>((K + 32 * g - 1) / (32 * g));
-    a->OT = (n_out + kOutCols - 1) / kOutCols;
+    a->KT = (a->recs + V.GPL - 1) / V.GPL;
+    a->OT = static_cast<int>(L.outlier_records);
     // 2-bit codebook as FP16 byte tables for PRMT (otf-llm section 2, rounded once)
     const double cb[4] = {-1.52, -0.45, 0.45, 1.52};
     for (int c = 0; c < 4; ++c) {
@@ -823,22 +810,34 @@ lbq_status prepare_args(const Variant& V, const void* packed, int64_t N, int64_t
     return LBQ_OK;
 }
 
-// Stages per warp that fit next to the activation planes; < 2 means "does not fit".
-int stages_per_warp(const DeviceInfo* dev, const Variant& V, int KT, int OT, int rb_cap) {
+// Stages per warp that fit in `budget` bytes next to the activation planes;
+// < 2 means "does not fit".
+int stages_per_warp(const Variant& V, int budget, int KT, int OT, int rb_cap) {
     const SmemPlan fixed = smem_plan(V.NW, V.stage, KT * V.GPL, OT, 0, V.MB, rb_cap);
-    int spw = (dev->max_smem - fixed.total - V.NW * kMaxStagesPerWarp * 8) / (V.NW * V.stage);
+    int spw = (budget - fixed.total - V.NW * kMaxStagesPerWarp * 8) / (V.NW * V.stage);
     return spw > kMaxStagesPerWarp ? kMaxStagesPerWarp : spw;
 }
 
-int grid_for(const DeviceInfo* dev, int n_rb) { return n_rb < dev->sms ? n_rb : dev->sms; }
-int rb_cap_for(int n_rb, int grid) { return (n_rb + grid - 1) / grid; }
+struct LaunchShape {
+    int grid, rb_cap, SPW;
+};
+
+// One persistent CTA per SM (fewer when there are fewer row blocks), each
+// owning a contiguous, balanced run of row blocks.
+LaunchShape launch_shape(const DeviceInfo* dev, const Variant& V, int n_rb, int KT, int OT) {
+    LaunchShape L;
+    L.grid = n_rb < dev->sms ? n_rb : dev->sms;
+    L.rb_cap = (n_rb + L.grid - 1) / L.grid;
+    L.SPW = stages_per_warp(V, dev->max_smem, KT, OT, L.rb_cap);
+    return L;
+}
 
 lbq_status launch_variant(DeviceInfo* dev, int vi, GemvArgs& a, void* stream, uint32_t flags) {
     const Variant& V = variant(vi);
-    const int grid = grid_for(dev, a.n_rb);
-    a.rb_cap = rb_cap_for(a.n_rb, grid);
-    a.SPW = stages_per_warp(dev, V, a.KT, a.OT, a.rb_cap);
-    if (a.SPW < 2) return LBQ_ERR_SHAPE;
+    const LaunchShape S = launch_shape(dev, V, a.n_rb, a.KT, a.OT);
+    if (S.SPW < 2) return LBQ_ERR_SHAPE;
+    a.rb_cap = S.rb_cap;
+    a.SPW = S.SPW;
     const SmemPlan P = smem_plan(V.NW, V.stage, a.KT * V.GPL, a.OT, a.SPW, V.MB, a.rb_cap);
     if (!dev->attr_set[vi]) {
         if (cudaFuncSetAttribute(V.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->max_smem) != cudaSuccess)
@@ -847,7 +846,7 @@ lbq_status launch_variant(DeviceInfo* dev, int vi, GemvArgs& a, void* stream, ui
     }
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(S.grid));
     cfg.blockDim = dim3(V.NW * 32);
     cfg.dynamicSmemBytes = P.total;
     cfg.stream = static_cast<cudaStream_t>(stream);
@@ -881,8 +880,7 @@ lbq_status launch_one(DeviceInfo* dev, int vi, int vfallback, const void* packed
     GemvArgs a;
     lbq_status st = prepare_args(variant(vi), packed, N, K, n_out, &a);
     if (st != LBQ_OK) return st;
-    if (vfallback >= 0 &&
-        stages_per_warp(dev, variant(vi), a.KT, a.OT, rb_cap_for(a.n_rb, grid_for(dev, a.n_rb))) < 2) {
+    if (vfallback >= 0 && launch_shape(dev, variant(vi), a.n_rb, a.KT, a.OT).SPW < 2) {
         vi = vfallback;
         st = prepare_args(variant(vi), packed, N, K, n_out, &a);
         if (st != LBQ_OK) return st;
@@ -925,9 +923,8 @@ lbq_status launch_smallm(const void* packed, int32_t M, int64_t N, int64_t K, in
     GemvArgs a;
     st = prepare_args(variant(1), packed, N, K, n_out, &a);     // variants 1..3 share the tiling
     if (st != LBQ_OK) return st;
-    const int rb_cap = rb_cap_for(a.n_rb, grid_for(dev, a.n_rb));
     const size_t ysz = y_dtype == LBQ_F32 ? 4 : 2;
-    if (stages_per_warp(dev, variant(1), a.KT, a.OT, rb_cap) < 2) {
+    if (launch_shape(dev, variant(1), a.n_rb, a.KT, a.OT).SPW < 2) {
         // K too wide for two activation planes: one GEMV pass per row
         for (int m = 0; m < M; ++m) {
             st = launch_one(dev, 0, 5, packed, N, K, n_out, static_cast<const __half*>(X) + m * ldx, ldx,
@@ -938,7 +935,7 @@ lbq_status launch_smallm(const void* packed, int32_t M, int64_t N, int64_t K, in
         return LBQ_OK;
     }
     int vmax = 3;
-    while (vmax > 1 && stages_per_warp(dev, variant(vmax), a.KT, a.OT, rb_cap) < 4) --vmax;
+    while (vmax > 1 && launch_shape(dev, variant(vmax), a.n_rb, a.KT, a.OT).SPW < 4) --vmax;
     int vi = 1;
     while (vi < vmax && variant(vi).MB < M) ++vi;
     const int MB = variant(vi).MB;

@@ -24,6 +24,11 @@ constexpr int kGroup = 32;
 constexpr double kScaleFloor = 1e-8;    // SPECTRA 3.4: s = max(range / 15, 1e-8)
 constexpr double kOlsEps = 1e-8;        // otf-llm 3: OLS denominator epsilon (value is a reading)
 constexpr uint32_t kHeaderBytes = 128;
+// part offsets inside a dense record (4 rows x 32 groups)
+constexpr uint64_t kW4ScaleOff = 4 * 32 * 16;                 // 2048
+constexpr uint64_t kW4ZeroOff = kW4ScaleOff + 4 * 32 * 2;     // 2304
+constexpr uint64_t kW2SOff = 4 * 32 * 8;                      // 1024
+constexpr uint64_t kW2ZOff = kW2SOff + 4 * 32 * 2;            // 1280
 
 // otf-llm section 2 codebook, rounded once to FP16 (bit patterns and values)
 constexpr double kCodebookDecimal[4] = {-1.52, -0.45, 0.45, 1.52};
@@ -195,10 +200,23 @@ void write_header(uint8_t* dst, const char magic[8], int64_t N, int64_t K, int32
     std::memcpy(dst + 32, &n_out, 4);
     std::memcpy(dst + 36, &group, 4);
     std::memcpy(dst + 40, &L.total_bytes, 8);
-    for (int i = 0; i < 5; ++i) {
-        std::memcpy(dst + 48 + 16 * i, &L.offset[i], 8);
-        std::memcpy(dst + 56 + 16 * i, &L.row_stride[i], 8);
-    }
+    const uint64_t f[7] = {L.area_offset, L.row_block_bytes, L.record_bytes, L.records,
+                           L.outlier_record_bytes, L.outlier_records, L.idx_offset};
+    std::memcpy(dst + 48, f, sizeof(f));
+}
+
+// Byte offset of (row n, group g) inside the blob's record area: the record of
+// row block n/4 and group block g/32, plus the row-major (row, group) index.
+struct RecordAddr {
+    uint64_t rec;     // start of the record
+    int slot;         // (row in block) * 32 + (group in record)
+};
+inline RecordAddr record_addr(const lbq_layout& L, int64_t n, int64_t g) {
+    RecordAddr a;
+    a.rec = L.area_offset + uint64_t(n / lbq::kRowsPerBlock) * L.row_block_bytes +
+            uint64_t(g / lbq::kRecordGroups) * L.record_bytes;
+    a.slot = int(n % lbq::kRowsPerBlock) * lbq::kRecordGroups + int(g % lbq::kRecordGroups);
+    return a;
 }
 
 // Shared front matter of both packers: validation, header, outlier sections.
@@ -220,13 +238,19 @@ lbq_status pack_common(lbq_kind kind, const float* W, int64_t N, int64_t K, cons
     is_out->assign(static_cast<size_t>(K), 0);
     for (int32_t j = 0; j < n_out; ++j) (*is_out)[idx[j]] = 1;
     if (n_out > 0) {
-        std::memcpy(out + L->offset[3], idx, sizeof(int32_t) * n_out);
-        uint8_t* vals = out + L->offset[4];
-        const uint64_t ldv = L->row_stride[4];
+        std::memcpy(out + L->idx_offset, idx, sizeof(int32_t) * n_out);
+        // outlier records follow the dense records of each row block
         parallel_for(N, [&](int64_t b, int64_t e) {
             for (int64_t n = b; n < e; ++n) {
-                uint16_t* r = reinterpret_cast<uint16_t*>(vals + n * ldv);
-                for (int32_t j = 0; j < n_out; ++j) r[j] = f64_to_f16_bits(W[n * K + idx[j]]);
+                const uint64_t base = L->area_offset + uint64_t(n / lbq::kRowsPerBlock) * L->row_block_bytes +
+                                      L->records * L->record_bytes;
+                const int r = int(n % lbq::kRowsPerBlock);
+                for (int32_t j = 0; j < n_out; ++j) {
+                    const uint64_t off = base + uint64_t(j / lbq::kOutlierCols) * L->outlier_record_bytes +
+                                         uint64_t(r * lbq::kOutlierCols + j % lbq::kOutlierCols) * 2;
+                    const uint16_t h = f64_to_f16_bits(W[n * K + idx[j]]);
+                    std::memcpy(out + off, &h, 2);
+                }
             }
         });
     }
@@ -265,30 +289,23 @@ const char* lbq_status_string(lbq_status s) {
 lbq_status lbq_blob_layout(lbq_kind kind, int64_t N, int64_t K, int32_t n_out, lbq_layout* out) {
     if (!out) return LBQ_ERR_NULL;
     if (!shape_ok(N, K, n_out)) return LBQ_ERR_SHAPE;
-    uint64_t rows[3];
-    if (kind == LBQ_KIND_W4) {
-        rows[0] = K / 2;
-        rows[1] = K / kGroup * 2;
-        rows[2] = K / 64;
-    } else if (kind == LBQ_KIND_W2CB) {
-        rows[0] = K / 4;
-        rows[1] = K / kGroup * 2;
-        rows[2] = K / kGroup * 2;
-    } else {
+    uint64_t per_row;   // bytes of one row of a record: packed + scale/S + zero/Z for 32 groups
+    if (kind == LBQ_KIND_W4)
+        per_row = 16 * lbq::kRecordGroups + 2 * lbq::kRecordGroups + lbq::kRecordGroups / 2;
+    else if (kind == LBQ_KIND_W2CB)
+        per_row = 8 * lbq::kRecordGroups + 2 * lbq::kRecordGroups + 2 * lbq::kRecordGroups;
+    else
         return LBQ_ERR_UNSUPPORTED;
-    }
-    uint64_t cur = lbq::kSectionAlign;
-    for (int i = 0; i < 3; ++i) {
-        out->row_stride[i] = round_up(rows[i], lbq::kRowAlign);
-        out->offset[i] = cur;
-        cur = round_up(cur + uint64_t(N) * out->row_stride[i], lbq::kSectionAlign);
-    }
-    out->offset[3] = cur;
-    out->row_stride[3] = 0;
-    cur = round_up(cur + 4ull * n_out, lbq::kSectionAlign);
-    out->offset[4] = cur;
-    out->row_stride[4] = round_up(2ull * n_out, lbq::kRowAlign);
-    out->total_bytes = round_up(cur + uint64_t(N) * out->row_stride[4], lbq::kSectionAlign);
+    const uint64_t group_k = uint64_t(lbq::kRecordGroups) * kGroup;
+    out->area_offset = lbq::kSectionAlign;
+    out->record_bytes = lbq::kRowsPerBlock * per_row;
+    out->records = (uint64_t(K) + group_k - 1) / group_k;
+    out->outlier_record_bytes = n_out > 0 ? uint64_t(lbq::kRowsPerBlock) * lbq::kOutlierCols * 2 : 0;
+    out->outlier_records = (uint64_t(n_out) + lbq::kOutlierCols - 1) / lbq::kOutlierCols;
+    out->row_block_bytes = out->records * out->record_bytes + out->outlier_records * out->outlier_record_bytes;
+    const uint64_t n_rb = (uint64_t(N) + lbq::kRowsPerBlock - 1) / lbq::kRowsPerBlock;
+    out->idx_offset = round_up(out->area_offset + n_rb * out->row_block_bytes, lbq::kSectionAlign);
+    out->total_bytes = round_up(out->idx_offset + 4ull * n_out, lbq::kSectionAlign);
     return LBQ_OK;
 }
 
@@ -371,10 +388,8 @@ lbq_status lbq_pack_w4(const float* W, int64_t N, int64_t K, const int32_t* idx,
         double w[kGroup];
         uint8_t q[kGroup];
         for (int64_t n = b; n < e; ++n) {
-            uint8_t* qrow = out + L.offset[0] + n * L.row_stride[0];
-            uint16_t* srow = reinterpret_cast<uint16_t*>(out + L.offset[1] + n * L.row_stride[1]);
-            uint8_t* zrow = out + L.offset[2] + n * L.row_stride[2];
             for (int64_t g = 0; g < ng; ++g) {
+                const RecordAddr ra = record_addr(L, n, g);
                 double wmin = HUGE_VAL, wmax = -HUGE_VAL;
                 for (int k = 0; k < kGroup; ++k) {
                     const int64_t col = g * kGroup + k;
@@ -390,13 +405,16 @@ lbq_status lbq_pack_w4(const float* W, int64_t N, int64_t K, const int32_t* idx,
                     t = t + z;
                     q[k] = static_cast<uint8_t>(std::min(std::max(std::nearbyint(t), 0.0), 15.0));
                 }
-                for (int k = 0; k < 16; ++k) qrow[g * 16 + k] = static_cast<uint8_t>(q[k] | (q[k + 16] << 4));
-                srow[g] = f64_to_f16_bits(s);
+                uint8_t* qdst = out + ra.rec + uint64_t(ra.slot) * 16;
+                for (int k = 0; k < 16; ++k) qdst[k] = static_cast<uint8_t>(q[k] | (q[k + 16] << 4));
+                const uint16_t sh = f64_to_f16_bits(s);
+                std::memcpy(out + ra.rec + kW4ScaleOff + uint64_t(ra.slot) * 2, &sh, 2);
                 const uint8_t zi = static_cast<uint8_t>(z);
+                uint8_t* zdst = out + ra.rec + kW4ZeroOff + (ra.slot >> 1);   // (row * 32 + group) / 2
                 if (g % 2 == 0)
-                    zrow[g / 2] = zi;
+                    *zdst = zi;
                 else
-                    zrow[g / 2] = static_cast<uint8_t>(zrow[g / 2] | (zi << 4));
+                    *zdst = static_cast<uint8_t>(*zdst | (zi << 4));
             }
         }
     });
@@ -416,10 +434,8 @@ lbq_status lbq_pack_w2cb(const float* W, int64_t N, int64_t K, const int32_t* id
         double w[kGroup], d[kGroup], cq[kGroup];
         uint8_t q[kGroup];
         for (int64_t n = b; n < e; ++n) {
-            uint8_t* crow = out + L.offset[0] + n * L.row_stride[0];
-            uint16_t* Srow = reinterpret_cast<uint16_t*>(out + L.offset[1] + n * L.row_stride[1]);
-            uint16_t* Zrow = reinterpret_cast<uint16_t*>(out + L.offset[2] + n * L.row_stride[2]);
             for (int64_t g = 0; g < ng; ++g) {
+                const RecordAddr ra = record_addr(L, n, g);
                 for (int k = 0; k < kGroup; ++k) {
                     const int64_t col = g * kGroup + k;
                     w[k] = is_out[col] ? 0.0 : static_cast<double>(W[n * K + col]);
@@ -465,11 +481,13 @@ lbq_status lbq_pack_w2cb(const float* W, int64_t N, int64_t K, const int32_t* id
                 const double S = num / (den + kOlsEps);
                 const double SZ = S * cbar;
                 const double Z = mu - SZ;
-                Srow[g] = f64_to_f16_bits(S);
-                Zrow[g] = f64_to_f16_bits(Z);
+                const uint16_t Sh = f64_to_f16_bits(S), Zh = f64_to_f16_bits(Z);
+                std::memcpy(out + ra.rec + kW2SOff + uint64_t(ra.slot) * 2, &Sh, 2);
+                std::memcpy(out + ra.rec + kW2ZOff + uint64_t(ra.slot) * 2, &Zh, 2);
+                uint8_t* cdst = out + ra.rec + uint64_t(ra.slot) * 8;
                 for (int i = 0; i < kGroup / 4; ++i)
-                    crow[g * 8 + i] = static_cast<uint8_t>(q[4 * i] | (q[4 * i + 1] << 2) | (q[4 * i + 2] << 4) |
-                                                          (q[4 * i + 3] << 6));
+                    cdst[i] = static_cast<uint8_t>(q[4 * i] | (q[4 * i + 1] << 2) | (q[4 * i + 2] << 4) |
+                                                   (q[4 * i + 3] << 6));
             }
         }
     });

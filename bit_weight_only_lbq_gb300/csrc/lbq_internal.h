@@ -10,8 +10,10 @@ namespace lbq {
 
 constexpr int64_t kMaxK = 65536;          // x of one row block must fit in shared memory
 constexpr int32_t kMaxOutliers = 8192;    // gathered outlier activations live in shared memory
-constexpr uint64_t kSectionAlign = 256;   // every blob section starts on this boundary
-constexpr uint64_t kRowAlign = 16;        // rows of 2-D sections are padded to this
+constexpr uint64_t kSectionAlign = 256;   // the record area and the index array start on this boundary
+constexpr int kRowsPerBlock = 4;          // rows of a row block (one record row-block)
+constexpr int kRecordGroups = 32;         // groups of 32 weights per dense record (1024 k)
+constexpr int kOutlierCols = 256;         // outlier columns per outlier record
 constexpr int kMaxM = 64;                 // largest batch of the small-M entry point
 
 uint16_t host_f64_to_f16(double v);

@@ -46,8 +46,10 @@ class LbqError(RuntimeError):
 
 
 class Layout(ctypes.Structure):
-    _fields_ = [("offset", ctypes.c_uint64 * 5), ("row_stride", ctypes.c_uint64 * 5),
-                ("total_bytes", ctypes.c_uint64)]
+    _fields_ = [("area_offset", ctypes.c_uint64), ("row_block_bytes", ctypes.c_uint64),
+                ("record_bytes", ctypes.c_uint64), ("records", ctypes.c_uint64),
+                ("outlier_record_bytes", ctypes.c_uint64), ("outlier_records", ctypes.c_uint64),
+                ("idx_offset", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
 
 
 _lib = None
@@ -113,7 +115,9 @@ def _ptr(a: np.ndarray) -> int:
 def blob_layout(kind: int, N: int, K: int, n_out: int) -> dict:
     L = Layout()
     _check(lib().lbq_blob_layout(kind, N, K, n_out, ctypes.byref(L)), "lbq_blob_layout")
-    return {"offsets": list(L.offset), "strides": list(L.row_stride), "total": int(L.total_bytes)}
+    return {"area": L.area_offset, "rb_bytes": L.row_block_bytes, "rec_bytes": L.record_bytes, "recs": L.records,
+            "out_rec_bytes": L.outlier_record_bytes, "out_recs": L.outlier_records, "idx": L.idx_offset,
+            "total": L.total_bytes}
 
 
 def _as_f32(W) -> np.ndarray:

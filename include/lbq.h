@@ -43,20 +43,23 @@
  *   [16:24)  i64 N                      [24:32)  i64 K
  *   [32:36)  i32 n_out                  [36:40)  u32 group size = 32
  *   [40:48)  u64 total blob bytes
- *   [48:128) five (u64 offset, u64 row stride) pairs, one per section:
- *     4-bit : 0 qweight  N x K/2 bytes, byte k of a group = q_k | q_{k+16} << 4
- *             1 scales   N x K/32 FP16
- *             2 zeros    N x K/64 bytes, z_{2m} | z_{2m+1} << 4
- *             3 idx      n_out int32 (1-D, stride 0)
- *             4 vals     N x n_out FP16 (row n = W[n, idx])
- *     2-bit : 0 codes    N x K/4 bytes, byte = q0 | q1<<2 | q2<<4 | q3<<6 (k = 4i+j)
- *             1 S        N x K/32 FP16
- *             2 Z        N x K/32 FP16
- *             3 idx, 4 vals as above
- *   Sections start on 256-byte boundaries (the first at offset 256); each row
- *   of a 2-D section is zero-padded to a multiple of 16 bytes.  The byte
- *   layout inside a row is the one the pages print; the padding and section
- *   alignment let the kernels fetch tiles with the Tensor Memory Accelerator.
+ *   [48:104) the seven u64 fields of lbq_layout, in order, from area_offset
+ *            to idx_offset; [104:128) zero.
+ *   Rows are taken 4 at a time (a row block; rows past N are zero).  Row block
+ *   rb starts at area_offset + rb * row_block_bytes and holds `records` dense
+ *   records, one per block of 32 groups along K (groups past K/32 are zero),
+ *   then `outlier_records` outlier records.  Inside a record each part is
+ *   row-major over (row 0..3, group 0..31) and keeps the byte encoding the
+ *   pages print:
+ *     4-bit record (2368 B): qweight, 16 B per group, byte k = q_k | q_{k+16} << 4;
+ *                            FP16 scale per group (at 2048);
+ *                            zero points, byte = z_{2m} | z_{2m+1} << 4 (at 2304).
+ *     2-bit record (1536 B): codes, 8 B per group, byte = q0|q1<<2|q2<<4|q3<<6
+ *                            for four consecutive k; FP16 S (at 1024); FP16 Z (at 1280).
+ *     outlier record (2048 B): 256 FP16 values W[n, idx_j] per row.
+ *   The n_out int32 outlier indices start at idx_offset (a 256-byte boundary).
+ *   A row block is one contiguous byte range, so a kernel streams any run of its
+ *   records with a single bulk copy.
  */
 #ifndef LBQ_H
 #define LBQ_H
@@ -86,9 +89,14 @@ typedef enum { LBQ_F16 = 0, LBQ_F32 = 1 } lbq_dtype;
 typedef enum { LBQ_KIND_W4 = 0, LBQ_KIND_W2CB = 1 } lbq_kind;
 
 typedef struct {
-    uint64_t offset[5];       /* byte offset of each section from the blob start */
-    uint64_t row_stride[5];   /* bytes between rows (0 for the 1-D idx section) */
-    uint64_t total_bytes;     /* size of the whole blob */
+    uint64_t area_offset;           /* start of the row-block area (256) */
+    uint64_t row_block_bytes;       /* bytes per block of 4 rows */
+    uint64_t record_bytes;          /* bytes per dense record: 2368 (4-bit) or 1536 (2-bit) */
+    uint64_t records;               /* dense records per row block = ceil(K / 1024) */
+    uint64_t outlier_record_bytes;  /* 2048 when n_out > 0, else 0 */
+    uint64_t outlier_records;       /* outlier records per row block = ceil(n_out / 256) */
+    uint64_t idx_offset;            /* start of the n_out int32 outlier indices */
+    uint64_t total_bytes;           /* size of the whole blob */
 } lbq_layout;
 
 /* Library version (major * 10000 + minor * 100 + patch) and blob format version. */
@@ -100,8 +108,7 @@ const char* lbq_status_string(lbq_status s);
 
 /* ---------------------------------------------------------------- host side */
 
-/* Section offsets and strides of a blob of the given kind and shape (the layout
- * above).  Errors: LBQ_ERR_NULL (out), LBQ_ERR_SHAPE. */
+/* Sizes and offsets of a blob of the given kind and shape (the layout above).  Errors: LBQ_ERR_NULL (out), LBQ_ERR_SHAPE. */
 lbq_status lbq_blob_layout(lbq_kind kind, int64_t N, int64_t K, int32_t n_out, lbq_layout* out);
 
 /* Total blob bytes, or 0 when the shape is invalid. */

@@ -32,16 +32,27 @@ Readings where the pages are silent (each listed in the design notes):
 
 Blob format (version 1), all integers little-endian, written here from the
 layout description, independently of the C++ packer:
-  [0:8)   magic  b"LBQW4G32" (4-bit) or b"LBQW2C32" (2-bit codebook)
-  [8:12)  u32 version = 1        [12:16) u32 header bytes = 128
-  [16:24) i64 N                  [24:32) i64 K
-  [32:36) i32 n_out              [36:40) u32 group size = 32
-  [40:48) u64 total blob bytes
-  [48:128) five (u64 offset, u64 row stride) pairs for the sections
-     4-bit : qweight, scales, zeros, outlier idx, outlier vals
-     2-bit : codes,   S,      Z,     outlier idx, outlier vals
-  Every section starts on a 256-byte boundary (the first at 256); every row of
-  a 2-D section is padded with zero bytes to a multiple of 16 bytes.
+  [0:8)    magic b"LBQW4G32" (4-bit) or b"LBQW2C32" (2-bit codebook)
+  [8:12)   u32 version = 1           [12:16)  u32 header bytes = 128
+  [16:24)  i64 N                     [24:32)  i64 K
+  [32:36)  i32 n_out                 [36:40)  u32 group size = 32
+  [40:48)  u64 total blob bytes
+  [48:56)  u64 offset of the row-block area (256)
+  [56:64)  u64 bytes per row block
+  [64:72)  u64 bytes per dense record   [72:80)  u64 dense records per row block
+  [80:88)  u64 bytes per outlier record [88:96)  u64 outlier records per row block
+  [96:104) u64 offset of the outlier index array (n_out int32)
+  [104:128) zero
+Rows are taken 4 at a time (a row block; rows past N are zero).  A row block
+holds ceil(K/1024) dense records, one per block of 32 groups along K (groups
+past K/32 are zero), then ceil(n_out/256) outlier records.  Inside a record,
+each of the three parts is row-major over (row 0..3, group 0..31):
+  4-bit  record (2368 B): qweight 16 B per group (byte k = q_k | q_{k+16} << 4),
+         then FP16 scale per group, then zero points z_{2m} | z_{2m+1} << 4 per byte;
+  2-bit  record (1536 B): codes 8 B per group (byte = q0 | q1<<2 | q2<<4 | q3<<6),
+         then FP16 S per group, then FP16 Z per group;
+  outlier record (2048 B): 256 FP16 values of W[n, idx_j] per row.
+The idx array starts on a 256-byte boundary after the row-block area.
 """
 from __future__ import annotations
 
@@ -57,7 +68,6 @@ CODEBOOK_DECIMAL = (-1.52, -0.45, 0.45, 1.52)   # otf-llm section 2
 W2_OUTLIER_FRAC = 0.035   # otf-llm section 4 / quickstart "32 0.035"
 HEADER_BYTES = 128
 SECTION_ALIGN = 256
-ROW_ALIGN = 16
 MAGIC_W4 = b"LBQW4G32"
 MAGIC_W2 = b"LBQW2C32"
 VERSION = 1
@@ -101,69 +111,110 @@ def _up(x: int, a: int) -> int:
     return (x + a - 1) // a * a
 
 
-def layout(kind: str, N: int, K: int, n_out: int) -> dict:
-    """Offsets and row strides of the five sections (see module docstring)."""
+REC_GROUPS = 32          # groups per dense record (1024 k)
+ROWS_PER_BLOCK = 4
+OUT_COLS = 256           # outlier columns per outlier record
+
+
+def record_parts(kind: str) -> tuple:
+    """Bytes per row of the three parts of a dense record: packed, scale/S, zero/Z."""
     if kind == "w4":
-        rows = (K // 2, K // 32 * 2, K // 64)          # qweight, scales, zeros: bytes per row
-    elif kind == "w2":
-        rows = (K // 4, K // 32 * 2, K // 32 * 2)      # codes, S, Z
-    else:
-        raise ValueError(kind)
-    ld = [_up(r, ROW_ALIGN) for r in rows]
-    off = []
-    cur = SECTION_ALIGN
-    for l in ld:
-        off.append(cur)
-        cur = _up(cur + N * l, SECTION_ALIGN)
-    off_idx = cur
-    cur = _up(cur + 4 * n_out, SECTION_ALIGN)
-    ld_v = _up(2 * n_out, ROW_ALIGN)
-    off_vals = cur
-    total = _up(cur + N * ld_v, SECTION_ALIGN)
-    return {
-        "offsets": off + [off_idx, off_vals],
-        "strides": ld + [0, ld_v],
-        "total": total,
-    }
+        return 16 * REC_GROUPS, 2 * REC_GROUPS, REC_GROUPS // 2
+    if kind == "w2":
+        return 8 * REC_GROUPS, 2 * REC_GROUPS, 2 * REC_GROUPS
+    raise ValueError(kind)
 
 
-def _write_blob(kind: str, N: int, K: int, idx: np.ndarray, sec_rows: list, vals16: np.ndarray) -> np.ndarray:
+def layout(kind: str, N: int, K: int, n_out: int) -> dict:
+    """Sizes and offsets of a blob (see module docstring)."""
+    parts = record_parts(kind)
+    rec = ROWS_PER_BLOCK * sum(parts)
+    nrec = -(-K // (REC_GROUPS * G))
+    out_rec = ROWS_PER_BLOCK * OUT_COLS * 2 if n_out else 0
+    n_outrec = -(-n_out // OUT_COLS)
+    rb_bytes = nrec * rec + n_outrec * out_rec
+    n_rb = -(-N // ROWS_PER_BLOCK)
+    area = SECTION_ALIGN
+    idx_off = _up(area + n_rb * rb_bytes, SECTION_ALIGN)
+    total = _up(idx_off + 4 * n_out, SECTION_ALIGN)
+    return {"area": area, "rb_bytes": rb_bytes, "rec_bytes": rec, "recs": nrec, "out_rec_bytes": out_rec,
+            "out_recs": n_outrec, "idx": idx_off, "total": total, "n_rb": n_rb}
+
+
+def _pad2(a: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    out = np.zeros((rows, cols), dtype=a.dtype)
+    out[:a.shape[0], :a.shape[1]] = a
+    return out
+
+
+def _write_blob(kind: str, N: int, K: int, idx: np.ndarray, part_rows: list, vals16: np.ndarray) -> np.ndarray:
+    """part_rows: the three per-row byte arrays (N x bytes) in the pages' layout."""
     n_out = int(idx.size)
     L = layout(kind, N, K, n_out)
+    n_rb, nrec = L["n_rb"], L["recs"]
+    rows = n_rb * ROWS_PER_BLOCK
+    chunks = []
+    for data, per_row in zip(part_rows, record_parts(kind)):
+        b = np.ascontiguousarray(data).view(np.uint8).reshape(N, -1)
+        b = _pad2(b, rows, nrec * per_row)
+        # (row block, row, record, bytes) -> (row block, record, row, bytes)
+        chunks.append(b.reshape(n_rb, ROWS_PER_BLOCK, nrec, per_row).transpose(0, 2, 1, 3)
+                      .reshape(n_rb, nrec, ROWS_PER_BLOCK * per_row))
+    dense = np.concatenate(chunks, axis=2).reshape(n_rb, nrec * L["rec_bytes"])
+    pieces = [dense]
+    if n_out:
+        nor = L["out_recs"]
+        v = _pad2(np.ascontiguousarray(vals16.astype("<f2")).view(np.uint8).reshape(N, 2 * n_out),
+                  rows, nor * OUT_COLS * 2)
+        pieces.append(v.reshape(n_rb, ROWS_PER_BLOCK, nor, OUT_COLS * 2).transpose(0, 2, 1, 3)
+                      .reshape(n_rb, nor * L["out_rec_bytes"]))
+    area = np.concatenate(pieces, axis=1)
     blob = np.zeros(L["total"], dtype=np.uint8)
+    blob[L["area"]:L["area"] + area.size] = area.reshape(-1)
     hdr = bytearray(HEADER_BYTES)
     hdr[0:8] = MAGIC_W4 if kind == "w4" else MAGIC_W2
     struct.pack_into("<IIqqiIQ", hdr, 8, VERSION, HEADER_BYTES, N, K, n_out, G, L["total"])
-    for i in range(5):
-        struct.pack_into("<QQ", hdr, 48 + 16 * i, L["offsets"][i], L["strides"][i])
+    struct.pack_into("<7Q", hdr, 48, L["area"], L["rb_bytes"], L["rec_bytes"], L["recs"], L["out_rec_bytes"],
+                     L["out_recs"], L["idx"])
     blob[:HEADER_BYTES] = np.frombuffer(bytes(hdr), dtype=np.uint8)
-    for i, data in enumerate(sec_rows):
-        data = np.ascontiguousarray(data).view(np.uint8).reshape(N, -1)
-        o, ld = L["offsets"][i], L["strides"][i]
-        view = blob[o:o + N * ld].reshape(N, ld)
-        view[:, :data.shape[1]] = data
     if n_out:
-        o = L["offsets"][3]
-        blob[o:o + 4 * n_out] = np.ascontiguousarray(idx.astype("<i4")).view(np.uint8)
-        o, ld = L["offsets"][4], L["strides"][4]
-        view = blob[o:o + N * ld].reshape(N, ld)
-        view[:, :2 * n_out] = np.ascontiguousarray(vals16.astype("<f2")).view(np.uint8).reshape(N, 2 * n_out)
+        blob[L["idx"]:L["idx"] + 4 * n_out] = np.ascontiguousarray(idx.astype("<i4")).view(np.uint8)
     return blob
 
 
 def read_header(blob: np.ndarray) -> dict:
     b = bytes(blob[:HEADER_BYTES])
-    magic = b[0:8]
     version, hbytes, N, K, n_out, group, total = struct.unpack_from("<IIqqiIQ", b, 8)
-    secs = [struct.unpack_from("<QQ", b, 48 + 16 * i) for i in range(5)]
-    return {"magic": magic, "version": version, "header_bytes": hbytes, "N": N, "K": K,
-            "n_out": n_out, "group": group, "total": total,
-            "offsets": [s[0] for s in secs], "strides": [s[1] for s in secs]}
+    area, rb_bytes, rec, recs, out_rec, out_recs, idx = struct.unpack_from("<7Q", b, 48)
+    return {"magic": b[0:8], "version": version, "header_bytes": hbytes, "N": N, "K": K, "n_out": n_out,
+            "group": group, "total": total, "area": area, "rb_bytes": rb_bytes, "rec_bytes": rec, "recs": recs,
+            "out_rec_bytes": out_rec, "out_recs": out_recs, "idx": idx}
 
 
-def _section(blob: np.ndarray, hdr: dict, i: int, row_bytes: int) -> np.ndarray:
-    o, ld, N = hdr["offsets"][i], hdr["strides"][i], hdr["N"]
-    return blob[o:o + N * ld].reshape(N, ld)[:, :row_bytes]
+def _read_parts(blob: np.ndarray, kind: str):
+    """The three per-row byte arrays (N x bytes, pages' layout), idx and vals."""
+    h = read_header(blob)
+    N, n_out = h["N"], h["n_out"]
+    n_rb = -(-N // ROWS_PER_BLOCK)
+    area = blob[h["area"]:h["area"] + n_rb * h["rb_bytes"]].reshape(n_rb, h["rb_bytes"])
+    nrec = h["recs"]
+    dense = area[:, :nrec * h["rec_bytes"]].reshape(n_rb, nrec, h["rec_bytes"])
+    out, off = [], 0
+    for per_row in record_parts(kind):
+        w = ROWS_PER_BLOCK * per_row
+        p = dense[:, :, off:off + w].reshape(n_rb, nrec, ROWS_PER_BLOCK, per_row).transpose(0, 2, 1, 3)
+        out.append(np.ascontiguousarray(p.reshape(n_rb * ROWS_PER_BLOCK, nrec * per_row)[:N]))
+        off += w
+    if n_out:
+        nor = h["out_recs"]
+        v = area[:, nrec * h["rec_bytes"]:].reshape(n_rb, nor, ROWS_PER_BLOCK, OUT_COLS * 2).transpose(0, 2, 1, 3)
+        v = v.reshape(n_rb * ROWS_PER_BLOCK, nor * OUT_COLS * 2)[:N, :2 * n_out]
+        vals = np.ascontiguousarray(v).view("<f2").astype(F64)
+        idx = np.ascontiguousarray(blob[h["idx"]:h["idx"] + 4 * n_out]).view("<i4").astype(np.int32)
+    else:
+        vals = np.zeros((N, 0), F64)
+        idx = np.zeros(0, np.int32)
+    return h, out, idx, vals
 
 
 # ---------------------------------------------------------------------------
@@ -286,26 +337,15 @@ def pack_w4(W: np.ndarray, idx=None) -> np.ndarray:
 def unpack_w4(blob: np.ndarray):
     """Inverse of the layout: q (N,K) uint8, z (N,K/32) uint8, s16 (N,K/32) FP64,
     idx (n_out,) int32, vals (N,n_out) FP64."""
-    h = read_header(blob)
+    h, (qb, sb, zb), idx, vals = _read_parts(blob, "w4")
     assert h["magic"] == MAGIC_W4
-    N, K, n_out = h["N"], h["K"], h["n_out"]
-    qb = _section(blob, h, 0, K // 2).reshape(N, K // 32, 16)
+    N, K = h["N"], h["K"]
+    qb = qb[:, :K // 2].reshape(N, K // 32, 16)
     q = np.concatenate([qb & 0x0F, qb >> 4], axis=2).reshape(N, K)
-    s16 = np.ascontiguousarray(_section(blob, h, 1, K // 16)).view("<f2").astype(F64)
-    zb = _section(blob, h, 2, K // 64)
+    s16 = np.ascontiguousarray(sb[:, :K // 16]).view("<f2").astype(F64)
+    zb = zb[:, :K // 64]
     z = np.stack([zb & 0x0F, zb >> 4], axis=2).reshape(N, K // 32)
-    idx, vals = _unpack_outliers(blob, h)
     return q, z, s16, idx, vals
-
-
-def _unpack_outliers(blob, h):
-    N, n_out = h["N"], h["n_out"]
-    if n_out == 0:
-        return np.zeros(0, np.int32), np.zeros((N, 0), F64)
-    o = h["offsets"][3]
-    idx = np.ascontiguousarray(blob[o:o + 4 * n_out]).view("<i4").astype(np.int32)
-    vals = np.ascontiguousarray(_section(blob, h, 4, 2 * n_out)).view("<f2").astype(F64)
-    return idx, vals
 
 
 def dequant_w4(blob: np.ndarray, rows=None) -> np.ndarray:
@@ -375,14 +415,13 @@ def pack_w2cb(W: np.ndarray, idx=None) -> np.ndarray:
 
 
 def unpack_w2(blob: np.ndarray):
-    h = read_header(blob)
+    h, (cb, Sb, Zb), idx, vals = _read_parts(blob, "w2")
     assert h["magic"] == MAGIC_W2
     N, K = h["N"], h["K"]
-    cb = _section(blob, h, 0, K // 4)
+    cb = cb[:, :K // 4]
     q = np.stack([(cb >> (2 * j)) & 3 for j in range(4)], axis=2).reshape(N, K)
-    S16 = np.ascontiguousarray(_section(blob, h, 1, K // 16)).view("<f2").astype(F64)
-    Z16 = np.ascontiguousarray(_section(blob, h, 2, K // 16)).view("<f2").astype(F64)
-    idx, vals = _unpack_outliers(blob, h)
+    S16 = np.ascontiguousarray(Sb[:, :K // 16]).view("<f2").astype(F64)
+    Z16 = np.ascontiguousarray(Zb[:, :K // 16]).view("<f2").astype(F64)
     return q, S16, Z16, idx, vals
 
 
@@ -406,8 +445,9 @@ def dequant(blob: np.ndarray, rows=None) -> np.ndarray:
 
 
 def outliers(blob: np.ndarray):
-    h = read_header(blob)
-    return _unpack_outliers(blob, h)
+    kind = "w4" if bytes(blob[:8]) == MAGIC_W4 else "w2"
+    _, _, idx, vals = _read_parts(blob, kind)
+    return idx, vals
 
 
 def gemm(blob: np.ndarray, X: np.ndarray, rows=None) -> np.ndarray:

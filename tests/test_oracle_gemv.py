@@ -21,38 +21,44 @@ def _f16_value(bits: int) -> Fraction:
 
 
 def _decode(blob):
+    """Independent reading of the documented blob layout, element by element."""
     b = bytes(blob)
     magic = b[:8]
     N, K = struct.unpack_from("<qq", b, 16)
     n_out = struct.unpack_from("<i", b, 32)[0]
-    secs = [struct.unpack_from("<QQ", b, 48 + 16 * i) for i in range(5)]
+    area, rb_bytes, rec_bytes, recs, out_rec_bytes, out_recs, idx_off = struct.unpack_from("<7Q", b, 48)
     W = [[Fraction(0)] * K for _ in range(N)]
     for n in range(N):
+        rb, r = divmod(n, 4)
         for g in range(K // 32):
+            blk, gl = divmod(g, 32)
+            rec = area + rb * rb_bytes + blk * rec_bytes
             if magic == b"LBQW4G32":
-                so, sl = secs[1]
-                s = _f16_value(struct.unpack_from("<H", b, so + n * sl + 2 * g)[0])
-                zo, zl = secs[2]
-                zb = b[zo + n * zl + g // 2]
-                z = (zb >> 4) if g % 2 else (zb & 15)
-                qo, ql = secs[0]
+                s = _f16_value(struct.unpack_from("<H", b, rec + 2048 + (r * 32 + gl) * 2)[0])
+                zb = b[rec + 2304 + r * 16 + gl // 2]
+                z = (zb >> 4) if gl % 2 else (zb & 15)
                 for k in range(32):
-                    byte = b[qo + n * ql + g * 16 + (k % 16)]
+                    byte = b[rec + (r * 32 + gl) * 16 + (k % 16)]
                     q = (byte >> 4) if k >= 16 else (byte & 15)
                     W[n][g * 32 + k] = (q - z) * s
             else:
-                so, sl = secs[1]
-                S = _f16_value(struct.unpack_from("<H", b, so + n * sl + 2 * g)[0])
-                Z = _f16_value(struct.unpack_from("<H", b, secs[2][0] + n * secs[2][1] + 2 * g)[0])
+                S = _f16_value(struct.unpack_from("<H", b, rec + 1024 + (r * 32 + gl) * 2)[0])
+                Z = _f16_value(struct.unpack_from("<H", b, rec + 1280 + (r * 32 + gl) * 2)[0])
                 for k in range(32):
-                    kk = g * 32 + k
-                    byte = b[secs[0][0] + n * secs[0][1] + kk // 4]
-                    q = (byte >> (2 * (kk % 4))) & 3
+                    byte = b[rec + (r * 32 + gl) * 8 + k // 4]
+                    q = (byte >> (2 * (k % 4))) & 3
                     C = [-Fraction(389, 256), -Fraction(1843, 4096), Fraction(1843, 4096), Fraction(389, 256)][q]
-                    W[n][kk] = S * C + Z
-    idx = list(struct.unpack_from("<%di" % n_out, b, secs[3][0])) if n_out else []
-    vals = [[_f16_value(struct.unpack_from("<H", b, secs[4][0] + n * secs[4][1] + 2 * j)[0])
-             for j in range(n_out)] for n in range(N)]
+                    W[n][g * 32 + k] = S * C + Z
+    idx = list(struct.unpack_from("<%di" % n_out, b, idx_off)) if n_out else []
+    vals = []
+    for n in range(N):
+        rb, r = divmod(n, 4)
+        row = []
+        for j in range(n_out):
+            o, jj = divmod(j, 256)
+            off = area + rb * rb_bytes + recs * rec_bytes + o * out_rec_bytes + (r * 256 + jj) * 2
+            row.append(_f16_value(struct.unpack_from("<H", b, off)[0]))
+        vals.append(row)
     return W, idx, vals
 
 

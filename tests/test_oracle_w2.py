@@ -25,10 +25,10 @@ def test_worked_group(golden):
     assert q[0, :32].tolist() == codes0
     assert q[0, 32:].tolist() == [int(v) for v in g["codes_group1"]]
     blob = O.pack_w2cb(w)
-    h = O.read_header(blob)
-    assert blob[h["offsets"][0]:h["offsets"][0] + 16].tolist() == [int(v, 16) for v in g["code_bytes"]]
-    assert blob[h["offsets"][1]:h["offsets"][1] + 4].view("<u2").tolist() == [int(v, 16) for v in g["S_f16_bits"]]
-    assert blob[h["offsets"][2]:h["offsets"][2] + 4].view("<u2").tolist() == [int(v, 16) for v in g["Z_f16_bits"]]
+    rec = O.read_header(blob)["area"]            # row block 0, record 0, row 0
+    assert blob[rec:rec + 16].tolist() == [int(v, 16) for v in g["code_bytes"]]
+    assert blob[rec + 1024:rec + 1028].view("<u2").tolist() == [int(v, 16) for v in g["S_f16_bits"]]
+    assert blob[rec + 1280:rec + 1284].view("<u2").tolist() == [int(v, 16) for v in g["Z_f16_bits"]]
 
 
 def test_ols_matches_least_squares():

@@ -19,15 +19,14 @@ def test_worked_group_codes_and_bytes(golden):
     assert np.all(s == 1.0)
     blob = O.pack_w4(w)
     h = O.read_header(blob)
-    qb = blob[h["offsets"][0]:h["offsets"][0] + 32]
-    assert qb.tolist() == [int(v, 16) for v in g["qweight_bytes"]]
-    sb = blob[h["offsets"][1]:h["offsets"][1] + 4].view("<u2")
-    assert sb.tolist() == [int(v, 16) for v in g["scale_f16_bits"]]
-    zb = blob[h["offsets"][2]:h["offsets"][2] + 1]
-    assert zb.tolist() == [int(v, 16) for v in g["zero_bytes"]]
-    # padding bytes of the 16-byte row are zero
-    assert not blob[h["offsets"][1] + 4:h["offsets"][1] + 16].any()
-    assert not blob[h["offsets"][2] + 1:h["offsets"][2] + 16].any()
+    rec = h["area"]                               # row block 0, record 0, row 0
+    assert blob[rec:rec + 32].tolist() == [int(v, 16) for v in g["qweight_bytes"]]
+    assert blob[rec + 2048:rec + 2052].view("<u2").tolist() == [int(v, 16) for v in g["scale_f16_bits"]]
+    assert blob[rec + 2304:rec + 2305].tolist() == [int(v, 16) for v in g["zero_bytes"]]
+    # groups 2..31 of the record and rows 1..3 of the row block are zero padding
+    assert not blob[rec + 32:rec + 2048].any()
+    assert not blob[rec + 2052:rec + 2304].any()
+    assert not blob[rec + 2305:rec + 2368].any()
 
 
 def test_round_half_even_points():
@@ -114,20 +113,28 @@ def test_byte_budget_4_625_bits_per_weight():
     """SPECTRA section 7.2: Group-32 costs 4.625 bits per weight (4 + 16/32 + 4/32)."""
     N, K = 16, 4096
     L = O.layout("w4", N, K, 0)
-    payload = N * (L["strides"][0] + L["strides"][1] + L["strides"][2])
-    assert payload * 8 / (N * K) == 4.625
+    assert L["rb_bytes"] * L["n_rb"] * 8 / (N * K) == 4.625
+    assert O.layout("w2", N, K, 0)["rb_bytes"] * 4 * 8 / (N * K) == 3.0
+
+
+def _golden_layout(g, key):
+    return {k: int(v) for k, v in (item.split("=") for item in g[key])}
 
 
 def test_layout_golden(golden):
     g = golden("blob_layout_example.txt")
-    L = O.layout("w4", 3, 64, 2)
-    assert L["offsets"] == [int(v) for v in g["w4_N3_K64_nout2_offsets"]]
-    assert L["strides"] == [int(v) for v in g["w4_N3_K64_nout2_strides"]]
-    assert L["total"] == int(g["w4_N3_K64_nout2_total"][0])
-    L = O.layout("w2", 2, 128, 5)
-    assert L["offsets"] == [int(v) for v in g["w2_N2_K128_nout5_offsets"]]
-    assert L["strides"] == [int(v) for v in g["w2_N2_K128_nout5_strides"]]
-    assert L["total"] == int(g["w2_N2_K128_nout5_total"][0])
+    for key, kind, N, K, n in (("w4_N3_K64_nout2", "w4", 3, 64, 2), ("w4_N5_K2112_nout0", "w4", 5, 2112, 0),
+                               ("w2_N2_K128_nout5", "w2", 2, 128, 5)):
+        want = _golden_layout(g, key)
+        L = O.layout(kind, N, K, n)
+        assert {k: L[k] for k in want} == want, key
+        rng = np.random.default_rng(N)
+        W = rng.standard_normal((N, K)).astype(np.float32)
+        idx = np.arange(n, dtype=np.int32) * 3
+        blob = (O.pack_w4 if kind == "w4" else O.pack_w2cb)(W, idx)
+        h = O.read_header(blob)
+        assert len(blob) == want["total"] and {k: h[k] for k in want if k in h} == \
+            {k: want[k] for k in want if k in h}
 
 
 def test_outlier_columns_are_isolated():

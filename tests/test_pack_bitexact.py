@@ -34,18 +34,18 @@ def test_golden_groups_through_cpp(lbq, golden):
     g = golden("w4_worked_example.txt")
     w = np.array([float(v) for v in g["w_group0"] + g["w_group1"]], dtype=np.float32)[None, :]
     blob = lbq.pack_w4(w)
-    L = lbq.blob_layout(lbq.LBQ_KIND_W4, 1, 64, 0)
-    assert blob[L["offsets"][0]:L["offsets"][0] + 32].tolist() == [int(v, 16) for v in g["qweight_bytes"]]
-    assert blob[L["offsets"][2]] == int(g["zero_bytes"][0], 16)
+    rec = lbq.blob_layout(lbq.LBQ_KIND_W4, 1, 64, 0)["area"]
+    assert blob[rec:rec + 32].tolist() == [int(v, 16) for v in g["qweight_bytes"]]
+    assert blob[rec + 2304] == int(g["zero_bytes"][0], 16)
     g2 = golden("w2_worked_example.txt")
     w = np.empty((1, 64), np.float32)
     w[0, :32] = [O.C16[int(c)] / 16 + 0.125 for c in g2["codes_group0"]]
     w[0, 32:] = 0.25
     blob = lbq.pack_w2cb(w)
-    L = lbq.blob_layout(lbq.LBQ_KIND_W2CB, 1, 64, 0)
-    assert blob[L["offsets"][0]:L["offsets"][0] + 16].tolist() == [int(v, 16) for v in g2["code_bytes"]]
-    assert blob[L["offsets"][1]:L["offsets"][1] + 4].view("<u2").tolist() == [int(v, 16) for v in g2["S_f16_bits"]]
-    assert blob[L["offsets"][2]:L["offsets"][2] + 4].view("<u2").tolist() == [int(v, 16) for v in g2["Z_f16_bits"]]
+    rec = lbq.blob_layout(lbq.LBQ_KIND_W2CB, 1, 64, 0)["area"]
+    assert blob[rec:rec + 16].tolist() == [int(v, 16) for v in g2["code_bytes"]]
+    assert blob[rec + 1024:rec + 1028].view("<u2").tolist() == [int(v, 16) for v in g2["S_f16_bits"]]
+    assert blob[rec + 1280:rec + 1284].view("<u2").tolist() == [int(v, 16) for v in g2["Z_f16_bits"]]
 
 
 def test_layouts_match_oracle(lbq):
@@ -53,7 +53,7 @@ def test_layouts_match_oracle(lbq):
         for N, K, n in ((1, 64, 0), (3, 64, 2), (1000, 4160, 143), (7, 65536, 8192)):
             a = lbq.blob_layout(kind, N, K, n)
             b = O.layout(name, N, K, n)
-            assert a["offsets"] == b["offsets"] and a["strides"] == b["strides"] and a["total"] == b["total"]
+            assert a == {k: b[k] for k in a}
 
 
 def test_llama8b_qproj_rows_bitexact(lbq):
