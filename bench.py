@@ -11,10 +11,13 @@ decode configurations (see bit_weight_only_lbq_gb300/synth.py).  The packed
 weights of a step (291 MB) are held in 3 rotating replicas, so consecutive steps
 never find their weights in the 126 MB L2.
 
-The step is captured once per replica as a CUDA graph of the 16 launches
-chained with programmatic dependent launch, and timed with CUDA events around
-K replays.  The dominant kernel (4-bit GEMV on the gate/up/down shapes) is
-then timed launch by launch with CUDA events for the roofline figure.
+A step is three grouped launches, one per row of the path, each a fused sweep
+over its matrices (lbq_gemv_grouped): the 4-bit layer sweep, the 2-bit layer
+sweep and the small-M batch.  The step is captured once per replica as a CUDA
+graph (the three launches chained with programmatic dependent launch) and
+timed with CUDA events around K replays.  Each grouped launch is then timed on
+its own (rotating copies, >= 512 MB per pass) for the roofline figure, and each
+of the 16 matrices alone for the per-call table.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 For N > 1 run under torch.distributed.run: every rank runs an independent
@@ -43,10 +46,9 @@ REPLICAS = 3
 SMALL_M = 4
 SAMPLE_ROWS_MAX = 1024
 L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)
-# DRAM bytes per launch of the dominant kernel from the ncu capture in
-# profiles/w4_gemv_57344x4096.md (135.857664 MB read + 3.044864 MB written for 57344 rows,
-# scaled to the 14336-row gate/up launch); valid only for the kernel source it was taken on.
-TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "8460985e64cf94b3", "bytes_per_launch": (135857664 + 3044864) / 4}      # rows of each matrix kept on the host for the oracle's timed sample
+# DRAM bytes (read + write) per grouped launch from ncu captures of the same
+# launches (profiles/); valid only for the kernel source they were taken on.
+TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "none", "traffic": {}}
 METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
 W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
 W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
@@ -163,6 +165,35 @@ def reps_i(reps, i):
     return [reps[r][i] for r in range(len(reps))]
 
 
+GROUPS = (("w4_layer_sweep", "w4"), ("w2_layer_sweep", "w2"), ("w4_smallM_gate_down", "w4m"))
+
+
+def group_members(layer, kind):
+    return [i for i, e in enumerate(layer) if e["kind"] == kind]
+
+
+def group_args(lbq, layer, members, blobs, xs, ys):
+    """Problem tuples of a grouped launch; blobs/xs/ys indexed like layer."""
+    probs = []
+    for i in members:
+        e = layer[i]
+        probs.append((blobs[i], e["N"], e["K"], e["n_out"], xs[i], e["K"], ys[i], e["N"]))
+    return probs
+
+
+def launch_group(lbq, layer, kind, blobs, xs, ys, pdl):
+    members = group_members(layer, kind)
+    lk = lbq.LBQ_KIND_W2CB if kind == "w2" else lbq.LBQ_KIND_W4
+    M = layer[members[0]]["M"]
+    lbq.gemv_grouped(lk, group_args(lbq, layer, members, blobs, xs, ys), M=M, pdl=pdl)
+
+
+def group_launch_count(lbq, layer, kind, blobs, xs, ys):
+    members = group_members(layer, kind)
+    lk = lbq.LBQ_KIND_W2CB if kind == "w2" else lbq.LBQ_KIND_W4
+    return lbq.gemv_grouped_launches(lk, group_args(lbq, layer, members, blobs, xs, ys), M=layer[members[0]]["M"])
+
+
 def launch(lbq, e, blob, x, y, pdl):
     if e["kind"] == "w4":
         lbq.gemv_w4a16(blob, e["N"], e["K"], e["n_out"], x, y, pdl=pdl)
@@ -239,7 +270,8 @@ def run_reference(args, rank, world):
 
 def config_dict():
     return {"workload": "llama3_8b_layer_decode: 7 linears W4A16 G32 (cfg2) + 7 linears W2 Lloyd-Max G32 with "
-                        "top-3.5% FP16 outliers (cfg3) + W4 gate/down small-M M=4 (cfg4), one token",
+                        "top-3.5% FP16 outliers (cfg3) + W4 gate/down small-M M=4 (cfg4), one token; each row "
+                        "one fused sweep (grouped launch) over its matrices",
             "linears": [list(x) for x in synth.LLAMA3_8B_LINEARS], "small_m": SMALL_M,
             "l2": "inputs larger than L2: 3 rotating replicas of the 291 MB step",
             "parallelism": "replicas (one independent layer per GPU)"}
@@ -289,20 +321,23 @@ def main():
         reps.append([torch.from_numpy(e["blob"]).to(dev) for e in layer])
     xs = [torch.from_numpy(np.ascontiguousarray(e["x"])).to(dev) for e in layer]
     ys = [torch.empty((e["M"], e["N"]), dtype=torch.float16, device=dev) for e in layer]
+    launches_per_step = sum(group_launch_count(lbq, layer, kind, reps[0], xs, ys) for _, kind in GROUPS)
+
+    def step_launches(blobs):
+        for _, kind in GROUPS:
+            launch_group(lbq, layer, kind, blobs, xs, ys, pdl=True)
 
     stream = torch.cuda.Stream(device=dev)
     graphs = []
     with torch.cuda.stream(stream):
         for r in range(REPLICAS):                      # eager warm-up (sets kernel attributes)
-            for i, e in enumerate(layer):
-                launch(lbq, e, reps[r][i], xs[i], ys[i], pdl=True)
+            step_launches(reps[r])
         stream.synchronize()
         assert lbq.device_error(stream) == 0
         for r in range(REPLICAS):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for i, e in enumerate(layer):
-                    launch(lbq, e, reps[r][i], xs[i], ys[i], pdl=True)
+                step_launches(reps[r])
             graphs.append(g)
 
     clocks = ClockSampler(local_rank)
@@ -332,10 +367,9 @@ def main():
         dist.barrier()
     clk = clocks.summary(t_wall0, t_wall1)
 
-    # per-kernel timing: each kernel launched back to back over the rotating
-    # replicas inside a CUDA graph (chained with programmatic dependent launch,
-    # as in the step), CUDA events around every replay; also the dominant
-    # kernel (4-bit gate/up/down) chained on its own for the roofline figure
+    # timing of one launch kind on its own: back to back over rotating copies
+    # inside a CUDA graph (chained with programmatic dependent launch, as in
+    # the step), CUDA events around every replay, on the launching stream
     def time_graph(g, launches, replays):
         with torch.cuda.stream(stream):
             g.replay()
@@ -347,33 +381,39 @@ def main():
                 g.replay()
                 b_.record(stream)
             stream.synchronize()
-        per_launch = [a_.elapsed_time(b_) / launches for a_, b_ in evs]
-        return per_launch
+        return [a_.elapsed_time(b_) / launches for a_, b_ in evs]
 
-    # enough distinct copies of every blob that one pass over them streams >= 512 MB
-    # (4x the L2), so no launch finds its weights in L2
-    copies = []
-    for i, e in enumerate(layer):
-        n = max(REPLICAS, -(-L2_ROTATION_BYTES // len(e["blob"])))
-        copies.append(reps_i(reps, i) + [reps[0][i].clone() for _ in range(n - REPLICAS)])
+    # enough distinct copies of every blob that one pass over a group streams
+    # >= 512 MB (4x the L2), so no launch finds its weights in L2
+    ncopy = {}
+    for _, kind in GROUPS:
+        gb = sum(len(layer[i]["blob"]) for i in group_members(layer, kind))
+        ncopy[kind] = max(REPLICAS, -(-L2_ROTATION_BYTES // gb))
+    ncopy_max = max(ncopy.values())
+    copies = [reps[r] for r in range(REPLICAS)] + [[b.clone() for b in reps[0]] for _ in range(ncopy_max - REPLICAS)]
 
-    def graph_of(seq, pdl=True):
+    def capture(fn):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for (i, r) in seq:
-                launch(lbq, layer[i], copies[i][r], xs[i], ys[i], pdl=pdl)
+            fn()
         return g
 
     replays = max(5, min(50, args.steps // 400))
-    per = []
-    for i in range(len(layer)):
-        seq = [(i, r) for r in range(len(copies[i]))]
-        per.append(time_graph(graph_of(seq), len(seq), replays))
-    dominant = [i for i, e in enumerate(layer) if e["kind"] == "w4" and e["name"] in ("gate_proj", "up_proj", "down_proj")]
-    ndom = min(len(copies[i]) for i in dominant)
-    dom_seq = [(i, r) for r in range(ndom) for i in dominant]
-    dom_ms = time_graph(graph_of(dom_seq), len(dom_seq), replays)
-    dom_ms_serial = time_graph(graph_of(dom_seq, pdl=False), len(dom_seq), replays)
+    per_group = {}
+    for gname, kind in GROUPS:
+        n = ncopy[kind]
+        g = capture(lambda: [launch_group(lbq, layer, kind, copies[r], xs, ys, pdl=True) for r in range(n)])
+        per_group[kind] = time_graph(g, n, replays)
+        del g
+    # per call: each matrix alone, chained over its own rotating copies
+    per_call = []
+    for i, e in enumerate(layer):
+        n = max(REPLICAS, -(-L2_ROTATION_BYTES // len(e["blob"])))
+        extra = [reps[0][i].clone() for _ in range(max(0, n - ncopy_max))]
+        blobs = [copies[r % ncopy_max][i] for r in range(min(n, ncopy_max))] + extra
+        g = capture(lambda: [launch(lbq, e, b, xs[i], ys[i], pdl=True) for b in blobs])
+        per_call.append(time_graph(g, len(blobs), replays))
+        del g, extra
     clocks.stop()
     assert lbq.device_error(stream) == 0
 
@@ -398,44 +438,52 @@ def main():
     peak, peak_kind = load_peaks()
     ms_step = ms_total / args.steps
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
-    dom_bytes = sum(layer[i]["bytes"] for i in dominant) / len(dominant)
-    dom_avg_ms = statistics.mean(dom_ms)
-    achieved = dom_bytes / (dom_avg_ms * 1e-3) / 1e9
+    groups_detail = []
+    for gname, kind in GROUPS:
+        gbytes = sum(layer[i]["bytes"] for i in group_members(layer, kind))
+        us = statistics.mean(per_group[kind]) * 1e3
+        groups_detail.append({"launch": gname, "matrices": [layer[i]["name"] for i in group_members(layer, kind)],
+                              "bytes": gbytes, "us_per_launch": round(us, 3),
+                              "GB_s": round(gbytes / (us * 1e-6) / 1e9, 1),
+                              "frac_of_peak": round(gbytes / (us * 1e-6) / 1e9 / peak, 4)})
+    dom = max(groups_detail, key=lambda d: d["us_per_launch"])
+    achieved = dom["GB_s"]
     detail = []
     for i, e in enumerate(layer):
-        us = statistics.median(per[i]) * 1e3
+        us = statistics.median(per_call[i]) * 1e3
         gbs = e["bytes"] / (us * 1e-6) / 1e9
         detail.append({"kernel": e["kind"], "linear": e["name"], "N": e["N"], "K": e["K"], "n_out": e["n_out"],
                        "M": e["M"], "us_per_call": round(us, 3), "GB_s": round(gbs, 1),
                        "frac_of_peak": round(gbs / peak, 4)})
     w4_bytes = sum(e["bytes"] for e in layer if e["kind"] == "w4")
     w2_bytes = sum(e["bytes"] for e in layer if e["kind"] == "w2")
+    us_w4 = statistics.mean(per_group["w4"]) * 1e3
+    us_w2 = statistics.mean(per_group["w2"]) * 1e3
+    capture_ok = kernel_source_hash() == TRAFFIC_CAPTURE["kernel_sha256_prefix"]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp16 activations, fp32 accumulate (w4 / w2 weights)",
         "data": "synthetic (seeded; shapes and distributions of the decode configs)",
         "config": config_dict(),
-        "gpu_launches": len(layer) * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "step_bytes": step_bytes,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": (TRAFFIC_CAPTURE["bytes_per_launch"]
-                                 if kernel_source_hash() == TRAFFIC_CAPTURE["kernel_sha256_prefix"] else None),
-                     "kernel": "lbq_gemv_kernel<W4,MB=1> on gate/up/down: chained launches in a CUDA graph, "
-                               "CUDA events around each replay, average per launch",
-                     "serialized_launch_GB_s": round(dom_bytes / (statistics.mean(dom_ms_serial) * 1e-3) / 1e9, 1),
+                     "traffic": TRAFFIC_CAPTURE["traffic"].get(dom["launch"]) if capture_ok else None,
+                     "kernel": "lbq_gemv_kernel, grouped launch %s (%d B algorithmic per launch): launches back to "
+                               "back in a CUDA graph over rotating copies, CUDA events around each replay, "
+                               "average per launch" % (dom["launch"], dom["bytes"]),
                      "peak_source": peak_kind},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "detail": {"per_kernel": detail,
+        "detail": {"per_launch": groups_detail, "per_call": detail,
                    "implied_tokens_per_s": {
+                       "llama3_8b_w4_32_layers_from_layer_sweep": round(1.0 / (32 * us_w4 * 1e-6), 1),
+                       "llama3_8b_w2_32_layers_from_layer_sweep": round(1.0 / (32 * us_w2 * 1e-6), 1),
                        "llama3_8b_w4_32_layers_from_per_call": round(
-                           1.0 / (32 * sum(statistics.median(per[i]) for i, e in enumerate(layer)
-                                           if e["kind"] == "w4") * 1e-3), 1),
-                       "llama3_8b_w2_32_layers_from_per_call": round(
-                           1.0 / (32 * sum(statistics.median(per[i]) for i, e in enumerate(layer)
-                                           if e["kind"] == "w2") * 1e-3), 1)},
+                           1.0 / (32 * sum(statistics.median(per_call[i]) for i, e in enumerate(layer)
+                                           if e["kind"] == "w4") * 1e-3), 1)},
                    "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes},
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -451,6 +499,8 @@ def run_single(args):
     """One kernel configuration, launched steps times after warmup (for ncu captures)."""
     import torch
     from bit_weight_only_lbq_gb300 import lbq
+    if args.single.startswith("sweep:"):
+        return run_single_sweep(args, args.single.split(":")[1])
     kind, N, K, n_out, M = args.single.split(":")
     N, K, n_out, M = int(N), int(K), int(n_out), int(M)
     rng = np.random.default_rng(0)
@@ -478,6 +528,37 @@ def run_single(args):
     nbytes = algorithmic_bytes("w2" if kind == "w2" else "w4", N, K, n_out, M)
     assert lbq.device_error() == 0
     print(json.dumps({"single": args.single, "bytes": nbytes, "us_median": statistics.median(us),
+                      "GB_s": nbytes / (statistics.median(us) * 1e-6) / 1e9}), flush=True)
+    return 0
+
+
+def run_single_sweep(args, kind):
+    """One grouped launch of the step (w4, w2 or w4m), launched steps times after
+    warmup without graphs (for ncu captures of exactly that launch)."""
+    import torch
+    from bit_weight_only_lbq_gb300 import lbq
+    layer = make_workload(lbq, 0)
+    dev = torch.device("cuda", 0)
+    blobs = [torch.from_numpy(e["blob"]).to(dev) if e["kind"] == kind else None for e in layer]
+    xs = [torch.from_numpy(np.ascontiguousarray(e["x"])).to(dev) for e in layer]
+    ys = [torch.empty((e["M"], e["N"]), dtype=torch.float16, device=dev) for e in layer]
+    for _ in range(max(1, args.warmup)):
+        launch_group(lbq, layer, kind, blobs, xs, ys, pdl=False)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch_group(lbq, layer, kind, blobs, xs, ys, pdl=False)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in ts]
+    nbytes = sum(e["bytes"] for e in layer if e["kind"] == kind)
+    assert lbq.device_error() == 0
+    print(json.dumps({"single": args.single, "bytes": nbytes,
+                      "launches": group_launch_count(lbq, layer, kind, blobs, xs, ys),
+                      "us_median": statistics.median(us),
                       "GB_s": nbytes / (statistics.median(us) * 1e-6) / 1e9}), flush=True)
     return 0
 

@@ -10,26 +10,29 @@
 // accumulated into the same registers.
 //
 // GB300 design (the pages' kernels are Triton code for Ampere laptops):
+//  * one launch serves a group of independent problems (a layer's linears, or
+//    a list of them); their row blocks (4 output rows, all of K) form one
+//    sequence that a persistent grid of <= one CTA per SM cuts into
+//    contiguous, byte-balanced ranges;
 //  * the blob stores each (4-row block x 32-group block) as one contiguous
-//    record (packed codes, then scales/S, then zeros/Z), so a tile of GPL
-//    records is one contiguous range of HBM;
-//  * one persistent CTA per SM; each warp owns a private ring of shared-memory
-//    stages that its lane 0 refills with one bulk copy per tile
-//    (cp.async.bulk, the Tensor Memory Accelerator's 1-D mode) completing on
-//    an mbarrier, so each SM keeps tens of KB in flight with no per-thread
-//    address arithmetic;
-//  * a tile is 4 output rows x (32 * GPL) groups; a lane owns GPL groups and
-//    keeps their activations in registers for the tile's 4 rows; the CTA's
-//    tiles are cut into contiguous per-warp ranges (split-K inside the CTA
-//    when it owns few row blocks), partial rows are combined in warp order;
+//    record (packed codes, then scales/S, then zeros/Z); a CTA's items
+//    (records and outlier records) are cut into contiguous per-warp ranges
+//    (split-K inside the CTA when it owns few row blocks);
+//  * each warp owns a private ring of shared-memory stages that its lane 0
+//    refills with one bulk copy per item (cp.async.bulk, the Tensor Memory
+//    Accelerator's 1-D mode) completing on an mbarrier; the warp moves an item
+//    into registers and hands the stage back before computing on it, so every
+//    stage but the one just read stays in flight;
 //  * 4-bit: a nibble masked in place is an exact FP16 subnormal (q * 2^-24);
 //    a mixed-precision FMA (FP16 inputs, exact FP32 product) accumulates
 //    q * x in FP32, and the zero point enters once per group as z * sum(x);
 //  * 2-bit: a byte-permute (PRMT) table lookup turns 2-bit codes into FP16
 //    codebook values; S multiplies the codebook dot product, Z the group's
 //    activation sum;
-//  * outlier columns are streamed as extra 4 x 256 FP16 tiles of the same row
+//  * outlier columns are streamed as extra 4 x 256 FP16 items of the same row
 //    block and accumulated before the cross-lane reduction;
+//  * partial rows of row blocks shared by several warps are combined in warp
+//    order, so results do not depend on timing;
 //  * every wait is bounded (2 s of %globaltimer); a timeout records
 //    LBQ_ERR_TIMEOUT in a device error word and the warp drains its copies.
 
@@ -46,50 +49,55 @@ namespace {
 
 __device__ unsigned int g_lbq_error_word;
 
-constexpr int kTR = 4;                 // output rows per tile (row block)
-constexpr int kOutCols = 256;          // outlier columns per outlier tile
-constexpr int kOutTileBytes = kTR * kOutCols * 2;     // 2048
+constexpr int kTR = 4;                                 // output rows per row block
+constexpr int kOutCols = 256;                          // outlier columns per outlier record
+constexpr int kOutRecBytes = kTR * kOutCols * 2;       // 2048
 constexpr int kMaxStagesPerWarp = 8;
+constexpr int kMaxGroup = LBQ_MAX_GROUP;               // problems per launch
+constexpr int kMaxGrid = 192;                          // CTAs per launch (>= SMs of a GB300)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 enum Kind { kW4 = 0, kW2 = 1 };
 
-constexpr int round128(int b) { return (b + 127) / 128 * 128; }
-
-// Dense record (one row block x 32 groups, the blob's unit) and tile geometry:
-// a tile is GPL consecutive records of one row block; a lane owns one group of
-// each record.
-template <int KIND, int GPL>
-struct Geo {
+// Dense record geometry (one row block x 32 groups, the blob's unit); lane g
+// of a warp owns group g of each of the record's 4 rows.
+template <int KIND>
+struct Rec {
     static constexpr int kPacked = KIND == kW4 ? 16 : 8;               // packed bytes per (row, group)
     static constexpr int kOff1 = kTR * 32 * kPacked;                   // scales / S
     static constexpr int kOff2 = kOff1 + kTR * 32 * 2;                 // zeros / Z
-    static constexpr int kRec = kOff2 + (KIND == kW4 ? kTR * 16 : kTR * 32 * 2);   // 2368 / 1536
-    static constexpr int kDense = GPL * kRec;
-    static constexpr int kStage = round128(kDense > kOutTileBytes ? kDense : kOutTileBytes);
+    static constexpr int kBytes = kOff2 + (KIND == kW4 ? kTR * 16 : kTR * 32 * 2);   // 2368 / 1536
+    static constexpr int kStage = kBytes > kOutRecBytes ? kBytes : kOutRecBytes;    // multiple of 16
     static constexpr uint32_t kMagicLo = 0x5751424Cu;                            // "LBQW"
     static constexpr uint32_t kMagicHi = KIND == kW4 ? 0x32334734u : 0x32334332u;  // "4G32" / "2C32"
 };
 
-struct GemvArgs {
+// One problem of a launch (launch parameter space, read through the constant cache).
+struct ProbArg {
     const uint8_t* blob;
     const uint8_t* area;   // first row block
-    const __half* x;       // activation rows, leading dimension ldx (elements)
     const int32_t* idx;
+    const __half* x;       // activation rows, leading dimension ldx (elements)
     void* y;               // output rows, leading dimension ldy (elements)
-    long long N, K;
     long long ldx, ldy;
+    long long N, K;
     long long rb_bytes;    // bytes per row block
     int recs;              // dense records per row block
-    int mrows;             // activation rows in this launch (<= MB of the kernel)
-    int n_out;
-    int y_f32;
-    int n_rb;              // row blocks of kTR rows
-    int KT;                // dense tiles per row block (records / GPL, rounded up)
     int OT;                // outlier records per row block
+    int n_out;
+    int ub;                // index of its first row block in the launch's sequence
+};
+
+struct GroupArgs {
+    int count;             // problems
+    int nunits;            // row blocks of all problems
+    int mrows;             // activation rows in this launch (<= MB of the kernel)
+    int y_f32;
     int SPW;               // stages per warp
     int rb_cap;            // most row blocks any CTA owns
     uint32_t lut_lo, lut_hi;   // 2-bit codebook: low / high bytes of the FP16 centroids
+    int cta_ub[kMaxGrid + 1];  // CTA c owns row blocks [cta_ub[c], cta_ub[c + 1])
+    ProbArg p[kMaxGroup];
 };
 
 // ----------------------------------------------------------------- PTX helpers
@@ -158,6 +166,10 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+
+// Orders this thread's (and, through a preceding warp barrier, its warp's)
+// shared-memory reads before later async-proxy writes to the same stage.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -231,166 +243,154 @@ __device__ __forceinline__ uint4 permuted_chunk(const uint32_t (&n)[16], int j) 
 
 // uint4 index of chunk j of group g in one activation plane
 __device__ __forceinline__ int x_chunk_index(int g, int j) { return ((g >> 5) * 4 + j) * 32 + (g & 31); }
-// half index of element k (0..K) of one activation plane
-template <int KIND>
-__device__ __forceinline__ int x_half_index(int k) {
-    const int g = k >> 5, kk = k & 31;
-    int slot;
-    if (KIND == kW4) {
-        const int hi = kk >> 4, r = kk & 15;
-        slot = 8 * (r >> 2) + 2 * ((r & 1) + 2 * hi) + ((r >> 1) & 1);
-    } else {
-        const int v = kk >> 4, r = kk & 15;
-        slot = 16 * v + 4 * (r & 3) + 2 * (r >> 3) + ((r >> 2) & 1);
-    }
-    return x_chunk_index(g, slot >> 3) * 8 + (slot & 7);
+
+// ------------------------------------------------------ shared-memory plan
+//
+// [ring: NW * SPW stages][yacc][part][seg][mbarriers][staging of the CTA's problems]
+// Staging of one problem: MB permuted activation planes, MB planes of group
+// sums, the outlier-channel bitmask, MB rows of gathered outlier activations.
+
+struct FixedPlan {
+    int ring, yacc, part, seg, bars, stg, total;
+};
+
+__host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline FixedPlan fixed_plan(int NW, int stage, int SPW, int MB, int rb_cap) {
+    FixedPlan p;
+    int off = 0;
+    p.ring = off;
+    off += NW * SPW * stage;
+    p.yacc = off;
+    off += rb_cap * kTR * MB * 4;
+    p.part = off;
+    off += NW * 2 * kTR * MB * 4;
+    p.seg = off;
+    off += NW * 2 * 4;
+    off = round_up(off, 16);
+    p.bars = off;
+    off += NW * SPW * 8;
+    off = round_up(off, 128);
+    p.stg = off;
+    p.total = off + 128;   // slack for aligning the base to 128 bytes
+    return p;
 }
 
-// --------------------------------------------------------------- tile math
+__host__ __device__ inline int staging_bytes(int MB, int recs, int OT) {
+    const int ng = recs * 32;
+    return MB * ng * 64 + MB * ng * 4 + ng * 4 + MB * OT * kOutCols * 2;
+}
 
-// 4-bit dense tile.  A nibble masked in place is the FP16 subnormal q * 2^-24
-// (low nibble) or 16 q * 2^-24 (high nibble); the mixed-precision FMA turns it
-// into the exact FP32 product with x.  Per group: dot = lo + hi / 16 =
-// 2^-24 sum_k q_k x_k and w.x = s (sum_k q_k x_k - z X_g) = 2^24 s (dot - z X_g 2^-24);
+// ----------------------------------------------------------- item math
+// A dense item is one record; every lane holds its group of the 4 rows.
+
+// 4-bit record, one activation row.  A nibble masked in place is the FP16
+// subnormal q * 2^-24 (low nibble) or 16 q * 2^-24 (high nibble); the mixed FMA
+// turns it into the exact FP32 product with x.  Per group:
+// w.x = s (sum_k q_k x_k - z X_g) = 2^24 s (lo + hi / 16 - z X_g 2^-24);
 // the final 2^24 is applied once per output.
-template <int MB, int GPL>
-__device__ __forceinline__ void w4_dense_tile(const uint8_t* st, int nrec, const uint4* xq, int xq_plane,
-                                              const float* xs24, int xs_plane, int mrows, int lane,
-                                              float (&acc)[MB][kTR]) {
-    using G = Geo<kW4, GPL>;
+__device__ __forceinline__ void w4_record_m1(const uint4 (&q)[kTR], const float (&s)[kTR], const float (&zf)[kTR],
+                                             const uint4* xq, float xsz, float (&acc)[kTR]) {
+    const uint4 xr[4] = {xq[0], xq[32], xq[64], xq[96]};
 #pragma unroll
-    for (int h = 0; h < GPL; ++h) {
-        if (h >= nrec) break;                          // short last tile
-        const uint8_t* rec = st + h * G::kRec;
-        const uint4* qw = reinterpret_cast<const uint4*>(rec);
-        const __half* sc = reinterpret_cast<const __half*>(rec + G::kOff1);
-        const uint8_t* zp = rec + G::kOff2;
-        const int gl = lane;                           // group within the record
-        if constexpr (MB == 1) {
-            const uint4 xr[4] = {xq[h * 128], xq[h * 128 + 32], xq[h * 128 + 64], xq[h * 128 + 96]};
-            const float xsz = xs24[h * 32];
+    for (int r = 0; r < kTR; ++r) {
+        float lo = 0.f, hi = 0.f;
 #pragma unroll
-            for (int r = 0; r < kTR; ++r) {
-                const uint4 q = qw[r * 32 + gl];
-                const float s = __half2float(sc[r * 32 + gl]);
-                const uint32_t zb = zp[r * 16 + (gl >> 1)];
-                const float zf = static_cast<float>((zb >> ((lane & 1) * 4)) & 15u);
-                float l0 = 0.f, l1 = 0.f, h0 = 0.f, h1 = 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t w = u4w(q, j), w8 = w >> 8;
-                    l0 = fma2_mixed(w & 0x000F000Fu, xr[j].x, l0);
-                    l1 = fma2_mixed(w8 & 0x000F000Fu, xr[j].y, l1);
-                    h0 = fma2_mixed(w & 0x00F000F0u, xr[j].z, h0);
-                    h1 = fma2_mixed(w8 & 0x00F000F0u, xr[j].w, h1);
-                }
-                const float t = fmaf(-zf, xsz, fmaf(h0 + h1, 0.0625f, l0 + l1));
-                acc[0][r] = fmaf(s, t, acc[0][r]);
-            }
-        } else {
-            uint32_t u[kTR][16];
-            float s[kTR], zf[kTR];
-#pragma unroll
-            for (int r = 0; r < kTR; ++r) {
-                const uint4 q = qw[r * 32 + gl];
-                s[r] = __half2float(sc[r * 32 + gl]);
-                const uint32_t zb = zp[r * 16 + (gl >> 1)];
-                zf[r] = static_cast<float>((zb >> ((lane & 1) * 4)) & 15u);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t w = u4w(q, j), w8 = w >> 8;
-                    u[r][4 * j + 0] = w & 0x000F000Fu;
-                    u[r][4 * j + 1] = w8 & 0x000F000Fu;
-                    u[r][4 * j + 2] = w & 0x00F000F0u;
-                    u[r][4 * j + 3] = w8 & 0x00F000F0u;
-                }
-            }
-#pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                if (m < mrows) {
-                    const uint4* xp = xq + m * xq_plane + h * 128;
-                    const uint4 xr[4] = {xp[0], xp[32], xp[64], xp[96]};
-                    const float xsz = xs24[m * xs_plane + h * 32];
-#pragma unroll
-                    for (int r = 0; r < kTR; ++r) {
-                        float l0 = 0.f, l1 = 0.f, h0 = 0.f, h1 = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            l0 = fma2_mixed(u[r][4 * j + 0], xr[j].x, l0);
-                            l1 = fma2_mixed(u[r][4 * j + 1], xr[j].y, l1);
-                            h0 = fma2_mixed(u[r][4 * j + 2], xr[j].z, h0);
-                            h1 = fma2_mixed(u[r][4 * j + 3], xr[j].w, h1);
-                        }
-                        const float t = fmaf(-zf[r], xsz, fmaf(h0 + h1, 0.0625f, l0 + l1));
-                        acc[m][r] = fmaf(s[r], t, acc[m][r]);
-                    }
-                }
-            }
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t w = u4w(q[r], j), w8 = w >> 8;
+            lo = fma2_mixed(w & 0x000F000Fu, xr[j].x, lo);
+            hi = fma2_mixed(w & 0x00F000F0u, xr[j].z, hi);
+            lo = fma2_mixed(w8 & 0x000F000Fu, xr[j].y, lo);
+            hi = fma2_mixed(w8 & 0x00F000F0u, xr[j].w, hi);
         }
+        const float t = fmaf(-zf[r], xsz, fmaf(hi, 0.0625f, lo));
+        acc[r] = fmaf(s[r], t, acc[r]);
     }
 }
 
-// 2-bit dense tile: four codes -> PRMT selector (c, c+4 per code) -> two FP16
-// codebook pairs; w.x = S sum_k C[q_k] x_k + Z X_g.
-template <int GPL>
-__device__ __forceinline__ void w2_dense_tile(const uint8_t* st, int nrec, const uint4* xq, const float* xsum,
-                                              int lane, uint32_t lut_lo, uint32_t lut_hi, float (&acc)[kTR]) {
-    using G = Geo<kW2, GPL>;
-#pragma unroll
-    for (int h = 0; h < GPL; ++h) {
-        if (h >= nrec) break;                          // short last tile
-        const uint8_t* rec = st + h * G::kRec;
-        const uint2* cw = reinterpret_cast<const uint2*>(rec);
-        const __half* Sg = reinterpret_cast<const __half*>(rec + G::kOff1);
-        const __half* Zg = reinterpret_cast<const __half*>(rec + G::kOff2);
-        const int gl = lane;
-        const uint4 xr[4] = {xq[h * 128], xq[h * 128 + 32], xq[h * 128 + 64], xq[h * 128 + 96]};
-        const float xs = xsum[h * 32];
-#pragma unroll
-        for (int r = 0; r < kTR; ++r) {
-            const uint2 c = cw[r * 32 + gl];
-            const float S = __half2float(Sg[r * 32 + gl]);
-            const float Z = __half2float(Zg[r * 32 + gl]);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-                const uint32_t w = v ? c.y : c.x;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const uint32_t t = (w >> (2 * s)) & 0x03030303u;
-                    const uint32_t sel = t * 0x11u + 0x40404040u;     // nibbles (c, c + 4) per code
-                    const uint32_t h01 = prmt(lut_lo, lut_hi, sel);
-                    const uint32_t h23 = prmt(lut_lo, lut_hi, sel >> 16);
-                    const int mw = (v * 4 + s) * 2;                    // word of the group's 64 x bytes
-                    d[s & 1] = fma2_mixed(h01, u4w(xr[mw >> 2], mw & 3), d[s & 1]);
-                    d[2 + (s & 1)] = fma2_mixed(h23, u4w(xr[(mw + 1) >> 2], (mw + 1) & 3), d[2 + (s & 1)]);
-                }
-            }
-            acc[r] = fmaf(S, (d[0] + d[1]) + (d[2] + d[3]), fmaf(Z, xs, acc[r]));
-        }
-    }
-}
-
-// One outlier tile: lane owns outlier columns [ot*256 + lane*8, +8) of the 4
-// rows; xo_tile + m * xo_plane holds x[idx] of activation row m.  `scale`
-// converts to the unit of the dense accumulator (2^-24 for 4-bit, 1 for 2-bit).
+// 4-bit record, MB activation rows: the unpacked words are shared by the rows.
 template <int MB>
-__device__ __forceinline__ void outlier_tile(const uint8_t* st, const __half* xo_tile, int xo_plane, int mrows,
-                                             int lane, float scale, float (&acc)[MB][kTR]) {
-    uint4 v[kTR];
+__device__ __forceinline__ void w4_record_mb(const uint4 (&q)[kTR], const float (&s)[kTR], const float (&zf)[kTR],
+                                             const uint4* xq, int xq_plane, const float* xs24, int xs_plane,
+                                             int mrows, float (&acc)[MB][kTR]) {
+    uint32_t u[kTR][16];
 #pragma unroll
-    for (int r = 0; r < kTR; ++r) v[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+    for (int r = 0; r < kTR; ++r)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t w = u4w(q[r], j), w8 = w >> 8;
+            u[r][4 * j + 0] = w & 0x000F000Fu;
+            u[r][4 * j + 1] = w8 & 0x000F000Fu;
+            u[r][4 * j + 2] = w & 0x00F000F0u;
+            u[r][4 * j + 3] = w8 & 0x00F000F0u;
+        }
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
         if (m < mrows) {
-            const uint4 xv = reinterpret_cast<const uint4*>(xo_tile + m * xo_plane)[lane];
+            const uint4* xp = xq + m * xq_plane;
+            const uint4 xr[4] = {xp[0], xp[32], xp[64], xp[96]};
+            const float xsz = xs24[m * xs_plane];
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) {
+                float lo = 0.f, hi = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    lo = fma2_mixed(u[r][4 * j + 0], xr[j].x, lo);
+                    hi = fma2_mixed(u[r][4 * j + 2], xr[j].z, hi);
+                    lo = fma2_mixed(u[r][4 * j + 1], xr[j].y, lo);
+                    hi = fma2_mixed(u[r][4 * j + 3], xr[j].w, hi);
+                }
+                const float t = fmaf(-zf[r], xsz, fmaf(hi, 0.0625f, lo));
+                acc[m][r] = fmaf(s[r], t, acc[m][r]);
+            }
+        }
+    }
+}
+
+// 2-bit record: four codes -> PRMT selector (c, c+4 per code) -> two FP16
+// codebook pairs; w.x = S sum_k C[q_k] x_k + Z X_g.
+__device__ __forceinline__ void w2_record(const uint2 (&c)[kTR], const float (&S)[kTR], const float (&Z)[kTR],
+                                          const uint4* xq, float xs, uint32_t lut_lo, uint32_t lut_hi,
+                                          float (&acc)[kTR]) {
+    const uint4 xr[4] = {xq[0], xq[32], xq[64], xq[96]};
+#pragma unroll
+    for (int r = 0; r < kTR; ++r) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            const uint32_t w = v ? c[r].y : c[r].x;
+#pragma unroll
+            for (int sh = 0; sh < 4; ++sh) {
+                const uint32_t t = (w >> (2 * sh)) & 0x03030303u;
+                const uint32_t sel = t * 0x11u + 0x40404040u;     // nibbles (c, c + 4) per code
+                const uint32_t h01 = prmt(lut_lo, lut_hi, sel);
+                const uint32_t h23 = prmt(lut_lo, lut_hi, sel >> 16);
+                const int mw = (v * 4 + sh) * 2;                   // word of the group's 64 x bytes
+                d[sh & 1] = fma2_mixed(h01, u4w(xr[mw >> 2], mw & 3), d[sh & 1]);
+                d[2 + (sh & 1)] = fma2_mixed(h23, u4w(xr[(mw + 1) >> 2], (mw + 1) & 3), d[2 + (sh & 1)]);
+            }
+        }
+        acc[r] = fmaf(S[r], (d[0] + d[1]) + (d[2] + d[3]), fmaf(Z[r], xs, acc[r]));
+    }
+}
+
+// One outlier record: lane owns outlier columns [lane*8, +8) of the record's 256
+// for the 4 rows; xo + m * xo_plane holds x[idx] of activation row m.  `unit`
+// converts to the unit of the dense accumulator (2^-24 for 4-bit, 1 for 2-bit).
+template <int MB>
+__device__ __forceinline__ void outlier_record(const uint4 (&v)[kTR], const __half* xo, int xo_plane, int mrows,
+                                               int lane, float unit, float (&acc)[MB][kTR]) {
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+        if (m < mrows) {
+            const uint4 xv = reinterpret_cast<const uint4*>(xo + m * xo_plane)[lane];
 #pragma unroll
             for (int r = 0; r < kTR; ++r) {
                 float a0 = fma2_mixed(v[r].x, xv.x, 0.f);
                 float a1 = fma2_mixed(v[r].y, xv.y, 0.f);
                 a0 = fma2_mixed(v[r].z, xv.z, a0);
                 a1 = fma2_mixed(v[r].w, xv.w, a1);
-                acc[m][r] = fmaf(a0 + a1, scale, acc[m][r]);
+                acc[m][r] = fmaf(a0 + a1, unit, acc[m][r]);
             }
         }
     }
@@ -417,99 +417,88 @@ __device__ __forceinline__ float reduce_rows4(const float (&acc)[4], int lane) {
 
 // ------------------------------------------------------------------ kernel
 
-struct SmemPlan {
-    int ring, xs, xsum, xo, omask, yacc, part, seg, bars, total;
-};
+__device__ __forceinline__ int unit_end(const GroupArgs& a, int q) { return q + 1 < a.count ? a.p[q + 1].ub : a.nunits; }
 
-// NW warps, rb_cap: most row blocks a CTA owns; MB: activation planes.
-__host__ __device__ inline SmemPlan smem_plan(int NW, int stage, int KTg, int OT, int SPW, int MB, int rb_cap) {
-    // KTg: 32-group blocks covered by the dense tiles (KT * GPL)
-    SmemPlan p;
-    int off = 0;
-    p.ring = off;
-    off += NW * SPW * stage;
-    p.xs = off;
-    off += MB * KTg * 32 * 64;
-    p.xsum = off;
-    off += MB * KTg * 32 * 4;
-    p.xo = off;
-    off += MB * OT * kOutCols * 2;
-    p.omask = off;
-    off += KTg * 32 * 4;                   // one bit per k: outlier channel
-    p.yacc = off;
-    off += rb_cap * kTR * MB * 4;
-    p.part = off;
-    off += NW * 2 * kTR * MB * 4;
-    p.seg = off;
-    off += NW * 2 * 4;                     // per warp: first and last row block it touched
-    off = (off + 7) / 8 * 8;
-    p.bars = off;
-    off += NW * SPW * 8;
-    p.total = off + 128;   // slack for aligning the base to 128 bytes
-    return p;
-}
-
-template <int KIND, int MB, int NW, int GPL>
-__global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_constant__ GemvArgs a) {
-    using G = Geo<KIND, GPL>;
+template <int KIND, int MB, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_constant__ GroupArgs a) {
+    using RC = Rec<KIND>;
     constexpr int kThreads = NW * 32;
     constexpr float kUnit = KIND == kW4 ? 5.9604644775390625e-8f : 1.f;   // 2^-24 for the 4-bit products
     extern __shared__ __align__(128) uint8_t smem_raw[];
     // align by offsetting the shared array itself, so the compiler keeps the
     // shared address space (LDS with immediate offsets, no generic addressing)
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    const int KTg = a.KT * GPL;
-    const SmemPlan P = smem_plan(NW, G::kStage, KTg, a.OT, a.SPW, MB, a.rb_cap);
-    uint8_t* ring = smem + P.ring;
-    uint4* xs = reinterpret_cast<uint4*>(smem + P.xs);
-    float* xsum = reinterpret_cast<float*>(smem + P.xsum);
-    __half* xo = reinterpret_cast<__half*>(smem + P.xo);
-    uint32_t* omask = reinterpret_cast<uint32_t*>(smem + P.omask);
+    const int SPW = a.SPW;
+    const FixedPlan P = fixed_plan(NW, RC::kStage, SPW, MB, a.rb_cap);
     float* yacc = reinterpret_cast<float*>(smem + P.yacc);
     float* part = reinterpret_cast<float*>(smem + P.part);
     int* seg = reinterpret_cast<int*>(smem + P.seg);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + P.bars);
+    uint8_t* stg = smem + P.stg;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int SPW = a.SPW;
-    const int TPR = a.KT + a.OT;                    // tiles per row block
-    const int ngroups = KTg * 32;                   // groups per (padded) activation plane
-    const int xq_plane = ngroups * 4;               // uint4 chunks per plane
-    const int xo_plane = a.OT * kOutCols;
     const int mrows = a.mrows;
-    const int rb_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * a.n_rb) / gridDim.x);
-    const int rb_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * a.n_rb) / gridDim.x);
-    const int R = rb_end - rb_begin;
-    const int n_tiles = R * TPR;                    // this CTA's tiles, row block major
-    // each warp takes a contiguous share of the CTA's tiles (split-K when row blocks are few)
-    const int w_begin = (warp * n_tiles) / NW;
-    const int w_end = ((warp + 1) * n_tiles) / NW;
-    const int my_tiles = w_end - w_begin;
-    uint64_t* my_bars = bars + warp * SPW;
-    uint8_t* my_ring = ring + warp * SPW * G::kStage;
-    const uint64_t policy = policy_evict_first();
+    const int u0 = a.cta_ub[blockIdx.x], u1 = a.cta_ub[blockIdx.x + 1];
+    const int R = u1 - u0;
 
-    // issue pointer (lane 0 only): next tile's row block and k tile
-    int i_rb = w_begin / TPR, i_kk = w_begin - (w_begin / TPR) * TPR, i_slot = 0;
-    auto issue_next = [&]() {
-        uint8_t* dst = my_ring + i_slot * G::kStage;
-        uint64_t* bar = my_bars + i_slot;
-        const uint8_t* rb_src = a.area + static_cast<long long>(rb_begin + i_rb) * a.rb_bytes;
-        if (i_kk < a.KT) {
-            const int r0 = i_kk * GPL;
-            const int nrec = a.recs - r0 < GPL ? a.recs - r0 : GPL;
-            const uint32_t bytes = static_cast<uint32_t>(nrec * G::kRec);
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_load(dst, rb_src + static_cast<long long>(r0) * G::kRec, bytes, bar, policy);
-        } else {
-            mbar_arrive_expect_tx(bar, kOutTileBytes);
-            bulk_load(dst, rb_src + static_cast<long long>(a.recs) * G::kRec +
-                               static_cast<long long>(i_kk - a.KT) * kOutTileBytes,
-                      kOutTileBytes, bar, policy);
+    // problems this CTA touches: qf .. qf + np - 1; its items (records and
+    // outlier records of its row blocks, in memory order)
+    int qf = 0;
+    while (qf + 1 < a.count && a.p[qf + 1].ub <= u0) ++qf;
+    int np = 0, n_items = 0;
+    if (R > 0)
+        for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) {
+            const int lo = max(u0, a.p[q].ub), hi = min(u1, unit_end(a, q));
+            n_items += (hi - lo) * (a.p[q].recs + a.p[q].OT);
+            ++np;
         }
-        if (++i_kk == TPR) {
+    // this warp's contiguous share of the items, and where it starts
+    const int ib = static_cast<int>((static_cast<long long>(warp) * n_items) / NW);
+    const int ie = static_cast<int>((static_cast<long long>(warp + 1) * n_items) / NW);
+    const int my_items = ie - ib;
+    int s_q = qf, s_stg = 0, s_u = u0, s_kk = 0;
+    if (my_items > 0) {
+        int before = 0;
+        for (;;) {
+            const int lo = max(u0, a.p[s_q].ub), hi = min(u1, unit_end(a, s_q));
+            const int TPR = a.p[s_q].recs + a.p[s_q].OT;
+            const int items = (hi - lo) * TPR;
+            if (ib < before + items) {
+                const int j = ib - before;
+                s_u = lo + j / TPR;
+                s_kk = j - (j / TPR) * TPR;
+                break;
+            }
+            before += items;
+            s_stg += staging_bytes(MB, a.p[s_q].recs, a.p[s_q].OT);
+            ++s_q;
+        }
+    }
+    uint64_t* my_bars = reinterpret_cast<uint64_t*>(smem + P.bars) + warp * SPW;
+    uint8_t* my_ring = smem + P.ring + warp * SPW * RC::kStage;
+
+    // issue pointer (lane 0 only): problem, row block, item, source address, slot
+    int i_q = s_q, i_u = s_u, i_kk = s_kk, i_slot = 0;
+    int i_recs = a.p[s_q].recs, i_TPR = i_recs + a.p[s_q].OT, i_uend = min(u1, unit_end(a, s_q));
+    const uint8_t* i_src = a.p[s_q].area + static_cast<long long>(s_u - a.p[s_q].ub) * a.p[s_q].rb_bytes +
+                           (s_kk < i_recs ? static_cast<long long>(s_kk) * RC::kBytes
+                                          : static_cast<long long>(i_recs) * RC::kBytes +
+                                                static_cast<long long>(s_kk - i_recs) * kOutRecBytes);
+    const uint64_t policy = policy_evict_first();
+    auto issue_next = [&]() {
+        const uint32_t bytes = i_kk < i_recs ? static_cast<uint32_t>(RC::kBytes) : static_cast<uint32_t>(kOutRecBytes);
+        uint64_t* bar = my_bars + i_slot;
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(my_ring + i_slot * RC::kStage, i_src, bytes, bar, policy);
+        i_src += bytes;   // the row blocks of a problem are contiguous
+        if (++i_kk == i_TPR) {
             i_kk = 0;
-            ++i_rb;
+            if (++i_u == i_uend && ++i_q < a.count) {
+                // next problem, entered at its first row block
+                i_recs = a.p[i_q].recs;
+                i_TPR = i_recs + a.p[i_q].OT;
+                i_uend = min(u1, unit_end(a, i_q));
+                i_src = a.p[i_q].area;
+            }
         }
         if (++i_slot == SPW) i_slot = 0;
     };
@@ -518,105 +507,143 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     if (lane == 0) {
         for (int s = 0; s < SPW; ++s) mbar_init(my_bars + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        const int pre = my_tiles < SPW ? my_tiles : SPW;
+        const int pre = my_items < SPW ? my_items : SPW;
         for (int t = 0; t < pre; ++t) issue_next();
     }
-    // blob header: loaded now (three 16-byte loads in flight), compared after the main loop,
-    // so the check never delays this CTA's prologue
+    // blob header of problem blockIdx.x: loaded now, compared after the main
+    // loop, so the check never delays this CTA's prologue
     uint4 hdr0 = make_uint4(0u, 0u, 0u, 0u), hdr1 = hdr0, hdr2 = hdr0;
-    if (blockIdx.x == 0 && tid == 0) {
-        const uint4* h = reinterpret_cast<const uint4*>(a.blob);
+    const bool check_hdr = static_cast<int>(blockIdx.x) < a.count && tid == 0;
+    if (check_hdr) {
+        const uint4* h = reinterpret_cast<const uint4*>(a.p[blockIdx.x].blob);
         hdr0 = h[0];
         hdr1 = h[1];
         hdr2 = h[2];
     }
-    // outlier-channel bitmask and the row accumulators (no dependence on the previous grid)
-    for (int i = tid; i < ngroups; i += kThreads) omask[i] = 0u;
+    // outlier-channel bitmasks and the row accumulators (no dependence on the previous grid)
+    bool any_out = false;
+    {
+        int off = 0;
+        for (int j = 0, q = qf; j < np; ++j, ++q) {
+            const int ng = a.p[q].recs * 32;
+            if (a.p[q].n_out > 0) {
+                any_out = true;
+                uint32_t* om = reinterpret_cast<uint32_t*>(stg + off + MB * ng * 68);
+                for (int i = tid; i < ng; i += kThreads) om[i] = 0u;
+            }
+            off += staging_bytes(MB, a.p[q].recs, a.p[q].OT);
+        }
+    }
     for (int i = tid; i < R * kTR * MB; i += kThreads) yacc[i] = 0.f;
     pdl_trigger();
-    if (a.n_out > 0) {
+    if (any_out) {
         __syncthreads();
-        for (int j = tid; j < a.n_out; j += kThreads) {
-            const int k = a.idx[j];
-            if (k >= 0 && k < a.K)
-                atomicOr(&omask[k >> 5], 1u << (k & 31));
-            else
-                record_error(LBQ_ERR_OUTLIER_IDX);   // corrupted blob: never index outside x
+        int off = 0;
+        for (int j = 0, q = qf; j < np; ++j, ++q) {
+            const int ng = a.p[q].recs * 32;
+            uint32_t* om = reinterpret_cast<uint32_t*>(stg + off + MB * ng * 68);
+            const int n_out = a.p[q].n_out;
+            const int32_t* idx = a.p[q].idx;
+            const long long K = a.p[q].K;
+            for (int i = tid; i < n_out; i += kThreads) {
+                const int k = idx[i];
+                if (k >= 0 && k < K)
+                    atomicOr(&om[k >> 5], 1u << (k & 31));
+                else
+                    record_error(LBQ_ERR_OUTLIER_IDX);   // corrupted blob: never index outside x
+            }
+            off += staging_bytes(MB, a.p[q].recs, a.p[q].OT);
         }
     }
     __syncthreads();
     pdl_wait();
 
-    // stage x: a thread takes whole groups (four 16-byte loads), zeroes outlier
-    // channels, writes the permuted chunks and the group sum X~_g (times kUnit)
-    for (int base = tid; base < MB * ngroups; base += kThreads * 2) {
-        uint4 raw[2][4];
+    // stage x of every problem: a thread takes whole groups (four 16-byte loads),
+    // zeroes outlier channels, writes the permuted chunks and the group sum X~_g
+    // (times kUnit); then x[idx] (the unmasked values) for the outlier records
+    {
+        int off = 0;
+        for (int j = 0, q = qf; j < np; ++j, ++q) {
+            const ProbArg& pa = a.p[q];
+            const int ng = pa.recs * 32;
+            uint4* xs = reinterpret_cast<uint4*>(stg + off);
+            float* xsum = reinterpret_cast<float*>(stg + off + MB * ng * 64);
+            const uint32_t* om = reinterpret_cast<const uint32_t*>(stg + off + MB * ng * 68);
+            __half* xo = reinterpret_cast<__half*>(stg + off + MB * ng * 68 + ng * 4);
+            const int xq_plane = ng * 4;
+            for (int base = tid; base < MB * ng; base += kThreads * 2) {
+                uint4 raw[2][4];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int i = base + b * kThreads;
-            const int m = i / ngroups, g = i - m * ngroups;
+                for (int b = 0; b < 2; ++b) {
+                    const int i = base + b * kThreads;
+                    const int m = i / ng, g = i - m * ng;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                raw[b][j] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < MB * ngroups && m < mrows && g * 32 < a.K)
-                    raw[b][j] = *reinterpret_cast<const uint4*>(a.x + m * a.ldx + g * 32 + j * 8);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-            const int i = base + b * kThreads;
-            if (i < MB * ngroups) {
-                const int m = i / ngroups, g = i - m * ngroups;
-                uint32_t n[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    n[4 * j + 0] = raw[b][j].x;
-                    n[4 * j + 1] = raw[b][j].y;
-                    n[4 * j + 2] = raw[b][j].z;
-                    n[4 * j + 3] = raw[b][j].w;
-                }
-                const uint32_t om = a.n_out > 0 ? omask[g] : 0u;
-                if (om) {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const uint32_t keep = ((om >> (2 * e)) & 1u ? 0xFFFF0000u : 0xFFFFFFFFu) &
-                                              ((om >> (2 * e + 1)) & 1u ? 0x0000FFFFu : 0xFFFFFFFFu);
-                        n[e] &= keep;
+                    for (int c = 0; c < 4; ++c) {
+                        raw[b][c] = make_uint4(0u, 0u, 0u, 0u);
+                        if (i < MB * ng && m < mrows && g * 32 < pa.K)
+                            raw[b][c] = *reinterpret_cast<const uint4*>(pa.x + m * pa.ldx + g * 32 + c * 8);
                     }
                 }
-                float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    s0 = fma2_mixed(n[e], 0x3C003C00u, s0);         // + x_{2e} + x_{2e+1}
-                    s1 = fma2_mixed(n[e + 1], 0x3C003C00u, s1);
+                for (int b = 0; b < 2; ++b) {
+                    const int i = base + b * kThreads;
+                    if (i < MB * ng) {
+                        const int m = i / ng, g = i - m * ng;
+                        uint32_t n[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            n[4 * c + 0] = raw[b][c].x;
+                            n[4 * c + 1] = raw[b][c].y;
+                            n[4 * c + 2] = raw[b][c].z;
+                            n[4 * c + 3] = raw[b][c].w;
+                        }
+                        const uint32_t omw = pa.n_out > 0 ? om[g] : 0u;
+                        if (omw) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const uint32_t keep = ((omw >> (2 * e)) & 1u ? 0xFFFF0000u : 0xFFFFFFFFu) &
+                                                      ((omw >> (2 * e + 1)) & 1u ? 0x0000FFFFu : 0xFFFFFFFFu);
+                                n[e] &= keep;
+                            }
+                        }
+                        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            s0 = fma2_mixed(n[e], 0x3C003C00u, s0);         // + x_{2e} + x_{2e+1}
+                            s1 = fma2_mixed(n[e + 1], 0x3C003C00u, s1);
+                        }
+                        xsum[i] = (s0 + s1) * kUnit;
+                        uint4* dst = xs + m * xq_plane;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) dst[x_chunk_index(g, c)] = permuted_chunk<KIND>(n, c);
+                    }
                 }
-                xsum[i] = (s0 + s1) * kUnit;
-                uint4* dst = xs + m * xq_plane;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) dst[x_chunk_index(g, j)] = permuted_chunk<KIND>(n, j);
             }
+            const int xo_plane = pa.OT * kOutCols;
+            for (int i = tid; i < MB * xo_plane; i += kThreads) {
+                const int m = i / xo_plane, jj = i - m * xo_plane;
+                __half v = __float2half(0.f);
+                if (jj < pa.n_out && m < mrows) {
+                    const int k = pa.idx[jj];
+                    if (k >= 0 && k < pa.K) v = pa.x[m * pa.ldx + k];
+                }
+                xo[i] = v;
+            }
+            off += staging_bytes(MB, pa.recs, pa.OT);
         }
-    }
-    // x[idx] of every activation row, from global memory (the unmasked values)
-    for (int i = tid; i < MB * xo_plane; i += kThreads) {
-        const int m = i / xo_plane, j = i - m * xo_plane;
-        __half v = __float2half(0.f);
-        if (j < a.n_out && m < mrows) {
-            const int k = a.idx[j];
-            if (k >= 0 && k < a.K) v = a.x[m * a.ldx + k];
-        }
-        xo[i] = v;
     }
     __syncthreads();
 
-    // main loop: this warp's tiles through its ring; a segment is a run of tiles of one row block
+    // main loop: this warp's items through its ring; a segment is a run of
+    // items of one row block
     bool ok = true;
-    int c_rb = w_begin / TPR, c_kk = w_begin - (w_begin / TPR) * TPR, c_slot = 0;
+    int c_q = s_q, c_u = s_u, c_kk = s_kk, c_slot = 0, c_stg = s_stg;
     uint32_t c_phase = 0;
-    const int first_rb = my_tiles > 0 ? c_rb : -1, last_rb = my_tiles > 0 ? (w_end - 1) / TPR : -1;
+    int c_recs = a.p[s_q].recs, c_OT = a.p[s_q].OT, c_TPR = c_recs + c_OT, c_uend = min(u1, unit_end(a, s_q));
+    const int first_lu = my_items > 0 ? s_u - u0 : -1;
     if (lane == 0) {
-        seg[2 * warp] = first_rb;
-        seg[2 * warp + 1] = last_rb != first_rb ? last_rb : -1;
+        seg[2 * warp] = first_lu;
+        seg[2 * warp + 1] = -1;
     }
     float acc[MB][kTR];
 #pragma unroll
@@ -624,34 +651,70 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
 #pragma unroll
         for (int r = 0; r < kTR; ++r) acc[m][r] = 0.f;
     int t = 0;
-    for (; t < my_tiles; ++t) {
+    for (; t < my_items; ++t) {
         const bool got = mbar_wait(my_bars + c_slot, c_phase);
         if (!__all_sync(0xffffffffu, got)) {   // warp-uniform: any lane timing out aborts the warp
             ok = false;
             break;
         }
-        const uint8_t* st = my_ring + c_slot * G::kStage;
-        if (c_kk < a.KT) {
-            const uint4* xq = xs + c_kk * GPL * 128 + lane;
-            const float* xsg = xsum + c_kk * GPL * 32 + lane;
-            const int nrec = a.recs - c_kk * GPL;            // records in this tile (>= GPL except at the end)
-            if constexpr (KIND == kW4)
-                w4_dense_tile<MB, GPL>(st, nrec, xq, xq_plane, xsg, ngroups, mrows, lane, acc);
-            else
-                w2_dense_tile<GPL>(st, nrec, xq, xsg, lane, a.lut_lo, a.lut_hi, acc[0]);
-        } else {
-            outlier_tile<MB>(st, xo + (c_kk - a.KT) * kOutCols, xo_plane, mrows, lane, kUnit, acc);
+        const uint8_t* st = my_ring + c_slot * RC::kStage;
+        const bool dense = c_kk < c_recs;
+        // move the item into registers, then hand the stage back to the copy engine
+        uint4 q4[kTR];
+        uint2 q2[kTR];
+        float f1[kTR], f2[kTR];
+        if (KIND == kW4 || !dense) {
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+        }
+        if (dense) {
+            if constexpr (KIND == kW4) {
+#pragma unroll
+                for (int r = 0; r < kTR; ++r) {
+                    f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                    const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)];
+                    f2[r] = static_cast<float>((zb >> ((lane & 1) * 4)) & 15u);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kTR; ++r) {
+                    q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
+                    f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                    f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
+                }
+            }
         }
         __syncwarp();
-        // refill the stage: every lane's reads of it completed before __syncwarp
-        if (lane == 0 && t + SPW < my_tiles) issue_next();
+        if (lane == 0 && t + SPW < my_items) {
+            fence_proxy_async();
+            issue_next();
+        }
         if (++c_slot == SPW) {
             c_slot = 0;
             c_phase ^= 1u;
         }
+        const int ng = c_recs * 32;
+        if (dense) {
+            const uint4* xq = reinterpret_cast<const uint4*>(stg + c_stg) + c_kk * 128 + lane;
+            const float* xsg = reinterpret_cast<const float*>(stg + c_stg + MB * ng * 64) + c_kk * 32 + lane;
+            if constexpr (KIND == kW4) {
+                if constexpr (MB == 1)
+                    w4_record_m1(q4, f1, f2, xq, *xsg, acc[0]);
+                else
+                    w4_record_mb<MB>(q4, f1, f2, xq, ng * 4, xsg, ng, mrows, acc);
+            } else {
+                w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
+            }
+        } else {
+            const __half* xo = reinterpret_cast<const __half*>(stg + c_stg + MB * ng * 68 + ng * 4) +
+                               (c_kk - c_recs) * kOutCols;
+            outlier_record<MB>(q4, xo, c_OT * kOutCols, mrows, lane, kUnit, acc);
+        }
         // end of a segment: reduce over lanes and park the row partials
-        if (++c_kk == TPR || t + 1 == my_tiles) {
-            const int pslot = (c_rb == first_rb) ? 0 : (c_rb == last_rb ? 1 : -1);
+        const bool last = t + 1 == my_items;
+        if (++c_kk == c_TPR || last) {
+            const int lu = c_u - u0;
+            const int pslot = (lu == first_lu) ? 0 : (last ? 1 : -1);
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
                 if (m < mrows) {
@@ -659,7 +722,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                     if ((lane & 7) == 0) {
                         const int r = lane >> 3;
                         if (pslot < 0)
-                            yacc[(c_rb * kTR + r) * MB + m] = tot;             // row block owned by this warp alone
+                            yacc[(lu * kTR + r) * MB + m] = tot;             // row block owned by this warp alone
                         else
                             part[((warp * 2 + pslot) * kTR + r) * MB + m] = tot;
                     }
@@ -667,9 +730,17 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
 #pragma unroll
                 for (int r = 0; r < kTR; ++r) acc[m][r] = 0.f;
             }
-            if (c_kk == TPR) {
+            if (last && lane == 0 && lu != first_lu) seg[2 * warp + 1] = lu;
+            if (c_kk == c_TPR) {
                 c_kk = 0;
-                ++c_rb;
+                if (++c_u == c_uend && !last) {
+                    c_stg += staging_bytes(MB, c_recs, c_OT);
+                    ++c_q;
+                    c_recs = a.p[c_q].recs;
+                    c_OT = a.p[c_q].OT;
+                    c_TPR = c_recs + c_OT;
+                    c_uend = min(u1, unit_end(a, c_q));
+                }
             }
         }
     }
@@ -677,7 +748,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         if (lane == 0) {
             record_error(LBQ_ERR_TIMEOUT);
             // drain the copies this warp still has in flight before its shared memory goes away
-            const int outstanding = (my_tiles - t) < SPW ? (my_tiles - t) : SPW;
+            const int outstanding = (my_items - t) < SPW ? (my_items - t) : SPW;
             for (int u = 0; u < outstanding; ++u) {
                 const int slot = (c_slot + u) % SPW;
                 const uint32_t ph = (slot >= c_slot) ? c_phase : (c_phase ^ 1u);
@@ -688,31 +759,36 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     }
     __syncthreads();
 
-    if (blockIdx.x == 0 && tid == 0) {
+    if (check_hdr) {
+        const ProbArg& pa = a.p[blockIdx.x];
         const long long n_hdr = (static_cast<long long>(hdr1.y) << 32) | hdr1.x;
         const long long k_hdr = (static_cast<long long>(hdr1.w) << 32) | hdr1.z;
-        if (hdr0.x != G::kMagicLo || hdr0.y != G::kMagicHi || hdr0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != a.N ||
-            k_hdr != a.K || static_cast<int>(hdr2.x) != a.n_out)
+        if (hdr0.x != RC::kMagicLo || hdr0.y != RC::kMagicHi || hdr0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != pa.N ||
+            k_hdr != pa.K || static_cast<int>(hdr2.x) != pa.n_out)
             record_error(LBQ_ERR_FORMAT);
     }
     // combine: owned row blocks are already in yacc; shared ones add the parked
     // partials of their warps in warp order (deterministic)
     for (int i = tid; i < R * kTR * MB; i += kThreads) {
         const int m = i % MB, rr = i / MB;
-        const int rbl = rr / kTR, r = rr - rbl * kTR;
+        const int lu = rr / kTR, r = rr - lu * kTR;
         float y = yacc[i];
 #pragma unroll 4
         for (int w = 0; w < NW; ++w) {
-            if (seg[2 * w] == rbl) y += part[((w * 2 + 0) * kTR + r) * MB + m];
-            if (seg[2 * w + 1] == rbl) y += part[((w * 2 + 1) * kTR + r) * MB + m];
+            if (seg[2 * w] == lu) y += part[((w * 2 + 0) * kTR + r) * MB + m];
+            if (seg[2 * w + 1] == lu) y += part[((w * 2 + 1) * kTR + r) * MB + m];
         }
-        const long long n = static_cast<long long>(rb_begin + rbl) * kTR + r;
-        if (n < a.N && m < mrows) {
+        const int u = u0 + lu;
+        int q = qf;
+        while (q + 1 < a.count && a.p[q + 1].ub <= u) ++q;
+        const ProbArg& pa = a.p[q];
+        const long long n = static_cast<long long>(u - pa.ub) * kTR + r;
+        if (n < pa.N && m < mrows) {
             y *= 1.f / kUnit;
             if (a.y_f32)
-                reinterpret_cast<float*>(a.y)[m * a.ldy + n] = y;
+                reinterpret_cast<float*>(pa.y)[m * pa.ldy + n] = y;
             else
-                reinterpret_cast<__half*>(a.y)[m * a.ldy + n] = __float2half_rn(y);
+                reinterpret_cast<__half*>(pa.y)[m * pa.ldy + n] = __float2half_rn(y);
         }
     }
 }
@@ -726,8 +802,6 @@ struct DeviceInfo {
     bool ok = false;
     int sms = 0;
     int max_smem = 0;          // opt-in maximum per CTA
-    int smem_per_sm = 0;
-    int smem_reserved = 0;     // per CTA, reserved by the system
     bool attr_set[kNumVariantsMax] = {};
 };
 constexpr int kMaxDevices = 64;
@@ -745,9 +819,7 @@ lbq_status device_info(DeviceInfo** out) {
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return LBQ_ERR_CUDA;
         d.ok = (major == 10 && minor == 3);
         d.init = true;
@@ -759,47 +831,70 @@ lbq_status device_info(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Kernel variants: (kind, MB activation planes, warps, groups per lane)
+// Kernel variants: (kind, MB activation planes, warps)
 struct Variant {
-    int kind, MB, NW, GPL, stage;
+    int kind, MB, NW, stage;
     const void* fn;
 };
-template <int KIND, int MB, int NW, int GPL>
+template <int KIND, int MB, int NW>
 Variant make_variant() {
-    return Variant{KIND, MB, NW, GPL, Geo<KIND, GPL>::kStage,
-                   reinterpret_cast<const void*>(&lbq_gemv_kernel<KIND, MB, NW, GPL>)};
+    return Variant{KIND, MB, NW, Rec<KIND>::kStage, reinterpret_cast<const void*>(&lbq_gemv_kernel<KIND, MB, NW>)};
 }
 constexpr int kNumVariants = 7;
+constexpr int kVarW4 = 0, kVarW2 = 4, kVarW4Narrow = 5, kVarW2Narrow = 6;
 const Variant& variant(int v) {
     static const Variant table[kNumVariants] = {
-        make_variant<kW4, 1, 16, 2>(),   // 0: 4-bit GEMV
-        make_variant<kW4, 2, 8, 1>(),    // 1..3: 4-bit small-M, 2 / 4 / 8 activation rows per pass
-        make_variant<kW4, 4, 8, 1>(),
-        make_variant<kW4, 8, 8, 1>(),
-        make_variant<kW2, 1, 16, 2>(),   // 4: 2-bit codebook GEMV
-        make_variant<kW4, 1, 8, 1>(),    // 5, 6: smaller-footprint GEMVs for very wide K
-        make_variant<kW2, 1, 8, 1>(),
+        make_variant<kW4, 1, 16>(),   // 0: 4-bit GEMV
+        make_variant<kW4, 2, 8>(),    // 1..3: 4-bit small-M, 2 / 4 / 8 activation rows per pass
+        make_variant<kW4, 4, 8>(),
+        make_variant<kW4, 8, 8>(),
+        make_variant<kW2, 1, 16>(),   // 4: 2-bit codebook GEMV
+        make_variant<kW4, 1, 8>(),    // 5, 6: fewer warps, room for very wide K
+        make_variant<kW2, 1, 8>(),
     };
     return table[v];
 }
 
-lbq_status prepare_args(const Variant& V, const void* packed, int64_t N, int64_t K, int32_t n_out, GemvArgs* a) {
-    lbq_layout L;
-    lbq_status st = lbq_blob_layout(V.kind == kW4 ? LBQ_KIND_W4 : LBQ_KIND_W2CB, N, K, n_out, &L);
-    if (st != LBQ_OK) return st;
+// One problem as the host entry points describe it.
+struct HostProblem {
+    const void* packed;
+    int64_t N, K;
+    int32_t n_out;
+    const void* x;
+    int64_t ldx;
+    void* y;
+    int64_t ldy;
+};
+
+// Fill the launch arguments of a group (without the partition).
+lbq_status prepare_group(int kind, const HostProblem* P, int count, GroupArgs* a) {
     std::memset(a, 0, sizeof(*a));
-    const uint8_t* b = static_cast<const uint8_t*>(packed);
-    a->blob = b;
-    a->area = b + L.area_offset;
-    a->idx = reinterpret_cast<const int32_t*>(b + L.idx_offset);
-    a->rb_bytes = static_cast<long long>(L.row_block_bytes);
-    a->recs = static_cast<int>(L.records);
-    a->N = N;
-    a->K = K;
-    a->n_out = n_out;
-    a->n_rb = static_cast<int>((N + kTR - 1) / kTR);
-    a->KT = (a->recs + V.GPL - 1) / V.GPL;
-    a->OT = static_cast<int>(L.outlier_records);
+    a->count = count;
+    long long ub = 0;
+    for (int i = 0; i < count; ++i) {
+        lbq_layout L;
+        lbq_status st = lbq_blob_layout(kind == kW4 ? LBQ_KIND_W4 : LBQ_KIND_W2CB, P[i].N, P[i].K, P[i].n_out, &L);
+        if (st != LBQ_OK) return st;
+        ProbArg& p = a->p[i];
+        const uint8_t* b = static_cast<const uint8_t*>(P[i].packed);
+        p.blob = b;
+        p.area = b + L.area_offset;
+        p.idx = reinterpret_cast<const int32_t*>(b + L.idx_offset);
+        p.x = static_cast<const __half*>(P[i].x);
+        p.y = P[i].y;
+        p.ldx = P[i].ldx;
+        p.ldy = P[i].ldy;
+        p.N = P[i].N;
+        p.K = P[i].K;
+        p.rb_bytes = static_cast<long long>(L.row_block_bytes);
+        p.recs = static_cast<int>(L.records);
+        p.OT = static_cast<int>(L.outlier_records);
+        p.n_out = P[i].n_out;
+        p.ub = static_cast<int>(ub);
+        ub += (P[i].N + kTR - 1) / kTR;
+        if (ub > INT32_MAX / 2) return LBQ_ERR_SHAPE;
+    }
+    a->nunits = static_cast<int>(ub);
     // 2-bit codebook as FP16 byte tables for PRMT (otf-llm section 2, rounded once)
     const double cb[4] = {-1.52, -0.45, 0.45, 1.52};
     for (int c = 0; c < 4; ++c) {
@@ -810,35 +905,70 @@ lbq_status prepare_args(const Variant& V, const void* packed, int64_t N, int64_t
     return LBQ_OK;
 }
 
-// Stages per warp that fit in `budget` bytes next to the activation planes;
-// < 2 means "does not fit".
-int stages_per_warp(const Variant& V, int budget, int KT, int OT, int rb_cap) {
-    const SmemPlan fixed = smem_plan(V.NW, V.stage, KT * V.GPL, OT, 0, V.MB, rb_cap);
-    int spw = (budget - fixed.total - V.NW * kMaxStagesPerWarp * 8) / (V.NW * V.stage);
+int unit_end_host(const GroupArgs& a, int q) { return q + 1 < a.count ? a.p[q + 1].ub : a.nunits; }
+
+// Persistent grid of <= one CTA per SM; CTA c owns a contiguous run of row
+// blocks whose bytes are about 1/grid of the total.  Returns the largest
+// staging area any CTA needs; sets grid, cta_ub and rb_cap.
+int partition(const DeviceInfo* dev, int MB, GroupArgs& a, int* grid) {
+    long long total = 0;
+    for (int q = 0; q < a.count; ++q) total += static_cast<long long>(unit_end_host(a, q) - a.p[q].ub) * a.p[q].rb_bytes;
+    int G = dev->sms < kMaxGrid ? dev->sms : kMaxGrid;
+    if (G > a.nunits) G = a.nunits;
+    a.cta_ub[0] = 0;
+    int q = 0;
+    long long before = 0;   // bytes of the problems before q
+    for (int c = 1; c < G; ++c) {
+        const long long target = (total * c) / G;
+        while (q + 1 < a.count && before + static_cast<long long>(unit_end_host(a, q) - a.p[q].ub) * a.p[q].rb_bytes <= target) {
+            before += static_cast<long long>(unit_end_host(a, q) - a.p[q].ub) * a.p[q].rb_bytes;
+            ++q;
+        }
+        // first row block of q whose start is at or past the target
+        const long long into = target - before;
+        long long u = a.p[q].ub + (into + a.p[q].rb_bytes - 1) / a.p[q].rb_bytes;
+        if (u > unit_end_host(a, q)) u = unit_end_host(a, q);
+        if (u < a.cta_ub[c - 1]) u = a.cta_ub[c - 1];
+        a.cta_ub[c] = static_cast<int>(u);
+    }
+    a.cta_ub[G] = a.nunits;
+    int rb_cap = 1, stg_max = 0;
+    for (int c = 0; c < G; ++c) {
+        const int u0 = a.cta_ub[c], u1 = a.cta_ub[c + 1];
+        if (u1 - u0 > rb_cap) rb_cap = u1 - u0;
+        int s = 0;
+        if (u1 > u0)
+            for (int p = 0; p < a.count; ++p)
+                if (a.p[p].ub < u1 && unit_end_host(a, p) > u0) s += staging_bytes(MB, a.p[p].recs, a.p[p].OT);
+        if (s > stg_max) stg_max = s;
+    }
+    a.rb_cap = rb_cap;
+    *grid = G;
+    return stg_max;
+}
+
+// Stages per warp that fit next to the staging area; < 2 means "does not fit".
+int stages_per_warp(const DeviceInfo* dev, const Variant& V, int rb_cap, int stg_max) {
+    const FixedPlan f = fixed_plan(V.NW, V.stage, 0, V.MB, rb_cap);
+    const int budget = dev->max_smem - f.total - stg_max - V.NW * kMaxStagesPerWarp * 8 - 128;
+    const int spw = budget / (V.NW * V.stage);
     return spw > kMaxStagesPerWarp ? kMaxStagesPerWarp : spw;
 }
 
-struct LaunchShape {
-    int grid, rb_cap, SPW;
-};
-
-// One persistent CTA per SM (fewer when there are fewer row blocks), each
-// owning a contiguous, balanced run of row blocks.
-LaunchShape launch_shape(const DeviceInfo* dev, const Variant& V, int n_rb, int KT, int OT) {
-    LaunchShape L;
-    L.grid = n_rb < dev->sms ? n_rb : dev->sms;
-    L.rb_cap = (n_rb + L.grid - 1) / L.grid;
-    L.SPW = stages_per_warp(V, dev->max_smem, KT, OT, L.rb_cap);
-    return L;
+// Plan one launch of variant vi over the group; LBQ_ERR_SHAPE when it does not fit.
+lbq_status plan_group(const DeviceInfo* dev, int vi, GroupArgs& a, int* grid, size_t* smem) {
+    const Variant& V = variant(vi);
+    const int stg_max = partition(dev, V.MB, a, grid);
+    const int spw = stages_per_warp(dev, V, a.rb_cap, stg_max);
+    if (spw < 2) return LBQ_ERR_SHAPE;
+    a.SPW = spw;
+    *smem = static_cast<size_t>(fixed_plan(V.NW, V.stage, spw, V.MB, a.rb_cap).total + stg_max);
+    return LBQ_OK;
 }
 
-lbq_status launch_variant(DeviceInfo* dev, int vi, GemvArgs& a, void* stream, uint32_t flags) {
+lbq_status launch_planned(DeviceInfo* dev, int vi, const GroupArgs& a, int grid, size_t smem, void* stream,
+                          uint32_t flags) {
     const Variant& V = variant(vi);
-    const LaunchShape S = launch_shape(dev, V, a.n_rb, a.KT, a.OT);
-    if (S.SPW < 2) return LBQ_ERR_SHAPE;
-    a.rb_cap = S.rb_cap;
-    a.SPW = S.SPW;
-    const SmemPlan P = smem_plan(V.NW, V.stage, a.KT * V.GPL, a.OT, a.SPW, V.MB, a.rb_cap);
     if (!dev->attr_set[vi]) {
         if (cudaFuncSetAttribute(V.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dev->max_smem) != cudaSuccess)
             return LBQ_ERR_CUDA;
@@ -846,16 +976,16 @@ lbq_status launch_variant(DeviceInfo* dev, int vi, GemvArgs& a, void* stream, ui
     }
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(S.grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(V.NW * 32);
-    cfg.dynamicSmemBytes = P.total;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (flags & LBQ_FLAG_PDL) ? 1 : 0;
-    void* args[] = {&a};
+    void* args[] = {const_cast<GroupArgs*>(&a)};
     if (cudaLaunchKernelExC(&cfg, V.fn, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return LBQ_ERR_CUDA;
@@ -863,94 +993,124 @@ lbq_status launch_variant(DeviceInfo* dev, int vi, GemvArgs& a, void* stream, ui
     return LBQ_OK;
 }
 
-lbq_status check_common(const void* packed, int64_t N, int64_t K, int32_t n_out, lbq_dtype y_dtype) {
-    if (N < 1 || N > INT32_MAX - 8 || K < 64 || K > lbq::kMaxK || K % 64 || n_out < 0 || n_out > K ||
-        n_out > lbq::kMaxOutliers)
-        return LBQ_ERR_SHAPE;
-    if (y_dtype != LBQ_F16 && y_dtype != LBQ_F32) return LBQ_ERR_UNSUPPORTED;
-    if (!aligned(packed, 16)) return LBQ_ERR_ALIGN;
-    return LBQ_OK;
-}
-
-// Launch a GEMV-shaped call (mrows activation rows, one pass) on the preferred
-// variant, or on its smaller-footprint fallback when shared memory is short.
-lbq_status launch_one(DeviceInfo* dev, int vi, int vfallback, const void* packed, int64_t N, int64_t K,
-                      int32_t n_out, const void* x, int64_t ldx, void* y, int64_t ldy, int mrows, lbq_dtype y_dtype,
-                      void* stream, uint32_t flags) {
-    GemvArgs a;
-    lbq_status st = prepare_args(variant(vi), packed, N, K, n_out, &a);
+// One pass (mrows <= MB activation rows) over a group: the preferred variant,
+// else its narrower fallback, else the group split in halves (launched back to
+// back; the later half follows a kernel of this same call, which writes no blob,
+// so it may overlap it).  With launches != nullptr nothing is launched and the
+// kernels the pass would launch are counted instead.
+lbq_status launch_pass(DeviceInfo* dev, int kind, int vi, int vfallback, const HostProblem* P, int count, int mrows,
+                       bool y_f32, void* stream, uint32_t flags, int* launches) {
+    static thread_local GroupArgs a;   // ~4 KB: kept off the caller's stack
+    lbq_status st = prepare_group(kind, P, count, &a);
     if (st != LBQ_OK) return st;
-    if (vfallback >= 0 && launch_shape(dev, variant(vi), a.n_rb, a.KT, a.OT).SPW < 2) {
-        vi = vfallback;
-        st = prepare_args(variant(vi), packed, N, K, n_out, &a);
-        if (st != LBQ_OK) return st;
-    }
-    a.x = static_cast<const __half*>(x);
-    a.y = y;
-    a.ldx = ldx;
-    a.ldy = ldy;
     a.mrows = mrows;
-    a.y_f32 = (y_dtype == LBQ_F32);
-    return launch_variant(dev, vi, a, stream, flags);
-}
-
-lbq_status launch_gemv(int kind, const void* packed, int64_t N, int64_t K, int32_t n_out, const void* x, void* y,
-                       lbq_dtype y_dtype, void* stream, uint32_t flags) {
-    if (!packed || !x || !y) return LBQ_ERR_NULL;
-    lbq_status st = check_common(packed, N, K, n_out, y_dtype);
-    if (st != LBQ_OK) return st;
-    if (!aligned(x, 16) || !aligned(y, y_dtype == LBQ_F32 ? 4 : 2)) return LBQ_ERR_ALIGN;
-    DeviceInfo* dev = nullptr;
-    st = device_info(&dev);
-    if (st != LBQ_OK) return st;
-    return kind == kW4 ? launch_one(dev, 0, 5, packed, N, K, n_out, x, K, y, N, 1, y_dtype, stream, flags)
-                       : launch_one(dev, 4, 6, packed, N, K, n_out, x, K, y, N, 1, y_dtype, stream, flags);
-}
-
-lbq_status launch_smallm(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out, const void* X,
-                         int64_t ldx, void* Y, int64_t ldy, lbq_dtype y_dtype, void* stream, uint32_t flags) {
-    if (!packed || !X || !Y) return LBQ_ERR_NULL;
-    lbq_status st = check_common(packed, N, K, n_out, y_dtype);
-    if (st != LBQ_OK) return st;
-    if (M < 1 || M > lbq::kMaxM || ldx < K || ldy < N) return LBQ_ERR_SHAPE;
-    if (!aligned(X, 16) || ldx % 8 || !aligned(Y, y_dtype == LBQ_F32 ? 4 : 2)) return LBQ_ERR_ALIGN;
-    DeviceInfo* dev = nullptr;
-    st = device_info(&dev);
-    if (st != LBQ_OK) return st;
-    if (M == 1) return launch_one(dev, 0, 5, packed, N, K, n_out, X, ldx, Y, ldy, 1, y_dtype, stream, flags);
-    // widest activation block that fits in shared memory next to the weight ring,
-    // then the narrowest one that still covers M in a single pass
-    GemvArgs a;
-    st = prepare_args(variant(1), packed, N, K, n_out, &a);     // variants 1..3 share the tiling
-    if (st != LBQ_OK) return st;
-    const size_t ysz = y_dtype == LBQ_F32 ? 4 : 2;
-    if (launch_shape(dev, variant(1), a.n_rb, a.KT, a.OT).SPW < 2) {
-        // K too wide for two activation planes: one GEMV pass per row
-        for (int m = 0; m < M; ++m) {
-            st = launch_one(dev, 0, 5, packed, N, K, n_out, static_cast<const __half*>(X) + m * ldx, ldx,
-                            static_cast<uint8_t*>(Y) + m * ldy * ysz, ldy, 1, y_dtype, stream,
-                            m == 0 ? flags : LBQ_FLAG_PDL);
-            if (st != LBQ_OK) return st;
-        }
-        return LBQ_OK;
+    a.y_f32 = y_f32 ? 1 : 0;
+    int grid = 0;
+    size_t smem = 0;
+    st = plan_group(dev, vi, a, &grid, &smem);
+    if (st == LBQ_ERR_SHAPE && vfallback >= 0) {
+        vi = vfallback;
+        st = plan_group(dev, vi, a, &grid, &smem);
     }
-    int vmax = 3;
-    while (vmax > 1 && launch_shape(dev, variant(vmax), a.n_rb, a.KT, a.OT).SPW < 4) --vmax;
-    int vi = 1;
-    while (vi < vmax && variant(vi).MB < M) ++vi;
-    const int MB = variant(vi).MB;
-    a.ldx = ldx;
-    a.ldy = ldy;
-    a.y_f32 = (y_dtype == LBQ_F32);
+    if (st == LBQ_OK) {
+        if (launches) {
+            ++*launches;
+            return LBQ_OK;
+        }
+        return launch_planned(dev, vi, a, grid, smem, stream, flags);
+    }
+    if (st != LBQ_ERR_SHAPE || count == 1) return st;
+    const int h = count / 2;
+    st = launch_pass(dev, kind, vi, vfallback, P, h, mrows, y_f32, stream, flags, launches);
+    if (st != LBQ_OK) return st;
+    return launch_pass(dev, kind, vi, vfallback, P + h, count - h, mrows, y_f32, stream, flags | LBQ_FLAG_PDL,
+                       launches);
+}
+
+lbq_status check_problem(const HostProblem& p, int M, lbq_dtype y_dtype) {
+    if (!p.packed || !p.x || !p.y) return LBQ_ERR_NULL;
+    if (p.N < 1 || p.N > INT32_MAX - 8 || p.K < 64 || p.K > lbq::kMaxK || p.K % 64 || p.n_out < 0 || p.n_out > p.K ||
+        p.n_out > lbq::kMaxOutliers)
+        return LBQ_ERR_SHAPE;
+    if (p.ldx < p.K || p.ldy < p.N) return LBQ_ERR_SHAPE;
+    if (M > 1 && static_cast<long long>(M) * p.ldx > (1ll << 40)) return LBQ_ERR_SHAPE;
+    if (!aligned(p.packed, 16) || !aligned(p.x, 16) || p.ldx % 8 || !aligned(p.y, y_dtype == LBQ_F32 ? 4 : 2))
+        return LBQ_ERR_ALIGN;
+    return LBQ_OK;
+}
+
+// Passes of `MB`-row activation blocks over the group (offsets applied to x and y).
+lbq_status run_passes(DeviceInfo* dev, int kind, int vi, int vf, int MB, const HostProblem* P, int count, int M,
+                      bool f32, void* stream, uint32_t flags, int* launches) {
+    const size_t ysz = f32 ? 4 : 2;
+    HostProblem Q[kMaxGroup];
     for (int m0 = 0; m0 < M; m0 += MB) {
-        a.x = static_cast<const __half*>(X) + m0 * ldx;
-        a.y = static_cast<uint8_t*>(Y) + m0 * ldy * ysz;
-        a.mrows = M - m0 < MB ? M - m0 : MB;
-        // later passes follow a pass of this same call, which never writes the blob
-        st = launch_variant(dev, vi, a, stream, m0 == 0 ? flags : LBQ_FLAG_PDL);
+        for (int i = 0; i < count; ++i) {
+            Q[i] = P[i];
+            Q[i].x = static_cast<const __half*>(P[i].x) + m0 * P[i].ldx;
+            Q[i].y = static_cast<uint8_t*>(P[i].y) + m0 * P[i].ldy * ysz;
+        }
+        // later passes follow a pass of this same call, which never writes a blob
+        lbq_status st = launch_pass(dev, kind, vi, vf, Q, count, M - m0 < MB ? M - m0 : MB, f32, stream,
+                                    m0 == 0 ? flags : (flags | LBQ_FLAG_PDL), launches);
         if (st != LBQ_OK) return st;
     }
     return LBQ_OK;
+}
+
+// Every entry point ends here: validate, then one pass (M = 1), or passes of
+// the narrowest small-M variant (2, 4 or 8 activation rows) covering M whose
+// activation planes fit in shared memory for every problem on its own (a group
+// is split into several launches when its problems do not fit together), or
+// one GEMV pass per activation row when K is too wide for two planes.
+lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dtype, void* stream, uint32_t flags,
+               int* launches) {
+    if (count < 1 || count > kMaxGroup || M < 1 || M > lbq::kMaxM) return LBQ_ERR_SHAPE;
+    if (y_dtype != LBQ_F16 && y_dtype != LBQ_F32) return LBQ_ERR_UNSUPPORTED;
+    if (kind == kW2 && M != 1) return LBQ_ERR_UNSUPPORTED;
+    for (int i = 0; i < count; ++i) {
+        lbq_status st = check_problem(P[i], M, y_dtype);
+        if (st != LBQ_OK) return st;
+    }
+    DeviceInfo* dev = nullptr;
+    lbq_status st = device_info(&dev);
+    if (st != LBQ_OK) return st;
+    const bool f32 = y_dtype == LBQ_F32;
+    const int vi = kind == kW4 ? kVarW4 : kVarW2, vf = kind == kW4 ? kVarW4Narrow : kVarW2Narrow;
+    if (M == 1) return launch_pass(dev, kind, vi, vf, P, count, 1, f32, stream, flags, launches);
+    int v = 1;
+    while (v < 3 && variant(v).MB < M) ++v;
+    for (; v >= 1; --v) {
+        bool fits = true;
+        for (int i = 0; i < count && fits; ++i) {
+            int n = 0;
+            fits = launch_pass(dev, kind, v, -1, P + i, 1, variant(v).MB, f32, stream, 0u, &n) == LBQ_OK;
+        }
+        if (fits) break;
+    }
+    if (v >= 1) return run_passes(dev, kind, v, -1, variant(v).MB, P, count, M, f32, stream, flags, launches);
+    return run_passes(dev, kind, vi, vf, 1, P, count, M, f32, stream, flags, launches);
+}
+
+lbq_status run_one(int kind, const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out, const void* x,
+                   int64_t ldx, void* y, int64_t ldy, lbq_dtype y_dtype, void* stream, uint32_t flags) {
+    if (!packed || !x || !y) return LBQ_ERR_NULL;
+    HostProblem p{packed, N, K, n_out, x, ldx, y, ldy};
+    return run(kind, &p, 1, M, y_dtype, stream, flags, nullptr);
+}
+
+lbq_status grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M, lbq_dtype y_dtype,
+                   void* stream, uint32_t flags, int* launches) {
+    if (!problems) return LBQ_ERR_NULL;
+    if (kind != LBQ_KIND_W4 && kind != LBQ_KIND_W2CB) return LBQ_ERR_UNSUPPORTED;
+    if (count < 1 || count > kMaxGroup) return LBQ_ERR_SHAPE;
+    HostProblem P[kMaxGroup];
+    for (int i = 0; i < count; ++i) {
+        const lbq_problem& q = problems[i];
+        if (q.reserved != 0) return LBQ_ERR_SHAPE;
+        P[i] = HostProblem{q.packed, q.N, q.K, q.n_out, q.x, q.ldx, q.y, q.ldy};
+    }
+    return run(kind == LBQ_KIND_W4 ? kW4 : kW2, P, count, M, y_dtype, stream, flags, launches);
 }
 
 }  // namespace
@@ -959,34 +1119,49 @@ extern "C" {
 
 lbq_status lbq_gemv_w4a16_ex(const void* packed, int64_t N, int64_t K, int32_t n_out, const void* x_f16, void* y,
                              lbq_dtype y_dtype, void* stream, uint32_t flags) {
-    return launch_gemv(kW4, packed, N, K, n_out, x_f16, y, y_dtype, stream, flags);
+    return run_one(kW4, packed, 1, N, K, n_out, x_f16, K, y, N, y_dtype, stream, flags);
 }
 
 lbq_status lbq_gemv_w2cb_outlier_ex(const void* packed, int64_t N, int64_t K, int32_t n_out, const void* x_f16,
                                     void* y, lbq_dtype y_dtype, void* stream, uint32_t flags) {
-    return launch_gemv(kW2, packed, N, K, n_out, x_f16, y, y_dtype, stream, flags);
+    return run_one(kW2, packed, 1, N, K, n_out, x_f16, K, y, N, y_dtype, stream, flags);
 }
 
 lbq_status lbq_gemv_w4a16(const void* packed, int64_t N, int64_t K, int32_t n_out, const void* x_f16, void* y,
                           lbq_dtype y_dtype, void* stream) {
-    return launch_gemv(kW4, packed, N, K, n_out, x_f16, y, y_dtype, stream, 0u);
+    return run_one(kW4, packed, 1, N, K, n_out, x_f16, K, y, N, y_dtype, stream, 0u);
 }
 
 lbq_status lbq_gemv_w2cb_outlier(const void* packed, int64_t N, int64_t K, int32_t n_out, const void* x_f16,
                                  void* y, lbq_dtype y_dtype, void* stream) {
-    return launch_gemv(kW2, packed, N, K, n_out, x_f16, y, y_dtype, stream, 0u);
+    return run_one(kW2, packed, 1, N, K, n_out, x_f16, K, y, N, y_dtype, stream, 0u);
 }
 
 lbq_status lbq_gemm_w4a16_smallM_ex(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
                                     const void* X_f16, int64_t ldx, void* Y, int64_t ldy, lbq_dtype y_dtype,
                                     void* stream, uint32_t flags) {
-    return launch_smallm(packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, flags);
+    return run_one(kW4, packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, flags);
 }
 
 lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
                                  const void* X_f16, int64_t ldx, void* Y, int64_t ldy, lbq_dtype y_dtype,
                                  void* stream) {
-    return launch_smallm(packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, 0u);
+    return run_one(kW4, packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, 0u);
+}
+
+
+lbq_status lbq_gemv_grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
+                            lbq_dtype y_dtype, void* stream, uint32_t flags) {
+    return grouped(kind, problems, count, M, y_dtype, stream, flags, nullptr);
+}
+
+lbq_status lbq_gemv_grouped_launches(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
+                                     lbq_dtype y_dtype, int32_t* launches) {
+    if (!launches) return LBQ_ERR_NULL;
+    int n = 0;
+    const lbq_status st = grouped(kind, problems, count, M, y_dtype, nullptr, 0u, &n);
+    *launches = st == LBQ_OK ? n : 0;
+    return st;
 }
 
 lbq_status lbq_device_error(void* stream) {

@@ -22,6 +22,7 @@ LBQ_F32 = 1
 LBQ_KIND_W4 = 0
 LBQ_KIND_W2CB = 1
 LBQ_FLAG_PDL = 1
+LBQ_MAX_GROUP = 32
 
 STATUS = {
     0: "LBQ_OK", 1: "LBQ_ERR_NULL", 2: "LBQ_ERR_SHAPE", 3: "LBQ_ERR_ALIGN", 4: "LBQ_ERR_OUTLIER_IDX",
@@ -35,7 +36,8 @@ EXPORTS = (
     "lbq_w4_packed_bytes", "lbq_w2cb_packed_bytes", "lbq_select_outliers_w4",
     "lbq_select_outliers_impact", "lbq_pack_w4", "lbq_pack_w2cb", "lbq_gemv_w4a16",
     "lbq_gemv_w2cb_outlier", "lbq_gemm_w4a16_smallM", "lbq_gemv_w4a16_ex",
-    "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_device_error",
+    "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
+    "lbq_device_error",
 )
 
 
@@ -50,6 +52,13 @@ class Layout(ctypes.Structure):
                 ("record_bytes", ctypes.c_uint64), ("records", ctypes.c_uint64),
                 ("outlier_record_bytes", ctypes.c_uint64), ("outlier_records", ctypes.c_uint64),
                 ("idx_offset", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
+
+
+class Problem(ctypes.Structure):
+    """lbq_problem: one problem of a grouped launch (device pointers)."""
+    _fields_ = [("packed", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("n_out", ctypes.c_int32), ("reserved", ctypes.c_int32), ("x", ctypes.c_void_p),
+                ("ldx", ctypes.c_int64), ("y", ctypes.c_void_p), ("ldy", ctypes.c_int64)]
 
 
 _lib = None
@@ -91,6 +100,10 @@ def lib():
                                                         c_vp, c_u32]),
             "lbq_gemm_w4a16_smallM_ex": (ctypes.c_int, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp,
                                                         c_i64, ctypes.c_int, c_vp, c_u32]),
+            "lbq_gemv_grouped": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(Problem), c_i32, c_i32, ctypes.c_int,
+                                                c_vp, c_u32]),
+            "lbq_gemv_grouped_launches": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(Problem), c_i32, c_i32,
+                                                         ctypes.c_int, ctypes.POINTER(c_i32)]),
             "lbq_device_error": (ctypes.c_int, [c_vp]),
         }
         for name, (res, args) in sig.items():
@@ -226,6 +239,39 @@ def gemm_w4a16_smallM(packed, M: int, N: int, K: int, n_out: int, X, ldx: int, Y
     yd = _ydtype(Y) if y_dtype is None else y_dtype
     _check(lib().lbq_gemm_w4a16_smallM_ex(_dev_ptr(packed), M, N, K, n_out, _dev_ptr(X), ldx, _dev_ptr(Y), ldy, yd,
                                           _stream(stream), LBQ_FLAG_PDL if pdl else 0), "lbq_gemm_w4a16_smallM")
+
+
+def _problems(problems, y_dtype):
+    arr = (Problem * len(problems))()
+    yd = y_dtype
+    for i, p in enumerate(problems):
+        if len(p) == 6:
+            packed, N, K, n_out, x, y = p
+            ldx, ldy = K, N
+        else:
+            packed, N, K, n_out, x, ldx, y, ldy = p
+        if yd is None:
+            yd = _ydtype(y)
+        arr[i] = Problem(_dev_ptr(packed), N, K, n_out, 0, _dev_ptr(x), ldx, _dev_ptr(y), ldy)
+    return arr, yd
+
+
+def gemv_grouped(kind: int, problems, M: int = 1, stream=None, pdl: bool = False, y_dtype: int | None = None):
+    """One launch over independent problems.  problems: sequence of
+    (packed, N, K, n_out, x, y) or (packed, N, K, n_out, x, ldx, y, ldy); x / y
+    are CUDA tensors or device addresses; ldx defaults to K, ldy to N."""
+    arr, yd = _problems(problems, y_dtype)
+    _check(lib().lbq_gemv_grouped(kind, arr, len(problems), M, yd, _stream(stream), LBQ_FLAG_PDL if pdl else 0),
+           "lbq_gemv_grouped")
+
+
+def gemv_grouped_launches(kind: int, problems, M: int = 1, y_dtype: int | None = None) -> int:
+    """Kernels gemv_grouped would launch for the same arguments."""
+    arr, yd = _problems(problems, y_dtype)
+    n = c_i32(0)
+    _check(lib().lbq_gemv_grouped_launches(kind, arr, len(problems), M, yd, ctypes.byref(n)),
+           "lbq_gemv_grouped_launches")
+    return n.value
 
 
 def device_error(stream=None) -> int:

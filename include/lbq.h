@@ -204,6 +204,49 @@ lbq_status lbq_gemm_w4a16_smallM_ex(const void* packed, int32_t M, int64_t N, in
                                     int32_t n_out, const void* X_f16, int64_t ldx, void* Y,
                                     int64_t ldy, lbq_dtype y_dtype, void* stream, uint32_t flags);
 
+/* Grouped launch: several independent problems of one kind in ONE kernel
+ * launch (a decode layer's linears, or any list of them).  This is the "fused
+ * layer sweep" of a decode step: the persistent grid streams the row blocks of
+ * all problems back to back, so the fixed cost of a launch is paid once per
+ * group instead of once per matrix.  Each problem computes exactly what the
+ * single-problem entry point of its kind computes (lbq_gemv_w4a16 /
+ * lbq_gemm_w4a16_smallM for LBQ_KIND_W4, lbq_gemv_w2cb_outlier for
+ * LBQ_KIND_W2CB); results may differ from a single call only in FP32
+ * summation order.
+ * problems : host array of count descriptors (1 <= count <= LBQ_MAX_GROUP);
+ *            every pointer inside is a device pointer with the alignment of
+ *            the single-problem entry points; ldx % 8 == 0, ldx >= K,
+ *            ldy >= N; reserved must be 0.  The array is read during the call
+ *            only.
+ * M        : activation rows, shared by all problems (1 <= M <= 64; the 2-bit
+ *            kind supports M = 1 only).
+ * The problems must be independent: no problem's y may overlap any problem's
+ * x, y or blob.  Launched as one kernel when the problems' activations fit in
+ * shared memory together, else as several back-to-back kernels.
+ * Errors: as the single-problem entry points, per problem; LBQ_ERR_SHAPE for
+ * count out of range or reserved != 0. */
+#define LBQ_MAX_GROUP 32
+typedef struct {
+    const void* packed;  /* device blob of (N, K, n_out) */
+    int64_t N;
+    int64_t K;
+    int32_t n_out;
+    int32_t reserved;    /* must be 0 */
+    const void* x;       /* device, M rows of K FP16, leading dimension ldx (elements) */
+    int64_t ldx;
+    void* y;             /* device, M rows of N values of y_dtype, leading dimension ldy */
+    int64_t ldy;
+} lbq_problem;
+lbq_status lbq_gemv_grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
+                            lbq_dtype y_dtype, void* stream, uint32_t flags);
+
+/* How many kernels lbq_gemv_grouped would launch for these arguments (1 when
+ * the group fits one launch).  Validates exactly as lbq_gemv_grouped and reads
+ * the current device's attributes, but launches nothing.
+ * launches: host; set to 0 on error.  Errors: as lbq_gemv_grouped. */
+lbq_status lbq_gemv_grouped_launches(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
+                                     lbq_dtype y_dtype, int32_t* launches);
+
 /* Synchronise the stream, then return and clear the device-side error word of
  * the current device (LBQ_OK when no kernel recorded an error).  Errors from
  * the synchronisation itself are reported as LBQ_ERR_CUDA. */
