@@ -53,6 +53,10 @@ constexpr int kTR = 4;                                 // output rows per row bl
 constexpr int kOutCols = 256;                          // outlier columns per outlier record
 constexpr int kOutRecBytes = kTR * kOutCols * 2;       // 2048
 constexpr int kMaxStagesPerWarp = 8;
+// Deeper per-warp rings than this only delay every warp's first item (the copies
+// of all warps queue together) without raising the streaming rate: measured on
+// GB300, one-record stages, 16 warps.
+constexpr int kStagesM1 = 2, kStagesMB = 4;
 constexpr int kMaxGroup = LBQ_MAX_GROUP;               // problems per launch
 constexpr int kMaxGrid = 192;                          // CTAs per launch (>= SMs of a GB300)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -161,15 +165,28 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Lane 0 of the warp (the others skip it): arm the stage's mbarrier with the
+// byte count and start the copy.  All lanes execute this code path, so the
+// bookkeeping around it stays warp-uniform.  The warp's reads of the stage
+// are ordered before it by the __syncwarp() that precedes every call (the
+// consumer-release / producer-acquire order of an mbarrier pipeline).
+__device__ __forceinline__ void bulk_issue_lane0(int lane, uint32_t dst, uint32_t bar, const void* src, uint32_t bytes,
+                                                 uint64_t policy) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.eq.s32 p, %0, 0;\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%2], %4;\n\t"
+        "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%1], [%3], %4, [%2], %5;\n\t}" ::"r"(lane),
+        "r"(dst), "r"(bar), "l"(src), "r"(bytes), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
-
-// Orders this thread's (and, through a preceding warp barrier, its warp's)
-// shared-memory reads before later async-proxy writes to the same stage.
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -292,18 +309,24 @@ __host__ __device__ inline int staging_bytes(int MB, int recs, int OT) {
 __device__ __forceinline__ void w4_record_m1(const uint4 (&q)[kTR], const float (&s)[kTR], const float (&zf)[kTR],
                                              const uint4* xq, float xsz, float (&acc)[kTR]) {
     const uint4 xr[4] = {xq[0], xq[32], xq[64], xq[96]};
+    // the 4 rows' 8 accumulation chains are interleaved for instruction-level parallelism
+    float lo[kTR], hi[kTR];
+#pragma unroll
+    for (int r = 0; r < kTR; ++r) lo[r] = hi[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int r = 0; r < kTR; ++r) {
+            const uint32_t w = u4w(q[r], j), w8 = w >> 8;
+            lo[r] = fma2_mixed(w & 0x000F000Fu, xr[j].x, lo[r]);
+            hi[r] = fma2_mixed(w & 0x00F000F0u, xr[j].z, hi[r]);
+            lo[r] = fma2_mixed(w8 & 0x000F000Fu, xr[j].y, lo[r]);
+            hi[r] = fma2_mixed(w8 & 0x00F000F0u, xr[j].w, hi[r]);
+        }
+    }
 #pragma unroll
     for (int r = 0; r < kTR; ++r) {
-        float lo = 0.f, hi = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t w = u4w(q[r], j), w8 = w >> 8;
-            lo = fma2_mixed(w & 0x000F000Fu, xr[j].x, lo);
-            hi = fma2_mixed(w & 0x00F000F0u, xr[j].z, hi);
-            lo = fma2_mixed(w8 & 0x000F000Fu, xr[j].y, lo);
-            hi = fma2_mixed(w8 & 0x00F000F0u, xr[j].w, hi);
-        }
-        const float t = fmaf(-zf[r], xsz, fmaf(hi, 0.0625f, lo));
+        const float t = fmaf(-zf[r], xsz, fmaf(hi[r], 0.0625f, lo[r]));
         acc[r] = fmaf(s[r], t, acc[r]);
     }
 }
@@ -330,17 +353,22 @@ __device__ __forceinline__ void w4_record_mb(const uint4 (&q)[kTR], const float 
             const uint4* xp = xq + m * xq_plane;
             const uint4 xr[4] = {xp[0], xp[32], xp[64], xp[96]};
             const float xsz = xs24[m * xs_plane];
+            float lo[kTR], hi[kTR];
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) lo[r] = hi[r] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int r = 0; r < kTR; ++r) {
+                    lo[r] = fma2_mixed(u[r][4 * j + 0], xr[j].x, lo[r]);
+                    hi[r] = fma2_mixed(u[r][4 * j + 2], xr[j].z, hi[r]);
+                    lo[r] = fma2_mixed(u[r][4 * j + 1], xr[j].y, lo[r]);
+                    hi[r] = fma2_mixed(u[r][4 * j + 3], xr[j].w, hi[r]);
+                }
+            }
 #pragma unroll
             for (int r = 0; r < kTR; ++r) {
-                float lo = 0.f, hi = 0.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    lo = fma2_mixed(u[r][4 * j + 0], xr[j].x, lo);
-                    hi = fma2_mixed(u[r][4 * j + 2], xr[j].z, hi);
-                    lo = fma2_mixed(u[r][4 * j + 1], xr[j].y, lo);
-                    hi = fma2_mixed(u[r][4 * j + 3], xr[j].w, hi);
-                }
-                const float t = fmaf(-zf[r], xsz, fmaf(hi, 0.0625f, lo));
+                const float t = fmaf(-zf[r], xsz, fmaf(hi[r], 0.0625f, lo[r]));
                 acc[m][r] = fmaf(s[r], t, acc[m][r]);
             }
         }
@@ -353,25 +381,28 @@ __device__ __forceinline__ void w2_record(const uint2 (&c)[kTR], const float (&S
                                           const uint4* xq, float xs, uint32_t lut_lo, uint32_t lut_hi,
                                           float (&acc)[kTR]) {
     const uint4 xr[4] = {xq[0], xq[32], xq[64], xq[96]};
+    // the 4 rows' 8 accumulation chains are interleaved for instruction-level parallelism
+    float d0[kTR], d1[kTR];
 #pragma unroll
-    for (int r = 0; r < kTR; ++r) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < kTR; ++r) d0[r] = d1[r] = 0.f;
 #pragma unroll
-        for (int v = 0; v < 2; ++v) {
-            const uint32_t w = v ? c[r].y : c[r].x;
+    for (int v = 0; v < 2; ++v) {
 #pragma unroll
-            for (int sh = 0; sh < 4; ++sh) {
+        for (int sh = 0; sh < 4; ++sh) {
+            const int mw = (v * 4 + sh) * 2;                       // word of the group's 64 x bytes
+            const uint32_t xa = u4w(xr[mw >> 2], mw & 3), xb = u4w(xr[(mw + 1) >> 2], (mw + 1) & 3);
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) {
+                const uint32_t w = v ? c[r].y : c[r].x;
                 const uint32_t t = (w >> (2 * sh)) & 0x03030303u;
                 const uint32_t sel = t * 0x11u + 0x40404040u;     // nibbles (c, c + 4) per code
-                const uint32_t h01 = prmt(lut_lo, lut_hi, sel);
-                const uint32_t h23 = prmt(lut_lo, lut_hi, sel >> 16);
-                const int mw = (v * 4 + sh) * 2;                   // word of the group's 64 x bytes
-                d[sh & 1] = fma2_mixed(h01, u4w(xr[mw >> 2], mw & 3), d[sh & 1]);
-                d[2 + (sh & 1)] = fma2_mixed(h23, u4w(xr[(mw + 1) >> 2], (mw + 1) & 3), d[2 + (sh & 1)]);
+                d0[r] = fma2_mixed(prmt(lut_lo, lut_hi, sel), xa, d0[r]);
+                d1[r] = fma2_mixed(prmt(lut_lo, lut_hi, sel >> 16), xb, d1[r]);
             }
         }
-        acc[r] = fmaf(S[r], (d[0] + d[1]) + (d[2] + d[3]), fmaf(Z[r], xs, acc[r]));
     }
+#pragma unroll
+    for (int r = 0; r < kTR; ++r) acc[r] = fmaf(S[r], d0[r] + d1[r], fmaf(Z[r], xs, acc[r]));
 }
 
 // One outlier record: lane owns outlier columns [lane*8, +8) of the record's 256
@@ -476,7 +507,8 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     uint64_t* my_bars = reinterpret_cast<uint64_t*>(smem + P.bars) + warp * SPW;
     uint8_t* my_ring = smem + P.ring + warp * SPW * RC::kStage;
 
-    // issue pointer (lane 0 only): problem, row block, item, source address, slot
+    // issue pointer (warp-uniform; only lane 0 executes the copies): problem,
+    // row block, item, source address, slot
     int i_q = s_q, i_u = s_u, i_kk = s_kk, i_slot = 0;
     int i_recs = a.p[s_q].recs, i_TPR = i_recs + a.p[s_q].OT, i_uend = min(u1, unit_end(a, s_q));
     const uint8_t* i_src = a.p[s_q].area + static_cast<long long>(s_u - a.p[s_q].ub) * a.p[s_q].rb_bytes +
@@ -484,11 +516,10 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                                           : static_cast<long long>(i_recs) * RC::kBytes +
                                                 static_cast<long long>(s_kk - i_recs) * kOutRecBytes);
     const uint64_t policy = policy_evict_first();
+    const uint32_t ring_u32 = smem_u32(my_ring), bars_u32 = smem_u32(my_bars);
     auto issue_next = [&]() {
         const uint32_t bytes = i_kk < i_recs ? static_cast<uint32_t>(RC::kBytes) : static_cast<uint32_t>(kOutRecBytes);
-        uint64_t* bar = my_bars + i_slot;
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_load(my_ring + i_slot * RC::kStage, i_src, bytes, bar, policy);
+        bulk_issue_lane0(lane, ring_u32 + i_slot * RC::kStage, bars_u32 + i_slot * 8, i_src, bytes, policy);
         i_src += bytes;   // the row blocks of a problem are contiguous
         if (++i_kk == i_TPR) {
             i_kk = 0;
@@ -507,6 +538,9 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     if (lane == 0) {
         for (int s = 0; s < SPW; ++s) mbar_init(my_bars + s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    {
         const int pre = my_items < SPW ? my_items : SPW;
         for (int t = 0; t < pre; ++t) issue_next();
     }
@@ -612,7 +646,9 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                             s0 = fma2_mixed(n[e], 0x3C003C00u, s0);         // + x_{2e} + x_{2e+1}
                             s1 = fma2_mixed(n[e + 1], 0x3C003C00u, s1);
                         }
-                        xsum[i] = (s0 + s1) * kUnit;
+                        // 4-bit: the zero point arrives as z * 2^-24 (even groups) or
+                        // 16 z * 2^-24 (odd groups, high nibble), so odd sums are staged / 16
+                        xsum[i] = (KIND == kW4 && (g & 1)) ? (s0 + s1) * 0.0625f : (s0 + s1);
                         uint4* dst = xs + m * xq_plane;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) dst[x_chunk_index(g, c)] = permuted_chunk<KIND>(n, c);
@@ -634,8 +670,8 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     }
     __syncthreads();
 
-    // main loop: this warp's items through its ring; a segment is a run of
-    // items of one row block
+    // main loop: this warp's items through its ring, one segment (a run of
+    // items of one row block: its dense records, then its outlier records) at a time
     bool ok = true;
     int c_q = s_q, c_u = s_u, c_kk = s_kk, c_slot = 0, c_stg = s_stg;
     uint32_t c_phase = 0;
@@ -645,102 +681,111 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         seg[2 * warp] = first_lu;
         seg[2 * warp + 1] = -1;
     }
+    // lane 0 of a record's zero byte holds group 2m in the low nibble, lane 1
+    // group 2m+1 in the high one; masked in place it is the FP16 subnormal
+    // z * 2^-24 or 16 z * 2^-24 (the group sums of odd groups are staged / 16)
+    const uint32_t zmask = (lane & 1) ? 0xF0u : 0x0Fu;
     float acc[MB][kTR];
 #pragma unroll
     for (int m = 0; m < MB; ++m)
 #pragma unroll
         for (int r = 0; r < kTR; ++r) acc[m][r] = 0.f;
     int t = 0;
-    for (; t < my_items; ++t) {
-        const bool got = mbar_wait(my_bars + c_slot, c_phase);
-        if (!__all_sync(0xffffffffu, got)) {   // warp-uniform: any lane timing out aborts the warp
-            ok = false;
-            break;
-        }
-        const uint8_t* st = my_ring + c_slot * RC::kStage;
-        const bool dense = c_kk < c_recs;
-        // move the item into registers, then hand the stage back to the copy engine
-        uint4 q4[kTR];
-        uint2 q2[kTR];
-        float f1[kTR], f2[kTR];
-        if (KIND == kW4 || !dense) {
-#pragma unroll
-            for (int r = 0; r < kTR; ++r) q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
-        }
-        if (dense) {
-            if constexpr (KIND == kW4) {
-#pragma unroll
-                for (int r = 0; r < kTR; ++r) {
-                    f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
-                    const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)];
-                    f2[r] = static_cast<float>((zb >> ((lane & 1) * 4)) & 15u);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < kTR; ++r) {
-                    q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
-                    f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
-                    f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && t + SPW < my_items) {
-            fence_proxy_async();
-            issue_next();
-        }
-        if (++c_slot == SPW) {
-            c_slot = 0;
-            c_phase ^= 1u;
-        }
+    while (t < my_items && ok) {
+        const int seg_n = min(my_items - t, c_TPR - c_kk);
+        const int nd = max(0, min(seg_n, c_recs - c_kk));      // dense items of the segment
         const int ng = c_recs * 32;
-        if (dense) {
-            const uint4* xq = reinterpret_cast<const uint4*>(stg + c_stg) + c_kk * 128 + lane;
-            const float* xsg = reinterpret_cast<const float*>(stg + c_stg + MB * ng * 64) + c_kk * 32 + lane;
-            if constexpr (KIND == kW4) {
-                if constexpr (MB == 1)
-                    w4_record_m1(q4, f1, f2, xq, *xsg, acc[0]);
-                else
-                    w4_record_mb<MB>(q4, f1, f2, xq, ng * 4, xsg, ng, mrows, acc);
-            } else {
-                w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
+        const uint4* xq = reinterpret_cast<const uint4*>(stg + c_stg) + c_kk * 128 + lane;
+        const float* xsg = reinterpret_cast<const float*>(stg + c_stg + MB * ng * 64) + c_kk * 32 + lane;
+        const __half* xo = reinterpret_cast<const __half*>(stg + c_stg + MB * ng * 68 + ng * 4) +
+                           max(0, c_kk - c_recs) * kOutCols;
+        const int t_end = t + seg_n, t_dense = t + nd;
+        for (; t < t_end; ++t) {
+            const bool got = mbar_wait(my_bars + c_slot, c_phase);
+            if (!__all_sync(0xffffffffu, got)) {   // warp-uniform: any lane timing out aborts the warp
+                ok = false;
+                break;
             }
-        } else {
-            const __half* xo = reinterpret_cast<const __half*>(stg + c_stg + MB * ng * 68 + ng * 4) +
-                               (c_kk - c_recs) * kOutCols;
-            outlier_record<MB>(q4, xo, c_OT * kOutCols, mrows, lane, kUnit, acc);
-        }
-        // end of a segment: reduce over lanes and park the row partials
-        const bool last = t + 1 == my_items;
-        if (++c_kk == c_TPR || last) {
-            const int lu = c_u - u0;
-            const int pslot = (lu == first_lu) ? 0 : (last ? 1 : -1);
+            const uint8_t* st = my_ring + c_slot * RC::kStage;
+            const bool dense = t < t_dense;
+            // move the item into registers, then hand the stage back to the copy engine
+            uint4 q4[kTR];
+            uint2 q2[kTR];
+            float f1[kTR], f2[kTR];
+            if (KIND == kW4 || !dense) {
 #pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                if (m < mrows) {
-                    const float tot = reduce_rows4(acc[m], lane);
-                    if ((lane & 7) == 0) {
-                        const int r = lane >> 3;
-                        if (pslot < 0)
-                            yacc[(lu * kTR + r) * MB + m] = tot;             // row block owned by this warp alone
-                        else
-                            part[((warp * 2 + pslot) * kTR + r) * MB + m] = tot;
+                for (int r = 0; r < kTR; ++r) q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+            }
+            if (dense) {
+                if constexpr (KIND == kW4) {
+#pragma unroll
+                    for (int r = 0; r < kTR; ++r) {
+                        f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                        const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)] & zmask;
+                        f2[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(zb)));
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kTR; ++r) {
+                        q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
+                        f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                        f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
                     }
                 }
-#pragma unroll
-                for (int r = 0; r < kTR; ++r) acc[m][r] = 0.f;
             }
-            if (last && lane == 0 && lu != first_lu) seg[2 * warp + 1] = lu;
-            if (c_kk == c_TPR) {
-                c_kk = 0;
-                if (++c_u == c_uend && !last) {
-                    c_stg += staging_bytes(MB, c_recs, c_OT);
-                    ++c_q;
-                    c_recs = a.p[c_q].recs;
-                    c_OT = a.p[c_q].OT;
-                    c_TPR = c_recs + c_OT;
-                    c_uend = min(u1, unit_end(a, c_q));
+            __syncwarp();
+            if (t + SPW < my_items) issue_next();
+            if (++c_slot == SPW) {
+                c_slot = 0;
+                c_phase ^= 1u;
+            }
+            if (dense) {
+                if constexpr (KIND == kW4) {
+                    if constexpr (MB == 1)
+                        w4_record_m1(q4, f1, f2, xq, *xsg, acc[0]);
+                    else
+                        w4_record_mb<MB>(q4, f1, f2, xq, ng * 4, xsg, ng, mrows, acc);
+                } else {
+                    w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
                 }
+                xq += 128;
+                xsg += 32;
+            } else {
+                outlier_record<MB>(q4, xo, c_OT * kOutCols, mrows, lane, kUnit, acc);
+                xo += kOutCols;
+            }
+        }
+        if (!ok) break;
+        // end of a segment: reduce over lanes and park the row partials
+        const bool last = t == my_items;
+        const int lu = c_u - u0;
+        const int pslot = (lu == first_lu) ? 0 : (last ? 1 : -1);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            if (m < mrows) {
+                const float tot = reduce_rows4(acc[m], lane);
+                if ((lane & 7) == 0) {
+                    const int r = lane >> 3;
+                    if (pslot < 0)
+                        yacc[(lu * kTR + r) * MB + m] = tot;             // row block owned by this warp alone
+                    else
+                        part[((warp * 2 + pslot) * kTR + r) * MB + m] = tot;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) acc[m][r] = 0.f;
+        }
+        if (last && lane == 0 && lu != first_lu) seg[2 * warp + 1] = lu;
+        c_kk += seg_n;
+        if (c_kk == c_TPR && !last) {
+            c_kk = 0;
+            if (++c_u == c_uend) {
+                c_stg += staging_bytes(MB, c_recs, c_OT);
+                ++c_q;
+                c_recs = a.p[c_q].recs;
+                c_OT = a.p[c_q].OT;
+                c_TPR = c_recs + c_OT;
+                c_uend = min(u1, unit_end(a, c_q));
             }
         }
     }
@@ -845,8 +890,8 @@ constexpr int kVarW4 = 0, kVarW2 = 4, kVarW4Narrow = 5, kVarW2Narrow = 6;
 const Variant& variant(int v) {
     static const Variant table[kNumVariants] = {
         make_variant<kW4, 1, 16>(),   // 0: 4-bit GEMV
-        make_variant<kW4, 2, 8>(),    // 1..3: 4-bit small-M, 2 / 4 / 8 activation rows per pass
-        make_variant<kW4, 4, 8>(),
+        make_variant<kW4, 2, 12>(),   // 1..3: 4-bit small-M, 2 / 4 / 8 activation rows per pass
+        make_variant<kW4, 4, 12>(),
         make_variant<kW4, 8, 8>(),
         make_variant<kW2, 1, 16>(),   // 4: 2-bit codebook GEMV
         make_variant<kW4, 1, 8>(),    // 5, 6: fewer warps, room for very wide K
@@ -952,7 +997,8 @@ int stages_per_warp(const DeviceInfo* dev, const Variant& V, int rb_cap, int stg
     const FixedPlan f = fixed_plan(V.NW, V.stage, 0, V.MB, rb_cap);
     const int budget = dev->max_smem - f.total - stg_max - V.NW * kMaxStagesPerWarp * 8 - 128;
     const int spw = budget / (V.NW * V.stage);
-    return spw > kMaxStagesPerWarp ? kMaxStagesPerWarp : spw;
+    const int cap = V.MB == 1 ? kStagesM1 : kStagesMB;
+    return spw > cap ? cap : spw;
 }
 
 // Plan one launch of variant vi over the group; LBQ_ERR_SHAPE when it does not fit.
