@@ -114,11 +114,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -147,22 +142,6 @@ __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, u
         __nanosleep(256);
     }
     return true;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_bounded(bar, parity, kWaitLimitNs);
-}
-
-// One contiguous global -> shared bulk copy (bytes % 16 == 0, both ends 16-byte
-// aligned) completing on an mbarrier, with an L2 eviction-priority hint.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                          uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
 }
 
 // Lane 0 of the warp (the others skip it): arm the stage's mbarrier with the
@@ -459,7 +438,8 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     // align by offsetting the shared array itself, so the compiler keeps the
     // shared address space (LDS with immediate offsets, no generic addressing)
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    const int SPW = a.SPW;
+    // M = 1 kernels always run 2 stages per warp (the host plans exactly that)
+    const int SPW = MB == 1 ? kStagesM1 : a.SPW;
     const FixedPlan P = fixed_plan(NW, RC::kStage, SPW, MB, a.rb_cap);
     float* yacc = reinterpret_cast<float*>(smem + P.yacc);
     float* part = reinterpret_cast<float*>(smem + P.part);
@@ -517,9 +497,9 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                                                 static_cast<long long>(s_kk - i_recs) * kOutRecBytes);
     const uint64_t policy = policy_evict_first();
     const uint32_t ring_u32 = smem_u32(my_ring), bars_u32 = smem_u32(my_bars);
-    auto issue_next = [&]() {
+    auto issue_next = [&](bool more) {
         const uint32_t bytes = i_kk < i_recs ? static_cast<uint32_t>(RC::kBytes) : static_cast<uint32_t>(kOutRecBytes);
-        bulk_issue_lane0(lane, ring_u32 + i_slot * RC::kStage, bars_u32 + i_slot * 8, i_src, bytes, policy);
+        bulk_issue_lane0(more ? lane : 1, ring_u32 + i_slot * RC::kStage, bars_u32 + i_slot * 8, i_src, bytes, policy);
         i_src += bytes;   // the row blocks of a problem are contiguous
         if (++i_kk == i_TPR) {
             i_kk = 0;
@@ -542,7 +522,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     __syncwarp();
     {
         const int pre = my_items < SPW ? my_items : SPW;
-        for (int t = 0; t < pre; ++t) issue_next();
+        for (int t = 0; t < pre; ++t) issue_next(true);
     }
     // blob header of problem blockIdx.x: loaded now, compared after the main
     // loop, so the check never delays this CTA's prologue
@@ -691,6 +671,22 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
 #pragma unroll
         for (int r = 0; r < kTR; ++r) acc[m][r] = 0.f;
     int t = 0;
+    // one step of the ring: wait for the stage (warp-uniform), run `body` on it
+    // after the refill of the stage has been handed to lane 0's copy engine
+    auto next_stage = [&](auto&& load, auto&& body) -> bool {
+        uint64_t* bar = my_bars + c_slot;
+        if (!__all_sync(0xffffffffu, mbar_try_wait(bar, c_phase)) &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(bar, c_phase, kWaitLimitNs)))
+            return false;                                  // a lane timed out: the warp aborts
+        const uint8_t* st = my_ring + c_slot * RC::kStage;
+        load(st);                                          // the item into registers
+        __syncwarp();
+        issue_next(t + SPW < my_items);                    // hand the stage back
+        c_slot = c_slot + 1 == SPW ? 0 : c_slot + 1;
+        c_phase ^= c_slot == 0 ? 1u : 0u;
+        body();
+        return true;
+    };
     while (t < my_items && ok) {
         const int seg_n = min(my_items - t, c_TPR - c_kk);
         const int nd = max(0, min(seg_n, c_recs - c_kk));      // dense items of the segment
@@ -700,60 +696,54 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         const __half* xo = reinterpret_cast<const __half*>(stg + c_stg + MB * ng * 68 + ng * 4) +
                            max(0, c_kk - c_recs) * kOutCols;
         const int t_end = t + seg_n, t_dense = t + nd;
-        for (; t < t_end; ++t) {
-            const bool got = mbar_wait(my_bars + c_slot, c_phase);
-            if (!__all_sync(0xffffffffu, got)) {   // warp-uniform: any lane timing out aborts the warp
-                ok = false;
-                break;
-            }
-            const uint8_t* st = my_ring + c_slot * RC::kStage;
-            const bool dense = t < t_dense;
-            // move the item into registers, then hand the stage back to the copy engine
-            uint4 q4[kTR];
-            uint2 q2[kTR];
-            float f1[kTR], f2[kTR];
-            if (KIND == kW4 || !dense) {
+        uint4 q4[kTR];
+        float f1[kTR], f2[kTR];
+        // dense records
+        for (; t < t_dense; ++t) {
+            if constexpr (KIND == kW4) {
+                ok = next_stage(
+                    [&](const uint8_t* st) {
 #pragma unroll
-                for (int r = 0; r < kTR; ++r) q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
-            }
-            if (dense) {
-                if constexpr (KIND == kW4) {
-#pragma unroll
-                    for (int r = 0; r < kTR; ++r) {
-                        f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
-                        const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)] & zmask;
-                        f2[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(zb)));
-                    }
-                } else {
-#pragma unroll
-                    for (int r = 0; r < kTR; ++r) {
-                        q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
-                        f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
-                        f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (t + SPW < my_items) issue_next();
-            if (++c_slot == SPW) {
-                c_slot = 0;
-                c_phase ^= 1u;
-            }
-            if (dense) {
-                if constexpr (KIND == kW4) {
-                    if constexpr (MB == 1)
-                        w4_record_m1(q4, f1, f2, xq, *xsg, acc[0]);
-                    else
-                        w4_record_mb<MB>(q4, f1, f2, xq, ng * 4, xsg, ng, mrows, acc);
-                } else {
-                    w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
-                }
-                xq += 128;
-                xsg += 32;
+                        for (int r = 0; r < kTR; ++r) {
+                            q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+                            f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                            const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)] & zmask;
+                            f2[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(zb)));
+                        }
+                    },
+                    [&]() {
+                        if constexpr (MB == 1)
+                            w4_record_m1(q4, f1, f2, xq, *xsg, acc[0]);
+                        else
+                            w4_record_mb<MB>(q4, f1, f2, xq, ng * 4, xsg, ng, mrows, acc);
+                    });
             } else {
-                outlier_record<MB>(q4, xo, c_OT * kOutCols, mrows, lane, kUnit, acc);
-                xo += kOutCols;
+                uint2 q2[kTR];
+                ok = next_stage(
+                    [&](const uint8_t* st) {
+#pragma unroll
+                        for (int r = 0; r < kTR; ++r) {
+                            q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
+                            f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                            f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
+                        }
+                    },
+                    [&]() { w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]); });
             }
+            if (!ok) break;
+            xq += 128;
+            xsg += 32;
+        }
+        // outlier records
+        for (; ok && t < t_end; ++t) {
+            ok = next_stage(
+                [&](const uint8_t* st) {
+#pragma unroll
+                    for (int r = 0; r < kTR; ++r) q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+                },
+                [&]() { outlier_record<MB>(q4, xo, c_OT * kOutCols, mrows, lane, kUnit, acc); });
+            if (!ok) break;
+            xo += kOutCols;
         }
         if (!ok) break;
         // end of a segment: reduce over lanes and park the row partials
