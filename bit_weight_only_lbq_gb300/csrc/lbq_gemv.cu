@@ -88,6 +88,7 @@ struct ProbArg {
     long long rb_bytes;    // bytes per row block
     int recs;              // dense records per row block
     int OT;                // outlier records per row block
+    int out_last;          // bytes of the last one (4 rows x its columns, rounded up to 8, x 2 B)
     int n_out;
     int ub;                // index of its first row block in the launch's sequence
 };
@@ -491,6 +492,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     // row block, item, source address, slot
     int i_q = s_q, i_u = s_u, i_kk = s_kk, i_slot = 0;
     int i_recs = a.p[s_q].recs, i_TPR = i_recs + a.p[s_q].OT, i_uend = min(u1, unit_end(a, s_q));
+    int i_last = a.p[s_q].out_last;
     const uint8_t* i_src = a.p[s_q].area + static_cast<long long>(s_u - a.p[s_q].ub) * a.p[s_q].rb_bytes +
                            (s_kk < i_recs ? static_cast<long long>(s_kk) * RC::kBytes
                                           : static_cast<long long>(i_recs) * RC::kBytes +
@@ -498,7 +500,9 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     const uint64_t policy = policy_evict_first();
     const uint32_t ring_u32 = smem_u32(my_ring), bars_u32 = smem_u32(my_bars);
     auto issue_next = [&](bool more) {
-        const uint32_t bytes = i_kk < i_recs ? static_cast<uint32_t>(RC::kBytes) : static_cast<uint32_t>(kOutRecBytes);
+        const uint32_t bytes = i_kk < i_recs        ? static_cast<uint32_t>(RC::kBytes)
+                               : i_kk + 1 == i_TPR ? static_cast<uint32_t>(i_last)
+                                                    : static_cast<uint32_t>(kOutRecBytes);
         bulk_issue_lane0(more ? lane : 1, ring_u32 + i_slot * RC::kStage, bars_u32 + i_slot * 8, i_src, bytes, policy);
         i_src += bytes;   // the row blocks of a problem are contiguous
         if (++i_kk == i_TPR) {
@@ -507,6 +511,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                 // next problem, entered at its first row block
                 i_recs = a.p[i_q].recs;
                 i_TPR = i_recs + a.p[i_q].OT;
+                i_last = a.p[i_q].out_last;
                 i_uend = min(u1, unit_end(a, i_q));
                 i_src = a.p[i_q].area;
             }
@@ -656,6 +661,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     int c_q = s_q, c_u = s_u, c_kk = s_kk, c_slot = 0, c_stg = s_stg;
     uint32_t c_phase = 0;
     int c_recs = a.p[s_q].recs, c_OT = a.p[s_q].OT, c_TPR = c_recs + c_OT, c_uend = min(u1, unit_end(a, s_q));
+    int c_out_last = a.p[s_q].out_last;
     const int first_lu = my_items > 0 ? s_u - u0 : -1;
     if (lane == 0) {
         seg[2 * warp] = first_lu;
@@ -734,12 +740,17 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
             xq += 128;
             xsg += 32;
         }
-        // outlier records
-        for (; ok && t < t_end; ++t) {
+        // outlier records: 256 columns each, the last one trimmed (its rows are
+        // `cols` wide); a lane owns 8 columns, lanes past the width read zeros
+        for (int o = max(0, c_kk - c_recs); ok && t < t_end; ++t, ++o) {
+            const int cols = o + 1 == c_OT ? c_out_last / 8 : kOutCols;
             ok = next_stage(
                 [&](const uint8_t* st) {
+                    const bool mine = lane * 8 < cols;
 #pragma unroll
-                    for (int r = 0; r < kTR; ++r) q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+                    for (int r = 0; r < kTR; ++r)
+                        q4[r] = mine ? *reinterpret_cast<const uint4*>(st + r * cols * 2 + lane * 16)
+                                     : make_uint4(0u, 0u, 0u, 0u);
                 },
                 [&]() { outlier_record<MB>(q4, xo, c_OT * kOutCols, mrows, lane, kUnit, acc); });
             if (!ok) break;
@@ -774,6 +785,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                 ++c_q;
                 c_recs = a.p[c_q].recs;
                 c_OT = a.p[c_q].OT;
+                c_out_last = a.p[c_q].out_last;
                 c_TPR = c_recs + c_OT;
                 c_uend = min(u1, unit_end(a, c_q));
             }
@@ -924,6 +936,9 @@ lbq_status prepare_group(int kind, const HostProblem* P, int count, GroupArgs* a
         p.rb_bytes = static_cast<long long>(L.row_block_bytes);
         p.recs = static_cast<int>(L.records);
         p.OT = static_cast<int>(L.outlier_records);
+        p.out_last = p.OT > 0 ? static_cast<int>(L.row_block_bytes - L.records * L.record_bytes -
+                                                 (L.outlier_records - 1) * L.outlier_record_bytes)
+                              : 0;
         p.n_out = P[i].n_out;
         p.ub = static_cast<int>(ub);
         ub += (P[i].N + kTR - 1) / kTR;

@@ -246,8 +246,11 @@ lbq_status pack_common(lbq_kind kind, const float* W, int64_t N, int64_t K, cons
                                       L->records * L->record_bytes;
                 const int r = int(n % lbq::kRowsPerBlock);
                 for (int32_t j = 0; j < n_out; ++j) {
-                    const uint64_t off = base + uint64_t(j / lbq::kOutlierCols) * L->outlier_record_bytes +
-                                         uint64_t(r * lbq::kOutlierCols + j % lbq::kOutlierCols) * 2;
+                    const int32_t rec = j / lbq::kOutlierCols;
+                    const uint64_t width = std::min<uint64_t>(
+                        lbq::kOutlierCols, round_up(uint64_t(n_out), lbq::kOutlierColAlign) - uint64_t(rec) * lbq::kOutlierCols);
+                    const uint64_t off = base + uint64_t(rec) * L->outlier_record_bytes +
+                                         (uint64_t(r) * width + uint64_t(j % lbq::kOutlierCols)) * 2;
                     const uint16_t h = f64_to_f16_bits(W[n * K + idx[j]]);
                     std::memcpy(out + off, &h, 2);
                 }
@@ -302,7 +305,9 @@ lbq_status lbq_blob_layout(lbq_kind kind, int64_t N, int64_t K, int32_t n_out, l
     out->records = (uint64_t(K) + group_k - 1) / group_k;
     out->outlier_record_bytes = n_out > 0 ? uint64_t(lbq::kRowsPerBlock) * lbq::kOutlierCols * 2 : 0;
     out->outlier_records = (uint64_t(n_out) + lbq::kOutlierCols - 1) / lbq::kOutlierCols;
-    out->row_block_bytes = out->records * out->record_bytes + out->outlier_records * out->outlier_record_bytes;
+    // the last outlier record holds the remaining columns rounded up to a multiple of 8
+    const uint64_t out_cols = round_up(uint64_t(n_out), lbq::kOutlierColAlign);
+    out->row_block_bytes = out->records * out->record_bytes + uint64_t(lbq::kRowsPerBlock) * 2 * out_cols;
     const uint64_t n_rb = (uint64_t(N) + lbq::kRowsPerBlock - 1) / lbq::kRowsPerBlock;
     out->idx_offset = round_up(out->area_offset + n_rb * out->row_block_bytes, lbq::kSectionAlign);
     out->total_bytes = round_up(out->idx_offset + 4ull * n_out, lbq::kSectionAlign);

@@ -4,7 +4,7 @@
 #include <cstdint>
 
 #define LBQ_VERSION_NUM 100          // 0.1.0
-#define LBQ_FORMAT_VERSION_NUM 1
+#define LBQ_FORMAT_VERSION_NUM 2
 
 namespace lbq {
 
@@ -13,7 +13,8 @@ constexpr int32_t kMaxOutliers = 8192;    // gathered outlier activations live i
 constexpr uint64_t kSectionAlign = 256;   // the record area and the index array start on this boundary
 constexpr int kRowsPerBlock = 4;          // rows of a row block (one record row-block)
 constexpr int kRecordGroups = 32;         // groups of 32 weights per dense record (1024 k)
-constexpr int kOutlierCols = 256;         // outlier columns per outlier record
+constexpr int kOutlierCols = 256;         // outlier columns per full outlier record
+constexpr int kOutlierColAlign = 8;       // the last outlier record's width is a multiple of this
 constexpr int kMaxM = 64;                 // largest batch of the small-M entry point
 
 uint16_t host_f64_to_f16(double v);

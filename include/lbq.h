@@ -36,10 +36,10 @@
  *    a blob whose header does not match the call, records a code in a
  *    device-side error word that lbq_device_error() reports and clears.
  *
- * Packed blob (format version 1; all integers little-endian)
+ * Packed blob (format version 2; all integers little-endian)
  * ----------------------------------------------------------
  *   [0:8)    magic "LBQW4G32" (4-bit) or "LBQW2C32" (2-bit codebook)
- *   [8:12)   u32 version = 1            [12:16)  u32 header bytes = 128
+ *   [8:12)   u32 version = 2            [12:16)  u32 header bytes = 128
  *   [16:24)  i64 N                      [24:32)  i64 K
  *   [32:36)  i32 n_out                  [36:40)  u32 group size = 32
  *   [40:48)  u64 total blob bytes
@@ -56,7 +56,10 @@
  *                            zero points, byte = z_{2m} | z_{2m+1} << 4 (at 2304).
  *     2-bit record (1536 B): codes, 8 B per group, byte = q0|q1<<2|q2<<4|q3<<6
  *                            for four consecutive k; FP16 S (at 1024); FP16 Z (at 1280).
- *     outlier record (2048 B): 256 FP16 values W[n, idx_j] per row.
+ *     outlier record: FP16 W[n, idx_j] for its columns j, row-major over
+ *                     (row 0..3, column); 256 columns (2048 B) except the last
+ *                     record of the row block, which holds the remaining columns
+ *                     rounded up to a multiple of 8 (columns past n_out are zero).
  *   The n_out int32 outlier indices start at idx_offset (a 256-byte boundary).
  *   A row block is one contiguous byte range, so a kernel streams any run of its
  *   records with a single bulk copy.
@@ -93,8 +96,9 @@ typedef struct {
     uint64_t row_block_bytes;       /* bytes per block of 4 rows */
     uint64_t record_bytes;          /* bytes per dense record: 2368 (4-bit) or 1536 (2-bit) */
     uint64_t records;               /* dense records per row block = ceil(K / 1024) */
-    uint64_t outlier_record_bytes;  /* 2048 when n_out > 0, else 0 */
-    uint64_t outlier_records;       /* outlier records per row block = ceil(n_out / 256) */
+    uint64_t outlier_record_bytes;  /* 2048 (a full outlier record) when n_out > 0, else 0 */
+    uint64_t outlier_records;       /* outlier records per row block = ceil(n_out / 256); together
+                                       they take 8 * round_up(n_out, 8) bytes */
     uint64_t idx_offset;            /* start of the n_out int32 outlier indices */
     uint64_t total_bytes;           /* size of the whole blob */
 } lbq_layout;

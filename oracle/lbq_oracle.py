@@ -30,17 +30,17 @@ Readings where the pages are silent (each listed in the design notes):
 * outlier columns are zeroed in the dense matrix before grouping and excluded
   from the background product (x with those channels zeroed).
 
-Blob format (version 1), all integers little-endian, written here from the
+Blob format (version 2), all integers little-endian, written here from the
 layout description, independently of the C++ packer:
   [0:8)    magic b"LBQW4G32" (4-bit) or b"LBQW2C32" (2-bit codebook)
-  [8:12)   u32 version = 1           [12:16)  u32 header bytes = 128
+  [8:12)   u32 version = 2           [12:16)  u32 header bytes = 128
   [16:24)  i64 N                     [24:32)  i64 K
   [32:36)  i32 n_out                 [36:40)  u32 group size = 32
   [40:48)  u64 total blob bytes
   [48:56)  u64 offset of the row-block area (256)
   [56:64)  u64 bytes per row block
   [64:72)  u64 bytes per dense record   [72:80)  u64 dense records per row block
-  [80:88)  u64 bytes per outlier record [88:96)  u64 outlier records per row block
+  [80:88)  u64 bytes per full outlier record [88:96)  u64 outlier records per row block
   [96:104) u64 offset of the outlier index array (n_out int32)
   [104:128) zero
 Rows are taken 4 at a time (a row block; rows past N are zero).  A row block
@@ -51,7 +51,10 @@ each of the three parts is row-major over (row 0..3, group 0..31):
          then FP16 scale per group, then zero points z_{2m} | z_{2m+1} << 4 per byte;
   2-bit  record (1536 B): codes 8 B per group (byte = q0 | q1<<2 | q2<<4 | q3<<6),
          then FP16 S per group, then FP16 Z per group;
-  outlier record (2048 B): 256 FP16 values of W[n, idx_j] per row.
+  outlier record j: W[n, idx_c] in FP16 for its columns c = 256 j .. 256 j + w_j - 1,
+         row-major over (row 0..3, column); w_j = 256 except for the last record,
+         whose width is rounded up to a multiple of 8 columns (columns past n_out
+         are zero), so a row block's outlier records take 8 * round_up(n_out, 8) bytes.
 The idx array starts on a 256-byte boundary after the row-block area.
 """
 from __future__ import annotations
@@ -70,7 +73,7 @@ HEADER_BYTES = 128
 SECTION_ALIGN = 256
 MAGIC_W4 = b"LBQW4G32"
 MAGIC_W2 = b"LBQW2C32"
-VERSION = 1
+VERSION = 2
 
 F64 = np.float64
 
@@ -113,7 +116,8 @@ def _up(x: int, a: int) -> int:
 
 REC_GROUPS = 32          # groups per dense record (1024 k)
 ROWS_PER_BLOCK = 4
-OUT_COLS = 256           # outlier columns per outlier record
+OUT_COLS = 256           # outlier columns per full outlier record
+OUT_COL_ALIGN = 8        # the last outlier record's width is a multiple of this
 
 
 def record_parts(kind: str) -> tuple:
@@ -132,13 +136,20 @@ def layout(kind: str, N: int, K: int, n_out: int) -> dict:
     nrec = -(-K // (REC_GROUPS * G))
     out_rec = ROWS_PER_BLOCK * OUT_COLS * 2 if n_out else 0
     n_outrec = -(-n_out // OUT_COLS)
-    rb_bytes = nrec * rec + n_outrec * out_rec
+    out_cols = _up(n_out, OUT_COL_ALIGN)                # columns stored, last record trimmed
+    rb_bytes = nrec * rec + ROWS_PER_BLOCK * 2 * out_cols
     n_rb = -(-N // ROWS_PER_BLOCK)
     area = SECTION_ALIGN
     idx_off = _up(area + n_rb * rb_bytes, SECTION_ALIGN)
     total = _up(idx_off + 4 * n_out, SECTION_ALIGN)
     return {"area": area, "rb_bytes": rb_bytes, "rec_bytes": rec, "recs": nrec, "out_rec_bytes": out_rec,
-            "out_recs": n_outrec, "idx": idx_off, "total": total, "n_rb": n_rb}
+            "out_recs": n_outrec, "idx": idx_off, "total": total, "n_rb": n_rb, "out_cols": out_cols}
+
+
+def outlier_widths(n_out: int) -> list:
+    """Columns of each outlier record of a row block (the last one trimmed)."""
+    cols = _up(n_out, OUT_COL_ALIGN)
+    return [min(OUT_COLS, cols - OUT_COLS * j) for j in range(-(-n_out // OUT_COLS))]
 
 
 def _pad2(a: np.ndarray, rows: int, cols: int) -> np.ndarray:
@@ -163,11 +174,13 @@ def _write_blob(kind: str, N: int, K: int, idx: np.ndarray, part_rows: list, val
     dense = np.concatenate(chunks, axis=2).reshape(n_rb, nrec * L["rec_bytes"])
     pieces = [dense]
     if n_out:
-        nor = L["out_recs"]
         v = _pad2(np.ascontiguousarray(vals16.astype("<f2")).view(np.uint8).reshape(N, 2 * n_out),
-                  rows, nor * OUT_COLS * 2)
-        pieces.append(v.reshape(n_rb, ROWS_PER_BLOCK, nor, OUT_COLS * 2).transpose(0, 2, 1, 3)
-                      .reshape(n_rb, nor * L["out_rec_bytes"]))
+                  rows, 2 * L["out_cols"]).reshape(n_rb, ROWS_PER_BLOCK, 2 * L["out_cols"])
+        c0 = 0
+        for w in outlier_widths(n_out):
+            # record: (row 0..3, its w columns), row-major
+            pieces.append(v[:, :, 2 * c0:2 * (c0 + w)].reshape(n_rb, ROWS_PER_BLOCK * 2 * w))
+            c0 += w
     area = np.concatenate(pieces, axis=1)
     blob = np.zeros(L["total"], dtype=np.uint8)
     blob[L["area"]:L["area"] + area.size] = area.reshape(-1)
@@ -206,9 +219,11 @@ def _read_parts(blob: np.ndarray, kind: str):
         out.append(np.ascontiguousarray(p.reshape(n_rb * ROWS_PER_BLOCK, nrec * per_row)[:N]))
         off += w
     if n_out:
-        nor = h["out_recs"]
-        v = area[:, nrec * h["rec_bytes"]:].reshape(n_rb, nor, ROWS_PER_BLOCK, OUT_COLS * 2).transpose(0, 2, 1, 3)
-        v = v.reshape(n_rb * ROWS_PER_BLOCK, nor * OUT_COLS * 2)[:N, :2 * n_out]
+        cols, off = [], nrec * h["rec_bytes"]
+        for w in outlier_widths(n_out):
+            cols.append(area[:, off:off + ROWS_PER_BLOCK * 2 * w].reshape(n_rb, ROWS_PER_BLOCK, 2 * w))
+            off += ROWS_PER_BLOCK * 2 * w
+        v = np.concatenate(cols, axis=2).reshape(n_rb * ROWS_PER_BLOCK, -1)[:N, :2 * n_out]
         vals = np.ascontiguousarray(v).view("<f2").astype(F64)
         idx = np.ascontiguousarray(blob[h["idx"]:h["idx"] + 4 * n_out]).view("<i4").astype(np.int32)
     else:

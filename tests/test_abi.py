@@ -32,7 +32,7 @@ def test_status_strings(lbq):
     L = lbq.lib()
     for code, name in lbq.STATUS.items():
         assert L.lbq_status_string(code).decode().startswith(name)
-    assert L.lbq_format_version() == 1
+    assert L.lbq_format_version() == 2
 
 
 def test_host_argument_errors(lbq):

@@ -56,7 +56,9 @@ def _decode(blob):
         row = []
         for j in range(n_out):
             o, jj = divmod(j, 256)
-            off = area + rb * rb_bytes + recs * rec_bytes + o * out_rec_bytes + (r * 256 + jj) * 2
+            # full records are 256 columns wide; the last one holds the rest rounded up to 8
+            width = min(256, -(-n_out // 8) * 8 - 256 * o)
+            off = area + rb * rb_bytes + recs * rec_bytes + o * out_rec_bytes + (r * width + jj) * 2
             row.append(_f16_value(struct.unpack_from("<H", b, off)[0]))
         vals.append(row)
     return W, idx, vals

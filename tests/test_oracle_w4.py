@@ -124,7 +124,7 @@ def _golden_layout(g, key):
 def test_layout_golden(golden):
     g = golden("blob_layout_example.txt")
     for key, kind, N, K, n in (("w4_N3_K64_nout2", "w4", 3, 64, 2), ("w4_N5_K2112_nout0", "w4", 5, 2112, 0),
-                               ("w2_N2_K128_nout5", "w2", 2, 128, 5)):
+                               ("w2_N2_K128_nout5", "w2", 2, 128, 5), ("w2_N4_K4096_nout300", "w2", 4, 4096, 300)):
         want = _golden_layout(g, key)
         L = O.layout(kind, N, K, n)
         assert {k: L[k] for k in want} == want, key
