@@ -849,6 +849,7 @@ struct DeviceInfo {
     bool ok = false;
     int sms = 0;
     int max_smem = 0;          // opt-in maximum per CTA
+    unsigned* err_word = nullptr;   // device address of the error word
     bool attr_set[kNumVariantsMax] = {};
 };
 constexpr int kMaxDevices = 64;
@@ -868,6 +869,9 @@ lbq_status device_info(DeviceInfo** out) {
             cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return LBQ_ERR_CUDA;
+        void* ew = nullptr;
+        if (cudaGetSymbolAddress(&ew, g_lbq_error_word) != cudaSuccess) return LBQ_ERR_CUDA;
+        d.err_word = static_cast<unsigned*>(ew);
         d.ok = (major == 10 && minor == 3);
         d.init = true;
     }
@@ -1129,6 +1133,22 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
     const bool f32 = y_dtype == LBQ_F32;
     const int vi = kind == kW4 ? kVarW4 : kVarW2, vf = kind == kW4 ? kVarW4Narrow : kVarW2Narrow;
     if (M == 1) return launch_pass(dev, kind, vi, vf, P, count, 1, f32, stream, flags, launches);
+    // M >= 16 without outlier columns: the tensor-core kernel, one launch per problem
+    bool dense_only = true;
+    for (int i = 0; i < count; ++i) dense_only = dense_only && P[i].n_out == 0;
+    if (kind == kW4 && M >= 16 && dense_only) {
+        for (int i = 0; i < count; ++i) {
+            if (launches) {
+                ++*launches;
+                continue;
+            }
+            st = lbq::launch_w4_mma(P[i].packed, P[i].N, P[i].K, M, P[i].x, P[i].ldx, P[i].y, P[i].ldy, f32,
+                                    dev->err_word, dev->sms, dev->max_smem, stream,
+                                    i == 0 ? flags : (flags | LBQ_FLAG_PDL));
+            if (st != LBQ_OK) return st;
+        }
+        return LBQ_OK;
+    }
     int v = 1;
     while (v < 3 && variant(v).MB < M) ++v;
     for (; v >= 1; --v) {

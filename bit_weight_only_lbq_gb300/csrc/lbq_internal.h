@@ -3,6 +3,8 @@
 
 #include <cstdint>
 
+#include "lbq.h"
+
 #define LBQ_VERSION_NUM 100          // 0.1.0
 #define LBQ_FORMAT_VERSION_NUM 2
 
@@ -18,6 +20,12 @@ constexpr int kOutlierColAlign = 8;       // the last outlier record's width is 
 constexpr int kMaxM = 64;                 // largest batch of the small-M entry point
 
 uint16_t host_f64_to_f16(double v);
+
+// Tensor-core 4-bit GEMM for 16 <= M <= 64 without outlier columns (lbq_mma.cu);
+// err_word is the device error word of the library.
+lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
+                         int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
+                         uint32_t flags);
 double host_f16_to_f64(uint16_t h);
 
 }  // namespace lbq
