@@ -12,15 +12,16 @@
 //    range of its 1024-k blocks; the 32 records of a k-block arrive by 32 bulk
 //    copies into slots 2384 bytes apart (16 bytes of padding, so 8 consecutive
 //    slots start in 8 different shared-memory bank groups), double buffered;
-//  * per 64-k stage every thread dequantises one (row, group): nibbles masked
-//    with the FP16 magic 1024 (exact 1024 + q), minus (1024 + z), times the
-//    FP16 scale (one rounding) - written as 16-byte rows of the no-swizzle
-//    K-major core-matrix layout (8 rows x 16 bytes per core matrix) that the
-//    tensor core reads directly; the activations of the stage are staged in
-//    the same layout with the same permutation of k inside each group;
-//  * one thread issues tcgen05.mma (M = 128, N = 16..64 activation rows,
-//    K = 16, FP16 x FP16 -> FP32 in tensor memory) and tcgen05.commit to an
-//    mbarrier that frees the stage buffer (double buffered);
+//  * per 256-k stage every thread dequantises 4 groups of one weight row:
+//    nibbles masked with the FP16 magic 1024 (exact 1024 + q), minus (1024 + z),
+//    times the FP16 scale (one rounding), stored straight into its row (lane)
+//    of tensor memory with tcgen05.st - the A operand never touches shared
+//    memory; the activations of the stage are staged in shared memory in the
+//    no-swizzle K-major core-matrix layout (8 rows x 16 bytes per core matrix)
+//    with the same permutation of k inside each group;
+//  * one thread issues tcgen05.mma (A from tensor memory, M = 128 rows,
+//    N = 16..64 activation rows, K = 16, FP16 x FP16 -> FP32 in tensor memory)
+//    and tcgen05.commit to an mbarrier that frees the stage (double buffered);
 //  * when a tile's K is split over a cluster of CTAs, each CTA moves its FP32
 //    partial from tensor memory to shared memory and the cluster's rank 0 adds
 //    the partials in rank order through distributed shared memory
@@ -44,9 +45,8 @@ constexpr int kTileRows = 128;            // MMA M
 constexpr int kTileRb = kTileRows / 4;    // row blocks per tile
 constexpr int kRecBytes = 2368;           // 4-bit dense record
 constexpr int kSlot = 2384;               // shared-memory stride of a record slot
-constexpr int kStageK = 64;               // k per A/B stage
+constexpr int kStageK = 256;              // k per A/B stage (8 groups)
 constexpr int kStagesPerBlock = 1024 / kStageK;
-constexpr int kAStage = kTileRows * kStageK * 2;   // 16 KB
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct MmaArgs {
@@ -176,21 +176,25 @@ __device__ __forceinline__ uint4 x_chunk(const uint32_t (&n)[16], int j) {
 struct Smem {
     static constexpr int kRecBuf = kTileRb * kSlot;            // one k-block of records
     static constexpr int rec = 0;
-    static constexpr int a = 2 * kRecBuf;                      // 2 A stages
-    static constexpr int b = a + 2 * kAStage;                  // 2 B stages (size depends on NM)
-    static __host__ __device__ constexpr int bars(int nm) { return b + 2 * nm * kStageK * 2; }
+    static constexpr int b = 2 * kRecBuf;                      // 2 activation (B) stages
+    static __host__ __device__ constexpr int bstage(int nm) { return nm * kStageK * 2; }
+    static __host__ __device__ constexpr int bars(int nm) { return b + 2 * bstage(nm); }
     static __host__ __device__ constexpr int total(int nm) { return bars(nm) + 64 + 1024; }   // + alignment slack
 };
 
+// Tensor memory: columns [0, 64) the FP32 accumulator (128 lanes x N), then two
+// A stages of 128 columns (128 rows x 256 FP16 k, two k per 32-bit column).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcol = 128;
+
 template <int NM>
 __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a) {
-    constexpr int kCols = NM <= 32 ? 32 : 64;                  // tensor-memory columns (power of 2 >= 32)
-    constexpr int kBStage = NM * kStageK * 2;
+    constexpr int kBStage = Smem::bstage(NM);
+    constexpr int kSbo = (kStageK / 8) * 128;                   // bytes between 8-row groups of a B stage
     constexpr uint32_t kIdesc = idesc_f16(kTileRows, NM);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* recbuf = smem + Smem::rec;
-    uint8_t* abuf = smem + Smem::a;
     uint8_t* bbuf = smem + Smem::b;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars(NM));
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kCols)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -250,26 +254,34 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
 
-    // activation staging: thread < 2 NM takes activation row xa, group xg of the stage
-    const bool xt = tid < 2 * NM;
-    const int xg = tid / NM, xa = tid - xg * NM;
-    uint4 xr[4];
+    // activation staging: NM rows x 8 groups per stage; thread takes tasks
+    // tid, tid + 256, ... (row xa = task % NM, group task / NM)
+    constexpr int kXTasks = NM * (kStageK / 32);
+    constexpr int kXPer = (kXTasks + kThreads - 1) / kThreads;
+    uint4 xr[kXPer][4];
     auto load_x = [&](int kb, int s) {
-        const long long k = static_cast<long long>(kb) * 1024 + s * kStageK + xg * 32;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) xr[c] = make_uint4(0u, 0u, 0u, 0u);
-        if (xt && xa < a.M && k < a.K) {
-            const uint4* p = reinterpret_cast<const uint4*>(a.x + xa * a.ldx + k);
+        for (int u = 0; u < kXPer; ++u) {
+            const int task = tid + u * kThreads;
+            const int xg = task / NM, xa = task - xg * NM;
+            const long long k = static_cast<long long>(kb) * 1024 + s * kStageK + xg * 32;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) xr[c] = p[c];
+            for (int c = 0; c < 4; ++c) xr[u][c] = make_uint4(0u, 0u, 0u, 0u);
+            if (task < kXTasks && xa < a.M && k < a.K) {
+                const uint4* p = reinterpret_cast<const uint4*>(a.x + xa * a.ldx + k);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) xr[u][c] = p[c];
+            }
         }
     };
     if (nkb > 0) load_x(kb0, 0);
 
-    // dequant task: MMA row m = 32 (warp % 4) + lane is weight row
-    // 4 (8 (warp % 4) + lane % 8) + lane / 8 of the tile; group gi of the stage
-    const int qd = warp & 3, gi = warp >> 2;
+    // dequant tasks: thread owns MMA row m = 32 (warp % 4) + lane = weight row
+    // 4 (8 (warp % 4) + lane % 8) + lane / 8 of the tile (tensor-memory lane m)
+    // and groups 4 (warp / 4) .. + 3 of each stage
+    const int qd = warp & 3, gh = warp >> 2;
     const int slot = 8 * qd + (lane & 7), r = lane >> 3, m = 32 * qd + lane;
+    const uint32_t tlane = static_cast<uint32_t>(32 * qd) << 16;
 
     bool bad = false;
     int gs = 0;                                   // stages issued to the tensor core
@@ -284,29 +296,37 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
         for (int s = 0; s < kStagesPerBlock; ++s, ++gs) {
             const int ab = gs & 1;
             if (gs >= 2 && !mbar_wait(mdone0 + 8 * ab, ((gs - 2) >> 1) & 1, kWaitLimitNs)) bad = true;
-            uint8_t* A = abuf + ab * kAStage;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             uint8_t* B = bbuf + ab * kBStage;
             // activations of this stage (prefetched), then prefetch the next stage's
-            if (xt) {
-                uint32_t n[16];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    n[4 * c + 0] = xr[c].x;
-                    n[4 * c + 1] = xr[c].y;
-                    n[4 * c + 2] = xr[c].z;
-                    n[4 * c + 3] = xr[c].w;
+            for (int u = 0; u < kXPer; ++u) {
+                const int task = tid + u * kThreads;
+                if (task < kXTasks) {
+                    const int xg = task / NM, xa = task - xg * NM;
+                    uint32_t n[16];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        n[4 * c + 0] = xr[u][c].x;
+                        n[4 * c + 1] = xr[u][c].y;
+                        n[4 * c + 2] = xr[u][c].z;
+                        n[4 * c + 3] = xr[u][c].w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(B + (xa >> 3) * kSbo + (4 * xg + j) * 128 + (xa & 7) * 16) =
+                            x_chunk(n, j);
                 }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(B + (xa >> 3) * 1024 + (4 * xg + j) * 128 + (xa & 7) * 16) = x_chunk(n, j);
             }
             if (s + 1 < kStagesPerBlock)
                 load_x(kb0 + b, s + 1);
             else if (b + 1 < nkb)
                 load_x(kb0 + b + 1, 0);
-            // weights: one (row, group) per thread
-            {
-                const int g = 2 * s + gi;
+            // weights: 4 groups of row m into tensor memory, 16 columns each
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int gi = 4 * gh + t;                       // group of the stage
+                const int g = (kStageK / 32) * s + gi;           // group of the record
                 const uint4 q = *reinterpret_cast<const uint4*>(rec + (r * 32 + g) * 16);
                 const uint32_t sb = *reinterpret_cast<const unsigned short*>(rec + 2048 + (r * 32 + g) * 2);
                 const uint32_t zb = rec[2304 + r * 16 + (g >> 1)];
@@ -314,26 +334,33 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
                 const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
                 const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
                 const uint32_t s2 = sb * 0x00010001u;
+                uint4 o[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(A + (m >> 3) * 1024 + (4 * gi + j) * 128 + (m & 7) * 16) =
-                        dequant_word(u4w(q, j), zlo2, zhi2, s2);
+                for (int j = 0; j < 4; ++j) o[j] = dequant_word(u4w(q, j), zlo2, zhi2, s2);
+                asm volatile(
+                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                    "%12, %13, %14, %15, %16};" ::"r"(tmem + tlane + kAcol + 128u * ab + 16u * gi),
+                    "r"(o[0].x), "r"(o[0].y), "r"(o[0].z), "r"(o[0].w), "r"(o[1].x), "r"(o[1].y), "r"(o[1].z),
+                    "r"(o[1].w), "r"(o[2].x), "r"(o[2].y), "r"(o[2].z), "r"(o[2].w), "r"(o[3].x), "r"(o[3].y),
+                    "r"(o[3].z), "r"(o[3].w)
+                    : "memory");
             }
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             bad = __syncthreads_or(bad);
             if (bad) break;
             if (tid == 0) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+                const uint32_t b0 = smem_u32(B);
 #pragma unroll
                 for (int ks = 0; ks < kStageK / 16; ++ks) {
-                    const uint64_t da = smem_desc(a0 + ks * 256, 128, 1024);
-                    const uint64_t db = smem_desc(b0 + ks * 256, 128, 1024);
+                    const uint64_t db = smem_desc(b0 + ks * 256, 128, kSbo);
                     const uint32_t acc = (gs > 0 || ks > 0) ? 1u : 0u;
                     asm volatile(
                         "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-                        "l"(da), "l"(db), "r"(kIdesc), "r"(acc)
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+                        "r"(tmem + kAcol + 128u * ab + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
                         : "memory");
                 }
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -426,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
     __syncthreads();
     if (warp == 0) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
