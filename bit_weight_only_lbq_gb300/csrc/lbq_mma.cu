@@ -179,7 +179,7 @@ struct Smem {
     static constexpr int b = 2 * kRecBuf;                      // 2 activation (B) stages
     static __host__ __device__ constexpr int bstage(int nm) { return nm * kStageK * 2; }
     static __host__ __device__ constexpr int bars(int nm) { return b + 2 * bstage(nm); }
-    static __host__ __device__ constexpr int total(int nm) { return bars(nm) + 64 + 1024; }   // + alignment slack
+    static __host__ __device__ constexpr int total(int nm) { return bars(nm) + 128 + 1024; }   // + alignment slack
 };
 
 // Tensor memory: columns [0, 64) the FP32 accumulator (128 lanes x N), then two
@@ -188,19 +188,25 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAcol = 128;
 
 template <int NM>
-__global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a) {
+__global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a) {
     constexpr int kBStage = Smem::bstage(NM);
     constexpr int kSbo = (kStageK / 8) * 128;                   // bytes between 8-row groups of a B stage
     constexpr uint32_t kIdesc = idesc_f16(kTileRows, NM);
+    constexpr int kWorkerWarps = kThreads / 32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* recbuf = smem + Smem::rec;
     uint8_t* bbuf = smem + Smem::b;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars(NM));
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
-    const uint32_t full0 = smem_u32(bars + 0), mdone0 = smem_u32(bars + 2), last_bar = smem_u32(bars + 4);
+    // mbarriers: full[2] records landed, ready[2] stage written, mdone[2] stage
+    // consumed by the tensor core, rfree[2] record buffer read, last
+    const uint32_t full0 = smem_u32(bars + 0), ready0 = smem_u32(bars + 2), mdone0 = smem_u32(bars + 4),
+                   rfree0 = smem_u32(bars + 6), last_bar = smem_u32(bars + 8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 10);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool mma_warp = warp == kWorkerWarps;                 // warp 8: copies and tensor-core issue
     const int S = a.S;
     const int rank = static_cast<int>(blockIdx.x) % S;         // rank in the cluster (cluster = S consecutive CTAs)
     const int tile = static_cast<int>(blockIdx.x) / S;
@@ -208,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
     const int nkb = kb1 - kb0;
     const int rb0 = tile * kTileRb;
     const int nvalid = min(kTileRb, a.n_rb - rb0);
+    const int nstages = nkb * kStagesPerBlock;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -216,8 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bars + i)) : "memory");
+        const uint32_t counts[9] = {1, 1, kWorkerWarps, kWorkerWarps, 1, 1, kWorkerWarps, kWorkerWarps, 1};
+        for (int i = 0; i < 9; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bars + i)), "r"(counts[i]) : "memory");
+        *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -225,164 +234,200 @@ __global__ void __launch_bounds__(kThreads, 1) lbq_w4_mma_kernel(const __grid_co
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_slot;
 
-    uint64_t policy;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-    // the 32 records of k-block kb into record buffer bi: warp 0, one copy per lane
-    auto issue_block = [&](int kb, int bi) {
-        const uint32_t bar = full0 + 8 * bi;
-        if (lane == 0)
-            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                         "r"(static_cast<uint32_t>(nvalid * kRecBytes))
-                         : "memory");
-        __syncwarp();
-        if (lane < nvalid) {
-            const uint8_t* src = a.area + static_cast<long long>(rb0 + lane) * a.rb_bytes +
-                                 static_cast<long long>(kb) * kRecBytes;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(recbuf + bi * Smem::kRecBuf + lane * kSlot)),
-                "l"(src), "r"(static_cast<uint32_t>(kRecBytes)), "r"(bar), "l"(policy)
-                : "memory");
+    // bounded wait that gives up at once after any thread of the CTA gave up
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(bar, parity)) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
+                return false;
+            }
+            __nanosleep(128);
         }
+        return true;
     };
-    int issued = 0;
-    if (warp == 0) {
-        if (nkb > 0) issue_block(kb0, 0);
-        if (nkb > 1) issue_block(kb0 + 1, 1);
-    }
-    issued = nkb < 2 ? nkb : 2;
+    auto arrive = [&](uint32_t bar) {
+        asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    };
+
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
-
-    // activation staging: NM rows x 8 groups per stage; thread takes tasks
-    // tid, tid + 256, ... (row xa = task % NM, group task / NM)
-    constexpr int kXTasks = NM * (kStageK / 32);
-    constexpr int kXPer = (kXTasks + kThreads - 1) / kThreads;
-    uint4 xr[kXPer][4];
-    auto load_x = [&](int kb, int s) {
-#pragma unroll
-        for (int u = 0; u < kXPer; ++u) {
-            const int task = tid + u * kThreads;
-            const int xg = task / NM, xa = task - xg * NM;
-            const long long k = static_cast<long long>(kb) * 1024 + s * kStageK + xg * 32;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) xr[u][c] = make_uint4(0u, 0u, 0u, 0u);
-            if (task < kXTasks && xa < a.M && k < a.K) {
-                const uint4* p = reinterpret_cast<const uint4*>(a.x + xa * a.ldx + k);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) xr[u][c] = p[c];
-            }
-        }
-    };
-    if (nkb > 0) load_x(kb0, 0);
-
-    // dequant tasks: thread owns MMA row m = 32 (warp % 4) + lane = weight row
-    // 4 (8 (warp % 4) + lane % 8) + lane / 8 of the tile (tensor-memory lane m)
-    // and groups 4 (warp / 4) .. + 3 of each stage
-    const int qd = warp & 3, gh = warp >> 2;
-    const int slot = 8 * qd + (lane & 7), r = lane >> 3, m = 32 * qd + lane;
-    const uint32_t tlane = static_cast<uint32_t>(32 * qd) << 16;
-
-    bool bad = false;
-    int gs = 0;                                   // stages issued to the tensor core
-    int consumed = 0;                             // k-blocks whose copies have landed
-    for (int b = 0; b < nkb && !bad; ++b) {
-        const int bi = b & 1;
-        if (!mbar_wait(full0 + 8 * bi, (b >> 1) & 1, kWaitLimitNs))
-            bad = true;
-        else
-            consumed = b + 1;
-        const uint8_t* rec = recbuf + bi * Smem::kRecBuf + slot * kSlot;
-        for (int s = 0; s < kStagesPerBlock; ++s, ++gs) {
-            const int ab = gs & 1;
-            if (gs >= 2 && !mbar_wait(mdone0 + 8 * ab, ((gs - 2) >> 1) & 1, kWaitLimitNs)) bad = true;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            uint8_t* B = bbuf + ab * kBStage;
-            // activations of this stage (prefetched), then prefetch the next stage's
-#pragma unroll
-            for (int u = 0; u < kXPer; ++u) {
-                const int task = tid + u * kThreads;
-                if (task < kXTasks) {
-                    const int xg = task / NM, xa = task - xg * NM;
-                    uint32_t n[16];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        n[4 * c + 0] = xr[u][c].x;
-                        n[4 * c + 1] = xr[u][c].y;
-                        n[4 * c + 2] = xr[u][c].z;
-                        n[4 * c + 3] = xr[u][c].w;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4*>(B + (xa >> 3) * kSbo + (4 * xg + j) * 128 + (xa & 7) * 16) =
-                            x_chunk(n, j);
-                }
-            }
-            if (s + 1 < kStagesPerBlock)
-                load_x(kb0 + b, s + 1);
-            else if (b + 1 < nkb)
-                load_x(kb0 + b + 1, 0);
-            // weights: 4 groups of row m into tensor memory, 16 columns each
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int gi = 4 * gh + t;                       // group of the stage
-                const int g = (kStageK / 32) * s + gi;           // group of the record
-                const uint4 q = *reinterpret_cast<const uint4*>(rec + (r * 32 + g) * 16);
-                const uint32_t sb = *reinterpret_cast<const unsigned short*>(rec + 2048 + (r * 32 + g) * 2);
-                const uint32_t zb = rec[2304 + r * 16 + (g >> 1)];
-                const uint32_t z = (g & 1) ? (zb >> 4) : (zb & 15u);
-                const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
-                const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
-                const uint32_t s2 = sb * 0x00010001u;
-                uint4 o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) o[j] = dequant_word(u4w(q, j), zlo2, zhi2, s2);
+    if (mma_warp) {
+        // ---------------------------------------------------------------- copies + tensor-core issue
+        uint64_t policy;
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+        auto issue_block = [&](int kb, int bi) {
+            const uint32_t bar = full0 + 8 * bi;
+            if (lane == 0)
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                             "r"(static_cast<uint32_t>(nvalid * kRecBytes))
+                             : "memory");
+            __syncwarp();
+            if (lane < nvalid) {
+                const uint8_t* src = a.area + static_cast<long long>(rb0 + lane) * a.rb_bytes +
+                                     static_cast<long long>(kb) * kRecBytes;
                 asm volatile(
-                    "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                    "%12, %13, %14, %15, %16};" ::"r"(tmem + tlane + kAcol + 128u * ab + 16u * gi),
-                    "r"(o[0].x), "r"(o[0].y), "r"(o[0].z), "r"(o[0].w), "r"(o[1].x), "r"(o[1].y), "r"(o[1].z),
-                    "r"(o[1].w), "r"(o[2].x), "r"(o[2].y), "r"(o[2].z), "r"(o[2].w), "r"(o[3].x), "r"(o[3].y),
-                    "r"(o[3].z), "r"(o[3].w)
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                    " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(recbuf + bi * Smem::kRecBuf + lane * kSlot)),
+                    "l"(src), "r"(static_cast<uint32_t>(kRecBytes)), "r"(bar), "l"(policy)
                     : "memory");
             }
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            bad = __syncthreads_or(bad);
-            if (bad) break;
-            if (tid == 0) {
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t b0 = smem_u32(B);
+        };
+        int issued = 0;
+        for (; issued < 2 && issued < nkb; ++issued) issue_block(kb0 + issued, issued);
+        for (int gs = 0; gs < nstages; ++gs) {
+            const int ab = gs & 1;
+            const bool ok = wait(ready0 + 8 * ab, (gs >> 1) & 1);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (lane == 0) {
+                if (ok && !*abort_flag) {
+                    const uint32_t b0 = smem_u32(bbuf + ab * kBStage);
 #pragma unroll
-                for (int ks = 0; ks < kStageK / 16; ++ks) {
-                    const uint64_t db = smem_desc(b0 + ks * 256, 128, kSbo);
-                    const uint32_t acc = (gs > 0 || ks > 0) ? 1u : 0u;
-                    asm volatile(
-                        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
-                        "r"(tmem + kAcol + 128u * ab + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
-                        : "memory");
+                    for (int ks = 0; ks < kStageK / 16; ++ks) {
+                        const uint64_t db = smem_desc(b0 + ks * 256, 128, kSbo);
+                        const uint32_t acc = (gs > 0 || ks > 0) ? 1u : 0u;
+                        asm volatile(
+                            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+                            "r"(tmem + kAcol + 128u * ab + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
+                            : "memory");
+                    }
                 }
+                // always commit, so the workers' waits on this stage complete
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                                  mdone0 + 8 * ab)
                              : "memory");
             }
+            __syncwarp();
+            // after the last stage of k-block b: refill its record buffer with k-block b + 2
+            if ((gs + 1) % kStagesPerBlock == 0) {
+                const int b = gs / kStagesPerBlock;
+                const bool freed = wait(rfree0 + 8 * (b & 1), (b >> 1) & 1);
+                if (freed && !*abort_flag && issued < nkb) {
+                    issue_block(kb0 + issued, issued & 1);
+                    ++issued;
+                }
+            }
         }
-        // every thread is past its reads of record buffer bi: refill it
-        if (!bad && warp == 0 && b + 2 < nkb) issue_block(kb0 + b + 2, bi);
-        if (!bad && b + 2 < nkb) ++issued;
+        if (lane == 0)   // tracks every tensor-core operation issued before it
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(last_bar)
+                         : "memory");
+        __syncwarp();
+        // drain: copies issued but never waited for by the workers (only after an abort)
+        if (*abort_flag)
+            for (int b = 0; b < issued; ++b) mbar_wait(full0 + 8 * (b & 1), (b >> 1) & 1, kWaitLimitNs / 8);
+    } else {
+        // ---------------------------------------------------------------- workers: activations + dequantisation
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
+        // activation staging: NM rows x 8 groups per stage; thread takes tasks
+        // tid, tid + 256, ... (row xa = task % NM, group task / NM)
+        constexpr int kXTasks = NM * (kStageK / 32);
+        constexpr int kXPer = (kXTasks + kThreads - 1) / kThreads;
+        uint4 xr[kXPer][4];
+        auto load_x = [&](int kb, int s) {
+#pragma unroll
+            for (int u = 0; u < kXPer; ++u) {
+                const int task = tid + u * kThreads;
+                const int xg = task / NM, xa = task - xg * NM;
+                const long long k = static_cast<long long>(kb) * 1024 + s * kStageK + xg * 32;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) xr[u][c] = make_uint4(0u, 0u, 0u, 0u);
+                if (task < kXTasks && xa < a.M && k < a.K) {
+                    const uint4* p = reinterpret_cast<const uint4*>(a.x + xa * a.ldx + k);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) xr[u][c] = p[c];
+                }
+            }
+        };
+        if (nkb > 0) load_x(kb0, 0);
+        // dequant tasks: thread owns MMA row m = 32 (warp % 4) + lane = weight row
+        // 4 (8 (warp % 4) + lane % 8) + lane / 8 of the tile (tensor-memory lane m)
+        // and groups 4 (warp / 4) .. + 3 of each stage
+        const int qd = warp & 3, gh = warp >> 2;
+        const int slot = 8 * qd + (lane & 7), r = lane >> 3;
+        const uint32_t tlane = static_cast<uint32_t>(32 * qd) << 16;
+        int gs = 0;
+        for (int b = 0; b < nkb; ++b) {
+            const int bi = b & 1;
+            const bool have = wait(full0 + 8 * bi, (b >> 1) & 1);
+            const uint8_t* rec = recbuf + bi * Smem::kRecBuf + slot * kSlot;
+            for (int s = 0; s < kStagesPerBlock; ++s, ++gs) {
+                const int ab = gs & 1;
+                bool ok = have;
+                if (gs >= 2) ok = wait(mdone0 + 8 * ab, ((gs - 2) >> 1) & 1) && ok;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (ok && !*abort_flag) {
+                    uint8_t* B = bbuf + ab * kBStage;
+                    // activations of this stage (prefetched), then prefetch the next stage's
+#pragma unroll
+                    for (int u = 0; u < kXPer; ++u) {
+                        const int task = tid + u * kThreads;
+                        if (task < kXTasks) {
+                            const int xg = task / NM, xa = task - xg * NM;
+                            uint32_t n[16];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                n[4 * c + 0] = xr[u][c].x;
+                                n[4 * c + 1] = xr[u][c].y;
+                                n[4 * c + 2] = xr[u][c].z;
+                                n[4 * c + 3] = xr[u][c].w;
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                *reinterpret_cast<uint4*>(B + (xa >> 3) * kSbo + (4 * xg + j) * 128 + (xa & 7) * 16) =
+                                    x_chunk(n, j);
+                        }
+                    }
+                    if (s + 1 < kStagesPerBlock)
+                        load_x(kb0 + b, s + 1);
+                    else if (b + 1 < nkb)
+                        load_x(kb0 + b + 1, 0);
+                    // weights: 4 groups of row m into tensor memory, 16 columns each
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int gi = 4 * gh + t;                       // group of the stage
+                        const int g = (kStageK / 32) * s + gi;           // group of the record
+                        const uint4 q = *reinterpret_cast<const uint4*>(rec + (r * 32 + g) * 16);
+                        const uint32_t sb = *reinterpret_cast<const unsigned short*>(rec + 2048 + (r * 32 + g) * 2);
+                        const uint32_t zb = rec[2304 + r * 16 + (g >> 1)];
+                        const uint32_t z = (g & 1) ? (zb >> 4) : (zb & 15u);
+                        const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
+                        const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
+                        const uint32_t s2 = sb * 0x00010001u;
+                        uint4 o[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) o[j] = dequant_word(u4w(q, j), zlo2, zhi2, s2);
+                        asm volatile(
+                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+                            "%11, %12, %13, %14, %15, %16};" ::"r"(tmem + tlane + kAcol + 128u * ab + 16u * gi),
+                            "r"(o[0].x), "r"(o[0].y), "r"(o[0].z), "r"(o[0].w), "r"(o[1].x), "r"(o[1].y), "r"(o[1].z),
+                            "r"(o[1].w), "r"(o[2].x), "r"(o[2].y), "r"(o[2].z), "r"(o[2].w), "r"(o[3].x), "r"(o[3].y),
+                            "r"(o[3].z), "r"(o[3].w)
+                            : "memory");
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    if (s + 1 == kStagesPerBlock) arrive(rfree0 + 8 * bi);  // this warp is done with the records
+                    arrive(ready0 + 8 * ab);
+                }
+            }
+        }
     }
-    // drain: copies issued but not consumed, and the tensor-core work
-    if (bad) {
-        if (tid == 0) atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
-        for (int b = consumed; b < issued; ++b) mbar_wait(full0 + 8 * (b & 1), (b >> 1) & 1, kWaitLimitNs / 8);
-    }
-    if (tid == 0 && gs > 0)
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(last_bar)
-                     : "memory");
-    bool got = gs == 0 || mbar_wait(last_bar, 0, kWaitLimitNs);
+    // the accumulator is complete once the last commit has arrived
+    const bool got = nstages == 0 || mbar_wait(last_bar, 0, kWaitLimitNs);
     if (!got && tid == 0) atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
-    bad = __syncthreads_or(bad || !got);
+    __syncthreads();
+    const bool bad = *abort_flag != 0 || !got;
+    const int gs = nstages;
+    const int qd = warp & 3;
+    const int m = 32 * qd + lane;
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
     // epilogue: warps 0-3 read rows 32 w .. 32 w + 31 of the accumulator
@@ -509,7 +554,7 @@ lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const 
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(tiles * S));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreads + 32);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
