@@ -290,6 +290,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="lbq", choices=["lbq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep70b", action="store_true", help="skip the Llama-3-70B weight sweep detail")
     ap.add_argument("--single", default=None,
                     help="kind:N:K:n_out:M - time one kernel configuration alone (profiling aid), "
                          "kind in w4, w2, w4m")
@@ -416,6 +417,9 @@ def main():
         g = capture(lambda: [launch(lbq, e, b, xs[i], ys[i], pdl=True) for b in blobs])
         per_call.append(time_graph(g, len(blobs), replays))
         del g, extra
+    sweep70b = None
+    if not args.no_sweep70b:
+        sweep70b = run_sweep70b(lbq, dev, stream)
     clocks.stop()
     assert lbq.device_error(stream) == 0
 
@@ -486,7 +490,8 @@ def main():
                        "llama3_8b_w4_32_layers_from_per_call": round(
                            1.0 / (32 * sum(statistics.median(per_call[i]) for i, e in enumerate(layer)
                                            if e["kind"] == "w4") * 1e-3), 1)},
-                   "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes},
+                   "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes,
+                   "llama3_70b_sweep": sweep70b},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layer)
@@ -495,6 +500,79 @@ def main():
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+def run_sweep70b(lbq, dev, stream, replays=5):
+    """Config 5: one decode token through every linear of a Llama-3-70B-shaped
+    model (80 layers x 7 linears + lm_head, W4A16 G32, M = 1): 40.2 GB of packed
+    weights streamed per token.  One layer is packed on the host (seeded, config
+    5 distribution) and replicated 80 times in device memory, so every layer
+    reads its own bytes; the lm_head is packed separately.  Timed as 81 grouped
+    launches per token (one per layer, one for the lm_head) and as 561
+    single-matrix launches, each captured in a CUDA graph with PDL chaining."""
+    import torch
+    t_pack = time.time()
+    layer = []
+    for li, (name, N, K) in enumerate(synth.LLAMA3_70B_LINEARS):
+        W = synth.weights_heavy_cols(N, K, config_id=5, layer_id=li)
+        layer.append((name, N, K, torch.from_numpy(lbq.pack_w4(W)).to(dev)))
+        del W
+    hn, hN, hK = synth.LLAMA3_70B_LM_HEAD
+    W = synth.weights_heavy_cols(hN, hK, config_id=5, layer_id=99)
+    head = torch.from_numpy(lbq.pack_w4(W)).to(dev)
+    del W
+    t_pack = time.time() - t_pack
+    layers = [[b for (_, _, _, b) in layer]] + [[b.clone() for (_, _, _, b) in layer]
+                                                for _ in range(synth.LLAMA3_70B_LAYERS - 1)]
+    xs = {K: torch.from_numpy(synth.activations(1, K, config_id=5, layer_id=K)[0]).to(dev)
+          for K in sorted({K for (_, _, K, _) in layer} | {hK})}
+    ys = [torch.empty(N, dtype=torch.float16, device=dev) for (_, N, _, _) in layer]
+    yh = torch.empty(hN, dtype=torch.float16, device=dev)
+    total = sum(algorithmic_bytes("w4", N, K, 0) for (_, N, K, _) in layer) * synth.LLAMA3_70B_LAYERS + \
+        algorithmic_bytes("w4", hN, hK, 0)
+
+    def token_grouped():
+        for blobs in layers:
+            lbq.gemv_grouped(lbq.LBQ_KIND_W4, [(blobs[i], N, K, 0, xs[K], ys[i])
+                                               for i, (_, N, K, _) in enumerate(layer)], pdl=True)
+        lbq.gemv_w4a16(head, hN, hK, 0, xs[hK], yh, pdl=True)
+
+    def token_per_call():
+        for blobs in layers:
+            for i, (_, N, K, _) in enumerate(layer):
+                lbq.gemv_w4a16(blobs[i], N, K, 0, xs[K], ys[i], pdl=True)
+        lbq.gemv_w4a16(head, hN, hK, 0, xs[hK], yh, pdl=True)
+
+    out = {"workload": "llama3_70b decode weight sweep: 80 x (q 8192x8192, k/v 1024x8192, o 8192x8192, gate/up "
+                       "28672x8192, down 8192x28672) + lm_head 128256x8192, W4A16 G32, M=1, one token",
+           "bytes_per_token": total, "host_pack_s": round(t_pack, 1),
+           "note": "one packed layer replicated 80x in HBM (each layer streams its own copy)"}
+    for label, fn, launches in (("fused_layer_sweeps", token_grouped, synth.LLAMA3_70B_LAYERS + 1),
+                                ("per_call", token_per_call, synth.LLAMA3_70B_LAYERS * 7 + 1)):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(replays):
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_))
+        ms = statistics.median(ts)
+        out[label] = {"us_per_token": round(ms * 1e3, 1), "GB_s": round(total / (ms * 1e-3) / 1e9, 1),
+                      "tokens_per_s": round(1e3 / ms, 1), "launches_per_token": launches}
+        del g
+    assert lbq.device_error(stream) == 0
+    del layers, head, layer
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_single(args):

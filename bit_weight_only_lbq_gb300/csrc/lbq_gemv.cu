@@ -840,6 +840,18 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     }
 }
 
+// Self-test of the bounded wait every kernel uses: one thread waits on an
+// mbarrier that nothing ever arrives on; after `limit_ns` the wait gives up, the
+// error word records LBQ_ERR_TIMEOUT and the kernel returns normally.
+__global__ void lbq_wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (!mbar_wait_bounded(&bar, 0, limit_ns)) record_error(LBQ_ERR_TIMEOUT);
+    }
+}
+
 // ------------------------------------------------------------ host helpers
 
 constexpr int kNumVariantsMax = 8;
@@ -1233,6 +1245,16 @@ lbq_status lbq_gemv_grouped_launches(lbq_kind kind, const lbq_problem* problems,
     const lbq_status st = grouped(kind, problems, count, M, y_dtype, nullptr, 0u, &n);
     *launches = st == LBQ_OK ? n : 0;
     return st;
+}
+
+lbq_status lbq_selftest_wait_timeout(uint32_t limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 5000000u) return LBQ_ERR_SHAPE;
+    DeviceInfo* dev = nullptr;
+    lbq_status st = device_info(&dev);
+    if (st != LBQ_OK) return st;
+    lbq_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_us) * 1000ull);
+    if (cudaGetLastError() != cudaSuccess) return LBQ_ERR_CUDA;
+    return LBQ_OK;
 }
 
 lbq_status lbq_device_error(void* stream) {

@@ -37,7 +37,7 @@ EXPORTS = (
     "lbq_select_outliers_impact", "lbq_pack_w4", "lbq_pack_w2cb", "lbq_gemv_w4a16",
     "lbq_gemv_w2cb_outlier", "lbq_gemm_w4a16_smallM", "lbq_gemv_w4a16_ex",
     "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
-    "lbq_device_error",
+    "lbq_selftest_wait_timeout", "lbq_device_error",
 )
 
 
@@ -104,6 +104,7 @@ def lib():
                                                 c_vp, c_u32]),
             "lbq_gemv_grouped_launches": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(Problem), c_i32, c_i32,
                                                          ctypes.c_int, ctypes.POINTER(c_i32)]),
+            "lbq_selftest_wait_timeout": (ctypes.c_int, [c_u32, c_vp]),
             "lbq_device_error": (ctypes.c_int, [c_vp]),
         }
         for name, (res, args) in sig.items():
@@ -272,6 +273,10 @@ def gemv_grouped_launches(kind: int, problems, M: int = 1, y_dtype: int | None =
     _check(lib().lbq_gemv_grouped_launches(kind, arr, len(problems), M, yd, ctypes.byref(n)),
            "lbq_gemv_grouped_launches")
     return n.value
+
+
+def selftest_wait_timeout(limit_us: int, stream=None):
+    _check(lib().lbq_selftest_wait_timeout(limit_us, _stream(stream)), "lbq_selftest_wait_timeout")
 
 
 def device_error(stream=None) -> int:

@@ -251,6 +251,16 @@ lbq_status lbq_gemv_grouped(lbq_kind kind, const lbq_problem* problems, int32_t 
 lbq_status lbq_gemv_grouped_launches(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
                                      lbq_dtype y_dtype, int32_t* launches);
 
+/* Self-test of the failure path shared by every kernel: launches one tiny
+ * kernel whose single thread waits, with the same bounded mbarrier wait the
+ * GEMV kernels use, on an mbarrier that nothing ever completes.  After
+ * limit_us microseconds (1 .. 5,000,000) the wait gives up, LBQ_ERR_TIMEOUT
+ * is recorded in the device error word and the kernel returns normally, so
+ * the context stays usable; lbq_device_error() then reports it.  No trap,
+ * no fault.  Errors: LBQ_ERR_SHAPE (limit out of range), LBQ_ERR_CUDA,
+ * LBQ_ERR_UNSUPPORTED. */
+lbq_status lbq_selftest_wait_timeout(uint32_t limit_us, void* stream);
+
 /* Synchronise the stream, then return and clear the device-side error word of
  * the current device (LBQ_OK when no kernel recorded an error).  Errors from
  * the synchronisation itself are reported as LBQ_ERR_CUDA. */
