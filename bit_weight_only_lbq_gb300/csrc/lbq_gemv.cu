@@ -71,7 +71,9 @@ struct Rec {
     static constexpr int kOff1 = kTR * 32 * kPacked;                   // scales / S
     static constexpr int kOff2 = kOff1 + kTR * 32 * 2;                 // zeros / Z
     static constexpr int kBytes = kOff2 + (KIND == kW4 ? kTR * 16 : kTR * 32 * 2);   // 2368 / 1536
-    static constexpr int kStage = kBytes > kOutRecBytes ? kBytes : kOutRecBytes;    // multiple of 16
+    // a stage holds one item: RPI consecutive records of a row block, or one outlier record
+    template <int RPI>
+    static __host__ __device__ constexpr int stage() { return RPI * kBytes > kOutRecBytes ? RPI * kBytes : kOutRecBytes; }
     static constexpr uint32_t kMagicLo = 0x5751424Cu;                            // "LBQW"
     static constexpr uint32_t kMagicHi = KIND == kW4 ? 0x32334734u : 0x32334332u;  // "4G32" / "2C32"
 };
@@ -430,9 +432,10 @@ __device__ __forceinline__ float reduce_rows4(const float (&acc)[4], int lane) {
 
 __device__ __forceinline__ int unit_end(const GroupArgs& a, int q) { return q + 1 < a.count ? a.p[q + 1].ub : a.nunits; }
 
-template <int KIND, int MB, int NW>
+template <int KIND, int MB, int NW, int RPI>
 __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_constant__ GroupArgs a) {
     using RC = Rec<KIND>;
+    constexpr int kStage = RC::template stage<RPI>();
     constexpr int kThreads = NW * 32;
     constexpr float kUnit = KIND == kW4 ? 5.9604644775390625e-8f : 1.f;   // 2^-24 for the 4-bit products
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -441,7 +444,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     // M = 1 kernels always run 2 stages per warp (the host plans exactly that)
     const int SPW = MB == 1 ? kStagesM1 : a.SPW;
-    const FixedPlan P = fixed_plan(NW, RC::kStage, SPW, MB, a.rb_cap);
+    const FixedPlan P = fixed_plan(NW, kStage, SPW, MB, a.rb_cap);
     float* yacc = reinterpret_cast<float*>(smem + P.yacc);
     float* part = reinterpret_cast<float*>(smem + P.part);
     int* seg = reinterpret_cast<int*>(smem + P.seg);
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     if (R > 0)
         for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) {
             const int lo = max(u0, a.p[q].ub), hi = min(u1, unit_end(a, q));
-            n_items += (hi - lo) * (a.p[q].recs + a.p[q].OT);
+            n_items += (hi - lo) * ((a.p[q].recs + RPI - 1) / RPI + a.p[q].OT);
             ++np;
         }
     // this warp's contiguous share of the items, and where it starts
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         int before = 0;
         for (;;) {
             const int lo = max(u0, a.p[s_q].ub), hi = min(u1, unit_end(a, s_q));
-            const int TPR = a.p[s_q].recs + a.p[s_q].OT;
+            const int TPR = (a.p[s_q].recs + RPI - 1) / RPI + a.p[s_q].OT;
             const int items = (hi - lo) * TPR;
             if (ib < before + items) {
                 const int j = ib - before;
@@ -486,31 +489,33 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         }
     }
     uint64_t* my_bars = reinterpret_cast<uint64_t*>(smem + P.bars) + warp * SPW;
-    uint8_t* my_ring = smem + P.ring + warp * SPW * RC::kStage;
+    uint8_t* my_ring = smem + P.ring + warp * SPW * kStage;
 
     // issue pointer (warp-uniform; only lane 0 executes the copies): problem,
     // row block, item, source address, slot
     int i_q = s_q, i_u = s_u, i_kk = s_kk, i_slot = 0;
-    int i_recs = a.p[s_q].recs, i_TPR = i_recs + a.p[s_q].OT, i_uend = min(u1, unit_end(a, s_q));
+    int i_recs = a.p[s_q].recs, i_di = (i_recs + RPI - 1) / RPI, i_TPR = i_di + a.p[s_q].OT;
+    int i_uend = min(u1, unit_end(a, s_q));
     int i_last = a.p[s_q].out_last;
     const uint8_t* i_src = a.p[s_q].area + static_cast<long long>(s_u - a.p[s_q].ub) * a.p[s_q].rb_bytes +
-                           (s_kk < i_recs ? static_cast<long long>(s_kk) * RC::kBytes
-                                          : static_cast<long long>(i_recs) * RC::kBytes +
-                                                static_cast<long long>(s_kk - i_recs) * kOutRecBytes);
+                           (s_kk < i_di ? static_cast<long long>(s_kk) * RPI * RC::kBytes
+                                        : static_cast<long long>(i_recs) * RC::kBytes +
+                                              static_cast<long long>(s_kk - i_di) * kOutRecBytes);
     const uint64_t policy = policy_evict_first();
     const uint32_t ring_u32 = smem_u32(my_ring), bars_u32 = smem_u32(my_bars);
     auto issue_next = [&](bool more) {
-        const uint32_t bytes = i_kk < i_recs        ? static_cast<uint32_t>(RC::kBytes)
+        const uint32_t bytes = i_kk < i_di         ? static_cast<uint32_t>(min(RPI, i_recs - i_kk * RPI) * RC::kBytes)
                                : i_kk + 1 == i_TPR ? static_cast<uint32_t>(i_last)
-                                                    : static_cast<uint32_t>(kOutRecBytes);
-        bulk_issue_lane0(more ? lane : 1, ring_u32 + i_slot * RC::kStage, bars_u32 + i_slot * 8, i_src, bytes, policy);
+                                                   : static_cast<uint32_t>(kOutRecBytes);
+        bulk_issue_lane0(more ? lane : 1, ring_u32 + i_slot * kStage, bars_u32 + i_slot * 8, i_src, bytes, policy);
         i_src += bytes;   // the row blocks of a problem are contiguous
         if (++i_kk == i_TPR) {
             i_kk = 0;
             if (++i_u == i_uend && ++i_q < a.count) {
                 // next problem, entered at its first row block
                 i_recs = a.p[i_q].recs;
-                i_TPR = i_recs + a.p[i_q].OT;
+                i_di = (i_recs + RPI - 1) / RPI;
+                i_TPR = i_di + a.p[i_q].OT;
                 i_last = a.p[i_q].out_last;
                 i_uend = min(u1, unit_end(a, i_q));
                 i_src = a.p[i_q].area;
@@ -660,7 +665,8 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     bool ok = true;
     int c_q = s_q, c_u = s_u, c_kk = s_kk, c_slot = 0, c_stg = s_stg;
     uint32_t c_phase = 0;
-    int c_recs = a.p[s_q].recs, c_OT = a.p[s_q].OT, c_TPR = c_recs + c_OT, c_uend = min(u1, unit_end(a, s_q));
+    int c_recs = a.p[s_q].recs, c_OT = a.p[s_q].OT, c_di = (c_recs + RPI - 1) / RPI, c_TPR = c_di + c_OT;
+    int c_uend = min(u1, unit_end(a, s_q));
     int c_out_last = a.p[s_q].out_last;
     const int first_lu = my_items > 0 ? s_u - u0 : -1;
     if (lane == 0) {
@@ -684,7 +690,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         if (!__all_sync(0xffffffffu, mbar_try_wait(bar, c_phase)) &&
             !__all_sync(0xffffffffu, mbar_wait_bounded(bar, c_phase, kWaitLimitNs)))
             return false;                                  // a lane timed out: the warp aborts
-        const uint8_t* st = my_ring + c_slot * RC::kStage;
+        const uint8_t* st = my_ring + c_slot * kStage;
         load(st);                                          // the item into registers
         __syncwarp();
         issue_next(t + SPW < my_items);                    // hand the stage back
@@ -695,54 +701,82 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
     };
     while (t < my_items && ok) {
         const int seg_n = min(my_items - t, c_TPR - c_kk);
-        const int nd = max(0, min(seg_n, c_recs - c_kk));      // dense items of the segment
+        const int nd = max(0, min(seg_n, c_di - c_kk));        // dense items of the segment
         const int ng = c_recs * 32;
-        const uint4* xq = reinterpret_cast<const uint4*>(stg + c_stg) + c_kk * 128 + lane;
-        const float* xsg = reinterpret_cast<const float*>(stg + c_stg + MB * ng * 64) + c_kk * 32 + lane;
+        const uint4* xq = reinterpret_cast<const uint4*>(stg + c_stg) + c_kk * RPI * 128 + lane;
+        const float* xsg = reinterpret_cast<const float*>(stg + c_stg + MB * ng * 64) + c_kk * RPI * 32 + lane;
         const __half* xo = reinterpret_cast<const __half*>(stg + c_stg + MB * ng * 68 + ng * 4) +
-                           max(0, c_kk - c_recs) * kOutCols;
+                           max(0, c_kk - c_di) * kOutCols;
         const int t_end = t + seg_n, t_dense = t + nd;
         uint4 q4[kTR];
         float f1[kTR], f2[kTR];
-        // dense records
-        for (; t < t_dense; ++t) {
+        // dense items: RPI consecutive records (the last item of a row block may
+        // hold fewer); with two records the stage is handed back once the
+        // second one is in registers
+        for (int dk = c_kk; t < t_dense; ++t, ++dk) {
+            const bool two = RPI == 2 && 2 * dk + 2 <= c_recs;
             if constexpr (KIND == kW4) {
+                auto load_rec = [&](const uint8_t* st) {
+#pragma unroll
+                    for (int r = 0; r < kTR; ++r) {
+                        q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
+                        f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                        const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)] & zmask;
+                        f2[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(zb)));
+                    }
+                };
+                auto compute = [&](const uint4* xqq, const float* xss) {
+                    if constexpr (MB == 1)
+                        w4_record_m1(q4, f1, f2, xqq, *xss, acc[0]);
+                    else
+                        w4_record_mb<MB>(q4, f1, f2, xqq, ng * 4, xss, ng, mrows, acc);
+                };
                 ok = next_stage(
                     [&](const uint8_t* st) {
-#pragma unroll
-                        for (int r = 0; r < kTR; ++r) {
-                            q4[r] = reinterpret_cast<const uint4*>(st)[r * 32 + lane];
-                            f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
-                            const uint32_t zb = st[RC::kOff2 + r * 16 + (lane >> 1)] & zmask;
-                            f2[r] = __half2float(__ushort_as_half(static_cast<unsigned short>(zb)));
+                        load_rec(st);
+                        if (two) {
+                            compute(xq, xsg);
+                            load_rec(st + RC::kBytes);
                         }
                     },
                     [&]() {
-                        if constexpr (MB == 1)
-                            w4_record_m1(q4, f1, f2, xq, *xsg, acc[0]);
+                        if (two)
+                            compute(xq + 128, xsg + 32);
                         else
-                            w4_record_mb<MB>(q4, f1, f2, xq, ng * 4, xsg, ng, mrows, acc);
+                            compute(xq, xsg);
                     });
             } else {
                 uint2 q2[kTR];
+                auto load_rec = [&](const uint8_t* st) {
+#pragma unroll
+                    for (int r = 0; r < kTR; ++r) {
+                        q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
+                        f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
+                        f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
+                    }
+                };
                 ok = next_stage(
                     [&](const uint8_t* st) {
-#pragma unroll
-                        for (int r = 0; r < kTR; ++r) {
-                            q2[r] = reinterpret_cast<const uint2*>(st)[r * 32 + lane];
-                            f1[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff1)[r * 32 + lane]);
-                            f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
+                        load_rec(st);
+                        if (two) {
+                            w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
+                            load_rec(st + RC::kBytes);
                         }
                     },
-                    [&]() { w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]); });
+                    [&]() {
+                        if (two)
+                            w2_record(q2, f1, f2, xq + 128, xsg[32], a.lut_lo, a.lut_hi, acc[0]);
+                        else
+                            w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
+                    });
             }
             if (!ok) break;
-            xq += 128;
-            xsg += 32;
+            xq += two ? 256 : 128;
+            xsg += two ? 64 : 32;
         }
         // outlier records: 256 columns each, the last one trimmed (its rows are
         // `cols` wide); a lane owns 8 columns, lanes past the width read zeros
-        for (int o = max(0, c_kk - c_recs); ok && t < t_end; ++t, ++o) {
+        for (int o = max(0, c_kk - c_di); ok && t < t_end; ++t, ++o) {
             const int cols = o + 1 == c_OT ? c_out_last / 8 : kOutCols;
             ok = next_stage(
                 [&](const uint8_t* st) {
@@ -786,7 +820,8 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                 c_recs = a.p[c_q].recs;
                 c_OT = a.p[c_q].OT;
                 c_out_last = a.p[c_q].out_last;
-                c_TPR = c_recs + c_OT;
+                c_di = (c_recs + RPI - 1) / RPI;
+                c_TPR = c_di + c_OT;
                 c_uend = min(u1, unit_end(a, c_q));
             }
         }
@@ -894,26 +929,27 @@ lbq_status device_info(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Kernel variants: (kind, MB activation planes, warps)
+// Kernel variants: (kind, MB activation planes, warps, records per item)
 struct Variant {
     int kind, MB, NW, stage;
     const void* fn;
 };
-template <int KIND, int MB, int NW>
+template <int KIND, int MB, int NW, int RPI>
 Variant make_variant() {
-    return Variant{KIND, MB, NW, Rec<KIND>::kStage, reinterpret_cast<const void*>(&lbq_gemv_kernel<KIND, MB, NW>)};
+    return Variant{KIND, MB, NW, Rec<KIND>::template stage<RPI>(),
+                   reinterpret_cast<const void*>(&lbq_gemv_kernel<KIND, MB, NW, RPI>)};
 }
 constexpr int kNumVariants = 7;
 constexpr int kVarW4 = 0, kVarW2 = 4, kVarW4Narrow = 5, kVarW2Narrow = 6;
 const Variant& variant(int v) {
     static const Variant table[kNumVariants] = {
-        make_variant<kW4, 1, 16>(),   // 0: 4-bit GEMV
-        make_variant<kW4, 2, 12>(),   // 1..3: 4-bit small-M, 2 / 4 / 8 activation rows per pass
-        make_variant<kW4, 4, 12>(),
-        make_variant<kW4, 8, 8>(),
-        make_variant<kW2, 1, 16>(),   // 4: 2-bit codebook GEMV
-        make_variant<kW4, 1, 8>(),    // 5, 6: fewer warps, room for very wide K
-        make_variant<kW2, 1, 8>(),
+        make_variant<kW4, 1, 16, 2>(),   // 0: 4-bit GEMV, two records per item
+        make_variant<kW4, 2, 12, 1>(),   // 1..3: 4-bit small-M, 2 / 4 / 8 activation rows per pass
+        make_variant<kW4, 4, 12, 1>(),
+        make_variant<kW4, 8, 8, 1>(),
+        make_variant<kW2, 1, 16, 2>(),   // 4: 2-bit codebook GEMV, two records per item
+        make_variant<kW4, 1, 8, 1>(),    // 5, 6: fewer warps and one-record stages: room for very wide K
+        make_variant<kW2, 1, 8, 1>(),
     };
     return table[v];
 }
