@@ -326,23 +326,27 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
         // tid, tid + 256, ... (row xa = task % NM, group task / NM)
         constexpr int kXTasks = NM * (kStageK / 32);
         constexpr int kXPer = (kXTasks + kThreads - 1) / kThreads;
-        uint4 xr[kXPer][4];
-        auto load_x = [&](int kb, int s) {
+        // two stages of activations in flight in registers (the stage loop below is
+        // unrolled, so the buffer index s & 1 is a compile-time constant)
+        uint4 xr[2][kXPer][4];
+        auto load_x = [&](uint4 (&dst)[kXPer][4], int g) {       // stage g of this CTA
+            const int kb = kb0 + g / kStagesPerBlock, s = g % kStagesPerBlock;
 #pragma unroll
             for (int u = 0; u < kXPer; ++u) {
                 const int task = tid + u * kThreads;
                 const int xg = task / NM, xa = task - xg * NM;
                 const long long k = static_cast<long long>(kb) * 1024 + s * kStageK + xg * 32;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) xr[u][c] = make_uint4(0u, 0u, 0u, 0u);
-                if (task < kXTasks && xa < a.M && k < a.K) {
+                for (int c = 0; c < 4; ++c) dst[u][c] = make_uint4(0u, 0u, 0u, 0u);
+                if (g < nstages && task < kXTasks && xa < a.M && k < a.K) {
                     const uint4* p = reinterpret_cast<const uint4*>(a.x + xa * a.ldx + k);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) xr[u][c] = p[c];
+                    for (int c = 0; c < 4; ++c) dst[u][c] = p[c];
                 }
             }
         };
-        if (nkb > 0) load_x(kb0, 0);
+        load_x(xr[0], 0);
+        load_x(xr[1], 1);
         // dequant tasks: thread owns MMA row m = 32 (warp % 4) + lane = weight row
         // 4 (8 (warp % 4) + lane % 8) + lane / 8 of the tile (tensor-memory lane m)
         // and groups 4 (warp / 4) .. + 3 of each stage
@@ -354,6 +358,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
             const int bi = b & 1;
             const bool have = wait(full0 + 8 * bi, (b >> 1) & 1);
             const uint8_t* rec = recbuf + bi * Smem::kRecBuf + slot * kSlot;
+#pragma unroll
             for (int s = 0; s < kStagesPerBlock; ++s, ++gs) {
                 const int ab = gs & 1;
                 bool ok = have;
@@ -370,10 +375,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
                             uint32_t n[16];
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
-                                n[4 * c + 0] = xr[u][c].x;
-                                n[4 * c + 1] = xr[u][c].y;
-                                n[4 * c + 2] = xr[u][c].z;
-                                n[4 * c + 3] = xr[u][c].w;
+                                n[4 * c + 0] = xr[s & 1][u][c].x;
+                                n[4 * c + 1] = xr[s & 1][u][c].y;
+                                n[4 * c + 2] = xr[s & 1][u][c].z;
+                                n[4 * c + 3] = xr[s & 1][u][c].w;
                             }
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
@@ -381,10 +386,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
                                     x_chunk(n, j);
                         }
                     }
-                    if (s + 1 < kStagesPerBlock)
-                        load_x(kb0 + b, s + 1);
-                    else if (b + 1 < nkb)
-                        load_x(kb0 + b + 1, 0);
+                    load_x(xr[s & 1], gs + 2);
                     // weights: 4 groups of row m into tensor memory, 16 columns each
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
