@@ -9,55 +9,69 @@
 //
 // GB300 design:
 //  * a CTA owns a tile of 128 weight rows (32 row blocks of the blob) and a
-//    range of its 1024-k blocks; the 32 records of a k-block arrive by 32 bulk
-//    copies into slots 2384 bytes apart (16 bytes of padding, so 8 consecutive
-//    slots start in 8 different shared-memory bank groups), double buffered;
-//  * per 256-k stage every thread dequantises 4 groups of one weight row:
-//    nibbles masked with the FP16 magic 1024 (exact 1024 + q), minus (1024 + z),
-//    times the FP16 scale (one rounding), stored straight into its row (lane)
-//    of tensor memory with tcgen05.st - the A operand never touches shared
-//    memory; the activations of the stage are staged in shared memory in the
-//    no-swizzle K-major core-matrix layout (8 rows x 16 bytes per core matrix)
-//    with the same permutation of k inside each group;
-//  * one thread issues tcgen05.mma (A from tensor memory, M = 128 rows,
-//    N = 16..64 activation rows, K = 16, FP16 x FP16 -> FP32 in tensor memory)
-//    and tcgen05.commit to an mbarrier that frees the stage (double buffered);
+//    range of its 1024-k record blocks, walked in 256-k stages;
+//  * three tensor maps feed it through the Tensor Memory Accelerator: the
+//    nibbles of one stage for the 32 row blocks x 4 rows (16 KB, 128-byte
+//    swizzle, so the dequantising threads read shared memory without bank
+//    conflicts), the scales and zero points of a record block (10 KB), and
+//    the activations of the stage, written by the copy engine straight in the
+//    128-byte-swizzled K-major layout the tensor core reads (rows past M and
+//    columns past K arrive as zeros);
+//  * warp roles: one warp issues the copies, one issues tcgen05.mma, eight
+//    dequantise - each thread owns one weight row (its tensor-memory lane) and
+//    4 groups per stage: 1024 + q from the nibble masked into the FP16 magic
+//    exponent, minus (1024 + z) exactly, times the FP16 scale (one rounding),
+//    stored into tensor memory with tcgen05.st (k in natural order);
+//  * every hand-off is an mbarrier: rings of 4 nibble stages, 2 metadata
+//    blocks, 3-4 activation stages, and 3 A stages in tensor memory (freed by
+//    tcgen05.commit when the tensor core has read them);
+//  * tcgen05.mma: A from tensor memory (128 rows), B from shared memory
+//    (N = 16..64 activation rows), K = 16, FP16 x FP16 -> FP32 in tensor
+//    memory;
 //  * when a tile's K is split over a cluster of CTAs, each CTA moves its FP32
 //    partial from tensor memory to shared memory and the cluster's rank 0 adds
 //    the partials in rank order through distributed shared memory
 //    (deterministic, no global workspace);
 //  * every wait is bounded (2 s of %globaltimer); a timeout records
-//    LBQ_ERR_TIMEOUT, the CTA drains its copies and tensor-core work, frees its
-//    tensor memory and returns.
+//    LBQ_ERR_TIMEOUT, makes every other wait of the CTA give up at once, and the
+//    CTA drains its copies and tensor-core work, frees its tensor memory and
+//    returns.
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "lbq.h"
 #include "lbq_internal.h"
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTileRows = 128;            // MMA M
-constexpr int kTileRb = kTileRows / 4;    // row blocks per tile
-constexpr int kRecBytes = 2368;           // 4-bit dense record
-constexpr int kSlot = 2384;               // shared-memory stride of a record slot
-constexpr int kStageK = 256;              // k per A/B stage (8 groups)
+constexpr int kWorkers = 256;                // 8 dequantising warps
+constexpr int kThreads = kWorkers + 64;      // + copy warp + MMA warp
+constexpr int kTileRows = 128;               // MMA M
+constexpr int kTileRb = kTileRows / 4;       // row blocks per tile
+constexpr int kRecBytes = 2368;              // 4-bit dense record
+constexpr int kMetaBytes = 320;              // its scales (256) and zero points (64)
+constexpr int kStageK = 256;                 // k per stage (8 groups)
 constexpr int kStagesPerBlock = 1024 / kStageK;
+constexpr int kCodeStage = kTileRb * 4 * 128;   // 16 KB: 8 groups x 16 B for 128 rows
+constexpr int kMetaBlock = kTileRb * kMetaBytes;  // 10 KB
+constexpr int kNC = 4;                       // nibble stages in flight
+constexpr int kNA = 3;                       // A stages in tensor memory
+constexpr uint32_t kTmemCols = 512;          // accumulator [0, 64), A stages from column 128
+constexpr uint32_t kAcol = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 struct MmaArgs {
     const uint8_t* blob;
-    const uint8_t* area;
-    const __half* x;
     void* y;
     unsigned* err;
-    long long ldx, ldy;
+    long long ldy;
     long long N, K;
-    long long rb_bytes;
     int recs;       // k-blocks
     int n_rb;
     int M;          // activation rows (<= NM)
@@ -99,16 +113,16 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t l
     return true;
 }
 
-// UMMA shared-memory descriptor, K-major without swizzle: core matrices of
-// 8 rows x 16 bytes; `lbo` bytes between core matrices along K, `sbo` bytes
-// between core matrices along M/N; version 1 (tcgen05).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// UMMA shared-memory descriptor of a K-major operand in the 128-byte swizzled
+// layout: 8-row atoms of 8 x 128 bytes, 1024 bytes apart (SBO); version 1.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= 1ull << 46;                      // descriptor version for tcgen05
-    return d;                             // base offset 0, layout type 0 (no swizzle)
+    d |= static_cast<uint64_t>(1u) << 16;                 // LBO (unused for swizzled K-major)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;         // SBO
+    d |= 1ull << 46;                                      // descriptor version for tcgen05
+    d |= 2ull << 61;                                      // 128-byte swizzle
+    return d;
 }
 
 // Instruction descriptor of kind::f16: A, B FP16 (K-major), D FP32, M x N.
@@ -125,11 +139,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
-
 __device__ __forceinline__ uint32_t u4w(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
-
 __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -146,75 +158,63 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     return d;
 }
 
-// Word j (0..3) of a group's 16 qweight bytes (byte k = q_k | q_{k+16} << 4)
-// as 8 dequantised FP16 weights, in the order
-//   (w_{4j}, w_{4j+2}), (w_{4j+1}, w_{4j+3}), (w_{4j+16}, w_{4j+18}), (w_{4j+17}, w_{4j+19}):
-// 1024 + q is exact in FP16 (magic exponent), (1024 + q) - (1024 + z) = q - z exactly,
-// (1024 + 16 q) / 16 - (64 + z) = q - z exactly, then one rounding by s.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, uint32_t zlo2, uint32_t zhi2, uint32_t s2) {
-    const uint32_t w8 = w >> 8;
+// Word j (0..3) of a group's 16 qweight bytes (byte k = q_k | q_{k+16} << 4) as
+// 8 dequantised FP16 weights in natural order: lo[0] = (w_{4j}, w_{4j+1}),
+// lo[1] = (w_{4j+2}, w_{4j+3}), hi[0] = (w_{4j+16}, w_{4j+17}), hi[1] = (w_{4j+18}, w_{4j+19}).
+// 1024 + q is exact in FP16 (magic exponent), (1024 + q) - (1024 + z) = q - z
+// exactly, (1024 + 16 q) / 16 - (64 + z) = q - z exactly, then one rounding by s.
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zlo2, uint32_t zhi2, uint32_t s2, uint32_t (&lo)[2],
+                                             uint32_t (&hi)[2]) {
     const uint32_t sixteenth2 = 0x2C002C00u;   // FP16 1/16 in both halves
-    uint4 o;
-    o.x = hmul2(hsub2((w & 0x000F000Fu) | 0x64006400u, zlo2), s2);
-    o.y = hmul2(hsub2((w8 & 0x000F000Fu) | 0x64006400u, zlo2), s2);
-    o.z = hmul2(hfma2((w & 0x00F000F0u) | 0x64006400u, sixteenth2, zhi2), s2);
-    o.w = hmul2(hfma2((w8 & 0x00F000F0u) | 0x64006400u, sixteenth2, zhi2), s2);
-    return o;
+    const uint32_t b01 = prmt(w, 0u, 0x4140u), b23 = prmt(w, 0u, 0x4342u);   // bytes 0,1 / 2,3 to the halves
+    lo[0] = hmul2(hsub2((b01 & 0x000F000Fu) | 0x64006400u, zlo2), s2);
+    lo[1] = hmul2(hsub2((b23 & 0x000F000Fu) | 0x64006400u, zlo2), s2);
+    hi[0] = hmul2(hfma2((b01 & 0x00F000F0u) | 0x64006400u, sixteenth2, zhi2), s2);
+    hi[1] = hmul2(hfma2((b23 & 0x00F000F0u) | 0x64006400u, sixteenth2, zhi2), s2);
 }
-
-// The activations of one group in the same order, chunk j of 16 natural pairs
-// n_i = (x_{2i}, x_{2i+1}).
-__device__ __forceinline__ uint4 x_chunk(const uint32_t (&n)[16], int j) {
-    uint4 c;
-    c.x = prmt(n[2 * j], n[2 * j + 1], 0x5410u);
-    c.y = prmt(n[2 * j], n[2 * j + 1], 0x7632u);
-    c.z = prmt(n[8 + 2 * j], n[9 + 2 * j], 0x5410u);
-    c.w = prmt(n[8 + 2 * j], n[9 + 2 * j], 0x7632u);
-    return c;
-}
-
-struct Smem {
-    static constexpr int kRecBuf = kTileRb * kSlot;            // one k-block of records
-    static constexpr int rec = 0;
-    static constexpr int b = 2 * kRecBuf;                      // 2 activation (B) stages
-    static __host__ __device__ constexpr int bstage(int nm) { return nm * kStageK * 2; }
-    static __host__ __device__ constexpr int bars(int nm) { return b + 2 * bstage(nm); }
-    static __host__ __device__ constexpr int total(int nm) { return bars(nm) + 128 + 1024; }   // + alignment slack
-};
-
-// Tensor memory: columns [0, 64) the FP32 accumulator (128 lanes x N), then two
-// A stages of 128 columns (128 rows x 256 FP16 k, two k per 32-bit column).
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcol = 128;
 
 template <int NM>
-__global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a) {
-    constexpr int kBStage = Smem::bstage(NM);
-    constexpr int kSbo = (kStageK / 8) * 128;                   // bytes between 8-row groups of a B stage
+struct Geom {
+    static constexpr int kNB = NM >= 48 ? 3 : 4;                   // activation stages in flight
+    static constexpr int kBBox = NM * 128;                         // one 64-k box of NM rows
+    static constexpr int kBStage = 4 * kBBox;
+    static constexpr int code = 0;                                 // kNC x 16 KB (1024-aligned)
+    static constexpr int b = code + kNC * kCodeStage;              // kNB activation stages
+    static constexpr int meta = b + kNB * kBStage;                 // 2 x 10 KB
+    static constexpr int bars = meta + 2 * kMetaBlock;
+    static constexpr int nbars = 2 * kNC + 2 * 2 + 2 * kNB + 2 * kNA + 1;
+    static constexpr int total = bars + 8 * nbars + 16 + 1024;    // + tensor-memory slot, abort flag, stages issued, alignment
+};
+
+struct Maps {
+    CUtensorMap codes, meta, x;
+};
+
+template <int NM>
+__global__ void __launch_bounds__(kThreads, 1)
+    lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a, const __grid_constant__ Maps maps) {
+    using G = Geom<NM>;
+    constexpr int kNB = G::kNB;
     constexpr uint32_t kIdesc = idesc_f16(kTileRows, NM);
-    constexpr int kWorkerWarps = kThreads / 32;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* recbuf = smem + Smem::rec;
-    uint8_t* bbuf = smem + Smem::b;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars(NM));
-    // mbarriers: full[2] records landed, ready[2] stage written, mdone[2] stage
-    // consumed by the tensor core, rfree[2] record buffer read, last
-    const uint32_t full0 = smem_u32(bars + 0), ready0 = smem_u32(bars + 2), mdone0 = smem_u32(bars + 4),
-                   rfree0 = smem_u32(bars + 6), last_bar = smem_u32(bars + 8);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 10);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::bars);
+    // mbarriers: code full/empty [kNC], meta full/empty [2], b full/empty [kNB], a full/empty [kNA], last
+    const uint32_t cfull = smem_u32(bars), cempty = cfull + 8 * kNC, mfull = cempty + 8 * kNC, mempty = mfull + 16,
+                   bfull = mempty + 16, bempty = bfull + 8 * kNB, afull = bempty + 8 * kNB, aempty = afull + 8 * kNA,
+                   last_bar = aempty + 8 * kNA;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + G::nbars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + G::nbars) + 1;
+    volatile int* issued_flag = reinterpret_cast<volatile int*>(bars + G::nbars) + 2;   // stages the copy warp issued
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool mma_warp = warp == kWorkerWarps;                 // warp 8: copies and tensor-core issue
     const int S = a.S;
     const int rank = static_cast<int>(blockIdx.x) % S;         // rank in the cluster (cluster = S consecutive CTAs)
     const int tile = static_cast<int>(blockIdx.x) / S;
     const int kb0 = rank * a.recs / S, kb1 = (rank + 1) * a.recs / S;
     const int nkb = kb1 - kb0;
-    const int rb0 = tile * kTileRb;
-    const int nvalid = min(kTileRb, a.n_rb - rb0);
     const int nstages = nkb * kStagesPerBlock;
+    const int rb0 = tile * kTileRb;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -222,11 +222,17 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (tid == 0) {
-        const uint32_t counts[9] = {1, 1, kWorkerWarps, kWorkerWarps, 1, 1, kWorkerWarps, kWorkerWarps, 1};
-        for (int i = 0; i < 9; ++i)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bars + i)), "r"(counts[i]) : "memory");
+    if (tid == 32) {
+        for (int i = 0; i < G::nbars; ++i) {
+            const uint32_t bar = cfull + 8 * i;
+            // arrivals: copies (1, with the byte count), 8 worker warps, or one tensor-core commit
+            const bool workers = (bar >= cempty && bar < mfull) || (bar >= mempty && bar < bfull) ||
+                                 (bar >= afull && bar < aempty);
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(workers ? kWorkers / 32 : 1)
+                         : "memory");
+        }
         *abort_flag = 0;
+        *issued_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -246,179 +252,149 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
                 atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
                 return false;
             }
-            __nanosleep(128);
+            __nanosleep(64);
         }
         return true;
     };
     auto arrive = [&](uint32_t bar) {
         asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
     };
+    auto expect = [&](uint32_t bar, uint32_t bytes) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+    };
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (mma_warp) {
-        // ---------------------------------------------------------------- copies + tensor-core issue
-        uint64_t policy;
-        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-        auto issue_block = [&](int kb, int bi) {
-            const uint32_t bar = full0 + 8 * bi;
-            if (lane == 0)
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
-                             "r"(static_cast<uint32_t>(nvalid * kRecBytes))
-                             : "memory");
-            __syncwarp();
-            if (lane < nvalid) {
-                const uint8_t* src = a.area + static_cast<long long>(rb0 + lane) * a.rb_bytes +
-                                     static_cast<long long>(kb) * kRecBytes;
+    if (warp == kWorkers / 32) {
+        // ------------------------------------------------------------------ copies
+        if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
+            int s = 0;
+            for (; s < nstages; ++s) {
+                const int kb = kb0 + s / kStagesPerBlock, sl = s % kStagesPerBlock, blk = s / kStagesPerBlock;
+                if (sl == 0) {
+                    const int m = blk & 1;
+                    if (blk >= 2 && !wait(mempty + 8 * m, ((blk - 2) >> 1) & 1)) break;
+                    expect(mfull + 8 * m, kMetaBlock);
+                    asm volatile(
+                        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem + G::meta + m * kMetaBlock)),
+                        "l"(&maps.meta), "r"(0), "r"(kb), "r"(rb0), "r"(mfull + 8 * m)
+                        : "memory");
+                }
+                const int c = s % kNC;
+                if (s >= kNC && !wait(cempty + 8 * c, ((s - kNC) / kNC) & 1)) break;
+                expect(cfull + 8 * c, kCodeStage);
                 asm volatile(
-                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-                    " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(recbuf + bi * Smem::kRecBuf + lane * kSlot)),
-                    "l"(src), "r"(static_cast<uint32_t>(kRecBytes)), "r"(bar), "l"(policy)
+                    "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem + G::code + c * kCodeStage)),
+                    "l"(&maps.codes), "r"(128 * sl), "r"(0), "r"(kb), "r"(rb0), "r"(cfull + 8 * c)
                     : "memory");
+                const int bs = s % kNB;
+                if (s >= kNB && !wait(bempty + 8 * bs, ((s - kNB) / kNB) & 1)) break;
+                expect(bfull + 8 * bs, G::kBStage);
+                const int k0 = kb * 1024 + sl * kStageK;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    asm volatile(
+                        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + G::b + bs * G::kBStage + j * G::kBBox)),
+                        "l"(&maps.x), "r"(k0 + 64 * j), "r"(0), "r"(bfull + 8 * bs)
+                        : "memory");
             }
-        };
-        int issued = 0;
-        for (; issued < 2 && issued < nkb; ++issued) issue_block(kb0 + issued, issued);
-        for (int gs = 0; gs < nstages; ++gs) {
-            const int ab = gs & 1;
-            const bool ok = wait(ready0 + 8 * ab, (gs >> 1) & 1);
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (lane == 0) {
+            *issued_flag = s;
+        }
+        __syncwarp();
+    } else if (warp == kWorkers / 32 + 1) {
+        // ------------------------------------------------------------------ tensor-core issue
+        if (lane == 0) {
+            for (int s = 0; s < nstages; ++s) {
+                const int as = s % kNA, bs = s % kNB;
+                const bool ok = wait(afull + 8 * as, (s / kNA) & 1) && wait(bfull + 8 * bs, (s / kNB) & 1);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 if (ok && !*abort_flag) {
-                    const uint32_t b0 = smem_u32(bbuf + ab * kBStage);
+                    const uint32_t b0 = smem_u32(smem + G::b + bs * G::kBStage);
 #pragma unroll
                     for (int ks = 0; ks < kStageK / 16; ++ks) {
-                        const uint64_t db = smem_desc(b0 + ks * 256, 128, kSbo);
-                        const uint32_t acc = (gs > 0 || ks > 0) ? 1u : 0u;
+                        const uint64_t db = smem_desc_sw128(b0 + (ks >> 2) * G::kBBox + (ks & 3) * 32);
+                        const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
                         asm volatile(
                             "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                             "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
-                            "r"(tmem + kAcol + 128u * ab + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
+                            "r"(tmem + kAcol + 128u * as + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
                             : "memory");
                     }
                 }
-                // always commit, so the workers' waits on this stage complete
+                // always commit, so that every wait on these stages completes
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 mdone0 + 8 * ab)
+                                 aempty + 8 * as)
+                             : "memory");
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                                 bempty + 8 * bs)
                              : "memory");
             }
-            __syncwarp();
-            // after the last stage of k-block b: refill its record buffer with k-block b + 2
-            if ((gs + 1) % kStagesPerBlock == 0) {
-                const int b = gs / kStagesPerBlock;
-                const bool freed = wait(rfree0 + 8 * (b & 1), (b >> 1) & 1);
-                if (freed && !*abort_flag && issued < nkb) {
-                    issue_block(kb0 + issued, issued & 1);
-                    ++issued;
-                }
-            }
-        }
-        if (lane == 0)   // tracks every tensor-core operation issued before it
+            // tracks every tensor-core operation issued before it
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(last_bar)
                          : "memory");
+        }
         __syncwarp();
-        // drain: copies issued but never waited for by the workers (only after an abort)
-        if (*abort_flag)
-            for (int b = 0; b < issued; ++b) mbar_wait(full0 + 8 * (b & 1), (b >> 1) & 1, kWaitLimitNs / 8);
     } else {
-        // ---------------------------------------------------------------- workers: activations + dequantisation
-        asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
-        // activation staging: NM rows x 8 groups per stage; thread takes tasks
-        // tid, tid + 256, ... (row xa = task % NM, group task / NM)
-        constexpr int kXTasks = NM * (kStageK / 32);
-        constexpr int kXPer = (kXTasks + kThreads - 1) / kThreads;
-        // two stages of activations in flight in registers (the stage loop below is
-        // unrolled, so the buffer index s & 1 is a compile-time constant)
-        uint4 xr[2][kXPer][4];
-        auto load_x = [&](uint4 (&dst)[kXPer][4], int g) {       // stage g of this CTA
-            const int kb = kb0 + g / kStagesPerBlock, s = g % kStagesPerBlock;
-#pragma unroll
-            for (int u = 0; u < kXPer; ++u) {
-                const int task = tid + u * kThreads;
-                const int xg = task / NM, xa = task - xg * NM;
-                const long long k = static_cast<long long>(kb) * 1024 + s * kStageK + xg * 32;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) dst[u][c] = make_uint4(0u, 0u, 0u, 0u);
-                if (g < nstages && task < kXTasks && xa < a.M && k < a.K) {
-                    const uint4* p = reinterpret_cast<const uint4*>(a.x + xa * a.ldx + k);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) dst[u][c] = p[c];
-                }
-            }
-        };
-        load_x(xr[0], 0);
-        load_x(xr[1], 1);
-        // dequant tasks: thread owns MMA row m = 32 (warp % 4) + lane = weight row
-        // 4 (8 (warp % 4) + lane % 8) + lane / 8 of the tile (tensor-memory lane m)
-        // and groups 4 (warp / 4) .. + 3 of each stage
+        // ------------------------------------------------------------------ dequantisation
+        // thread owns tensor-memory lane m = 32 (warp % 4) + lane = weight row
+        // 4 rb + r of the tile, rb = 8 (warp % 4) + 2 (lane / 8) + (lane / 4) % 2,
+        // r = lane % 4: the 8 lanes of a quarter warp read 8 different 16-byte
+        // bank groups of the swizzled nibble stage; groups 4 (warp / 4) .. + 3
         const int qd = warp & 3, gh = warp >> 2;
-        const int slot = 8 * qd + (lane & 7), r = lane >> 3;
+        const int rb = 8 * qd + 2 * (lane >> 3) + ((lane >> 2) & 1), r = lane & 3;
+        const int row128 = rb * 4 + r;                              // 128-byte row of the nibble stage
         const uint32_t tlane = static_cast<uint32_t>(32 * qd) << 16;
-        int gs = 0;
-        for (int b = 0; b < nkb; ++b) {
-            const int bi = b & 1;
-            const bool have = wait(full0 + 8 * bi, (b >> 1) & 1);
-            const uint8_t* rec = recbuf + bi * Smem::kRecBuf + slot * kSlot;
+        for (int s = 0; s < nstages; ++s) {
+            const int sl = s % kStagesPerBlock, blk = s / kStagesPerBlock;
+            const int c = s % kNC, as = s % kNA, m = blk & 1;
+            bool ok = true;
+            if (sl == 0) ok = wait(mfull + 8 * m, (blk >> 1) & 1) && ok;
+            ok = wait(cfull + 8 * c, (s / kNC) & 1) && ok;
+            if (s >= kNA) ok = wait(aempty + 8 * as, ((s - kNA) / kNA) & 1) && ok;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (ok && !*abort_flag) {
+                const uint8_t* cs = smem + G::code + c * kCodeStage + row128 * 128;
+                const uint8_t* ms = smem + G::meta + m * kMetaBlock + rb * kMetaBytes;
+                const int g0 = 8 * sl + 4 * gh;                     // first of this thread's groups in the record
+                const uint2 sc = *reinterpret_cast<const uint2*>(ms + r * 64 + g0 * 2);          // 4 FP16 scales
+                const uint32_t zw = *reinterpret_cast<const unsigned short*>(ms + 256 + r * 16 + g0 / 2);  // 4 zeros
 #pragma unroll
-            for (int s = 0; s < kStagesPerBlock; ++s, ++gs) {
-                const int ab = gs & 1;
-                bool ok = have;
-                if (gs >= 2) ok = wait(mdone0 + 8 * ab, ((gs - 2) >> 1) & 1) && ok;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                if (ok && !*abort_flag) {
-                    uint8_t* B = bbuf + ab * kBStage;
-                    // activations of this stage (prefetched), then prefetch the next stage's
+                for (int t = 0; t < 4; ++t) {
+                    const int g8 = 4 * gh + t;                      // group of the stage
+                    const uint4 q = *reinterpret_cast<const uint4*>(cs + ((g8 ^ (row128 & 7)) << 4));
+                    const uint32_t z = (zw >> (4 * t)) & 15u;
+                    const uint32_t sb = (t < 2 ? sc.x : sc.y) >> (16 * (t & 1)) & 0xFFFFu;
+                    const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
+                    const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
+                    const uint32_t s2 = sb * 0x00010001u;
+                    uint32_t v[16];
 #pragma unroll
-                    for (int u = 0; u < kXPer; ++u) {
-                        const int task = tid + u * kThreads;
-                        if (task < kXTasks) {
-                            const int xg = task / NM, xa = task - xg * NM;
-                            uint32_t n[16];
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                n[4 * c + 0] = xr[s & 1][u][c].x;
-                                n[4 * c + 1] = xr[s & 1][u][c].y;
-                                n[4 * c + 2] = xr[s & 1][u][c].z;
-                                n[4 * c + 3] = xr[s & 1][u][c].w;
-                            }
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                *reinterpret_cast<uint4*>(B + (xa >> 3) * kSbo + (4 * xg + j) * 128 + (xa & 7) * 16) =
-                                    x_chunk(n, j);
-                        }
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t lo[2], hi[2];
+                        dequant_word(u4w(q, j), zlo2, zhi2, s2, lo, hi);
+                        v[2 * j] = lo[0];
+                        v[2 * j + 1] = lo[1];
+                        v[8 + 2 * j] = hi[0];
+                        v[9 + 2 * j] = hi[1];
                     }
-                    load_x(xr[s & 1], gs + 2);
-                    // weights: 4 groups of row m into tensor memory, 16 columns each
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int gi = 4 * gh + t;                       // group of the stage
-                        const int g = (kStageK / 32) * s + gi;           // group of the record
-                        const uint4 q = *reinterpret_cast<const uint4*>(rec + (r * 32 + g) * 16);
-                        const uint32_t sb = *reinterpret_cast<const unsigned short*>(rec + 2048 + (r * 32 + g) * 2);
-                        const uint32_t zb = rec[2304 + r * 16 + (g >> 1)];
-                        const uint32_t z = (g & 1) ? (zb >> 4) : (zb & 15u);
-                        const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
-                        const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
-                        const uint32_t s2 = sb * 0x00010001u;
-                        uint4 o[4];
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) o[j] = dequant_word(u4w(q, j), zlo2, zhi2, s2);
-                        asm volatile(
-                            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-                            "%11, %12, %13, %14, %15, %16};" ::"r"(tmem + tlane + kAcol + 128u * ab + 16u * gi),
-                            "r"(o[0].x), "r"(o[0].y), "r"(o[0].z), "r"(o[0].w), "r"(o[1].x), "r"(o[1].y), "r"(o[1].z),
-                            "r"(o[1].w), "r"(o[2].x), "r"(o[2].y), "r"(o[2].z), "r"(o[2].w), "r"(o[3].x), "r"(o[3].y),
-                            "r"(o[3].z), "r"(o[3].w)
-                            : "memory");
-                    }
-                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                        "%12, %13, %14, %15, %16};" ::"r"(tmem + tlane + kAcol + 128u * as + 16u * g8),
+                        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+                        : "memory");
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor core reads
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                    if (s + 1 == kStagesPerBlock) arrive(rfree0 + 8 * bi);  // this warp is done with the records
-                    arrive(ready0 + 8 * ab);
-                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                arrive(cempty + 8 * c);                                 // this warp is done with the nibbles
+                if (sl == kStagesPerBlock - 1) arrive(mempty + 8 * m);  // and with the block's metadata
+                arrive(afull + 8 * as);
             }
         }
     }
@@ -427,14 +403,28 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
     if (!got && tid == 0) atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
     __syncthreads();
     const bool bad = *abort_flag != 0 || !got;
-    const int gs = nstages;
-    const int qd = warp & 3;
-    const int m = 32 * qd + lane;
+    // after an abort, the last copies issued may still be in flight: wait for them
+    // (a stage the copy warp never issued is not waited for)
+    if (bad && tid == kWorkers) {
+        const int is = *issued_flag;
+        for (int s = is > kNC ? is - kNC : 0; s < is; ++s)
+            mbar_wait(cfull + 8 * (s % kNC), (s / kNC) & 1, kWaitLimitNs / 64);
+        for (int s = is > kNB ? is - kNB : 0; s < is; ++s)
+            mbar_wait(bfull + 8 * (s % kNB), (s / kNB) & 1, kWaitLimitNs / 64);
+        const int ib = (is + kStagesPerBlock - 1) / kStagesPerBlock;
+        for (int blk = ib > 2 ? ib - 2 : 0; blk < ib; ++blk)
+            mbar_wait(mfull + 8 * (blk & 1), (blk >> 1) & 1, kWaitLimitNs / 64);
+    }
+    __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
     // epilogue: warps 0-3 read rows 32 w .. 32 w + 31 of the accumulator
+    const int qd = warp & 3;
+    const int m = 32 * qd + lane;
+    const int erb = 8 * qd + 2 * (lane >> 3) + ((lane >> 2) & 1), er = lane & 3;
     float d[NM];
     if (warp < 4) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the previous kernel is done with y
 #pragma unroll
         for (int c = 0; c < NM / 16; ++c) {
             uint32_t v[16];
@@ -446,10 +436,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
                 : "r"(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 16 * c));
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-            for (int i = 0; i < 16; ++i) d[16 * c + i] = (gs > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
+            for (int i = 0; i < 16; ++i) d[16 * c + i] = (nstages > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
         }
     }
-    const long long n = static_cast<long long>(rb0 + 8 * qd + (lane & 7)) * 4 + (lane >> 3);
+    const long long n = static_cast<long long>(rb0 + erb) * 4 + er;
     auto write_y = [&](const float (&dv)[NM]) {
         if (n < a.N && !bad) {
 #pragma unroll
@@ -467,7 +457,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) lbq_w4_mma_kernel(const __gr
         if (warp < 4) write_y(d);
     } else {
         // split K: partials through distributed shared memory, added in rank order by rank 0
-        float* part = reinterpret_cast<float*>(recbuf);           // 128 x NM FP32, record buffers are free
+        float* part = reinterpret_cast<float*>(smem + G::code);   // 128 x NM FP32 over the (idle) nibble ring
         if (warp < 4)
 #pragma unroll
             for (int i = 0; i < NM; ++i) part[i * kTileRows + m] = d[i];
@@ -509,6 +499,26 @@ const void* kernel_fn() {
     return reinterpret_cast<const void*>(&lbq_w4_mma_kernel<NM>);
 }
 
+template <int NM>
+int smem_bytes() {
+    return Geom<NM>::total;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
 }  // namespace
 
 namespace lbq {
@@ -526,37 +536,70 @@ lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const 
     lbq_status st = lbq_blob_layout(LBQ_KIND_W4, N, K, 0, &L);
     if (st != LBQ_OK) return st;
     const int NM = mma_padded_rows(M);
-    const int smem = NM == 16 ? Smem::total(16) : NM == 32 ? Smem::total(32) : NM == 48 ? Smem::total(48) : Smem::total(64);
+    const int smem = NM == 16 ? smem_bytes<16>() : NM == 32 ? smem_bytes<32>() : NM == 48 ? smem_bytes<48>()
+                                                                                         : smem_bytes<64>();
     if (smem > max_smem) return LBQ_ERR_SHAPE;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    if (!encode) return LBQ_ERR_CUDA;
     MmaArgs a;
     std::memset(&a, 0, sizeof(a));
-    const uint8_t* b = static_cast<const uint8_t*>(packed);
+    uint8_t* b = static_cast<uint8_t*>(const_cast<void*>(packed));
     a.blob = b;
-    a.area = b + L.area_offset;
-    a.x = static_cast<const __half*>(x);
     a.y = y;
     a.err = err_word;
-    a.ldx = ldx;
     a.ldy = ldy;
     a.N = N;
     a.K = K;
-    a.rb_bytes = static_cast<long long>(L.row_block_bytes);
     a.recs = static_cast<int>(L.records);
     a.n_rb = static_cast<int>((N + 3) / 4);
     a.M = M;
     a.y_f32 = y_f32 ? 1 : 0;
+    // tensor maps: nibbles (byte of a row's codes, row, record block, row block),
+    // metadata (u16 of a record's scales + zeros, record block, row block),
+    // activations (k, activation row)
+    static thread_local Maps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const cuuint32_t one[4] = {1, 1, 1, 1};
+    {
+        const cuuint64_t dims[4] = {512, 4, static_cast<cuuint64_t>(a.recs), static_cast<cuuint64_t>(a.n_rb)};
+        const cuuint64_t strides[3] = {512, static_cast<cuuint64_t>(kRecBytes), L.row_block_bytes};
+        const cuuint32_t box[4] = {128, 4, 1, static_cast<cuuint32_t>(kTileRb)};
+        if (encode(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, b + L.area_offset, dims, strides, box, one,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return LBQ_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[3] = {kMetaBytes / 2, static_cast<cuuint64_t>(a.recs), static_cast<cuuint64_t>(a.n_rb)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRecBytes), L.row_block_bytes};
+        const cuuint32_t box[3] = {kMetaBytes / 2, 1, static_cast<cuuint32_t>(kTileRb)};
+        if (encode(&maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, b + L.area_offset + 2048, dims, strides, box, one,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return LBQ_ERR_CUDA;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(NM)};
+        if (encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, one,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return LBQ_ERR_CUDA;
+    }
     const int tiles = (a.n_rb + kTileRb - 1) / kTileRb;
     int S = sms / tiles;
     if (S < 1) S = 1;
     if (S > 8) S = 8;
     if (S > a.recs) S = a.recs;
     a.S = S;
-    const void* fn = NM == 16 ? kernel_fn<16>() : NM == 32 ? kernel_fn<32>() : NM == 48 ? kernel_fn<48>() : kernel_fn<64>();
+    const void* fn = NM == 16 ? kernel_fn<16>() : NM == 32 ? kernel_fn<32>() : NM == 48 ? kernel_fn<48>()
+                                                                                      : kernel_fn<64>();
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return LBQ_ERR_CUDA;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(tiles * S));
-    cfg.blockDim = dim3(kThreads + 32);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[2];
@@ -573,7 +616,7 @@ lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    void* args[] = {&a};
+    void* args[] = {&a, &maps};
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
         (void)cudaGetLastError();
         return LBQ_ERR_CUDA;
