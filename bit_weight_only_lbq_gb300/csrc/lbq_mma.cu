@@ -27,7 +27,8 @@
 //    tcgen05.commit when the tensor core has read them);
 //  * tcgen05.mma: A from tensor memory (128 rows), B from shared memory
 //    (N = 16..64 activation rows), K = 16, FP16 x FP16 -> FP32 in tensor
-//    memory;
+//    memory; consecutive MMAs alternate between 2-4 accumulators (added in a
+//    fixed order at the end), so no MMA waits on the previous one's result;
 //  * when a tile's K is split over a cluster of CTAs, each CTA moves its FP32
 //    partial from tensor memory to shared memory and the cluster's rank 0 adds
 //    the partials in rank order through distributed shared memory
@@ -62,7 +63,7 @@ constexpr int kCodeStage = kTileRb * 4 * 128;   // 16 KB: 8 groups x 16 B for 12
 constexpr int kMetaBlock = kTileRb * kMetaBytes;  // 10 KB
 constexpr int kNC = 4;                       // nibble stages in flight
 constexpr int kNA = 3;                       // A stages in tensor memory
-constexpr uint32_t kTmemCols = 512;          // accumulator [0, 64), A stages from column 128
+constexpr uint32_t kTmemCols = 512;          // accumulators in [0, 128), A stages from column 128
 constexpr uint32_t kAcol = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -175,6 +176,9 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zlo2, uint32_t
 
 template <int NM>
 struct Geom {
+    // independent accumulators: consecutive MMAs of a stage go to different ones,
+    // so the tensor core never waits on its own previous result
+    static constexpr int kND = 128 / NM >= 4 ? 4 : 128 / NM;
     static constexpr int kNB = NM >= 48 ? 3 : 4;                   // activation stages in flight
     static constexpr int kBBox = NM * 128;                         // one 64-k box of NM rows
     static constexpr int kBStage = 4 * kBBox;
@@ -316,10 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int ks = 0; ks < kStageK / 16; ++ks) {
                         const uint64_t db = smem_desc_sw128(b0 + (ks >> 2) * G::kBBox + (ks & 3) * 32);
-                        const uint32_t acc = (s > 0 || ks > 0) ? 1u : 0u;
+                        const uint32_t acc = (s > 0 || ks >= G::kND) ? 1u : 0u;
                         asm volatile(
                             "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + NM * (ks % G::kND)),
                             "r"(tmem + kAcol + 128u * as + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
                             : "memory");
                     }
@@ -426,18 +430,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 4) {
         asm volatile("griddepcontrol.wait;" ::: "memory");   // the previous kernel is done with y
 #pragma unroll
-        for (int c = 0; c < NM / 16; ++c) {
-            uint32_t v[16];
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-                "%14, %15}, [%16];"
-                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                : "r"(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 16 * c));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        for (int i = 0; i < NM; ++i) d[i] = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) d[16 * c + i] = (nstages > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
-        }
+        for (int acc = 0; acc < G::kND; ++acc)   // the accumulators, added in a fixed order
+#pragma unroll
+            for (int c = 0; c < NM / 16; ++c) {
+                uint32_t v[16];
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                    "%13, %14, %15}, [%16];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                      "=r"(v[15])
+                    : "r"(tmem + (static_cast<uint32_t>(32 * warp) << 16) + NM * acc + 16 * c));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int i = 0; i < 16; ++i) d[16 * c + i] += (nstages > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
+            }
     }
     const long long n = static_cast<long long>(rb0 + erb) * 4 + er;
     auto write_y = [&](const float (&dv)[NM]) {
