@@ -22,8 +22,8 @@
 //    4 groups per stage: 1024 + q from the nibble masked into the FP16 magic
 //    exponent, minus (1024 + z) exactly, times the FP16 scale (one rounding),
 //    stored into tensor memory with tcgen05.st (k in natural order);
-//  * every hand-off is an mbarrier: rings of 4 nibble stages, 2 metadata
-//    blocks, 3-4 activation stages, and 3 A stages in tensor memory (freed by
+//  * every hand-off is an mbarrier: rings of 6-8 nibble stages, 2 metadata
+//    blocks, 2-4 activation stages, and 3 A stages in tensor memory (freed by
 //    tcgen05.commit when the tensor core has read them);
 //  * tcgen05.mma: A from tensor memory (128 rows), B from shared memory
 //    (N = 16..64 activation rows), K = 16, FP16 x FP16 -> FP32 in tensor
@@ -61,7 +61,6 @@ constexpr int kStageK = 256;                 // k per stage (8 groups)
 constexpr int kStagesPerBlock = 1024 / kStageK;
 constexpr int kCodeStage = kTileRb * 4 * 128;   // 16 KB: 8 groups x 16 B for 128 rows
 constexpr int kMetaBlock = kTileRb * kMetaBytes;  // 10 KB
-constexpr int kNC = 4;                       // nibble stages in flight
 constexpr int kNA = 3;                       // A stages in tensor memory
 constexpr uint32_t kTmemCols = 512;          // accumulators in [0, 128), A stages from column 128
 constexpr uint32_t kAcol = 128;
@@ -179,7 +178,10 @@ struct Geom {
     // independent accumulators: consecutive MMAs of a stage go to different ones,
     // so the tensor core never waits on its own previous result
     static constexpr int kND = 128 / NM >= 4 ? 4 : 128 / NM;
-    static constexpr int kNB = NM >= 48 ? 3 : 4;                   // activation stages in flight
+    // stages in flight: nibbles (16 KB each; the deeper the better against DRAM
+    // latency) and activations (NM x 512 B each), within 227 KB of shared memory
+    static constexpr int kNC = NM <= 32 ? 8 : 6;
+    static constexpr int kNB = NM <= 32 ? 4 : 2;
     static constexpr int kBBox = NM * 128;                         // one 64-k box of NM rows
     static constexpr int kBStage = 4 * kBBox;
     static constexpr int code = 0;                                 // kNC x 16 KB (1024-aligned)
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a, const __grid_constant__ Maps maps) {
     using G = Geom<NM>;
     constexpr int kNB = G::kNB;
+    constexpr int kNC = G::kNC;
     constexpr uint32_t kIdesc = idesc_f16(kTileRows, NM);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
