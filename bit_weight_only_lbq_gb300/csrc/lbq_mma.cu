@@ -17,18 +17,23 @@
 //    the activations of the stage, written by the copy engine straight in the
 //    128-byte-swizzled K-major layout the tensor core reads (rows past M and
 //    columns past K arrive as zeros);
-//  * warp roles: one warp issues the copies, one issues tcgen05.mma, eight
+//  * warp roles: one warp copies the weights (nibbles and metadata, which no
+//    earlier kernel writes, so it starts before the grid dependency resolves),
+//    one copies the activations, two issue tcgen05.mma (alternate stages, each
+//    into its own accumulator: a barrier wait holds the issuing thread until its
+//    earlier MMAs are taken, and the other warp issues meanwhile), sixteen
 //    dequantise - each thread owns one weight row (its tensor-memory lane) and
-//    4 groups per stage: 1024 + q from the nibble masked into the FP16 magic
+//    2 groups per stage: 1024 + q from the nibble masked into the FP16 magic
 //    exponent, minus (1024 + z) exactly, times the FP16 scale (one rounding),
-//    stored into tensor memory with tcgen05.st (k in natural order);
-//  * every hand-off is an mbarrier: rings of 6-8 nibble stages, 2 metadata
-//    blocks, 2-4 activation stages, and 3 A stages in tensor memory (freed by
+//    stored into tensor memory with tcgen05.st (k in natural order).  A stays in
+//    tensor memory rather than shared memory: written and read there it would
+//    cost 128 KB of shared-memory traffic per stage;
+//  * every hand-off is an mbarrier: rings of 6-10 nibble stages, 2 metadata
+//    blocks, 3-4 activation stages, and 3 A stages in tensor memory (freed by
 //    tcgen05.commit when the tensor core has read them);
 //  * tcgen05.mma: A from tensor memory (128 rows), B from shared memory
 //    (N = 16..64 activation rows), K = 16, FP16 x FP16 -> FP32 in tensor
-//    memory; consecutive MMAs alternate between 2-4 accumulators (added in a
-//    fixed order at the end), so no MMA waits on the previous one's result;
+//    memory; the two accumulators are added in a fixed order at the end;
 //  * when a tile's K is split over a cluster of CTAs, each CTA moves its FP32
 //    partial from tensor memory to shared memory and the cluster's rank 0 adds
 //    the partials in rank order through distributed shared memory
@@ -51,14 +56,20 @@
 
 namespace {
 
-constexpr int kWorkers = 256;                // 8 dequantising warps
-constexpr int kThreads = kWorkers + 64;      // + copy warp + MMA warp
+constexpr int kWorkerWarps = 16;             // dequantising warps: 4 per tensor-memory lane quarter
+constexpr int kWorkers = 32 * kWorkerWarps;
+// tensor-core issue is split over two warps taking alternate stages, each into
+// its own accumulator: a barrier wait holds its thread until the MMAs it issued
+// before have been taken by the tensor core, and the other warp issues meanwhile
+constexpr int kIssuers = 2;
+constexpr int kThreads = kWorkers + 64 + 32 * kIssuers;   // + weight-copy, activation-copy and MMA warps
 constexpr int kTileRows = 128;               // MMA M
 constexpr int kTileRb = kTileRows / 4;       // row blocks per tile
 constexpr int kRecBytes = 2368;              // 4-bit dense record
 constexpr int kMetaBytes = 320;              // its scales (256) and zero points (64)
 constexpr int kStageK = 256;                 // k per stage (8 groups)
 constexpr int kStagesPerBlock = 1024 / kStageK;
+constexpr int kGpw = 8 / (kWorkerWarps / 4);    // groups of a stage per dequantising warp
 constexpr int kCodeStage = kTileRb * 4 * 128;   // 16 KB: 8 groups x 16 B for 128 rows
 constexpr int kMetaBlock = kTileRb * kMetaBytes;  // 10 KB
 constexpr int kNA = 3;                       // A stages in tensor memory
@@ -103,13 +114,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete; false after the limit.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-    for (int i = 0; i < 64; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait(bar, parity))
         if (global_ns() - t0 > limit_ns) return false;
-        __nanosleep(128);
-    }
     return true;
 }
 
@@ -175,13 +183,10 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zlo2, uint32_t
 
 template <int NM>
 struct Geom {
-    // independent accumulators: consecutive MMAs of a stage go to different ones,
-    // so the tensor core never waits on its own previous result
-    static constexpr int kND = 128 / NM >= 4 ? 4 : 128 / NM;
-    // stages in flight: nibbles (16 KB each; the deeper the better against DRAM
-    // latency) and activations (NM x 512 B each), within 227 KB of shared memory
-    static constexpr int kNC = NM <= 32 ? 8 : 6;
-    static constexpr int kNB = NM <= 32 ? 4 : 2;
+    // stages in flight within 227 KB of shared memory: nibbles (16 KB each; the
+    // deeper the better against DRAM latency) and activations (NM x 512 B each)
+    static constexpr int kNC = NM == 16 ? 10 : NM <= 48 ? 8 : 6;
+    static constexpr int kNB = NM <= 32 ? 4 : 3;
     static constexpr int kBBox = NM * 128;                         // one 64-k box of NM rows
     static constexpr int kBStage = 4 * kBBox;
     static constexpr int code = 0;                                 // kNC x 16 KB (1024-aligned)
@@ -189,7 +194,7 @@ struct Geom {
     static constexpr int meta = b + kNB * kBStage;                 // 2 x 10 KB
     static constexpr int bars = meta + 2 * kMetaBlock;
     static constexpr int nbars = 2 * kNC + 2 * 2 + 2 * kNB + 2 * kNA + 1;
-    static constexpr int total = bars + 8 * nbars + 16 + 1024;    // + tensor-memory slot, abort flag, stages issued, alignment
+    static constexpr int total = bars + 8 * nbars + 32 + 1024;    // + flags, alignment
 };
 
 struct Maps {
@@ -212,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    last_bar = aempty + 8 * kNA;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + G::nbars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + G::nbars) + 1;
-    volatile int* issued_flag = reinterpret_cast<volatile int*>(bars + G::nbars) + 2;   // stages the copy warp issued
+    // stages (nibbles, activations) and record blocks (metadata) whose copies were issued
+    volatile int* issued = reinterpret_cast<volatile int*>(bars + G::nbars) + 2;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = a.S;
@@ -232,14 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 32) {
         for (int i = 0; i < G::nbars; ++i) {
             const uint32_t bar = cfull + 8 * i;
-            // arrivals: copies (1, with the byte count), 8 worker warps, or one tensor-core commit
+            // arrivals: copies (1, with the byte count), the dequantising warps,
+            // one tensor-core commit, or one commit per MMA warp (the last)
             const bool workers = (bar >= cempty && bar < mfull) || (bar >= mempty && bar < bfull) ||
                                  (bar >= afull && bar < aempty);
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(workers ? kWorkers / 32 : 1)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar),
+                         "r"(workers ? kWorkerWarps : bar == last_bar ? kIssuers : 1)
                          : "memory");
         }
         *abort_flag = 0;
-        *issued_flag = 0;
+        issued[0] = issued[1] = issued[2] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -249,8 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // bounded wait that gives up at once after any thread of the CTA gave up
     auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        // no sleep between polls: try_wait suspends the thread until the phase
+        // completes or a short hardware limit passes, and a sleep would only add
+        // wake-up latency to every hand-off
+        if (mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = global_ns();
         while (!mbar_try_wait(bar, parity)) {
             if (*abort_flag) return false;
@@ -259,7 +269,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
                 return false;
             }
-            __nanosleep(64);
         }
         return true;
     };
@@ -271,10 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (warp == kWorkers / 32) {
-        // ------------------------------------------------------------------ copies
+    auto commit = [&](uint32_t bar) {
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                     : "memory");
+    };
+    if (warp == kWorkerWarps) {
+        // ------------------------------------------------------------------ weight copies
+        // the packed weights are not written by earlier kernels: no wait on them
         if (lane == 0) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
             int s = 0;
             for (; s < nstages; ++s) {
                 const int kb = kb0 + s / kStagesPerBlock, sl = s % kStagesPerBlock, blk = s / kStagesPerBlock;
@@ -287,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem + G::meta + m * kMetaBlock)),
                         "l"(&maps.meta), "r"(0), "r"(kb), "r"(rb0), "r"(mfull + 8 * m)
                         : "memory");
+                    issued[2] = blk + 1;
                 }
                 const int c = s % kNC;
                 if (s >= kNC && !wait(cempty + 8 * c, ((s - kNC) / kNC) & 1)) break;
@@ -296,6 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem + G::code + c * kCodeStage)),
                     "l"(&maps.codes), "r"(128 * sl), "r"(0), "r"(kb), "r"(rb0), "r"(cfull + 8 * c)
                     : "memory");
+            }
+            issued[0] = s;
+        }
+        __syncwarp();
+    } else if (warp == kWorkerWarps + 1) {
+        // ------------------------------------------------------------------ activation copies
+        if (lane == 0) {
+            asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
+            int s = 0;
+            for (; s < nstages; ++s) {
+                const int kb = kb0 + s / kStagesPerBlock, sl = s % kStagesPerBlock;
                 const int bs = s % kNB;
                 if (s >= kNB && !wait(bempty + 8 * bs, ((s - kNB) / kNB) & 1)) break;
                 expect(bfull + 8 * bs, G::kBStage);
@@ -308,13 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         "l"(&maps.x), "r"(k0 + 64 * j), "r"(0), "r"(bfull + 8 * bs)
                         : "memory");
             }
-            *issued_flag = s;
+            issued[1] = s;
         }
         __syncwarp();
-    } else if (warp == kWorkers / 32 + 1) {
+    } else if (warp >= kWorkerWarps + 2) {
         // ------------------------------------------------------------------ tensor-core issue
+        // MMA warp iw takes stages iw, iw + kIssuers, ... into accumulator iw
+        const int iw = warp - (kWorkerWarps + 2);
         if (lane == 0) {
-            for (int s = 0; s < nstages; ++s) {
+            for (int s = iw; s < nstages; s += kIssuers) {
                 const int as = s % kNA, bs = s % kNB;
                 const bool ok = wait(afull + 8 * as, (s / kNA) & 1) && wait(bfull + 8 * bs, (s / kNB) & 1);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -323,25 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int ks = 0; ks < kStageK / 16; ++ks) {
                         const uint64_t db = smem_desc_sw128(b0 + (ks >> 2) * G::kBBox + (ks & 3) * 32);
-                        const uint32_t acc = (s > 0 || ks >= G::kND) ? 1u : 0u;
+                        const uint32_t acc = (s >= kIssuers || ks > 0) ? 1u : 0u;
                         asm volatile(
                             "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + NM * (ks % G::kND)),
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + NM * iw),
                             "r"(tmem + kAcol + 128u * as + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
                             : "memory");
                     }
                 }
                 // always commit, so that every wait on these stages completes
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 aempty + 8 * as)
-                             : "memory");
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                                 bempty + 8 * bs)
-                             : "memory");
+                commit(aempty + 8 * as);
+                commit(bempty + 8 * bs);
             }
-            // tracks every tensor-core operation issued before it
-            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(last_bar)
-                         : "memory");
+            commit(last_bar);   // tracks every tensor-core operation this thread issued
         }
         __syncwarp();
     } else {
@@ -349,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // thread owns tensor-memory lane m = 32 (warp % 4) + lane = weight row
         // 4 rb + r of the tile, rb = 8 (warp % 4) + 2 (lane / 8) + (lane / 4) % 2,
         // r = lane % 4: the 8 lanes of a quarter warp read 8 different 16-byte
-        // bank groups of the swizzled nibble stage; groups 4 (warp / 4) .. + 3
+        // bank groups of the swizzled nibble stage; groups kGpw (warp / 4) .. + kGpw - 1
         const int qd = warp & 3, gh = warp >> 2;
         const int rb = 8 * qd + 2 * (lane >> 3) + ((lane >> 2) & 1), r = lane & 3;
         const int row128 = rb * 4 + r;                              // 128-byte row of the nibble stage
@@ -357,23 +378,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < nstages; ++s) {
             const int sl = s % kStagesPerBlock, blk = s / kStagesPerBlock;
             const int c = s % kNC, as = s % kNA, m = blk & 1;
+            // lane 0 polls for the warp; __syncwarp then orders the other lanes
+            // after its acquire
             bool ok = true;
-            if (sl == 0) ok = wait(mfull + 8 * m, (blk >> 1) & 1) && ok;
-            ok = wait(cfull + 8 * c, (s / kNC) & 1) && ok;
-            if (s >= kNA) ok = wait(aempty + 8 * as, ((s - kNA) / kNA) & 1) && ok;
+            if (lane == 0) {
+                if (sl == 0) ok = wait(mfull + 8 * m, (blk >> 1) & 1) && ok;
+                ok = wait(cfull + 8 * c, (s / kNC) & 1) && ok;
+                if (s >= kNA) ok = wait(aempty + 8 * as, ((s - kNA) / kNA) & 1) && ok;
+            }
+            __syncwarp();
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (ok && !*abort_flag) {
                 const uint8_t* cs = smem + G::code + c * kCodeStage + row128 * 128;
                 const uint8_t* ms = smem + G::meta + m * kMetaBlock + rb * kMetaBytes;
-                const int g0 = 8 * sl + 4 * gh;                     // first of this thread's groups in the record
-                const uint2 sc = *reinterpret_cast<const uint2*>(ms + r * 64 + g0 * 2);          // 4 FP16 scales
-                const uint32_t zw = *reinterpret_cast<const unsigned short*>(ms + 256 + r * 16 + g0 / 2);  // 4 zeros
+                const int g0 = 8 * sl + kGpw * gh;                  // first of this thread's groups in the record
+                static_assert(kGpw == 2, "scale and zero-point loads below are for two groups per warp");
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(ms + r * 64 + g0 * 2);   // 2 FP16 scales
+                const uint32_t zw = ms[256 + r * 16 + g0 / 2];                                   // 2 zero points
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int g8 = 4 * gh + t;                      // group of the stage
+                for (int t = 0; t < kGpw; ++t) {
+                    const int g8 = kGpw * gh + t;                   // group of the stage
                     const uint4 q = *reinterpret_cast<const uint4*>(cs + ((g8 ^ (row128 & 7)) << 4));
                     const uint32_t z = (zw >> (4 * t)) & 15u;
-                    const uint32_t sb = (t < 2 ? sc.x : sc.y) >> (16 * (t & 1)) & 0xFFFFu;
+                    const uint32_t sb = sc >> (16 * t) & 0xFFFFu;
                     const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
                     const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
                     const uint32_t s2 = sb * 0x00010001u;
@@ -411,81 +439,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const bool bad = *abort_flag != 0 || !got;
     // after an abort, the last copies issued may still be in flight: wait for them
-    // (a stage the copy warp never issued is not waited for)
+    // (a stage the copy warps never issued is not waited for)
     if (bad && tid == kWorkers) {
-        const int is = *issued_flag;
-        for (int s = is > kNC ? is - kNC : 0; s < is; ++s)
+        const int ic = issued[0], ix = issued[1], im = issued[2];
+        for (int s = ic > kNC ? ic - kNC : 0; s < ic; ++s)
             mbar_wait(cfull + 8 * (s % kNC), (s / kNC) & 1, kWaitLimitNs / 64);
-        for (int s = is > kNB ? is - kNB : 0; s < is; ++s)
+        for (int s = ix > kNB ? ix - kNB : 0; s < ix; ++s)
             mbar_wait(bfull + 8 * (s % kNB), (s / kNB) & 1, kWaitLimitNs / 64);
-        const int ib = (is + kStagesPerBlock - 1) / kStagesPerBlock;
-        for (int blk = ib > 2 ? ib - 2 : 0; blk < ib; ++blk)
+        for (int blk = im > 2 ? im - 2 : 0; blk < im; ++blk)
             mbar_wait(mfull + 8 * (blk & 1), (blk >> 1) & 1, kWaitLimitNs / 64);
     }
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // epilogue: warps 0-3 read rows 32 w .. 32 w + 31 of the accumulator
-    const int qd = warp & 3;
+    // epilogue: warp w reads accumulator lanes 32 (w % 4) .. + 31 (its rows) and
+    // columns 16 (w / 4) .. + 15 (activation rows), so up to 16 warps share it
+    constexpr int kChunks = NM / 16;
+    const int qd = warp & 3, cc = warp >> 2;
+    const bool ep = warp < 4 * kChunks;
     const int m = 32 * qd + lane;
     const int erb = 8 * qd + 2 * (lane >> 3) + ((lane >> 2) & 1), er = lane & 3;
-    float d[NM];
-    if (warp < 4) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");   // the previous kernel is done with y
-#pragma unroll
-        for (int i = 0; i < NM; ++i) d[i] = 0.f;
-#pragma unroll
-        for (int acc = 0; acc < G::kND; ++acc)   // the accumulators, added in a fixed order
-#pragma unroll
-            for (int c = 0; c < NM / 16; ++c) {
-                uint32_t v[16];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-                    "%13, %14, %15}, [%16];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-                      "=r"(v[15])
-                    : "r"(tmem + (static_cast<uint32_t>(32 * warp) << 16) + NM * acc + 16 * c));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                for (int i = 0; i < 16; ++i) d[16 * c + i] += (nstages > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
-            }
-    }
     const long long n = static_cast<long long>(rb0 + erb) * 4 + er;
-    auto write_y = [&](const float (&dv)[NM]) {
+    float d[16];
+    if (ep) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) d[i] = 0.f;
+#pragma unroll
+        for (int acc = 0; acc < kIssuers; ++acc) {   // the accumulators, added in a fixed order
+            uint32_t v[16];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                "%13, %14, %15}, [%16];"
+                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                : "r"(tmem + (static_cast<uint32_t>(32 * qd) << 16) + NM * acc + 16 * cc));
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int i = 0; i < 16; ++i) d[i] += (nstages > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
+        }
+    }
+    auto write_y = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the previous kernel is done with y
         if (n < a.N && !bad) {
 #pragma unroll
-            for (int i = 0; i < NM; ++i) {
-                if (i < a.M) {
+            for (int i = 0; i < 16; ++i) {
+                const int row = 16 * cc + i;
+                if (row < a.M) {
                     if (a.y_f32)
-                        reinterpret_cast<float*>(a.y)[i * a.ldy + n] = dv[i];
+                        reinterpret_cast<float*>(a.y)[row * a.ldy + n] = d[i];
                     else
-                        reinterpret_cast<__half*>(a.y)[i * a.ldy + n] = __float2half_rn(dv[i]);
+                        reinterpret_cast<__half*>(a.y)[row * a.ldy + n] = __float2half_rn(d[i]);
                 }
             }
         }
     };
     if (S == 1) {
-        if (warp < 4) write_y(d);
+        if (ep) write_y();
     } else {
         // split K: partials through distributed shared memory, added in rank order by rank 0
-        float* part = reinterpret_cast<float*>(smem + G::code);   // 128 x NM FP32 over the (idle) nibble ring
-        if (warp < 4)
+        float* part = reinterpret_cast<float*>(smem + G::code);   // NM x 128 FP32 over the (idle) nibble ring
+        if (ep)
 #pragma unroll
-            for (int i = 0; i < NM; ++i) part[i * kTileRows + m] = d[i];
+            for (int i = 0; i < 16; ++i) part[(16 * cc + i) * kTileRows + m] = d[i];
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-        if (rank == 0 && warp < 4) {
+        if (rank == 0 && ep) {
             for (int p = 1; p < S; ++p) {
                 uint32_t remote;
                 asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(part)), "r"(p));
 #pragma unroll
-                for (int i = 0; i < NM; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     float v;
-                    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote + 4u * (i * kTileRows + m)));
+                    asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                                 : "=f"(v)
+                                 : "r"(remote + 4u * ((16 * cc + i) * kTileRows + m)));
                     d[i] += v;
                 }
             }
-            write_y(d);
+            write_y();
         }
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
