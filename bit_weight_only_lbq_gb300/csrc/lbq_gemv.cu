@@ -889,7 +889,7 @@ __global__ void lbq_wait_selftest_kernel(uint64_t limit_ns) {
 
 // ------------------------------------------------------------ host helpers
 
-constexpr int kNumVariantsMax = 8;
+constexpr int kNumVariantsMax = 16;
 
 struct DeviceInfo {
     bool init = false;
@@ -939,8 +939,9 @@ Variant make_variant() {
     return Variant{KIND, MB, NW, Rec<KIND>::template stage<RPI>(),
                    reinterpret_cast<const void*>(&lbq_gemv_kernel<KIND, MB, NW, RPI>)};
 }
-constexpr int kNumVariants = 7;
-constexpr int kVarW4 = 0, kVarW2 = 4, kVarW4Narrow = 5, kVarW2Narrow = 6;
+constexpr int kNumVariants = 9;
+static_assert(kNumVariants <= kNumVariantsMax, "DeviceInfo::attr_set holds one flag per variant");
+constexpr int kVarW4 = 0, kVarW2 = 4, kVarW4Narrow = 5, kVarW2Narrow = 6, kVarW4One = 7, kVarW2One = 8;
 const Variant& variant(int v) {
     static const Variant table[kNumVariants] = {
         make_variant<kW4, 1, 16, 2>(),   // 0: 4-bit GEMV, two records per item
@@ -950,8 +951,16 @@ const Variant& variant(int v) {
         make_variant<kW2, 1, 16, 2>(),   // 4: 2-bit codebook GEMV, two records per item
         make_variant<kW4, 1, 8, 1>(),    // 5, 6: fewer warps and one-record stages: room for very wide K
         make_variant<kW2, 1, 8, 1>(),
+        make_variant<kW4, 1, 16, 1>(),   // 7, 8: one-record stages, for groups whose staging leaves no
+        make_variant<kW2, 1, 16, 1>(),   //       room for two-record stages
     };
     return table[v];
+}
+// The variant to try when v does not fit a group's shared memory (-1: none):
+// M = 1 goes from two-record stages to one-record stages to half the warps.
+int fallback_variant(int v) {
+    return v == kVarW4 ? kVarW4One : v == kVarW4One ? kVarW4Narrow : v == kVarW2 ? kVarW2One
+                                                               : v == kVarW2One ? kVarW2Narrow : -1;
 }
 
 // One problem as the host entry points describe it.
@@ -1097,11 +1106,11 @@ lbq_status launch_planned(DeviceInfo* dev, int vi, const GroupArgs& a, int grid,
 }
 
 // One pass (mrows <= MB activation rows) over a group: the preferred variant,
-// else its narrower fallback, else the group split in halves (launched back to
+// else (fallback) its fallback chain, else the group split in halves (launched back to
 // back; the later half follows a kernel of this same call, which writes no blob,
 // so it may overlap it).  With launches != nullptr nothing is launched and the
 // kernels the pass would launch are counted instead.
-lbq_status launch_pass(DeviceInfo* dev, int kind, int vi, int vfallback, const HostProblem* P, int count, int mrows,
+lbq_status launch_pass(DeviceInfo* dev, int kind, int vi, bool fallback, const HostProblem* P, int count, int mrows,
                        bool y_f32, void* stream, uint32_t flags, int* launches) {
     static thread_local GroupArgs a;   // ~4 KB: kept off the caller's stack
     lbq_status st = prepare_group(kind, P, count, &a);
@@ -1111,10 +1120,8 @@ lbq_status launch_pass(DeviceInfo* dev, int kind, int vi, int vfallback, const H
     int grid = 0;
     size_t smem = 0;
     st = plan_group(dev, vi, a, &grid, &smem);
-    if (st == LBQ_ERR_SHAPE && vfallback >= 0) {
-        vi = vfallback;
-        st = plan_group(dev, vi, a, &grid, &smem);
-    }
+    for (int v = fallback ? fallback_variant(vi) : -1; st == LBQ_ERR_SHAPE && v >= 0; v = fallback_variant(v))
+        st = plan_group(dev, v, a, &grid, &smem), vi = v;
     if (st == LBQ_OK) {
         if (launches) {
             ++*launches;
@@ -1124,9 +1131,9 @@ lbq_status launch_pass(DeviceInfo* dev, int kind, int vi, int vfallback, const H
     }
     if (st != LBQ_ERR_SHAPE || count == 1) return st;
     const int h = count / 2;
-    st = launch_pass(dev, kind, vi, vfallback, P, h, mrows, y_f32, stream, flags, launches);
+    st = launch_pass(dev, kind, vi, fallback, P, h, mrows, y_f32, stream, flags, launches);
     if (st != LBQ_OK) return st;
-    return launch_pass(dev, kind, vi, vfallback, P + h, count - h, mrows, y_f32, stream, flags | LBQ_FLAG_PDL,
+    return launch_pass(dev, kind, vi, fallback, P + h, count - h, mrows, y_f32, stream, flags | LBQ_FLAG_PDL,
                        launches);
 }
 
@@ -1143,7 +1150,7 @@ lbq_status check_problem(const HostProblem& p, int M, lbq_dtype y_dtype) {
 }
 
 // Passes of `MB`-row activation blocks over the group (offsets applied to x and y).
-lbq_status run_passes(DeviceInfo* dev, int kind, int vi, int vf, int MB, const HostProblem* P, int count, int M,
+lbq_status run_passes(DeviceInfo* dev, int kind, int vi, bool fallback, int MB, const HostProblem* P, int count, int M,
                       bool f32, void* stream, uint32_t flags, int* launches) {
     const size_t ysz = f32 ? 4 : 2;
     HostProblem Q[kMaxGroup];
@@ -1154,7 +1161,7 @@ lbq_status run_passes(DeviceInfo* dev, int kind, int vi, int vf, int MB, const H
             Q[i].y = static_cast<uint8_t*>(P[i].y) + m0 * P[i].ldy * ysz;
         }
         // later passes follow a pass of this same call, which never writes a blob
-        lbq_status st = launch_pass(dev, kind, vi, vf, Q, count, M - m0 < MB ? M - m0 : MB, f32, stream,
+        lbq_status st = launch_pass(dev, kind, vi, fallback, Q, count, M - m0 < MB ? M - m0 : MB, f32, stream,
                                     m0 == 0 ? flags : (flags | LBQ_FLAG_PDL), launches);
         if (st != LBQ_OK) return st;
     }
@@ -1179,8 +1186,15 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
     lbq_status st = device_info(&dev);
     if (st != LBQ_OK) return st;
     const bool f32 = y_dtype == LBQ_F32;
-    const int vi = kind == kW4 ? kVarW4 : kVarW2, vf = kind == kW4 ? kVarW4Narrow : kVarW2Narrow;
-    if (M == 1) return launch_pass(dev, kind, vi, vf, P, count, 1, f32, stream, flags, launches);
+    const int vi = kind == kW4 ? kVarW4 : kVarW2;
+    if (M == 1) {
+        // fewer dense records than warps in the grid: one-record items keep more
+        // warps busy (latency rather than bandwidth decides these small calls)
+        long long recs = 0;
+        for (int i = 0; i < count; ++i) recs += (P[i].N + kTR - 1) / kTR * ((P[i].K + 1023) / 1024);
+        const int v0 = recs < static_cast<long long>(dev->sms) * variant(vi).NW ? fallback_variant(vi) : vi;
+        return launch_pass(dev, kind, v0, true, P, count, 1, f32, stream, flags, launches);
+    }
     // M >= 16 without outlier columns: the tensor-core kernel, one launch per problem
     bool dense_only = true;
     for (int i = 0; i < count; ++i) dense_only = dense_only && P[i].n_out == 0;
@@ -1203,12 +1217,12 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
         bool fits = true;
         for (int i = 0; i < count && fits; ++i) {
             int n = 0;
-            fits = launch_pass(dev, kind, v, -1, P + i, 1, variant(v).MB, f32, stream, 0u, &n) == LBQ_OK;
+            fits = launch_pass(dev, kind, v, false, P + i, 1, variant(v).MB, f32, stream, 0u, &n) == LBQ_OK;
         }
         if (fits) break;
     }
-    if (v >= 1) return run_passes(dev, kind, v, -1, variant(v).MB, P, count, M, f32, stream, flags, launches);
-    return run_passes(dev, kind, vi, vf, 1, P, count, M, f32, stream, flags, launches);
+    if (v >= 1) return run_passes(dev, kind, v, false, variant(v).MB, P, count, M, f32, stream, flags, launches);
+    return run_passes(dev, kind, vi, true, 1, P, count, M, f32, stream, flags, launches);
 }
 
 lbq_status run_one(int kind, const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out, const void* x,
