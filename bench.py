@@ -63,6 +63,24 @@ def algorithmic_bytes(kind: str, N: int, K: int, n_out: int, M: int = 1) -> int:
     return int(per_w * N * K + n_out * (4 + 2 * N) + 2 * K * M + 2 * N * M)
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's value (each rank calls it); the value itself
+    on one process.  Timings are reduced this way: the job takes as long as its
+    slowest rank."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes: int, world: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the bytes all ranks streamed (each rank runs its own
+    replica of the step) over the slowest rank's time."""
+    return step_bytes * world * steps / seconds / 1e9
+
+
 def kernel_source_hash() -> str:
     import hashlib
     src = os.path.join(ROOT, "bit_weight_only_lbq_gb300", "csrc", "lbq_gemv.cu")
@@ -362,11 +380,8 @@ def main():
         ev1.synchronize()
         t_wall1 = time.time()
         torch.cuda.synchronize()
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
         dist.barrier()
     clk = clocks.summary(t_wall0, t_wall1)
 
@@ -438,12 +453,12 @@ def main():
             for i in range(len(layer)):
                 h_y[i].copy_(ys[i], non_blocking=True)
             stream.synchronize()
-        e2e_s = time.perf_counter() - t0
-    e2e_value = step_bytes * e2e_steps / e2e_s / 1e9 * world
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    e2e_value = whole_job_gbs(step_bytes, world, e2e_steps, e2e_s)
 
     peak, peak_kind = load_peaks()
     ms_step = ms_total / args.steps
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, args.steps, ms_total * 1e-3)
     groups_detail = []
     for gname, kind in GROUPS:
         gbytes = sum(layer[i]["bytes"] for i in group_members(layer, kind))
