@@ -711,10 +711,10 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
         uint4 q4[kTR];
         float f1[kTR], f2[kTR];
         // dense items: RPI consecutive records (the last item of a row block may
-        // hold fewer); with two records the stage is handed back once the
-        // second one is in registers
+        // hold fewer); the stage is handed back once its last record is in
+        // registers, the records before it are computed while it is held
         for (int dk = c_kk; t < t_dense; ++t, ++dk) {
-            const bool two = RPI == 2 && 2 * dk + 2 <= c_recs;
+            const int nrec = min(RPI, c_recs - RPI * dk);
             if constexpr (KIND == kW4) {
                 auto load_rec = [&](const uint8_t* st) {
 #pragma unroll
@@ -734,17 +734,14 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                 ok = next_stage(
                     [&](const uint8_t* st) {
                         load_rec(st);
-                        if (two) {
-                            compute(xq, xsg);
-                            load_rec(st + RC::kBytes);
-                        }
+#pragma unroll
+                        for (int j = 1; j < RPI; ++j)
+                            if (j < nrec) {
+                                compute(xq + 128 * (j - 1), xsg + 32 * (j - 1));
+                                load_rec(st + j * RC::kBytes);
+                            }
                     },
-                    [&]() {
-                        if (two)
-                            compute(xq + 128, xsg + 32);
-                        else
-                            compute(xq, xsg);
-                    });
+                    [&]() { compute(xq + 128 * (nrec - 1), xsg + 32 * (nrec - 1)); });
             } else {
                 uint2 q2[kTR];
                 auto load_rec = [&](const uint8_t* st) {
@@ -758,21 +755,22 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                 ok = next_stage(
                     [&](const uint8_t* st) {
                         load_rec(st);
-                        if (two) {
-                            w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
-                            load_rec(st + RC::kBytes);
-                        }
+#pragma unroll
+                        for (int j = 1; j < RPI; ++j)
+                            if (j < nrec) {
+                                w2_record(q2, f1, f2, xq + 128 * (j - 1), xsg[32 * (j - 1)], a.lut_lo, a.lut_hi,
+                                          acc[0]);
+                                load_rec(st + j * RC::kBytes);
+                            }
                     },
                     [&]() {
-                        if (two)
-                            w2_record(q2, f1, f2, xq + 128, xsg[32], a.lut_lo, a.lut_hi, acc[0]);
-                        else
-                            w2_record(q2, f1, f2, xq, *xsg, a.lut_lo, a.lut_hi, acc[0]);
+                        w2_record(q2, f1, f2, xq + 128 * (nrec - 1), xsg[32 * (nrec - 1)], a.lut_lo, a.lut_hi,
+                                  acc[0]);
                     });
             }
             if (!ok) break;
-            xq += two ? 256 : 128;
-            xsg += two ? 64 : 32;
+            xq += 128 * nrec;
+            xsg += 32 * nrec;
         }
         // outlier records: 256 columns each, the last one trimmed (its rows are
         // `cols` wide); a lane owns 8 columns, lanes past the width read zeros
@@ -952,7 +950,7 @@ const Variant& variant(int v) {
         make_variant<kW4, 1, 8, 1>(),    // 5, 6: fewer warps and one-record stages: room for very wide K
         make_variant<kW2, 1, 8, 1>(),
         make_variant<kW4, 1, 16, 1>(),   // 7, 8: one-record stages, for groups whose staging leaves no
-        make_variant<kW2, 1, 16, 1>(),   //       room for two-record stages
+        make_variant<kW2, 1, 16, 1>(),   //       room for two-record stages, and single 4-bit calls
     };
     return table[v];
 }
@@ -1188,11 +1186,16 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
     const bool f32 = y_dtype == LBQ_F32;
     const int vi = kind == kW4 ? kVarW4 : kVarW2;
     if (M == 1) {
-        // fewer dense records than warps in the grid: one-record items keep more
-        // warps busy (latency rather than bandwidth decides these small calls)
+        // one-record items for calls with fewer dense records than warps in the
+        // grid (latency rather than bandwidth decides them) and for a single
+        // large 4-bit problem, >= 4 records per warp (measured: 14336 x 4096
+        // alone 9.1 us with one-record items, 9.8 us with two; 4096 x 4096 and
+        // grouped sweeps are faster with two)
         long long recs = 0;
         for (int i = 0; i < count; ++i) recs += (P[i].N + kTR - 1) / kTR * ((P[i].K + 1023) / 1024);
-        const int v0 = recs < static_cast<long long>(dev->sms) * variant(vi).NW ? fallback_variant(vi) : vi;
+        const long long warps = static_cast<long long>(dev->sms) * variant(vi).NW;
+        const bool one = recs < warps || (kind == kW4 && count == 1 && recs >= 4 * warps);
+        const int v0 = one ? fallback_variant(vi) : vi;
         return launch_pass(dev, kind, v0, true, P, count, 1, f32, stream, flags, launches);
     }
     // M >= 16 without outlier columns: the tensor-core kernel, one launch per problem

@@ -91,6 +91,21 @@ def test_cfg1_full_elementwise(lbq):
     assert_close(_run(lbq, "w4", blob, 4096, 4096, 0, x, f32=False), ref, fp16_out=True, what="cfg1 f16")
 
 
+def test_large_single_problem_elementwise(lbq):
+    """One large 4-bit problem (one-record items on 16 warps) with a K of 17
+    records per row block and outlier records after the dense ones; every row
+    compared."""
+    rng = np.random.default_rng(21)
+    N, K = 2052, 17408
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    x = rng.standard_normal(K).astype(np.float16)
+    x[rng.choice(K, size=K // 200, replace=False)] *= 100
+    for n_out in (0, 300):
+        idx = np.sort(rng.choice(K, size=n_out, replace=False)).astype(np.int32)
+        y = _run(lbq, "w4", lbq.pack_w4(W, idx), N, K, n_out, x)
+        assert_close(y, O.gemv(O.pack_w4(W, idx), x), what="large single n_out=%d" % n_out)
+
+
 def test_max_k_and_max_outliers(lbq):
     rng = np.random.default_rng(5)
     for kind in ("w4", "w2"):
