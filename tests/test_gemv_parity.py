@@ -96,7 +96,7 @@ def test_large_single_problem_elementwise(lbq):
     records per row block and outlier records after the dense ones; every row
     compared."""
     rng = np.random.default_rng(21)
-    N, K = 2052, 17408
+    N, K = 2300, 17408                        # 575 row blocks x 17 records: >= 4 per warp
     W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
     x = rng.standard_normal(K).astype(np.float16)
     x[rng.choice(K, size=K // 200, replace=False)] *= 100
