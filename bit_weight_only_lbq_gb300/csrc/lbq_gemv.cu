@@ -387,6 +387,49 @@ __device__ __forceinline__ void w2_record(const uint2 (&c)[kTR], const float (&S
     for (int r = 0; r < kTR; ++r) acc[r] = fmaf(S[r], d0[r] + d1[r], fmaf(Z[r], xs, acc[r]));
 }
 
+// 2-bit record, MB activation rows: the codebook pairs of the 4 rows are
+// decoded once (PRMT as above) and shared by the rows' FMAs.
+template <int MB>
+__device__ __forceinline__ void w2_record_mb(const uint2 (&c)[kTR], const float (&S)[kTR], const float (&Z)[kTR],
+                                             const uint4* xq, int xq_plane, const float* xs, int xs_plane,
+                                             uint32_t lut_lo, uint32_t lut_hi, int mrows, float (&acc)[MB][kTR]) {
+    uint32_t p[kTR][16];   // pair (v * 4 + sh) * 2 + h: codes of word v, shift sh, half h
+#pragma unroll
+    for (int r = 0; r < kTR; ++r)
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+#pragma unroll
+            for (int sh = 0; sh < 4; ++sh) {
+                const uint32_t t = ((v ? c[r].y : c[r].x) >> (2 * sh)) & 0x03030303u;
+                const uint32_t sel = t * 0x11u + 0x40404040u;
+                p[r][(v * 4 + sh) * 2] = prmt(lut_lo, lut_hi, sel);
+                p[r][(v * 4 + sh) * 2 + 1] = prmt(lut_lo, lut_hi, sel >> 16);
+            }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+        if (m < mrows) {
+            const uint4* xp = xq + m * xq_plane;
+            const uint4 xr[4] = {xp[0], xp[32], xp[64], xp[96]};
+            float d0[kTR], d1[kTR];
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) d0[r] = d1[r] = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const int mw = 2 * w;                              // word of the group's 64 x bytes
+                const uint32_t xa = u4w(xr[mw >> 2], mw & 3), xb = u4w(xr[(mw + 1) >> 2], (mw + 1) & 3);
+#pragma unroll
+                for (int r = 0; r < kTR; ++r) {
+                    d0[r] = fma2_mixed(p[r][2 * w], xa, d0[r]);
+                    d1[r] = fma2_mixed(p[r][2 * w + 1], xb, d1[r]);
+                }
+            }
+            const float xsm = xs[m * xs_plane];
+#pragma unroll
+            for (int r = 0; r < kTR; ++r) acc[m][r] = fmaf(S[r], d0[r] + d1[r], fmaf(Z[r], xsm, acc[m][r]));
+        }
+    }
+}
+
 // One outlier record: lane owns outlier columns [lane*8, +8) of the record's 256
 // for the 4 rows; xo + m * xo_plane holds x[idx] of activation row m.  `unit`
 // converts to the unit of the dense accumulator (2^-24 for 4-bit, 1 for 2-bit).
@@ -752,21 +795,23 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                         f2[r] = __half2float(reinterpret_cast<const __half*>(st + RC::kOff2)[r * 32 + lane]);
                     }
                 };
+                auto compute = [&](const uint4* xqq, const float* xss) {
+                    if constexpr (MB == 1)
+                        w2_record(q2, f1, f2, xqq, *xss, a.lut_lo, a.lut_hi, acc[0]);
+                    else
+                        w2_record_mb<MB>(q2, f1, f2, xqq, ng * 4, xss, ng, a.lut_lo, a.lut_hi, mrows, acc);
+                };
                 ok = next_stage(
                     [&](const uint8_t* st) {
                         load_rec(st);
 #pragma unroll
                         for (int j = 1; j < RPI; ++j)
                             if (j < nrec) {
-                                w2_record(q2, f1, f2, xq + 128 * (j - 1), xsg[32 * (j - 1)], a.lut_lo, a.lut_hi,
-                                          acc[0]);
+                                compute(xq + 128 * (j - 1), xsg + 32 * (j - 1));
                                 load_rec(st + j * RC::kBytes);
                             }
                     },
-                    [&]() {
-                        w2_record(q2, f1, f2, xq + 128 * (nrec - 1), xsg[32 * (nrec - 1)], a.lut_lo, a.lut_hi,
-                                  acc[0]);
-                    });
+                    [&]() { compute(xq + 128 * (nrec - 1), xsg + 32 * (nrec - 1)); });
             }
             if (!ok) break;
             xq += 128 * nrec;
@@ -937,9 +982,11 @@ Variant make_variant() {
     return Variant{KIND, MB, NW, Rec<KIND>::template stage<RPI>(),
                    reinterpret_cast<const void*>(&lbq_gemv_kernel<KIND, MB, NW, RPI>)};
 }
-constexpr int kNumVariants = 9;
+constexpr int kNumVariants = 12;
 static_assert(kNumVariants <= kNumVariantsMax, "DeviceInfo::attr_set holds one flag per variant");
 constexpr int kVarW4 = 0, kVarW2 = 4, kVarW4Narrow = 5, kVarW2Narrow = 6, kVarW4One = 7, kVarW2One = 8;
+// small-M variants (2, 4, 8 activation rows per pass) of each kind
+constexpr int kVarW4Small[3] = {1, 2, 3}, kVarW2Small[3] = {9, 10, 11};
 const Variant& variant(int v) {
     static const Variant table[kNumVariants] = {
         make_variant<kW4, 1, 16, 2>(),   // 0: 4-bit GEMV, two records per item
@@ -951,6 +998,9 @@ const Variant& variant(int v) {
         make_variant<kW2, 1, 8, 1>(),
         make_variant<kW4, 1, 16, 1>(),   // 7, 8: one-record stages, for groups whose staging leaves no
         make_variant<kW2, 1, 16, 1>(),   //       room for two-record stages, and single 4-bit calls
+        make_variant<kW2, 2, 12, 1>(),   // 9..11: 2-bit small-M, 2 / 4 / 8 activation rows per pass
+        make_variant<kW2, 4, 12, 1>(),
+        make_variant<kW2, 8, 8, 1>(),
     };
     return table[v];
 }
@@ -1175,7 +1225,6 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
                int* launches) {
     if (count < 1 || count > kMaxGroup || M < 1 || M > lbq::kMaxM) return LBQ_ERR_SHAPE;
     if (y_dtype != LBQ_F16 && y_dtype != LBQ_F32) return LBQ_ERR_UNSUPPORTED;
-    if (kind == kW2 && M != 1) return LBQ_ERR_UNSUPPORTED;
     for (int i = 0; i < count; ++i) {
         lbq_status st = check_problem(P[i], M, y_dtype);
         if (st != LBQ_OK) return st;
@@ -1214,17 +1263,21 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
         }
         return LBQ_OK;
     }
-    int v = 1;
-    while (v < 3 && variant(v).MB < M) ++v;
-    for (; v >= 1; --v) {
+    const int* small = kind == kW4 ? kVarW4Small : kVarW2Small;
+    int j = 0;
+    while (j < 2 && variant(small[j]).MB < M) ++j;
+    for (; j >= 0; --j) {
         bool fits = true;
         for (int i = 0; i < count && fits; ++i) {
             int n = 0;
-            fits = launch_pass(dev, kind, v, false, P + i, 1, variant(v).MB, f32, stream, 0u, &n) == LBQ_OK;
+            fits = launch_pass(dev, kind, small[j], false, P + i, 1, variant(small[j]).MB, f32, stream, 0u, &n) ==
+                   LBQ_OK;
         }
         if (fits) break;
     }
-    if (v >= 1) return run_passes(dev, kind, v, false, variant(v).MB, P, count, M, f32, stream, flags, launches);
+    if (j >= 0)
+        return run_passes(dev, kind, small[j], false, variant(small[j]).MB, P, count, M, f32, stream, flags,
+                          launches);
     return run_passes(dev, kind, vi, true, 1, P, count, M, f32, stream, flags, launches);
 }
 
@@ -1283,6 +1336,18 @@ lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64
                                  const void* X_f16, int64_t ldx, void* Y, int64_t ldy, lbq_dtype y_dtype,
                                  void* stream) {
     return run_one(kW4, packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, 0u);
+}
+
+lbq_status lbq_gemm_w2cb_outlier_smallM_ex(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
+                                           const void* X_f16, int64_t ldx, void* Y, int64_t ldy, lbq_dtype y_dtype,
+                                           void* stream, uint32_t flags) {
+    return run_one(kW2, packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, flags);
+}
+
+lbq_status lbq_gemm_w2cb_outlier_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
+                                        const void* X_f16, int64_t ldx, void* Y, int64_t ldy, lbq_dtype y_dtype,
+                                        void* stream) {
+    return run_one(kW2, packed, M, N, K, n_out, X_f16, ldx, Y, ldy, y_dtype, stream, 0u);
 }
 
 

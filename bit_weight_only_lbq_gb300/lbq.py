@@ -36,7 +36,8 @@ EXPORTS = (
     "lbq_w4_packed_bytes", "lbq_w2cb_packed_bytes", "lbq_select_outliers_w4",
     "lbq_select_outliers_impact", "lbq_pack_w4", "lbq_pack_w2cb", "lbq_gemv_w4a16",
     "lbq_gemv_w2cb_outlier", "lbq_gemm_w4a16_smallM", "lbq_gemv_w4a16_ex",
-    "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
+    "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_gemm_w2cb_outlier_smallM",
+    "lbq_gemm_w2cb_outlier_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
     "lbq_selftest_wait_timeout", "lbq_device_error",
 )
 
@@ -100,6 +101,10 @@ def lib():
                                                         c_vp, c_u32]),
             "lbq_gemm_w4a16_smallM_ex": (ctypes.c_int, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp,
                                                         c_i64, ctypes.c_int, c_vp, c_u32]),
+            "lbq_gemm_w2cb_outlier_smallM": (ctypes.c_int, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp,
+                                                            c_i64, ctypes.c_int, c_vp]),
+            "lbq_gemm_w2cb_outlier_smallM_ex": (ctypes.c_int, [c_vp, c_i32, c_i64, c_i64, c_i32, c_vp, c_i64,
+                                                               c_vp, c_i64, ctypes.c_int, c_vp, c_u32]),
             "lbq_gemv_grouped": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(Problem), c_i32, c_i32, ctypes.c_int,
                                                 c_vp, c_u32]),
             "lbq_gemv_grouped_launches": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(Problem), c_i32, c_i32,
@@ -240,6 +245,14 @@ def gemm_w4a16_smallM(packed, M: int, N: int, K: int, n_out: int, X, ldx: int, Y
     yd = _ydtype(Y) if y_dtype is None else y_dtype
     _check(lib().lbq_gemm_w4a16_smallM_ex(_dev_ptr(packed), M, N, K, n_out, _dev_ptr(X), ldx, _dev_ptr(Y), ldy, yd,
                                           _stream(stream), LBQ_FLAG_PDL if pdl else 0), "lbq_gemm_w4a16_smallM")
+
+
+def gemm_w2cb_outlier_smallM(packed, M: int, N: int, K: int, n_out: int, X, ldx: int, Y, ldy: int, stream=None,
+                             pdl: bool = False, y_dtype: int | None = None):
+    yd = _ydtype(Y) if y_dtype is None else y_dtype
+    _check(lib().lbq_gemm_w2cb_outlier_smallM_ex(_dev_ptr(packed), M, N, K, n_out, _dev_ptr(X), ldx, _dev_ptr(Y),
+                                                 ldy, yd, _stream(stream), LBQ_FLAG_PDL if pdl else 0),
+           "lbq_gemm_w2cb_outlier_smallM")
 
 
 def _problems(problems, y_dtype):

@@ -190,6 +190,18 @@ lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64
                                  const void* X_f16, int64_t ldx, void* Y, int64_t ldy,
                                  lbq_dtype y_dtype, void* stream);
 
+/* Batched 2-bit codebook GEMM with exact FP16 outlier columns for small M: the
+ * M-row form of lbq_gemv_w2cb_outlier (otf-llm section 5 and "Architecture &
+ * Key Innovations"; the batched form is this library's extension, the page
+ * states the M = 1 kernel):
+ *     Y[m, n] = sum_g [ S_{n,g} sum_{k in g} C[q_{n,k}] X~[m,k] + Z_{n,g} sum_{k in g} X~[m,k] ]
+ *               + sum_j vals[n,j] X[m, idx_j],  0 <= m < M
+ * Arguments, layouts and errors as lbq_gemm_w4a16_smallM, with a 2-bit blob;
+ * every M runs on the CUDA-core kernel (passes of 2, 4 or 8 activation rows). */
+lbq_status lbq_gemm_w2cb_outlier_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
+                                        const void* X_f16, int64_t ldx, void* Y, int64_t ldy,
+                                        lbq_dtype y_dtype, void* stream);
+
 /* Variants with launch flags.  LBQ_FLAG_PDL launches the kernel with
  * programmatic stream serialisation: it may start while the previous kernel
  * on the stream is still running, fetch its weights at once, and read x /
@@ -207,6 +219,9 @@ lbq_status lbq_gemv_w2cb_outlier_ex(const void* packed, int64_t N, int64_t K, in
 lbq_status lbq_gemm_w4a16_smallM_ex(const void* packed, int32_t M, int64_t N, int64_t K,
                                     int32_t n_out, const void* X_f16, int64_t ldx, void* Y,
                                     int64_t ldy, lbq_dtype y_dtype, void* stream, uint32_t flags);
+lbq_status lbq_gemm_w2cb_outlier_smallM_ex(const void* packed, int32_t M, int64_t N, int64_t K,
+                                           int32_t n_out, const void* X_f16, int64_t ldx, void* Y,
+                                           int64_t ldy, lbq_dtype y_dtype, void* stream, uint32_t flags);
 
 /* Grouped launch: several independent problems of one kind in ONE kernel
  * launch (a decode layer's linears, or any list of them).  This is the "fused
@@ -214,16 +229,15 @@ lbq_status lbq_gemm_w4a16_smallM_ex(const void* packed, int32_t M, int64_t N, in
  * all problems back to back, so the fixed cost of a launch is paid once per
  * group instead of once per matrix.  Each problem computes exactly what the
  * single-problem entry point of its kind computes (lbq_gemv_w4a16 /
- * lbq_gemm_w4a16_smallM for LBQ_KIND_W4, lbq_gemv_w2cb_outlier for
- * LBQ_KIND_W2CB); results may differ from a single call only in FP32
- * summation order.
+ * lbq_gemm_w4a16_smallM for LBQ_KIND_W4, lbq_gemv_w2cb_outlier /
+ * lbq_gemm_w2cb_outlier_smallM for LBQ_KIND_W2CB); results may differ from a
+ * single call only in FP32 summation order.
  * problems : host array of count descriptors (1 <= count <= LBQ_MAX_GROUP);
  *            every pointer inside is a device pointer with the alignment of
  *            the single-problem entry points; ldx % 8 == 0, ldx >= K,
  *            ldy >= N; reserved must be 0.  The array is read during the call
  *            only.
- * M        : activation rows, shared by all problems (1 <= M <= 64; the 2-bit
- *            kind supports M = 1 only).
+ * M        : activation rows, shared by all problems (1 <= M <= 64).
  * The problems must be independent: no problem's y may overlap any problem's
  * x, y or blob.  Launched as one kernel when the problems' activations fit in
  * shared memory together, else as several back-to-back kernels.

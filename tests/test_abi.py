@@ -71,6 +71,9 @@ def test_device_entry_points_reject_bad_args_without_gpu(lbq):
     assert L.lbq_gemm_w4a16_smallM(16, 65, 8, 64, 0, 16, 64, 16, 8, 0, None) == 2
     assert L.lbq_gemm_w4a16_smallM(16, 2, 8, 64, 0, 16, 60, 16, 8, 0, None) == 2   # ldx < K
     assert L.lbq_gemm_w4a16_smallM(16, 2, 8, 64, 0, 16, 68, 16, 8, 0, None) == 3   # ldx % 8
+    assert L.lbq_gemm_w2cb_outlier_smallM(16, 65, 8, 64, 0, 16, 64, 16, 8, 0, None) == 2
+    assert L.lbq_gemm_w2cb_outlier_smallM(16, 2, 8, 64, 0, 16, 60, 16, 8, 0, None) == 2   # ldx < K
+    assert L.lbq_gemm_w2cb_outlier_smallM(None, 2, 8, 64, 0, 16, 64, 16, 8, 0, None) == 1
 
 
 def test_grouped_entry_point_rejects_bad_args_without_gpu(lbq):
@@ -82,7 +85,10 @@ def test_grouped_entry_point_rejects_bad_args_without_gpu(lbq):
     assert L.lbq_gemv_grouped(0, arr, 0, 1, 0, None, 0) == 2
     assert L.lbq_gemv_grouped(0, arr, lbq.LBQ_MAX_GROUP + 1, 1, 0, None, 0) == 2
     assert L.lbq_gemv_grouped(5, arr, 1, 1, 0, None, 0) == 10          # unknown kind
-    assert L.lbq_gemv_grouped(1, arr, 1, 2, 0, None, 0) == 10          # 2-bit small M not provided
+    # 2-bit small M passes validation like M = 1 (here it then stops at the
+    # device query: no GPU)
+    assert L.lbq_gemv_grouped(1, arr, 1, 2, 0, None, 0) == L.lbq_gemv_grouped(1, arr, 1, 1, 0, None, 0) != 0
+    assert L.lbq_gemv_grouped(1, arr, 1, 65, 0, None, 0) == 2
     assert L.lbq_gemv_grouped(0, arr, 1, 65, 0, None, 0) == 2
     bad = (P * 2)(good, P(16, 8, 64, 0, 1, 16, 64, 16, 8))             # reserved != 0
     assert L.lbq_gemv_grouped(0, bad, 2, 1, 0, None, 0) == 2
