@@ -508,3 +508,112 @@ def fp16_ulp(v: np.ndarray) -> np.ndarray:
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     e = np.maximum(e, -14.0)
     return np.ldexp(1.0, (e - 10).astype(int))
+
+
+# ---------------------------------------------------------------------------
+# Selective weight refinement (StrataFlux paper, section 3 "Designing Precision
+# for Selective Refinement": "Weight Refinement", Eq. 2 and "Channel selection";
+# Appendix "StrataFlux Implementation": exact radix-sort selection)
+#
+#   y' = W_hat x + sum_{i in S(x)} x_i C[:, i]
+#   S(x): per chunk of 1,024 consecutive input channels, the k channels with the
+#         largest |x_i| (ties to the lower index; a chunk shorter than k gives all)
+#   C:    the refinement matrix, 4-bit integers with scale factors.
+# Readings (listed in the design notes): C is the 4-bit encoding of the weight
+# residual R = W - W_hat_eff (no refinement fitting: that needs calibration
+# data), quantised per input channel with the 4-bit Group-32 quantiser above
+# over groups of 32 consecutive output rows; each channel's column is one
+# contiguous record so that a selected column is fetched in one piece.
+# ---------------------------------------------------------------------------
+
+REFINE_CHUNK = 1024
+MAGIC_RF = b"LBQRFW4C"
+RF_VERSION = 1
+RF_HEADER = 64
+
+
+def refine_column_bytes(N: int) -> int:
+    """One column record: N/2 nibble bytes, N/32 FP16 scales, N/64 zero bytes, padded to 16."""
+    assert N % 64 == 0 and N > 0
+    return _up(N // 2 + N // 16 + N // 64, 16)
+
+
+def refine_layout(N: int, K: int) -> dict:
+    cb = refine_column_bytes(N)
+    return {"column_bytes": cb, "header": RF_HEADER, "total": RF_HEADER + K * cb,
+            "codes": 0, "scales": N // 2, "zeros": N // 2 + N // 16}
+
+
+def dequant_eff(blob: np.ndarray) -> np.ndarray:
+    """The matrix the resident GEMV applies, FP64: the dense dequantised weights,
+    with each outlier column replaced by its exact FP16 values."""
+    Wh = dequant(blob)
+    idx, vals = outliers(blob)
+    if idx.size:
+        Wh[:, idx] = vals
+    return Wh
+
+
+def pack_refine(R: np.ndarray) -> np.ndarray:
+    """Quantise the N x K FP32 residual column by column (groups of 32 rows) and
+    write the refinement blob:
+      [0:8) magic b"LBQRFW4C"  [8:12) u32 version 1  [12:16) u32 header bytes 64
+      [16:24) i64 N  [24:32) i64 K  [32:36) u32 group 32  [36:40) u32 column bytes
+      [40:48) u64 total bytes  [48:64) zero
+      then column i at 64 + i * column_bytes: nibbles (byte b of group g =
+      q_{32g+b} | q_{32g+b+16} << 4), FP16 scales, zero points z_{2m} | z_{2m+1} << 4."""
+    R = np.asarray(R, dtype=np.float32)
+    N, K = R.shape
+    L = refine_layout(N, K)
+    q, z, s = quantise_w4(R.astype(F64).T)           # rows = input channels, groups along N
+    s16 = fp16_round(s)
+    codes, zeros = pack_nibbles(q), pack_zero_points(z)
+    blob = np.zeros(L["total"], dtype=np.uint8)
+    blob[0:8] = np.frombuffer(MAGIC_RF, dtype=np.uint8)
+    hdr = np.array([RF_VERSION, RF_HEADER], dtype="<u4").view(np.uint8)
+    blob[8:16] = hdr
+    blob[16:32] = np.array([N, K], dtype="<i8").view(np.uint8)
+    blob[32:40] = np.array([G, L["column_bytes"]], dtype="<u4").view(np.uint8)
+    blob[40:48] = np.array([L["total"]], dtype="<u8").view(np.uint8)
+    cb = L["column_bytes"]
+    cols = blob[RF_HEADER:].reshape(K, cb)
+    cols[:, 0:N // 2] = codes
+    cols[:, N // 2:N // 2 + N // 16] = np.ascontiguousarray(s16.astype("<f2")).view(np.uint8).reshape(K, N // 16)
+    cols[:, N // 2 + N // 16:N // 2 + N // 16 + N // 64] = zeros
+    return blob
+
+
+def unpack_refine(blob: np.ndarray) -> np.ndarray:
+    """C (N x K, FP64) = (q - z) * s16 of every column record."""
+    assert bytes(blob[:8]) == MAGIC_RF
+    N = int(blob[16:24].view("<i8")[0])
+    K = int(blob[24:32].view("<i8")[0])
+    cb = int(blob[36:40].view("<u4")[0])
+    cols = blob[RF_HEADER:RF_HEADER + K * cb].reshape(K, cb)
+    qb = cols[:, :N // 2].reshape(K, N // 32, 16)
+    q = np.concatenate([qb & 0x0F, qb >> 4], axis=2).astype(F64)          # (K, N/32, 32)
+    s16 = np.ascontiguousarray(cols[:, N // 2:N // 2 + N // 16]).view("<f2").astype(F64)
+    zb = cols[:, N // 2 + N // 16:N // 2 + N // 16 + N // 64]
+    z = np.stack([zb & 0x0F, zb >> 4], axis=2).reshape(K, N // 32).astype(F64)
+    return ((q - z[..., None]) * s16[..., None]).reshape(K, N).T
+
+
+def select_refine(x: np.ndarray, k: int) -> np.ndarray:
+    """S(x): per chunk of 1,024 channels the min(k, chunk length) largest |x_i|,
+    ties to the lower index; ascending channel indices."""
+    a = np.abs(np.asarray(x, dtype=np.float16).astype(F64).reshape(-1))
+    out = []
+    for c0 in range(0, a.size, REFINE_CHUNK):
+        chunk = a[c0:c0 + REFINE_CHUNK]
+        out.append(top_indices(chunk, min(k, chunk.size)) + c0)
+    return np.concatenate(out).astype(np.int32) if out else np.zeros(0, np.int32)
+
+
+def refine_apply(blob: np.ndarray, x: np.ndarray, idx: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """y + sum_j x_{idx_j} C[:, idx_j], FP64, terms added in the order of idx."""
+    C = unpack_refine(blob)
+    xv = np.asarray(x, dtype=np.float16).astype(F64).reshape(-1)
+    out = np.asarray(y, dtype=F64).copy()
+    for i in np.asarray(idx, dtype=np.int64):
+        out = out + xv[i] * C[:, i]
+    return out
