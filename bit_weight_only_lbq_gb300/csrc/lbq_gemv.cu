@@ -1304,6 +1304,17 @@ lbq_status grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, in
 
 }  // namespace
 
+namespace lbq {
+lbq_status device_context(unsigned** err_word, int* sms) {
+    DeviceInfo* dev = nullptr;
+    const lbq_status st = device_info(&dev);
+    if (st != LBQ_OK) return st;
+    *err_word = dev->err_word;
+    *sms = dev->sms;
+    return LBQ_OK;
+}
+}  // namespace lbq
+
 extern "C" {
 
 lbq_status lbq_gemv_w4a16_ex(const void* packed, int64_t N, int64_t K, int32_t n_out, const void* x_f16, void* y,

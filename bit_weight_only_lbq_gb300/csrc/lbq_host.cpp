@@ -205,6 +205,26 @@ void write_header(uint8_t* dst, const char magic[8], int64_t N, int64_t K, int32
     std::memcpy(dst + 48, f, sizeof(f));
 }
 
+// SPECTRA 3.4 / App. A Prop. 2 on one group of 32 values, in FP64 with the
+// unrounded scale: s = max((wmax - wmin) / 15, 1e-8), z = clamp(round(-wmin / s)),
+// q = clamp(round(w / s + z)), rounding half to even.
+void quantise_group_w4(const double (&w)[kGroup], uint8_t (&q)[kGroup], double* s_out, uint8_t* z_out) {
+    double wmin = HUGE_VAL, wmax = -HUGE_VAL;
+    for (int k = 0; k < kGroup; ++k) {
+        wmin = std::min(wmin, w[k]);
+        wmax = std::max(wmax, w[k]);
+    }
+    const double s = std::max((wmax - wmin) / 15.0, kScaleFloor);
+    const double z = std::min(std::max(std::nearbyint(-wmin / s), 0.0), 15.0);
+    for (int k = 0; k < kGroup; ++k) {
+        double t = w[k] / s;
+        t = t + z;
+        q[k] = static_cast<uint8_t>(std::min(std::max(std::nearbyint(t), 0.0), 15.0));
+    }
+    *s_out = s;
+    *z_out = static_cast<uint8_t>(z);
+}
+
 // Byte offset of (row n, group g) inside the blob's record area: the record of
 // row block n/4 and group block g/32, plus the row-major (row, group) index.
 struct RecordAddr {
@@ -395,26 +415,17 @@ lbq_status lbq_pack_w4(const float* W, int64_t N, int64_t K, const int32_t* idx,
         for (int64_t n = b; n < e; ++n) {
             for (int64_t g = 0; g < ng; ++g) {
                 const RecordAddr ra = record_addr(L, n, g);
-                double wmin = HUGE_VAL, wmax = -HUGE_VAL;
                 for (int k = 0; k < kGroup; ++k) {
                     const int64_t col = g * kGroup + k;
                     w[k] = is_out[col] ? 0.0 : static_cast<double>(W[n * K + col]);
-                    wmin = std::min(wmin, w[k]);
-                    wmax = std::max(wmax, w[k]);
                 }
-                // SPECTRA 3.4 / App. A Prop. 2, in FP64 with the unrounded scale
-                const double s = std::max((wmax - wmin) / 15.0, kScaleFloor);
-                const double z = std::min(std::max(std::nearbyint(-wmin / s), 0.0), 15.0);
-                for (int k = 0; k < kGroup; ++k) {
-                    double t = w[k] / s;
-                    t = t + z;
-                    q[k] = static_cast<uint8_t>(std::min(std::max(std::nearbyint(t), 0.0), 15.0));
-                }
+                double s;
+                uint8_t zi;
+                quantise_group_w4(w, q, &s, &zi);
                 uint8_t* qdst = out + ra.rec + uint64_t(ra.slot) * 16;
                 for (int k = 0; k < 16; ++k) qdst[k] = static_cast<uint8_t>(q[k] | (q[k + 16] << 4));
                 const uint16_t sh = f64_to_f16_bits(s);
                 std::memcpy(out + ra.rec + kW4ScaleOff + uint64_t(ra.slot) * 2, &sh, 2);
-                const uint8_t zi = static_cast<uint8_t>(z);
                 uint8_t* zdst = out + ra.rec + kW4ZeroOff + (ra.slot >> 1);   // (row * 32 + group) / 2
                 if (g % 2 == 0)
                     *zdst = zi;
@@ -493,6 +504,126 @@ lbq_status lbq_pack_w2cb(const float* W, int64_t N, int64_t K, const int32_t* id
                 for (int i = 0; i < kGroup / 4; ++i)
                     cdst[i] = static_cast<uint8_t>(q[4 * i] | (q[4 * i + 1] << 2) | (q[4 * i + 2] << 4) |
                                                    (q[4 * i + 3] << 6));
+            }
+        }
+    });
+    return LBQ_OK;
+}
+
+// ------------------------------------------------------- selective refinement
+
+size_t lbq_refine_packed_bytes(int64_t N, int64_t K) {
+    if (N < 64 || N % 64 || N > INT32_MAX || K < 1 || K > lbq::kMaxK) return 0;
+    return lbq::kRefineHeader + static_cast<size_t>(K) * lbq::refine_column_bytes(N);
+}
+
+lbq_status lbq_pack_refine(const float* R, int64_t N, int64_t K, void* dst, size_t dst_bytes) {
+    if (!R || !dst) return LBQ_ERR_NULL;
+    const size_t total = lbq_refine_packed_bytes(N, K);
+    if (total == 0) return LBQ_ERR_SHAPE;
+    if (dst_bytes < total) return LBQ_ERR_BUFFER_TOO_SMALL;
+    if (!all_finite(R, N * K)) return LBQ_ERR_VALUE;
+    uint8_t* out = static_cast<uint8_t*>(dst);
+    std::memset(out, 0, total);
+    const uint64_t cb = lbq::refine_column_bytes(N);
+    std::memcpy(out, "LBQRFW4C", 8);
+    const uint32_t version = lbq::kRefineVersion, hbytes = lbq::kRefineHeader, group = kGroup,
+                   cb32 = static_cast<uint32_t>(cb);
+    const uint64_t tot = total;
+    std::memcpy(out + 8, &version, 4);
+    std::memcpy(out + 12, &hbytes, 4);
+    std::memcpy(out + 16, &N, 8);
+    std::memcpy(out + 24, &K, 8);
+    std::memcpy(out + 32, &group, 4);
+    std::memcpy(out + 36, &cb32, 4);
+    std::memcpy(out + 40, &tot, 8);
+    const int64_t ng = N / kGroup;
+    parallel_for(K, [&](int64_t b, int64_t e) {
+        double w[kGroup];
+        uint8_t q[kGroup];
+        for (int64_t i = b; i < e; ++i) {
+            uint8_t* col = out + lbq::kRefineHeader + uint64_t(i) * cb;
+            for (int64_t g = 0; g < ng; ++g) {
+                for (int k = 0; k < kGroup; ++k) w[k] = static_cast<double>(R[(g * kGroup + k) * K + i]);
+                double s;
+                uint8_t z;
+                quantise_group_w4(w, q, &s, &z);
+                for (int k = 0; k < 16; ++k) col[g * 16 + k] = static_cast<uint8_t>(q[k] | (q[k + 16] << 4));
+                const uint16_t sh = f64_to_f16_bits(s);
+                std::memcpy(col + N / 2 + g * 2, &sh, 2);
+                uint8_t* zb = col + N / 2 + N / 16 + g / 2;
+                *zb = (g % 2 == 0) ? z : static_cast<uint8_t>(*zb | (z << 4));
+            }
+        }
+    });
+    return LBQ_OK;
+}
+
+lbq_status lbq_dequant_host(const void* packed, size_t packed_bytes, float* W_hat) {
+    if (!packed || !W_hat) return LBQ_ERR_NULL;
+    const uint8_t* in = static_cast<const uint8_t*>(packed);
+    if (packed_bytes < kHeaderBytes) return LBQ_ERR_BUFFER_TOO_SMALL;
+    const bool w4 = std::memcmp(in, "LBQW4G32", 8) == 0, w2 = std::memcmp(in, "LBQW2C32", 8) == 0;
+    uint32_t version;
+    std::memcpy(&version, in + 8, 4);
+    if ((!w4 && !w2) || version != LBQ_FORMAT_VERSION_NUM) return LBQ_ERR_FORMAT;
+    int64_t N, K;
+    int32_t n_out;
+    std::memcpy(&N, in + 16, 8);
+    std::memcpy(&K, in + 24, 8);
+    std::memcpy(&n_out, in + 32, 4);
+    if (!shape_ok(N, K, n_out)) return LBQ_ERR_FORMAT;
+    lbq_layout L;
+    lbq_status st = lbq_blob_layout(w4 ? LBQ_KIND_W4 : LBQ_KIND_W2CB, N, K, n_out, &L);
+    if (st != LBQ_OK) return st;
+    if (packed_bytes < L.total_bytes) return LBQ_ERR_BUFFER_TOO_SMALL;
+    std::vector<int32_t> idx(static_cast<size_t>(n_out));
+    if (n_out > 0) std::memcpy(idx.data(), in + L.idx_offset, sizeof(int32_t) * n_out);
+    st = check_idx(idx.data(), n_out, K);
+    if (st != LBQ_OK) return LBQ_ERR_FORMAT;
+    const Codebook& cbk = codebook();
+    const int64_t ng = K / kGroup;
+    parallel_for(N, [&](int64_t b, int64_t e) {
+        for (int64_t n = b; n < e; ++n) {
+            for (int64_t g = 0; g < ng; ++g) {
+                const RecordAddr ra = record_addr(L, n, g);
+                float* wrow = W_hat + n * K + g * kGroup;
+                if (w4) {
+                    uint16_t sh;
+                    std::memcpy(&sh, in + ra.rec + kW4ScaleOff + uint64_t(ra.slot) * 2, 2);
+                    const double s = f16_bits_to_f64(sh);
+                    const uint8_t zb = in[ra.rec + kW4ZeroOff + (ra.slot >> 1)];
+                    const double z = (g % 2 == 0) ? (zb & 15) : (zb >> 4);
+                    const uint8_t* qb = in + ra.rec + uint64_t(ra.slot) * 16;
+                    for (int k = 0; k < 16; ++k) {
+                        const double lo = static_cast<double>(qb[k] & 15) - z, hi = static_cast<double>(qb[k] >> 4) - z;
+                        wrow[k] = static_cast<float>(lo * s);
+                        wrow[k + 16] = static_cast<float>(hi * s);
+                    }
+                } else {
+                    uint16_t Sh, Zh;
+                    std::memcpy(&Sh, in + ra.rec + kW2SOff + uint64_t(ra.slot) * 2, 2);
+                    std::memcpy(&Zh, in + ra.rec + kW2ZOff + uint64_t(ra.slot) * 2, 2);
+                    const double S = f16_bits_to_f64(Sh), Z = f16_bits_to_f64(Zh);
+                    const uint8_t* cq = in + ra.rec + uint64_t(ra.slot) * 8;
+                    for (int k = 0; k < kGroup; ++k) {
+                        const double sc = S * cbk.val[(cq[k / 4] >> (2 * (k % 4))) & 3];
+                        wrow[k] = static_cast<float>(sc + Z);
+                    }
+                }
+            }
+            // outlier columns: their exact FP16 values
+            const uint64_t base = L.area_offset + uint64_t(n / lbq::kRowsPerBlock) * L.row_block_bytes +
+                                  L.records * L.record_bytes;
+            const int r = int(n % lbq::kRowsPerBlock);
+            for (int32_t j = 0; j < n_out; ++j) {
+                const int32_t rec = j / lbq::kOutlierCols;
+                const uint64_t width = std::min<uint64_t>(
+                    lbq::kOutlierCols, round_up(uint64_t(n_out), lbq::kOutlierColAlign) - uint64_t(rec) * lbq::kOutlierCols);
+                uint16_t h;
+                std::memcpy(&h, in + base + uint64_t(rec) * L.outlier_record_bytes +
+                                    (uint64_t(r) * width + uint64_t(j % lbq::kOutlierCols)) * 2, 2);
+                W_hat[n * K + idx[j]] = static_cast<float>(f16_bits_to_f64(h));
             }
         }
     });

@@ -8,6 +8,12 @@
 #define LBQ_VERSION_NUM 100          // 0.1.0
 #define LBQ_FORMAT_VERSION_NUM 2
 
+#ifdef __CUDACC__
+#define LBQ_HOST_DEVICE __host__ __device__
+#else
+#define LBQ_HOST_DEVICE
+#endif
+
 namespace lbq {
 
 constexpr int64_t kMaxK = 65536;          // x of one row block must fit in shared memory
@@ -18,6 +24,21 @@ constexpr int kRecordGroups = 32;         // groups of 32 weights per dense reco
 constexpr int kOutlierCols = 256;         // outlier columns per full outlier record
 constexpr int kOutlierColAlign = 8;       // the last outlier record's width is a multiple of this
 constexpr int kMaxM = 64;                 // largest batch of the small-M entry point
+
+// selective refinement blob (lbq_pack_refine / lbq_refine_apply): 64-byte
+// header, then one record per input channel of N/2 nibble bytes, N/32 FP16
+// scales and N/64 zero-point bytes, padded to 16 bytes
+constexpr uint32_t kRefineHeader = 64;
+constexpr uint32_t kRefineVersion = 1;
+constexpr int kRefineChunk = 1024;        // channels per selection chunk
+constexpr int kRefineMaxK = 256;          // largest channels-per-chunk budget
+LBQ_HOST_DEVICE inline uint64_t refine_column_bytes(int64_t N) {
+    return (static_cast<uint64_t>(N / 2 + N / 16 + N / 64) + 15) / 16 * 16;
+}
+
+// The device error word of the library and the SM count of the current device
+// (lbq_gemv.cu); LBQ_ERR_UNSUPPORTED without an sm_103a device.
+lbq_status device_context(unsigned** err_word, int* sms);
 
 uint16_t host_f64_to_f16(double v);
 

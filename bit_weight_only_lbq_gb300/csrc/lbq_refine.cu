@@ -1,0 +1,227 @@
+// Selective weight refinement on sm_103a: exact per-chunk top-k channel
+// selection and the gathered 4-bit column correction
+//     y' = y + sum_{i in S(x)} x_i C[:, i]
+// (StrataFlux paper, section 3 "Weight Refinement", Eq. 2, and "Channel
+// selection": k channels of largest |x_i| per chunk of 1,024 input channels;
+// Appendix "StrataFlux Implementation": exact radix-sort selection instead of
+// bucket selection).  C is stored as one contiguous record per input channel
+// (lbq_pack_refine), so a selected column is fetched in one piece.
+//
+// GB300 design:
+//  * selection: one CTA of 1,024 threads per chunk, one channel per thread.
+//    The key (|x| as its 15 FP16 magnitude bits, then 1023 - channel) is unique,
+//    so a most-significant-digit radix select (9 + 8 + 8 bits, shared-memory
+//    histograms, a warp-parallel scan of the bins) finds the k-th largest key
+//    exactly; ties in |x| go to the lower channel.  The selected channels are
+//    written in ascending order with a ballot prefix sum.
+//  * apply: one CTA per 256 output rows, 8 warps taking every 8th selected
+//    column; a lane owns one 32-bit nibble word (8 rows) of a group and
+//    accumulates x_i (q - z) s in FP32 ((q - z) s is exact in FP32); the 8
+//    warps' partial rows are added in warp order (deterministic) and added to y.
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "lbq.h"
+#include "lbq_internal.h"
+
+namespace {
+
+constexpr int kChunk = lbq::kRefineChunk;
+constexpr int kApplyRows = 256;
+constexpr int kApplyWarps = 8;
+
+// Warp-parallel search of the histogram from its top bin down: the bin in which
+// the running count reaches `remaining`; returns it and the count above it.
+__device__ void find_bin(const unsigned* hist, int nbins, unsigned remaining, int lane, int* bin_out,
+                         unsigned* above_out) {
+    const int per = nbins / 32;                       // bins per lane, lane 0 the highest
+    const int top = nbins - per * lane;               // lane covers [top - per, top)
+    unsigned mine = 0;
+    for (int b = top - 1; b >= top - per; --b) mine += hist[b];
+    unsigned incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const unsigned excl = incl - mine;
+    const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining && excl < remaining);
+    const int src = __ffs(hit) - 1;
+    if (lane == src) {
+        unsigned cum = excl;
+        for (int b = top - 1; b >= top - per; --b) {
+            if (cum + hist[b] >= remaining) {
+                *bin_out = b;
+                *above_out = cum;
+                break;
+            }
+            cum += hist[b];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half* __restrict__ x, int K, int k,
+                                                                   int32_t* __restrict__ idx) {
+    __shared__ unsigned hist[512];
+    __shared__ int s_bin;
+    __shared__ unsigned s_above;
+    __shared__ unsigned warp_cnt[kChunk / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int base = blockIdx.x * kChunk;
+    const int len = min(kChunk, K - base);
+    const int kk = min(k, len);
+    const bool valid = t < len;
+    unsigned key = 0;
+    if (valid) {
+        const unsigned short h = __half_as_ushort(x[base + t]);
+        key = (static_cast<unsigned>(h & 0x7FFFu) << 10) | static_cast<unsigned>(kChunk - 1 - t);
+    }
+    // threshold = the kk-th largest key (every key when the chunk has <= k channels)
+    unsigned thr = 0;
+    if (kk < len) {
+        unsigned prefix = 0, remaining = static_cast<unsigned>(kk);
+        // digits: key bits 24..16 (512 bins), 15..8, 7..0 (256 bins each)
+        for (int pass = 0; pass < 3; ++pass) {
+            const int shift = pass == 0 ? 16 : pass == 1 ? 8 : 0;
+            const int nbins = pass == 0 ? 512 : 256;
+            for (int b = t; b < 512; b += kChunk) hist[b] = 0u;
+            __syncthreads();
+            const bool cand = valid && (pass == 0 || (key >> (shift + 8)) == prefix);
+            if (cand) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+            __syncthreads();
+            if (warp == 0) find_bin(hist, nbins, remaining, lane, &s_bin, &s_above);
+            __syncthreads();
+            prefix = (pass == 0) ? static_cast<unsigned>(s_bin) : ((prefix << 8) | static_cast<unsigned>(s_bin));
+            remaining -= s_above;
+            __syncthreads();
+        }
+        thr = prefix;   // all 25 bits: unique keys, so exactly kk keys are >= thr
+    }
+    const bool sel = valid && key >= thr;
+    // ascending output: ballot prefix sum over the CTA
+    const unsigned bal = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) warp_cnt[warp] = __popc(bal);
+    __syncthreads();
+    if (sel) {
+        unsigned off = __popc(bal & ((1u << lane) - 1u));
+        for (int w = 0; w < warp; ++w) off += warp_cnt[w];
+        idx[static_cast<long long>(blockIdx.x) * k + off] = base + t;
+    }
+}
+
+__global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint8_t* __restrict__ blob, int N, int K,
+                                                                      const __half* __restrict__ x,
+                                                                      const int32_t* __restrict__ idx, int nsel,
+                                                                      void* y, int y_f32, unsigned* err) {
+    __shared__ float part[kApplyWarps][kApplyRows];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row0 = blockIdx.x * kApplyRows;
+    const int g = (row0 >> 5) + (lane >> 2), wd = lane & 3;     // group and nibble word of this lane
+    const bool rows_ok = g * 32 < N;
+    const uint64_t cb = lbq::refine_column_bytes(N);
+    if (blockIdx.x == 0 && tid == 0) {
+        const unsigned* h = reinterpret_cast<const unsigned*>(blob);
+        long long n_hdr, k_hdr;
+        memcpy(&n_hdr, blob + 16, 8);
+        memcpy(&k_hdr, blob + 24, 8);
+        if (h[0] != 0x5251424Cu || h[1] != 0x43345746u || h[2] != lbq::kRefineVersion || n_hdr != N || k_hdr != K)
+            atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_FORMAT));
+    }
+    float acc[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) acc[b] = 0.f;
+    for (int j = warp; j < nsel; j += kApplyWarps) {
+        const int i = idx[j];
+        if (i < 0 || i >= K) {
+            if (lane == 0) atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
+            continue;
+        }
+        if (!rows_ok) continue;
+        const float xi = __half2float(x[i]);
+        const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(i) * cb;
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
+        const float s = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
+        const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
+        const float z = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float lo = (static_cast<float>((word >> (8 * b)) & 15u) - z) * s;       // row 4 wd + b
+            const float hi = (static_cast<float>((word >> (8 * b + 4)) & 15u) - z) * s;   // row 16 + 4 wd + b
+            acc[b] = fmaf(lo, xi, acc[b]);
+            acc[4 + b] = fmaf(hi, xi, acc[4 + b]);
+        }
+    }
+    const int rbase = (lane >> 2) * 32 + 4 * wd;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        part[warp][rbase + b] = acc[b];
+        part[warp][rbase + 16 + b] = acc[4 + b];
+    }
+    __syncthreads();
+    const int n = row0 + tid;
+    if (n < N) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kApplyWarps; ++w) tot += part[w][tid];
+        if (y_f32) {
+            float* yf = static_cast<float*>(y);
+            yf[n] = yf[n] + tot;
+        } else {
+            __half* yh = static_cast<__half*>(y);
+            yh[n] = __float2half_rn(__half2float(yh[n]) + tot);
+        }
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int64_t lbq_refine_selected_count(int64_t K, int32_t k) {
+    if (K < 1 || K > lbq::kMaxK || k < 1 || k > lbq::kRefineMaxK) return 0;
+    const int64_t full = K / kChunk, rest = K % kChunk;
+    return full * k + (rest < k ? rest : k);
+}
+
+lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* idx, void* stream) {
+    if (!x_f16 || !idx) return LBQ_ERR_NULL;
+    if (K < 1 || K > lbq::kMaxK || k < 1 || k > lbq::kRefineMaxK) return LBQ_ERR_SHAPE;
+    if (!aligned(x_f16, 2) || !aligned(idx, 4)) return LBQ_ERR_ALIGN;
+    unsigned* err = nullptr;
+    int sms = 0;
+    const lbq_status st = lbq::device_context(&err, &sms);
+    if (st != LBQ_OK) return st;
+    const unsigned grid = static_cast<unsigned>((K + kChunk - 1) / kChunk);
+    lbq_refine_select_kernel<<<grid, kChunk, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __half*>(x_f16), static_cast<int>(K), k, idx);
+    if (cudaGetLastError() != cudaSuccess) return LBQ_ERR_CUDA;
+    return LBQ_OK;
+}
+
+lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void* x_f16, const int32_t* idx,
+                            int32_t n_sel, void* y, lbq_dtype y_dtype, void* stream) {
+    if (!refine || !x_f16 || !y || (n_sel > 0 && !idx)) return LBQ_ERR_NULL;
+    if (N < 64 || N % 64 || N > INT32_MAX || K < 1 || K > lbq::kMaxK || n_sel < 0 || n_sel > K)
+        return LBQ_ERR_SHAPE;
+    if (y_dtype != LBQ_F16 && y_dtype != LBQ_F32) return LBQ_ERR_UNSUPPORTED;
+    if (!aligned(refine, 16) || !aligned(x_f16, 2) || !aligned(y, y_dtype == LBQ_F32 ? 4 : 2) ||
+        (idx && !aligned(idx, 4)))
+        return LBQ_ERR_ALIGN;
+    unsigned* err = nullptr;
+    int sms = 0;
+    const lbq_status st = lbq::device_context(&err, &sms);
+    if (st != LBQ_OK) return st;
+    const unsigned grid = static_cast<unsigned>((N + kApplyRows - 1) / kApplyRows);
+    lbq_refine_apply_kernel<<<grid, kApplyRows, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(refine), static_cast<int>(N), static_cast<int>(K),
+        static_cast<const __half*>(x_f16), idx, n_sel, y, y_dtype == LBQ_F32 ? 1 : 0, err);
+    if (cudaGetLastError() != cudaSuccess) return LBQ_ERR_CUDA;
+    return LBQ_OK;
+}
+
+}  // extern "C"

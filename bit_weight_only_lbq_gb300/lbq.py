@@ -38,7 +38,8 @@ EXPORTS = (
     "lbq_gemv_w2cb_outlier", "lbq_gemm_w4a16_smallM", "lbq_gemv_w4a16_ex",
     "lbq_gemv_w2cb_outlier_ex", "lbq_gemm_w4a16_smallM_ex", "lbq_gemm_w2cb_outlier_smallM",
     "lbq_gemm_w2cb_outlier_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
-    "lbq_selftest_wait_timeout", "lbq_device_error",
+    "lbq_selftest_wait_timeout", "lbq_device_error", "lbq_refine_packed_bytes", "lbq_pack_refine",
+    "lbq_dequant_host", "lbq_refine_selected_count", "lbq_refine_select", "lbq_refine_apply",
 )
 
 
@@ -111,6 +112,12 @@ def lib():
                                                          ctypes.c_int, ctypes.POINTER(c_i32)]),
             "lbq_selftest_wait_timeout": (ctypes.c_int, [c_u32, c_vp]),
             "lbq_device_error": (ctypes.c_int, [c_vp]),
+            "lbq_refine_packed_bytes": (c_sz, [c_i64, c_i64]),
+            "lbq_pack_refine": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_sz]),
+            "lbq_dequant_host": (ctypes.c_int, [c_vp, c_sz, c_vp]),
+            "lbq_refine_selected_count": (c_i64, [c_i64, c_i32]),
+            "lbq_refine_select": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_vp]),
+            "lbq_refine_apply": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_vp, c_i32, c_vp, ctypes.c_int, c_vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -197,6 +204,32 @@ def pack_w2cb(W, idx=None) -> np.ndarray:
     return out
 
 
+def pack_refine(R) -> np.ndarray:
+    """Refinement blob of an N x K residual (column records, see include/lbq.h)."""
+    R = _as_f32(R)
+    N, K = R.shape
+    nb = lib().lbq_refine_packed_bytes(N, K)
+    if nb == 0:
+        raise LbqError(2, "lbq_refine_packed_bytes")
+    out = np.empty(nb, np.uint8)
+    _check(lib().lbq_pack_refine(_ptr(R), N, K, _ptr(out), nb), "lbq_pack_refine")
+    return out
+
+
+def dequant_host(blob) -> np.ndarray:
+    """The N x K FP32 matrix a resident blob applies (outlier columns exact)."""
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    N = int(blob[16:24].view("<i8")[0])
+    K = int(blob[24:32].view("<i8")[0])
+    out = np.empty((N, K), np.float32)
+    _check(lib().lbq_dequant_host(_ptr(blob), blob.size, _ptr(out)), "lbq_dequant_host")
+    return out
+
+
+def refine_selected_count(K: int, k: int) -> int:
+    return int(lib().lbq_refine_selected_count(K, k))
+
+
 # ---------------------------------------------------------------- device side
 
 def _dev_ptr(t) -> int:
@@ -253,6 +286,18 @@ def gemm_w2cb_outlier_smallM(packed, M: int, N: int, K: int, n_out: int, X, ldx:
     _check(lib().lbq_gemm_w2cb_outlier_smallM_ex(_dev_ptr(packed), M, N, K, n_out, _dev_ptr(X), ldx, _dev_ptr(Y),
                                                  ldy, yd, _stream(stream), LBQ_FLAG_PDL if pdl else 0),
            "lbq_gemm_w2cb_outlier_smallM")
+
+
+def refine_select(x, K: int, k: int, idx, stream=None):
+    """S(x) of a device FP16 vector into the device int32 buffer idx."""
+    _check(lib().lbq_refine_select(_dev_ptr(x), K, k, _dev_ptr(idx), _stream(stream)), "lbq_refine_select")
+
+
+def refine_apply(refine, N: int, K: int, x, idx, n_sel: int, y, stream=None, y_dtype: int | None = None):
+    """y += sum over the n_sel selected channels of x_i C[:, i] (device buffers)."""
+    yd = _ydtype(y) if y_dtype is None else y_dtype
+    _check(lib().lbq_refine_apply(_dev_ptr(refine), N, K, _dev_ptr(x), _dev_ptr(idx) if n_sel else None, n_sel,
+                                  _dev_ptr(y), yd, _stream(stream)), "lbq_refine_apply")
 
 
 def _problems(problems, y_dtype):

@@ -280,6 +280,60 @@ lbq_status lbq_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * the synchronisation itself are reported as LBQ_ERR_CUDA. */
 lbq_status lbq_device_error(void* stream);
 
+/* ------------------------------------------------------------------------
+ * Selective weight refinement (StrataFlux paper, section 3 "Weight
+ * Refinement", Eq. 2, and "Channel selection"; Appendix "StrataFlux
+ * Implementation": exact radix-sort selection):
+ *     y' = y + sum_{i in S(x)} x_i C[:, i]
+ * S(x): for each chunk of 1,024 consecutive input channels (the last one may
+ * be shorter), the min(k, chunk length) channels of largest |x_i|, ties to the
+ * lower channel.  C: N x K refinement values as 4-bit integers with FP16 scale
+ * and 4-bit zero point per 32 consecutive output rows of a column (the 4-bit
+ * Group-32 rules of lbq_pack_w4 applied down each column), stored as one
+ * contiguous record per input channel:
+ *   [0:8) "LBQRFW4C"  [8:12) u32 version 1  [12:16) u32 header bytes 64
+ *   [16:24) i64 N  [24:32) i64 K  [32:36) u32 group 32  [36:40) u32 column bytes
+ *   [40:48) u64 total bytes  [48:64) zero; then column i at 64 + i * column
+ *   bytes: N/2 nibble bytes (byte b of group g = q_{32g+b} | q_{32g+b+16} << 4),
+ *   N/32 FP16 scales, N/64 bytes of zero points z_{2m} | z_{2m+1} << 4, zero
+ *   padding to a multiple of 16.
+ * The pages fit C to calibration data; this library encodes the residual the
+ * caller passes (e.g. W - W_hat from lbq_dequant_host), as DecDEC does.
+ * N % 64 == 0, 1 <= K <= 65536, 1 <= k <= 256. */
+
+/* Bytes of a refinement blob; 0 for an unsupported shape. */
+size_t lbq_refine_packed_bytes(int64_t N, int64_t K);
+
+/* Host: quantise the N x K FP32 row-major matrix R column by column and write
+ * the refinement blob into dst (caller-allocated host memory, dst_bytes >=
+ * lbq_refine_packed_bytes).  LBQ_ERR_VALUE for non-finite input. */
+lbq_status lbq_pack_refine(const float* R, int64_t N, int64_t K, void* dst, size_t dst_bytes);
+
+/* Host: the matrix a resident blob applies, as N x K FP32 row-major: the
+ * dequantised dense weights (4-bit (q - z) s, 2-bit S C[q] + Z, evaluated in
+ * FP64 and rounded once to FP32) with each outlier column replaced by its
+ * exact FP16 values.  packed: host copy of a blob of either kind. */
+lbq_status lbq_dequant_host(const void* packed, size_t packed_bytes, float* W_hat);
+
+/* Number of channels lbq_refine_select writes for (K, k); 0 for bad arguments. */
+int64_t lbq_refine_selected_count(int64_t K, int32_t k);
+
+/* Device: S(x) of a K-vector of FP16 activations, written to idx (device,
+ * lbq_refine_selected_count(K, k) int32): chunk c's channels at [c k, ...),
+ * ascending.  One CTA per chunk.  Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE,
+ * LBQ_ERR_ALIGN (x 2-byte, idx 4-byte aligned), LBQ_ERR_UNSUPPORTED,
+ * LBQ_ERR_CUDA. */
+lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* idx, void* stream);
+
+/* Device: y[n] += sum_{j < n_sel} x[idx_j] C[n, idx_j] for the refinement blob
+ * `refine` (device, 16-byte aligned) of shape (N, K); y (device, N values of
+ * y_dtype) is read and written, each element by one thread; the columns are
+ * summed in FP32 in a fixed order (deterministic).  An index outside [0, K)
+ * is skipped and reported as LBQ_ERR_VALUE, a header mismatch as
+ * LBQ_ERR_FORMAT, both through lbq_device_error. */
+lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void* x_f16, const int32_t* idx,
+                            int32_t n_sel, void* y, lbq_dtype y_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

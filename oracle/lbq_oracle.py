@@ -583,13 +583,16 @@ def pack_refine(R: np.ndarray) -> np.ndarray:
     return blob
 
 
-def unpack_refine(blob: np.ndarray) -> np.ndarray:
-    """C (N x K, FP64) = (q - z) * s16 of every column record."""
+def unpack_refine(blob: np.ndarray, cols=None) -> np.ndarray:
+    """C (N x K, FP64) = (q - z) * s16 of every column record (or only of the
+    listed columns, in that order: N x len(cols))."""
     assert bytes(blob[:8]) == MAGIC_RF
     N = int(blob[16:24].view("<i8")[0])
     K = int(blob[24:32].view("<i8")[0])
     cb = int(blob[36:40].view("<u4")[0])
-    cols = blob[RF_HEADER:RF_HEADER + K * cb].reshape(K, cb)
+    sel = np.arange(K) if cols is None else np.asarray(cols, dtype=np.int64)
+    K = sel.size
+    cols = blob[RF_HEADER:].reshape(-1, cb)[sel]
     qb = cols[:, :N // 2].reshape(K, N // 32, 16)
     q = np.concatenate([qb & 0x0F, qb >> 4], axis=2).astype(F64)          # (K, N/32, 32)
     s16 = np.ascontiguousarray(cols[:, N // 2:N // 2 + N // 16]).view("<f2").astype(F64)
@@ -611,9 +614,10 @@ def select_refine(x: np.ndarray, k: int) -> np.ndarray:
 
 def refine_apply(blob: np.ndarray, x: np.ndarray, idx: np.ndarray, y: np.ndarray) -> np.ndarray:
     """y + sum_j x_{idx_j} C[:, idx_j], FP64, terms added in the order of idx."""
-    C = unpack_refine(blob)
+    idx = np.asarray(idx, dtype=np.int64)
+    C = unpack_refine(blob, idx)                       # the selected columns only
     xv = np.asarray(x, dtype=np.float16).astype(F64).reshape(-1)
     out = np.asarray(y, dtype=F64).copy()
-    for i in np.asarray(idx, dtype=np.int64):
-        out = out + xv[i] * C[:, i]
+    for j, i in enumerate(idx):
+        out = out + xv[i] * C[:, j]
     return out

@@ -62,3 +62,53 @@ def test_llama8b_qproj_rows_bitexact(lbq):
     idx = lbq.select_outliers_w4(W)
     assert np.array_equal(idx, O.select_outliers_w4(W))
     assert np.array_equal(lbq.pack_w4(W, idx), O.pack_w4(W, idx))
+
+
+@pytest.mark.parametrize("kind", ["w4", "w2"])
+@pytest.mark.parametrize("N,K,n_out", [(4, 64, 0), (17, 192, 7), (64, 1088, 40), (33, 4160, 300)])
+def test_dequant_host_matches_oracle(lbq, kind, N, K, n_out):
+    """lbq_dequant_host: the matrix a blob applies, FP64 then one FP32 rounding."""
+    W = synth.random_matrix(N, K, seed=N + K + n_out, scale=0.02)
+    idx = np.sort(np.random.default_rng(N).choice(K, size=n_out, replace=False)).astype(np.int32)
+    pack, opack = (lbq.pack_w4, O.pack_w4) if kind == "w4" else (lbq.pack_w2cb, O.pack_w2cb)
+    got = lbq.dequant_host(pack(W, idx))
+    assert np.array_equal(got, O.dequant_eff(opack(W, idx)).astype(np.float32))
+
+
+@pytest.mark.parametrize("N,K", [(64, 1), (64, 3), (128, 1088), (192, 2049), (4096, 17)])
+def test_refine_pack_bitexact(lbq, N, K):
+    R = synth.random_matrix(N, K, seed=N * 3 + K, scale=1e-3)
+    R[:, 0] = 0.25                                   # a constant column (reconstructs to 0)
+    blob = lbq.pack_refine(R)
+    assert blob.size == lbq.lib().lbq_refine_packed_bytes(N, K) == O.refine_layout(N, K)["total"]
+    assert np.array_equal(blob, O.pack_refine(R))
+
+
+def test_refine_golden_through_cpp(lbq, golden):
+    g = golden("refine_column_example.txt")
+    q0 = np.array([int(t) for t in g["col0_q_group0"]])
+    R = np.zeros((64, 2), np.float32)
+    R[:32, 0] = (q0 - 3) / 1024.0
+    R[:, 1] = 0.5
+    blob = lbq.pack_refine(R)
+    cb = int(g["column_bytes"][0])
+    assert blob[:64].tolist() == [int(v, 16) for v in g["header"]]
+    assert blob[64:64 + cb].tolist() == [int(v, 16) for v in g["col0_record"]]
+    assert blob[64 + cb:64 + 2 * cb].tolist() == [int(v, 16) for v in g["col1_record"]]
+
+
+def test_refine_host_argument_checks(lbq):
+    L = lbq.lib()
+    assert L.lbq_refine_packed_bytes(96, 4) == 0           # N % 64
+    assert L.lbq_refine_packed_bytes(64, 0) == 0
+    assert L.lbq_refine_packed_bytes(64, 65537) == 0
+    assert L.lbq_refine_selected_count(2112, 8) == 8 + 8 + 8
+    assert L.lbq_refine_selected_count(2112, 100) == 100 + 100 + 64
+    assert L.lbq_refine_selected_count(64, 0) == 0 and L.lbq_refine_selected_count(64, 257) == 0
+    R = np.full((64, 2), np.nan, np.float32)
+    buf = np.empty(L.lbq_refine_packed_bytes(64, 2), np.uint8)
+    assert L.lbq_pack_refine(R.ctypes.data, 64, 2, buf.ctypes.data, buf.size) == 9   # LBQ_ERR_VALUE
+    assert L.lbq_pack_refine(R.ctypes.data, 64, 2, buf.ctypes.data, buf.size - 1) == 5  # too small
+    bad = np.zeros(256, np.uint8)
+    out = np.empty((1, 64), np.float32)
+    assert L.lbq_dequant_host(bad.ctypes.data, bad.size, out.ctypes.data) == 6        # LBQ_ERR_FORMAT
