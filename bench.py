@@ -162,7 +162,7 @@ def make_workload(lbq, rank: int):
         W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li + 100 * rank)
         x = synth.activations(1, K, config_id=2, layer_id=li)[0]
         layer.append(dict(kind="w4", name=name, N=N, K=K, n_out=0, M=1, blob=lbq.pack_w4(W), x=x,
-                          W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=np.zeros(0, np.int32)))
+                          W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=np.zeros(0, np.int32), li=li + 100 * rank))
     for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
         W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li + 100 * rank)
         prof = synth.profile_vectors(K, config_id=3, layer_id=li)
@@ -432,6 +432,7 @@ def main():
         g = capture(lambda: [launch(lbq, e, b, xs[i], ys[i], pdl=True) for b in blobs])
         per_call.append(time_graph(g, len(blobs), replays))
         del g, extra
+    refinement = run_refinement(lbq, layer, dev, stream)
     sweep70b = None
     if not args.no_sweep70b:
         sweep70b = run_sweep70b(lbq, dev, stream)
@@ -506,7 +507,7 @@ def main():
                            1.0 / (32 * sum(statistics.median(per_call[i]) for i, e in enumerate(layer)
                                            if e["kind"] == "w4") * 1e-3), 1)},
                    "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes,
-                   "llama3_70b_sweep": sweep70b},
+                   "llama3_70b_sweep": sweep70b, "selective_refinement": refinement},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layer)
@@ -515,6 +516,66 @@ def main():
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+REFINE_K = 16   # channels per 1,024-channel chunk (1.6 % of the input channels)
+
+
+def run_refinement(lbq, layer, dev, stream, replays=20):
+    """Selective refinement after each 4-bit linear of the layer: select the
+    REFINE_K largest |x_i| of every 1,024-channel chunk, then add their 4-bit
+    residual columns (C = Q4(W - W_hat)).  Timed as select + apply, chained in
+    a CUDA graph over rotating copies of the refinement blob (>= 512 MB), so the
+    gathered columns come from HBM."""
+    import torch
+    out = {"k_per_chunk": REFINE_K, "per_linear": []}
+    total_us = 0.0
+    for e in layer:
+        if e["kind"] != "w4":
+            continue
+        N, K = e["N"], e["K"]
+        R = (synth.weights_heavy_cols(N, K, config_id=2, layer_id=e["li"]) - lbq.dequant_host(e["blob"]))
+        rblob = lbq.pack_refine(R.astype(np.float32))
+        del R
+        n_sel = lbq.refine_selected_count(K, REFINE_K)
+        ncopy = max(2, min(64, -(-L2_ROTATION_BYTES // rblob.size)))
+        d0 = torch.from_numpy(rblob).to(dev)
+        copies = [d0] + [d0.clone() for _ in range(ncopy - 1)]
+        x = torch.from_numpy(np.ascontiguousarray(e["x"]).reshape(-1)).to(dev)
+        y = torch.zeros(N, dtype=torch.float32, device=dev)
+        idx = torch.empty(n_sel, dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            for c in copies[:2]:
+                lbq.refine_select(x, K, REFINE_K, idx, stream=stream)
+                lbq.refine_apply(c, N, K, x, idx, n_sel, y, stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in copies:
+                    lbq.refine_select(x, K, REFINE_K, idx)
+                    lbq.refine_apply(c, N, K, x, idx, n_sel, y)
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(replays):
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_) * 1e3 / len(copies))
+        us = statistics.median(ts)
+        cb = lbq.lib().lbq_refine_packed_bytes(N, 1) - 64
+        nbytes = n_sel * cb + 2 * K + 6 * n_sel + 8 * N
+        out["per_linear"].append({"linear": e["name"], "N": N, "K": K, "selected": n_sel,
+                                  "us_per_call": round(us, 3), "bytes": nbytes,
+                                  "GB_s": round(nbytes / (us * 1e-6) / 1e9, 1)})
+        total_us += us
+        del g, copies, d0
+    assert lbq.device_error(stream) == 0
+    torch.cuda.empty_cache()
+    out["layer_us"] = round(total_us, 2)
+    return out
 
 
 def run_sweep70b(lbq, dev, stream, replays=5):

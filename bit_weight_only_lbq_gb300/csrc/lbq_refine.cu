@@ -23,6 +23,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "lbq.h"
 #include "lbq_internal.h"
@@ -70,6 +71,9 @@ __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half*
     __shared__ unsigned s_above;
     __shared__ unsigned warp_cnt[kChunk / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    // launched with programmatic dependent launch: x may come from the kernel before
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int base = blockIdx.x * kChunk;
     const int len = min(kChunk, K - base);
     const int kk = min(k, len);
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint
     const int g = (row0 >> 5) + (lane >> 2), wd = lane & 3;     // group and nibble word of this lane
     const bool rows_ok = g * 32 < N;
     const uint64_t cb = lbq::refine_column_bytes(N);
+    // launched with programmatic dependent launch: idx, x and y come from the kernels before
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0 && tid == 0) {
         const unsigned* h = reinterpret_cast<const unsigned*>(blob);
         long long n_hdr, k_hdr;
@@ -133,25 +139,45 @@ __global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint
     float acc[8];
 #pragma unroll
     for (int b = 0; b < 8; ++b) acc[b] = 0.f;
-    for (int j = warp; j < nsel; j += kApplyWarps) {
-        const int i = idx[j];
-        if (i < 0 || i >= K) {
-            if (lane == 0) atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
-            continue;
-        }
-        if (!rows_ok) continue;
-        const float xi = __half2float(x[i]);
-        const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(i) * cb;
-        const uint32_t word = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
-        const float s = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
-        const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
-        const float z = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+    // four columns per round, all their loads issued before any is used
+    constexpr int kU = 4;
+    for (int j0 = warp; j0 < nsel; j0 += kApplyWarps * kU) {
+        int col_i[kU];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const float lo = (static_cast<float>((word >> (8 * b)) & 15u) - z) * s;       // row 4 wd + b
-            const float hi = (static_cast<float>((word >> (8 * b + 4)) & 15u) - z) * s;   // row 16 + 4 wd + b
-            acc[b] = fmaf(lo, xi, acc[b]);
-            acc[4 + b] = fmaf(hi, xi, acc[4 + b]);
+        for (int u = 0; u < kU; ++u) {
+            const int j = j0 + u * kApplyWarps;
+            col_i[u] = j < nsel ? idx[j] : -1;
+            if (j < nsel && (col_i[u] < 0 || col_i[u] >= K)) {
+                if (lane == 0) atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
+                col_i[u] = -1;
+            }
+        }
+        float xi[kU], sc[kU], zf[kU];
+        uint32_t word[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            xi[u] = 0.f;
+            sc[u] = 0.f;
+            zf[u] = 0.f;
+            word[u] = 0u;
+            if (col_i[u] >= 0 && rows_ok) {
+                const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(col_i[u]) * cb;
+                xi[u] = __half2float(x[col_i[u]]);
+                word[u] = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
+                sc[u] = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
+                const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
+                zf[u] = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const float lo = (static_cast<float>((word[u] >> (8 * b)) & 15u) - zf[u]) * sc[u];      // row 4 wd + b
+                const float hi = (static_cast<float>((word[u] >> (8 * b + 4)) & 15u) - zf[u]) * sc[u];  // row 16 + 4 wd + b
+                acc[b] = fmaf(lo, xi[u], acc[b]);
+                acc[4 + b] = fmaf(hi, xi[u], acc[4 + b]);
+            }
         }
     }
     const int rbase = (lane >> 2) * 32 + 4 * wd;
@@ -178,6 +204,29 @@ __global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous one on the stream runs; it touches memory only after
+// griddepcontrol.wait, so this is safe whatever that kernel wrote.
+template <class... Args>
+lbq_status launch_pdl(const void* fn, unsigned grid, unsigned block, void* stream, Args... args) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void* ptrs[] = {static_cast<void*>(&args)...};
+    if (cudaLaunchKernelExC(&cfg, fn, ptrs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return LBQ_ERR_CUDA;
+    }
+    return LBQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -197,10 +246,8 @@ lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* i
     const lbq_status st = lbq::device_context(&err, &sms);
     if (st != LBQ_OK) return st;
     const unsigned grid = static_cast<unsigned>((K + kChunk - 1) / kChunk);
-    lbq_refine_select_kernel<<<grid, kChunk, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const __half*>(x_f16), static_cast<int>(K), k, idx);
-    if (cudaGetLastError() != cudaSuccess) return LBQ_ERR_CUDA;
-    return LBQ_OK;
+    return launch_pdl(reinterpret_cast<const void*>(&lbq_refine_select_kernel), grid, kChunk, stream,
+                      static_cast<const __half*>(x_f16), static_cast<int>(K), k, idx);
 }
 
 lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void* x_f16, const int32_t* idx,
@@ -217,11 +264,10 @@ lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void
     const lbq_status st = lbq::device_context(&err, &sms);
     if (st != LBQ_OK) return st;
     const unsigned grid = static_cast<unsigned>((N + kApplyRows - 1) / kApplyRows);
-    lbq_refine_apply_kernel<<<grid, kApplyRows, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint8_t*>(refine), static_cast<int>(N), static_cast<int>(K),
-        static_cast<const __half*>(x_f16), idx, n_sel, y, y_dtype == LBQ_F32 ? 1 : 0, err);
-    if (cudaGetLastError() != cudaSuccess) return LBQ_ERR_CUDA;
-    return LBQ_OK;
+    return launch_pdl(reinterpret_cast<const void*>(&lbq_refine_apply_kernel), grid, kApplyRows, stream,
+                      static_cast<const uint8_t*>(refine), static_cast<int>(N), static_cast<int>(K),
+                      static_cast<const __half*>(x_f16), idx, static_cast<int>(n_sel), y, y_dtype == LBQ_F32 ? 1 : 0,
+                      err);
 }
 
 }  // extern "C"
