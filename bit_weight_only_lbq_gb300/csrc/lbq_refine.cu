@@ -24,6 +24,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "lbq.h"
 #include "lbq_internal.h"
@@ -31,6 +32,11 @@
 namespace {
 
 constexpr int kChunk = lbq::kRefineChunk;
+
+// Index scratch of lbq_refine_noalloc: one array per device, shared by every
+// call.  64 chunks (K <= 65536) x 256 channels (k <= 256) = 16384 indices, 64 KB.
+constexpr int kNoAllocIdxMax = (lbq::kMaxK / lbq::kRefineChunk) * lbq::kRefineMaxK;
+__device__ __align__(256) int32_t g_refine_idx_scratch[kNoAllocIdxMax];
 constexpr int kApplyRows = 256;
 constexpr int kApplyWarps = 8;
 
@@ -227,6 +233,29 @@ lbq_status launch_pdl(const void* fn, unsigned grid, unsigned block, void* strea
     return LBQ_OK;
 }
 
+// Device address of g_refine_idx_scratch for the current device, looked up
+// once per device.
+constexpr int kMaxDevicesNoAlloc = 64;
+std::mutex g_scratch_mu;
+int32_t* g_scratch_addr[kMaxDevicesNoAlloc] = {};
+
+lbq_status refine_scratch(int32_t** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LBQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevicesNoAlloc) return LBQ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_refine_idx_scratch) != cudaSuccess || !p) {
+            (void)cudaGetLastError();
+            return LBQ_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = static_cast<int32_t*>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return LBQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -268,6 +297,22 @@ lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void
                       static_cast<const uint8_t*>(refine), static_cast<int>(N), static_cast<int>(K),
                       static_cast<const __half*>(x_f16), idx, static_cast<int>(n_sel), y, y_dtype == LBQ_F32 ? 1 : 0,
                       err);
+}
+
+lbq_status lbq_refine_noalloc(const void* refine, int64_t N, int64_t K, int32_t k, const void* x_f16, void* y,
+                             lbq_dtype y_dtype, void* stream) {
+    if (!refine || !x_f16 || !y) return LBQ_ERR_NULL;
+    if (N < 64 || N % 64 || N > INT32_MAX || K < 1 || K > lbq::kMaxK || k < 1 || k > lbq::kRefineMaxK)
+        return LBQ_ERR_SHAPE;
+    const int64_t n_sel = lbq_refine_selected_count(K, k);
+    if (n_sel < 1 || n_sel > kNoAllocIdxMax) return LBQ_ERR_SHAPE;   // larger than the static scratch
+    int32_t* idx = nullptr;
+    lbq_status st = refine_scratch(&idx);
+    if (st != LBQ_OK) return st;
+    // the selection writes every index the apply reads: nothing to clear
+    st = lbq_refine_select(x_f16, K, k, idx, stream);
+    if (st != LBQ_OK) return st;
+    return lbq_refine_apply(refine, N, K, x_f16, idx, static_cast<int32_t>(n_sel), y, y_dtype, stream);
 }
 
 }  // extern "C"

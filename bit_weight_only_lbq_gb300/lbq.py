@@ -40,6 +40,7 @@ EXPORTS = (
     "lbq_gemm_w2cb_outlier_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
     "lbq_selftest_wait_timeout", "lbq_device_error", "lbq_refine_packed_bytes", "lbq_pack_refine",
     "lbq_dequant_host", "lbq_refine_selected_count", "lbq_refine_select", "lbq_refine_apply",
+    "lbq_refine_noalloc",
 )
 
 
@@ -118,6 +119,7 @@ def lib():
             "lbq_refine_selected_count": (c_i64, [c_i64, c_i32]),
             "lbq_refine_select": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_vp]),
             "lbq_refine_apply": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_vp, c_i32, c_vp, ctypes.c_int, c_vp]),
+            "lbq_refine_noalloc": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int, c_vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -298,6 +300,13 @@ def refine_apply(refine, N: int, K: int, x, idx, n_sel: int, y, stream=None, y_d
     yd = _ydtype(y) if y_dtype is None else y_dtype
     _check(lib().lbq_refine_apply(_dev_ptr(refine), N, K, _dev_ptr(x), _dev_ptr(idx) if n_sel else None, n_sel,
                                   _dev_ptr(y), yd, _stream(stream)), "lbq_refine_apply")
+
+
+def refine_noalloc(refine, N: int, K: int, k: int, x, y, stream=None, y_dtype: int | None = None):
+    """Select + apply with the library's static index scratch (calls must not overlap)."""
+    yd = _ydtype(y) if y_dtype is None else y_dtype
+    _check(lib().lbq_refine_noalloc(_dev_ptr(refine), N, K, k, _dev_ptr(x), _dev_ptr(y), yd, _stream(stream)),
+           "lbq_refine_noalloc")
 
 
 def _problems(problems, y_dtype):

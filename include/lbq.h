@@ -334,6 +334,20 @@ lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* i
 lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void* x_f16, const int32_t* idx,
                             int32_t n_sel, void* y, lbq_dtype y_dtype, void* stream);
 
+/* lbq_refine_select followed by lbq_refine_apply with no caller-provided index
+ * buffer: the selected channels go to a static device array inside the
+ * library (16384 int32 = 64 KB per device, enough for K <= 65536 with
+ * k <= 256; a larger selection would be rejected with LBQ_ERR_SHAPE).  The
+ * pages have no counterpart of this entry point: it is a convenience of this
+ * library, with the same results as the two-call form.
+ * Nothing in the scratch needs clearing: the selection writes every index the
+ * apply reads.  Races: the scratch is shared by all calls on a device, so two
+ * calls must not overlap in time - issue them on one stream, or order them
+ * with events; calls on different devices are independent.
+ * Arguments and errors as lbq_refine_select / lbq_refine_apply. */
+lbq_status lbq_refine_noalloc(const void* refine, int64_t N, int64_t K, int32_t k, const void* x_f16, void* y,
+                              lbq_dtype y_dtype, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,41 @@
+"""lbq_refine_noalloc (index scratch in a static device array) against the
+two-call form with a caller-provided index buffer: identical bits on two
+successive calls with different inputs; argument checks without a GPU."""
+import numpy as np
+import pytest
+
+from gpu_util import to_dev
+
+
+def test_noalloc_rejects_bad_shapes_without_gpu(lbq):
+    L = lbq.lib()
+    assert L.lbq_refine_noalloc(None, 64, 64, 1, 16, 16, 1, None) == 1          # null blob
+    assert L.lbq_refine_noalloc(16, 96, 64, 1, 16, 16, 1, None) == 2            # N % 64
+    assert L.lbq_refine_noalloc(16, 64, 64, 0, 16, 16, 1, None) == 2            # k < 1
+    assert L.lbq_refine_noalloc(16, 64, 64, 257, 16, 16, 1, None) == 2          # k > 256
+    assert L.lbq_refine_noalloc(16, 64, 65537, 4, 16, 16, 1, None) == 2         # K > 65536
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_two_call_form(lbq):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(77)
+    N, K, k = 4096, 14336, 16
+    R = (rng.standard_normal((N, K)) * 1e-3).astype(np.float32)
+    blob = to_dev(lbq.pack_refine(R))
+    n_sel = lbq.refine_selected_count(K, k)
+    for call in range(2):                                    # the scratch is reused by the second call
+        x = rng.standard_normal(K).astype(np.float16)
+        x[rng.choice(K, size=K // 200, replace=False)] *= 100
+        y0 = (rng.standard_normal(N) * 0.3).astype(np.float32)
+        d_x = to_dev(x)
+        y_ref = torch.from_numpy(y0.copy()).cuda()
+        idx = torch.empty(n_sel, dtype=torch.int32, device="cuda:0")
+        lbq.refine_select(d_x, K, k, idx)
+        lbq.refine_apply(blob, N, K, d_x, idx, n_sel, y_ref)
+        y_na = torch.from_numpy(y0.copy()).cuda()
+        lbq.refine_noalloc(blob, N, K, k, d_x, y_na)
+        torch.cuda.synchronize()
+        assert lbq.device_error() == 0
+        assert torch.equal(y_na, y_ref), "call %d" % call
+        assert not torch.equal(y_na, torch.from_numpy(y0).cuda())   # the correction did something
