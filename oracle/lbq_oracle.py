@@ -621,3 +621,19 @@ def refine_apply(blob: np.ndarray, x: np.ndarray, idx: np.ndarray, y: np.ndarray
     for j, i in enumerate(idx):
         out = out + xv[i] * C[:, j]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Fused embedding row gather (SPECTRA article, section 4.3 "SpectraFusedEmbedding:
+# Dynamic Row-Gather Dequantization"): only the rows of the requested token ids
+# are dequantised.  Reading: an output row is the row of the matrix the blob
+# applies (outlier columns exact), in FP64, rounded once to the output type.
+# ---------------------------------------------------------------------------
+
+def embed(blob: np.ndarray, ids, out_dtype=np.float16) -> np.ndarray:
+    ids = np.asarray(ids, dtype=np.int64)
+    rows = dequant(blob, ids)
+    idx, vals = outliers(blob)
+    if idx.size:
+        rows[:, idx] = vals[ids]
+    return fp16_round(rows) if out_dtype == np.float16 else rows.astype(np.float32)

@@ -147,3 +147,17 @@ def test_outlier_columns_are_isolated():
     i2, vals = O.outliers(blob)
     assert i2.tolist() == idx.tolist()
     assert np.array_equal(vals, W[:, idx].astype(np.float16).astype(np.float64))
+
+
+def test_embedding_gather_of_the_worked_row(golden):
+    """SPECTRA 4.3 row gather: the worked row (s = 1, so w_hat = q - z exactly),
+    gathered twice, in FP16 and FP32."""
+    g = golden("w4_worked_example.txt")
+    w = np.array([float(v) for v in g["w_group0"] + g["w_group1"]], dtype=np.float32)[None, :]
+    q = np.array([int(v) for v in g["q_group0"] + g["q_group1"]], dtype=np.float64)
+    z = np.repeat([float(v) for v in g["z"]], 32)
+    blob = O.pack_w4(np.vstack([w, 2 * w]))
+    for dt in (np.float16, np.float32):
+        rows = O.embed(blob, [0, 0], out_dtype=dt)
+        assert rows.dtype == dt
+        assert np.array_equal(rows.astype(np.float64), np.vstack([q - z, q - z]))
