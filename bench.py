@@ -645,10 +645,45 @@ def run_sweep70b(lbq, dev, stream, replays=5):
         out[label] = {"us_per_token": round(ms * 1e3, 1), "GB_s": round(total / (ms * 1e-3) / 1e9, 1),
                       "tokens_per_s": round(1e3 / ms, 1), "launches_per_token": launches}
         del g
+    out["embedding_gather"] = time_embed_gather(lbq, head, hN, hK, dev, stream)
     assert lbq.device_error(stream) == 0
     del layers, head, layer
     torch.cuda.empty_cache()
     return out
+
+
+EMBED_TOKENS = 128
+
+
+def time_embed_gather(lbq, table, V, D, dev, stream, batches=64, replays=10):
+    """Fused embedding row gather (FP16 rows) of EMBED_TOKENS random token ids from
+    a V x D 4-bit table; 64 different id batches per graph replay, so the rows
+    come from HBM rather than L2."""
+    import torch
+    rng = np.random.default_rng(1234)
+    ids = [torch.from_numpy(rng.integers(0, V, size=EMBED_TOKENS).astype(np.int32)).to(dev) for _ in range(batches)]
+    out = torch.empty((EMBED_TOKENS, D), dtype=torch.float16, device=dev)
+    with torch.cuda.stream(stream):
+        lbq.embed_gather(lbq.LBQ_KIND_W4, table, V, D, 0, ids[0], out, stream=stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for b in ids:
+                lbq.embed_gather(lbq.LBQ_KIND_W4, table, V, D, 0, b, out)
+        g.replay()
+        stream.synchronize()
+        ts = []
+        for _ in range(replays):
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            g.replay()
+            b_.record(stream)
+            b_.synchronize()
+            ts.append(a_.elapsed_time(b_) * 1e3 / batches)
+    us = statistics.median(ts)
+    nbytes = int(EMBED_TOKENS * D * (W4_BYTES_PER_WEIGHT + 2) + 4 * EMBED_TOKENS)
+    return {"table": "%d x %d W4A16 G32 (the sweep's lm_head blob)" % (V, D), "tokens": EMBED_TOKENS,
+            "us_per_call": round(us, 3), "bytes": nbytes, "GB_s": round(nbytes / (us * 1e-6) / 1e9, 1)}
 
 
 def run_single(args):

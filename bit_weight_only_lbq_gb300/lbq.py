@@ -40,7 +40,7 @@ EXPORTS = (
     "lbq_gemm_w2cb_outlier_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
     "lbq_selftest_wait_timeout", "lbq_device_error", "lbq_refine_packed_bytes", "lbq_pack_refine",
     "lbq_dequant_host", "lbq_refine_selected_count", "lbq_refine_select", "lbq_refine_apply",
-    "lbq_refine_noalloc",
+    "lbq_refine_noalloc", "lbq_embed_gather",
 )
 
 
@@ -120,6 +120,8 @@ def lib():
             "lbq_refine_select": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_vp]),
             "lbq_refine_apply": (ctypes.c_int, [c_vp, c_i64, c_i64, c_vp, c_vp, c_i32, c_vp, ctypes.c_int, c_vp]),
             "lbq_refine_noalloc": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int, c_vp]),
+            "lbq_embed_gather": (ctypes.c_int, [ctypes.c_int, c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_vp,
+                                                ctypes.c_int, c_vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -307,6 +309,14 @@ def refine_noalloc(refine, N: int, K: int, k: int, x, y, stream=None, y_dtype: i
     yd = _ydtype(y) if y_dtype is None else y_dtype
     _check(lib().lbq_refine_noalloc(_dev_ptr(refine), N, K, k, _dev_ptr(x), _dev_ptr(y), yd, _stream(stream)),
            "lbq_refine_noalloc")
+
+
+def embed_gather(kind: int, packed, V: int, D: int, n_out: int, ids, out, stream=None, out_dtype: int | None = None):
+    """Rows ids of a packed V x D table into out (T x D), dequantised (device buffers)."""
+    od = _ydtype(out) if out_dtype is None else out_dtype
+    T = ids.numel() if hasattr(ids, "numel") else int(np.asarray(ids).size)
+    _check(lib().lbq_embed_gather(kind, _dev_ptr(packed), V, D, n_out, _dev_ptr(ids) if T else None, T,
+                                  _dev_ptr(out) if T else None, od, _stream(stream)), "lbq_embed_gather")
 
 
 def _problems(problems, y_dtype):

@@ -280,6 +280,21 @@ lbq_status lbq_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * the synchronisation itself are reported as LBQ_ERR_CUDA. */
 lbq_status lbq_device_error(void* stream);
 
+/* Fused embedding row gather (SPECTRA article, section 4.3
+ * "SpectraFusedEmbedding: Dynamic Row-Gather Dequantization"): for each of the
+ * T token ids, the row of the packed V x D table (a blob of `kind` with n_out
+ * outlier columns) as the matrix the blob applies - dense part dequantised
+ * (4-bit (q - z) s; 2-bit S C[q] + Z evaluated in FP64) and rounded once to
+ * out_dtype, outlier columns exact - written to out[t * D .. + D).
+ * packed: device, 16-byte aligned; ids: device int32[T] in [0, V), 4-byte
+ * aligned; out: device, T x D of out_dtype, 16-byte aligned.  D % 64 == 0,
+ * D <= 65536; T = 0 is a no-op.  An id outside [0, V) leaves its output row
+ * untouched and is reported as LBQ_ERR_VALUE, a header mismatch as
+ * LBQ_ERR_FORMAT, both through lbq_device_error.  Stream-ordered, no
+ * allocation. */
+lbq_status lbq_embed_gather(lbq_kind kind, const void* packed, int64_t V, int64_t D, int32_t n_out,
+                            const int32_t* ids, int32_t T, void* out, lbq_dtype out_dtype, void* stream);
+
 /* ------------------------------------------------------------------------
  * Selective weight refinement (StrataFlux paper, section 3 "Weight
  * Refinement", Eq. 2, and "Channel selection"; Appendix "StrataFlux
