@@ -637,3 +637,43 @@ def embed(blob: np.ndarray, ids, out_dtype=np.float16) -> np.ndarray:
     if idx.size:
         rows[:, idx] = vals[ids]
     return fp16_round(rows) if out_dtype == np.float16 else rows.astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# 4-bit Group-32 KV cache (SPECTRA article, section 4.5 "Group-32 Microscaled
+# 4-Bit Key-Value Cache": key and value states quantised into asymmetric 4-bit
+# Group-32 blocks in place).  Readings: the quantiser of section 3.4 applied to
+# the FP16 states (FP64 statistics, round half to even); each cached token row
+# of `width` = heads x head_dim values is one record: width/2 nibble bytes,
+# width/32 FP16 scales, width/64 zero-point bytes, padded to 16 bytes; a read
+# returns (q - z) * s16 rounded once to FP16.
+# ---------------------------------------------------------------------------
+
+def kv_record_bytes(width: int) -> int:
+    assert width % 64 == 0 and width > 0
+    return _up(width // 2 + width // 16 + width // 64, 16)
+
+
+def kv_quantize(X: np.ndarray) -> np.ndarray:
+    """Records (rows x kv_record_bytes) of FP16 rows X (rows x width)."""
+    X = np.asarray(X, dtype=np.float16)
+    rows, width = X.shape
+    q, z, s = quantise_w4(X.astype(F64))
+    out = np.zeros((rows, kv_record_bytes(width)), dtype=np.uint8)
+    out[:, :width // 2] = pack_nibbles(q)
+    out[:, width // 2:width // 2 + width // 16] = \
+        np.ascontiguousarray(fp16_round(s).astype("<f2")).view(np.uint8).reshape(rows, width // 16)
+    out[:, width // 2 + width // 16:width // 2 + width // 16 + width // 64] = pack_zero_points(z)
+    return out
+
+
+def kv_dequant(rec: np.ndarray, width: int) -> np.ndarray:
+    """FP16 rows (rows x width) read back from records."""
+    rec = np.asarray(rec, dtype=np.uint8)
+    rows = rec.shape[0]
+    qb = rec[:, :width // 2].reshape(rows, width // 32, 16)
+    q = np.concatenate([qb & 0x0F, qb >> 4], axis=2).astype(F64)
+    s16 = np.ascontiguousarray(rec[:, width // 2:width // 2 + width // 16]).view("<f2").astype(F64)
+    zb = rec[:, width // 2 + width // 16:width // 2 + width // 16 + width // 64]
+    z = np.stack([zb & 0x0F, zb >> 4], axis=2).reshape(rows, width // 32).astype(F64)
+    return fp16_round(((q - z[..., None]) * s16[..., None]).reshape(rows, width))

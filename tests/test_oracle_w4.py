@@ -161,3 +161,36 @@ def test_embedding_gather_of_the_worked_row(golden):
         rows = O.embed(blob, [0, 0], out_dtype=dt)
         assert rows.dtype == dt
         assert np.array_equal(rows.astype(np.float64), np.vstack([q - z, q - z]))
+
+
+def test_kv_cache_record_of_the_worked_row(golden):
+    """SPECTRA 4.5 KV cache: the worked row (FP16-exact values) gives the worked
+    codes, scales and zero byte in its record, and reads back exactly."""
+    g = golden("w4_worked_example.txt")
+    w = np.array([float(v) for v in g["w_group0"] + g["w_group1"]], dtype=np.float16)[None, :]
+    rec = O.kv_quantize(w)
+    assert rec.shape == (1, O.kv_record_bytes(64)) and O.kv_record_bytes(64) == 48
+    assert rec[0, :32].tolist() == [int(v, 16) for v in g["qweight_bytes"]]
+    assert rec[0, 32:36].tolist() == [0x00, 0x3C, 0x00, 0x3C]          # FP16 1.0, 1.0
+    assert rec[0, 36] == int(g["zero_bytes"][0], 16)
+    q = np.array([int(v) for v in g["q_group0"] + g["q_group1"]], dtype=np.float64)
+    z = np.repeat([float(v) for v in g["z"]], 32)
+    assert np.array_equal(O.kv_dequant(rec, 64)[0].astype(np.float64), q - z)
+
+
+def test_kv_cache_roundtrip_bound():
+    """Prop. 2: every read-back value is within s16/2 + 15|s16 - s| of the state
+    (plus half an FP16 ulp of the read), for random states with spikes."""
+    rng = np.random.default_rng(8)
+    X = (rng.standard_normal((33, 1024)) * 3).astype(np.float16)
+    X[:, rng.choice(1024, size=6, replace=False)] *= 100
+    X[5, :32] = np.float16(0.75)                                       # a constant group reads back 0
+    back = O.kv_dequant(O.kv_quantize(X), 1024).astype(np.float64)
+    Xg = X.astype(np.float64).reshape(33, 32, 32)
+    s = np.maximum((Xg.max(2) - Xg.min(2)) / 15.0, 1e-8)
+    s16 = O.fp16_round(s).astype(np.float64)
+    bound = np.repeat(s16 / 2 + 15 * np.abs(s16 - s), 32, axis=1) + 0.5 * O.fp16_ulp(back)
+    err = np.abs(back - X.astype(np.float64))
+    err[5, :32] = 0.0
+    assert np.all(err <= bound * (1 + 1e-9))
+    assert np.array_equal(back[5, :32], np.zeros(32))
