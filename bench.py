@@ -433,6 +433,7 @@ def main():
         per_call.append(time_graph(g, len(blobs), replays))
         del g, extra
     refinement = run_refinement(lbq, layer, dev, stream)
+    kv_cache = time_kv_cache(lbq, dev, stream)
     sweep70b = None
     if not args.no_sweep70b:
         sweep70b = run_sweep70b(lbq, dev, stream)
@@ -507,7 +508,7 @@ def main():
                            1.0 / (32 * sum(statistics.median(per_call[i]) for i, e in enumerate(layer)
                                            if e["kind"] == "w4") * 1e-3), 1)},
                    "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes,
-                   "llama3_70b_sweep": sweep70b, "selective_refinement": refinement},
+                   "llama3_70b_sweep": sweep70b, "selective_refinement": refinement, "kv_cache_4bit": kv_cache},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(layer)
@@ -650,6 +651,56 @@ def run_sweep70b(lbq, dev, stream, replays=5):
     del layers, head, layer
     torch.cuda.empty_cache()
     return out
+
+
+KV_WIDTH = 1024            # Llama-3-8B: 8 KV heads x 128
+KV_CONTEXT = 131072
+
+
+def time_kv_cache(lbq, dev, stream, replays=10):
+    """4-bit Group-32 KV cache of one Llama-3-8B layer tensor (width 1024): the
+    quantise-on-write of one decode token (K and V: two calls), and the FP16
+    read of a 131072-token cache (77.6 MB of records, 268 MB of FP16 rows)."""
+    import torch
+    rb = lbq.kv_record_bytes(KV_WIDTH)
+    cache = torch.zeros((KV_CONTEXT, rb), dtype=torch.uint8, device=dev)
+    rng = np.random.default_rng(7)
+    states = torch.from_numpy(rng.standard_normal((KV_CONTEXT, KV_WIDTH)).astype(np.float16)).to(dev)
+    lbq.kv_quantize(states, KV_CONTEXT, KV_WIDTH, cache, 0)               # fill the cache
+    out = torch.empty((KV_CONTEXT, KV_WIDTH), dtype=torch.float16, device=dev)
+    tok = [states[i:i + 1] for i in range(2)]
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    fn()
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(replays):
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_) * 1e3 / n)
+        return statistics.median(ts)
+
+    us_w = timed(lambda: [lbq.kv_quantize(t, 1, KV_WIDTH, cache, KV_CONTEXT - 2 + i, stream=stream)
+                          for i, t in enumerate(tok)], 50)
+    us_r = timed(lambda: lbq.kv_dequant(cache, 0, KV_CONTEXT, KV_WIDTH, out, stream=stream), 5)
+    read_bytes = KV_CONTEXT * (rb + 2 * KV_WIDTH)
+    assert lbq.device_error(stream) == 0
+    del cache, states, out
+    torch.cuda.empty_cache()
+    return {"width": KV_WIDTH, "record_bytes": rb,
+            "append_one_token_k_and_v_us": round(us_w, 3),
+            "read_context": KV_CONTEXT, "read_us": round(us_r, 2), "read_bytes": read_bytes,
+            "read_GB_s": round(read_bytes / (us_r * 1e-6) / 1e9, 1)}
 
 
 EMBED_TOKENS = 128

@@ -40,7 +40,7 @@ EXPORTS = (
     "lbq_gemm_w2cb_outlier_smallM_ex", "lbq_gemv_grouped", "lbq_gemv_grouped_launches",
     "lbq_selftest_wait_timeout", "lbq_device_error", "lbq_refine_packed_bytes", "lbq_pack_refine",
     "lbq_dequant_host", "lbq_refine_selected_count", "lbq_refine_select", "lbq_refine_apply",
-    "lbq_refine_noalloc", "lbq_embed_gather",
+    "lbq_refine_noalloc", "lbq_embed_gather", "lbq_kv_record_bytes", "lbq_kv_quantize", "lbq_kv_dequant",
 )
 
 
@@ -122,6 +122,9 @@ def lib():
             "lbq_refine_noalloc": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_vp, ctypes.c_int, c_vp]),
             "lbq_embed_gather": (ctypes.c_int, [ctypes.c_int, c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_vp,
                                                 ctypes.c_int, c_vp]),
+            "lbq_kv_record_bytes": (c_sz, [c_i64]),
+            "lbq_kv_quantize": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_vp]),
+            "lbq_kv_dequant": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -317,6 +320,22 @@ def embed_gather(kind: int, packed, V: int, D: int, n_out: int, ids, out, stream
     T = ids.numel() if hasattr(ids, "numel") else int(np.asarray(ids).size)
     _check(lib().lbq_embed_gather(kind, _dev_ptr(packed), V, D, n_out, _dev_ptr(ids) if T else None, T,
                                   _dev_ptr(out) if T else None, od, _stream(stream)), "lbq_embed_gather")
+
+
+def kv_record_bytes(width: int) -> int:
+    return int(lib().lbq_kv_record_bytes(width))
+
+
+def kv_quantize(x, rows: int, width: int, cache, first_row: int, ldx: int | None = None, stream=None):
+    """Quantise rows of FP16 states (device) into records of the device cache."""
+    _check(lib().lbq_kv_quantize(_dev_ptr(x), ldx or width, rows, width, _dev_ptr(cache), first_row,
+                                 _stream(stream)), "lbq_kv_quantize")
+
+
+def kv_dequant(cache, first_row: int, rows: int, width: int, out, ldo: int | None = None, stream=None):
+    """Read cache records back as FP16 rows (device)."""
+    _check(lib().lbq_kv_dequant(_dev_ptr(cache), first_row, rows, width, _dev_ptr(out), ldo or width,
+                                _stream(stream)), "lbq_kv_dequant")
 
 
 def _problems(problems, y_dtype):

@@ -280,6 +280,30 @@ lbq_status lbq_selftest_wait_timeout(uint32_t limit_us, void* stream);
  * the synchronisation itself are reported as LBQ_ERR_CUDA. */
 lbq_status lbq_device_error(void* stream);
 
+/* 4-bit Group-32 KV cache (SPECTRA article, section 4.5 "Group-32 Microscaled
+ * 4-Bit Key-Value Cache": key and value states quantised into asymmetric 4-bit
+ * Group-32 blocks in place).  A cache is a caller-allocated device buffer of
+ * records, one per cached row (one token's heads x head_dim values of one
+ * tensor): width/2 nibble bytes (byte k of a group = q_k | q_{k+16} << 4),
+ * width/32 FP16 scales, width/64 bytes of zero points z_{2m} | z_{2m+1} << 4,
+ * zero padding to lbq_kv_record_bytes(width).  The quantiser is the one of
+ * lbq_pack_w4 (FP64 statistics from the FP16 states, round half to even), so
+ * the bytes equal the host recipe's; a constant group reads back as 0 (its
+ * scale floor 1e-8 rounds to 0 in FP16).  width % 64 == 0, 64 <= width <= 65536. */
+size_t lbq_kv_record_bytes(int64_t width);
+
+/* Device: quantise `rows` FP16 rows (x_f16, leading dimension ldx elements,
+ * 16-byte aligned, ldx % 8 == 0) into records first_row .. first_row + rows - 1
+ * of `cache` (16-byte aligned).  rows = 0 is a no-op. */
+lbq_status lbq_kv_quantize(const void* x_f16, int64_t ldx, int64_t rows, int64_t width, void* cache,
+                           int64_t first_row, void* stream);
+
+/* Device: read records first_row .. first_row + rows - 1 back as FP16 rows
+ * ((q - z) s rounded once) into out_f16 (leading dimension ldo, 16-byte
+ * aligned, ldo % 8 == 0). */
+lbq_status lbq_kv_dequant(const void* cache, int64_t first_row, int64_t rows, int64_t width, void* out_f16,
+                          int64_t ldo, void* stream);
+
 /* Fused embedding row gather (SPECTRA article, section 4.3
  * "SpectraFusedEmbedding: Dynamic Row-Gather Dequantization"): for each of the
  * T token ids, the row of the packed V x D table (a blob of `kind` with n_out
