@@ -11,8 +11,9 @@
 //
 // GB300 design: the write is tiny and latency-bound (one token = a few hundred
 // bytes), the read is memory-bound (0.58 B read, 2 B written per value).
-//  * quantise: one thread per pair of groups (64 values: both share a zero-point
-//    byte); the statistics and the division are FP64 with IEEE rounding and
+//  * quantise: one warp per pair of groups (64 values: both share a zero-point
+//    byte), a lane per value of each group; min / max by warp shuffles; the
+//    statistics and the division are FP64 with IEEE rounding and
 //    round-half-to-even, exactly the host recipe, so the records are
 //    bit-identical to the host / reference quantiser;
 //  * dequantise: a thread turns one 8-byte nibble load into 8 FP16 values
@@ -31,52 +32,47 @@ namespace {
 
 constexpr int kThreads = 256;
 
+__device__ __forceinline__ double warp_min(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmin(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ double warp_max(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// One warp per pair of groups (the two share a zero-point byte): lane l holds
+// value l of each group; min / max by shuffles, then each lane quantises its two
+// values, lanes 0..15 write the nibble bytes, lane 0 the scales and the zero byte.
 __global__ void __launch_bounds__(kThreads) lbq_kv_quantize_kernel(const __half* __restrict__ x, long long ldx,
                                                                    int rows, int width, uint8_t* __restrict__ cache,
                                                                    long long first_row, long long rec_bytes) {
     const int pairs = width / 64;
-    const long long item = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
-    if (item >= static_cast<long long>(rows) * pairs) return;
+    const int lane = threadIdx.x & 31;
+    const long long item = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    if (item >= static_cast<long long>(rows) * pairs) return;   // warp-uniform
     const int row = static_cast<int>(item / pairs), p = static_cast<int>(item % pairs);
     const __half* xr = x + row * ldx + p * 64;
     uint8_t* rec = cache + (first_row + row) * rec_bytes;
-    uint8_t zpair = 0;
+    uint32_t zpair = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int g = 2 * p + h;
-        double w[32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(xr + h * 32 + c * 8);
-            const __half* hv = reinterpret_cast<const __half*>(&v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[c * 8 + e] = static_cast<double>(__half2float(hv[e]));
-        }
-        double wmin = w[0], wmax = w[0];
-#pragma unroll
-        for (int k = 1; k < 32; ++k) {
-            wmin = fmin(wmin, w[k]);
-            wmax = fmax(wmax, w[k]);
-        }
+        const double w = static_cast<double>(__half2float(xr[h * 32 + lane]));
+        const double wmin = warp_min(w), wmax = warp_max(w);
         // s = max((wmax - wmin) / 15, 1e-8), z = clamp(round(-wmin / s)), q = clamp(round(w / s + z))
         const double s = fmax(__ddiv_rn(__dsub_rn(wmax, wmin), 15.0), 1e-8);
         const double z = fmin(fmax(rint(__ddiv_rn(-wmin, s)), 0.0), 15.0);
-        uint32_t q[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) q[k] = static_cast<uint32_t>(fmin(fmax(rint(__dadd_rn(__ddiv_rn(w[k], s), z)), 0.0), 15.0));
-        uint32_t words[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            words[j] = 0u;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) words[j] |= (q[4 * j + b] | (q[4 * j + b + 16] << 4)) << (8 * b);
-        }
-        *reinterpret_cast<uint4*>(rec + g * 16) = make_uint4(words[0], words[1], words[2], words[3]);
-        *reinterpret_cast<__half*>(rec + width / 2 + g * 2) = __double2half(s);
-        zpair |= static_cast<uint8_t>(static_cast<uint32_t>(z) << (4 * h));
+        const uint32_t q = static_cast<uint32_t>(fmin(fmax(rint(__dadd_rn(__ddiv_rn(w, s), z)), 0.0), 15.0));
+        const uint32_t q_hi = __shfl_down_sync(0xffffffffu, q, 16);          // value lane + 16
+        if (lane < 16) rec[g * 16 + lane] = static_cast<uint8_t>(q | (q_hi << 4));
+        if (lane == 0) *reinterpret_cast<__half*>(rec + width / 2 + g * 2) = __double2half(s);
+        zpair |= static_cast<uint32_t>(z) << (4 * h);
     }
-    rec[width / 2 + width / 16 + p] = zpair;
-    if (p == 0)   // the record's padding reads as zero
+    if (lane == 0) rec[width / 2 + width / 16 + p] = static_cast<uint8_t>(zpair);
+    if (p == 0 && lane == 0)   // the record's padding reads as zero
         for (long long b = width / 2 + width / 16 + width / 64; b < rec_bytes; ++b) rec[b] = 0;
 }
 
@@ -131,8 +127,9 @@ lbq_status lbq_kv_quantize(const void* x_f16, int64_t ldx, int64_t rows, int64_t
     int sms = 0;
     const lbq_status st = lbq::device_context(&err, &sms);
     if (st != LBQ_OK) return st;
-    const long long items = rows * (width / 64);
-    lbq_kv_quantize_kernel<<<static_cast<unsigned>((items + kThreads - 1) / kThreads), kThreads, 0,
+    const long long warps = rows * (width / 64);
+    const long long per_cta = kThreads / 32;
+    lbq_kv_quantize_kernel<<<static_cast<unsigned>((warps + per_cta - 1) / per_cta), kThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
         static_cast<const __half*>(x_f16), ldx, static_cast<int>(rows), static_cast<int>(width),
         static_cast<uint8_t*>(cache), first_row, static_cast<long long>(lbq_kv_record_bytes(width)));
