@@ -48,9 +48,9 @@ SAMPLE_ROWS_MAX = 1024
 L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)
 # DRAM bytes (read + write) per grouped launch from ncu captures of the same
 # launches (profiles/); valid only for the kernel source they were taken on.
-TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "aba681ea173ff2fd",
-                   "traffic": {"w4_layer_sweep": 129500928, "w2_layer_sweep": 99892992,
-                               "w4_smallM_gate_down": 68171520}}
+TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "e9b27fb1ef1c9782",
+                   "traffic": {"w4_layer_sweep": 129298688, "w2_layer_sweep": 100333056,
+                               "w4_smallM_gate_down": 68173824}}
 METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
 W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
 W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
@@ -531,6 +531,29 @@ def run_refinement(lbq, layer, dev, stream, replays=20):
     import torch
     out = {"k_per_chunk": REFINE_K, "per_linear": []}
     total_us = 0.0
+
+    def timed(fn, copies):
+        with torch.cuda.stream(stream):
+            for c in copies[:2]:
+                fn(c)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in copies:
+                    fn(c)
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(replays):
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_) * 1e3 / len(copies))
+        del g
+        return statistics.median(ts)
+
     for e in layer:
         if e["kind"] != "w4":
             continue
@@ -545,34 +568,19 @@ def run_refinement(lbq, layer, dev, stream, replays=20):
         x = torch.from_numpy(np.ascontiguousarray(e["x"]).reshape(-1)).to(dev)
         y = torch.zeros(N, dtype=torch.float32, device=dev)
         idx = torch.empty(n_sel, dtype=torch.int32, device=dev)
-        with torch.cuda.stream(stream):
-            for c in copies[:2]:
-                lbq.refine_select(x, K, REFINE_K, idx, stream=stream)
-                lbq.refine_apply(c, N, K, x, idx, n_sel, y, stream=stream)
-            stream.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for c in copies:
-                    lbq.refine_select(x, K, REFINE_K, idx)
-                    lbq.refine_apply(c, N, K, x, idx, n_sel, y)
-            g.replay()
-            stream.synchronize()
-            ts = []
-            for _ in range(replays):
-                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a_.record(stream)
-                g.replay()
-                b_.record(stream)
-                b_.synchronize()
-                ts.append(a_.elapsed_time(b_) * 1e3 / len(copies))
-        us = statistics.median(ts)
+
+        def two_call(c):
+            lbq.refine_select(x, K, REFINE_K, idx, stream=stream)
+            lbq.refine_apply(c, N, K, x, idx, n_sel, y, stream=stream)
+
+        us = timed(two_call, copies)
         cb = lbq.lib().lbq_refine_packed_bytes(N, 1) - 64
         nbytes = n_sel * cb + 2 * K + 6 * n_sel + 8 * N
         out["per_linear"].append({"linear": e["name"], "N": N, "K": K, "selected": n_sel,
                                   "us_per_call": round(us, 3), "bytes": nbytes,
                                   "GB_s": round(nbytes / (us * 1e-6) / 1e9, 1)})
         total_us += us
-        del g, copies, d0
+        del copies, d0
     assert lbq.device_error(stream) == 0
     torch.cuda.empty_cache()
     out["layer_us"] = round(total_us, 2)

@@ -314,10 +314,13 @@ __device__ __forceinline__ void w4_record_m1(const uint4 (&q)[kTR], const float 
 }
 
 // 4-bit record, MB activation rows: the unpacked words are shared by the rows.
+// Every plane is computed, also past the launch's rows (their staged planes are
+// zero and their sums are never stored): no branch per plane (measured 3 %
+// faster at M = 4).
 template <int MB>
 __device__ __forceinline__ void w4_record_mb(const uint4 (&q)[kTR], const float (&s)[kTR], const float (&zf)[kTR],
                                              const uint4* xq, int xq_plane, const float* xs24, int xs_plane,
-                                             int mrows, float (&acc)[MB][kTR]) {
+                                             float (&acc)[MB][kTR]) {
     uint32_t u[kTR][16];
 #pragma unroll
     for (int r = 0; r < kTR; ++r)
@@ -331,7 +334,7 @@ __device__ __forceinline__ void w4_record_mb(const uint4 (&q)[kTR], const float 
         }
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
-        if (m < mrows) {
+        {
             const uint4* xp = xq + m * xq_plane;
             const uint4 xr[4] = {xp[0], xp[32], xp[64], xp[96]};
             const float xsz = xs24[m * xs_plane];
@@ -388,11 +391,12 @@ __device__ __forceinline__ void w2_record(const uint2 (&c)[kTR], const float (&S
 }
 
 // 2-bit record, MB activation rows: the codebook pairs of the 4 rows are
-// decoded once (PRMT as above) and shared by the rows' FMAs.
+// decoded once (PRMT as above) and shared by the rows' FMAs; every plane is
+// computed, as for 4-bit.
 template <int MB>
 __device__ __forceinline__ void w2_record_mb(const uint2 (&c)[kTR], const float (&S)[kTR], const float (&Z)[kTR],
                                              const uint4* xq, int xq_plane, const float* xs, int xs_plane,
-                                             uint32_t lut_lo, uint32_t lut_hi, int mrows, float (&acc)[MB][kTR]) {
+                                             uint32_t lut_lo, uint32_t lut_hi, float (&acc)[MB][kTR]) {
     uint32_t p[kTR][16];   // pair (v * 4 + sh) * 2 + h: codes of word v, shift sh, half h
 #pragma unroll
     for (int r = 0; r < kTR; ++r)
@@ -407,7 +411,7 @@ __device__ __forceinline__ void w2_record_mb(const uint2 (&c)[kTR], const float 
             }
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
-        if (m < mrows) {
+        {
             const uint4* xp = xq + m * xq_plane;
             const uint4 xr[4] = {xp[0], xp[32], xp[64], xp[96]};
             float d0[kTR], d1[kTR];
@@ -475,8 +479,10 @@ __device__ __forceinline__ float reduce_rows4(const float (&acc)[4], int lane) {
 
 __device__ __forceinline__ int unit_end(const GroupArgs& a, int q) { return q + 1 < a.count ? a.p[q + 1].ub : a.nunits; }
 
+// The 8-warp M = 1 variants are built for two resident CTAs per SM (<= 128
+// registers a thread), so that a dependent launch's CTAs can start beside them.
 template <int KIND, int MB, int NW, int RPI>
-__global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_constant__ GroupArgs a) {
+__global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gemv_kernel(const __grid_constant__ GroupArgs a) {
     using RC = Rec<KIND>;
     constexpr int kStage = RC::template stage<RPI>();
     constexpr int kThreads = NW * 32;
@@ -772,7 +778,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                     if constexpr (MB == 1)
                         w4_record_m1(q4, f1, f2, xqq, *xss, acc[0]);
                     else
-                        w4_record_mb<MB>(q4, f1, f2, xqq, ng * 4, xss, ng, mrows, acc);
+                        w4_record_mb<MB>(q4, f1, f2, xqq, ng * 4, xss, ng, acc);
                 };
                 ok = next_stage(
                     [&](const uint8_t* st) {
@@ -799,7 +805,7 @@ __global__ void __launch_bounds__(NW * 32, 1) lbq_gemv_kernel(const __grid_const
                     if constexpr (MB == 1)
                         w2_record(q2, f1, f2, xqq, *xss, a.lut_lo, a.lut_hi, acc[0]);
                     else
-                        w2_record_mb<MB>(q2, f1, f2, xqq, ng * 4, xss, ng, a.lut_lo, a.lut_hi, mrows, acc);
+                        w2_record_mb<MB>(q2, f1, f2, xqq, ng * 4, xss, ng, a.lut_lo, a.lut_hi, acc);
                 };
                 ok = next_stage(
                     [&](const uint8_t* st) {
@@ -994,7 +1000,8 @@ const Variant& variant(int v) {
         make_variant<kW4, 4, 12, 1>(),
         make_variant<kW4, 8, 8, 1>(),
         make_variant<kW2, 1, 16, 2>(),   // 4: 2-bit codebook GEMV, two records per item
-        make_variant<kW4, 1, 8, 1>(),    // 5, 6: fewer warps and one-record stages: room for very wide K
+        make_variant<kW4, 1, 8, 1>(),    // 5, 6: fewer warps and one-record stages: room for very wide K;
+                                         //       two CTAs fit an SM (small single calls, see run())
         make_variant<kW2, 1, 8, 1>(),
         make_variant<kW4, 1, 16, 1>(),   // 7, 8: one-record stages, for groups whose staging leaves no
         make_variant<kW2, 1, 16, 1>(),   //       room for two-record stages, and single 4-bit calls
@@ -1238,13 +1245,19 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
         // one-record items for calls with fewer dense records than warps in the
         // grid (latency rather than bandwidth decides them) and for a single
         // large 4-bit problem, >= 4 records per warp (measured: 14336 x 4096
-        // alone 9.1 us with one-record items, 9.8 us with two; 4096 x 4096 and
-        // grouped sweeps are faster with two)
+        // alone 9.1 us with one-record items, 9.8 us with two; grouped sweeps
+        // are faster with two).  A single call with fewer than two records per
+        // warp runs on the 8-warp variant, two of whose CTAs fit an SM: the next
+        // launch's CTAs then start (and prefetch their weights) while this one
+        // finishes, instead of after it (measured in chained calls: 1024 x 4096
+        // 3.9 -> 2.9 us, 4096 x 4096 4.96 -> 4.79 us at 4-bit, 6.65 -> 5.98 us
+        // at 2-bit; 14336 x 4096 is slower on 8 warps, 9.1 -> 9.6 us)
         long long recs = 0;
         for (int i = 0; i < count; ++i) recs += (P[i].N + kTR - 1) / kTR * ((P[i].K + 1023) / 1024);
         const long long warps = static_cast<long long>(dev->sms) * variant(vi).NW;
         const bool one = recs < warps || (kind == kW4 && count == 1 && recs >= 4 * warps);
-        const int v0 = one ? fallback_variant(vi) : vi;
+        const bool dual = count == 1 && recs < 2 * warps;
+        const int v0 = dual ? (kind == kW4 ? kVarW4Narrow : kVarW2Narrow) : one ? fallback_variant(vi) : vi;
         return launch_pass(dev, kind, v0, true, P, count, 1, f32, stream, flags, launches);
     }
     // M >= 16 without outlier columns: the tensor-core kernel, one launch per problem

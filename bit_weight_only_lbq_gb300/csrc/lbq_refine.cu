@@ -14,10 +14,11 @@
 //    histograms, a warp-parallel scan of the bins) finds the k-th largest key
 //    exactly; ties in |x| go to the lower channel.  The selected channels are
 //    written in ascending order with a ballot prefix sum.
-//  * apply: one CTA per 256 output rows, 8 warps taking every 8th selected
-//    column; a lane owns one 32-bit nibble word (8 rows) of a group and
-//    accumulates x_i (q - z) s in FP32 ((q - z) s is exact in FP32); the 8
-//    warps' partial rows are added in warp order (deterministic) and added to y.
+//  * apply: one CTA per 256 output rows, W warps (8, or 32 for selections of
+//    more than 128 columns) taking every W-th selected column; a lane owns one
+//    32-bit nibble word (8 rows) of a group and accumulates x_i (q - z) s in
+//    FP32 ((q - z) s is exact in FP32); the W warps' partial rows are added in
+//    warp order (deterministic) and added to y.
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -38,7 +39,8 @@ constexpr int kChunk = lbq::kRefineChunk;
 constexpr int kNoAllocIdxMax = (lbq::kMaxK / lbq::kRefineChunk) * lbq::kRefineMaxK;
 __device__ __align__(256) int32_t g_refine_idx_scratch[kNoAllocIdxMax];
 constexpr int kApplyRows = 256;
-constexpr int kApplyWarps = 8;
+constexpr int kApplyWarpsMax = 32;
+constexpr int kApplyWideFrom = 128;   // selections longer than this use 32 warps
 
 // Warp-parallel search of the histogram from its top bin down: the bin in which
 // the running count reaches `remaining`; returns it and the count above it.
@@ -122,19 +124,9 @@ __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half*
     }
 }
 
-__global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint8_t* __restrict__ blob, int N, int K,
-                                                                      const __half* __restrict__ x,
-                                                                      const int32_t* __restrict__ idx, int nsel,
-                                                                      void* y, int y_f32, unsigned* err) {
-    __shared__ float part[kApplyWarps][kApplyRows];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = blockIdx.x * kApplyRows;
-    const int g = (row0 >> 5) + (lane >> 2), wd = lane & 3;     // group and nibble word of this lane
-    const bool rows_ok = g * 32 < N;
-    const uint64_t cb = lbq::refine_column_bytes(N);
-    // launched with programmatic dependent launch: idx, x and y come from the kernels before
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (blockIdx.x == 0 && tid == 0) {
+// Header of a refinement blob: magic, version, shape (block 0 checks it).
+__device__ __forceinline__ void check_refine_header(const uint8_t* blob, int N, int K, unsigned* err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         const unsigned* h = reinterpret_cast<const unsigned*>(blob);
         long long n_hdr, k_hdr;
         memcpy(&n_hdr, blob + 16, 8);
@@ -142,59 +134,78 @@ __global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint
         if (h[0] != 0x5251424Cu || h[1] != 0x43345746u || h[2] != lbq::kRefineVersion || n_hdr != N || k_hdr != K)
             atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_FORMAT));
     }
-    float acc[8];
+}
+
+// y[row0 + n] += sum_j x[idx_j] C[row0 + n, idx_j] for the CTA's 256 rows.  The
+// W warps take every W-th selected column; a lane owns one 32-bit nibble word
+// (8 rows) of a group and accumulates x_i (q - z) s in FP32 ((q - z) s is exact
+// in FP32); the warps' partial rows are added in warp order (deterministic) by
+// threads 0..255.
+template <int W>
+__device__ __forceinline__ void apply_tile(const uint8_t* __restrict__ blob, int N, int K, const __half* x,
+                                           const int32_t* idx, int nsel, void* y, int y_f32, unsigned* err,
+                                           float (*part)[kApplyRows]) {
+    constexpr int kApplyWarps = W;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int row0 = blockIdx.x * kApplyRows;
+    const int g = (row0 >> 5) + (lane >> 2), wd = lane & 3;     // group and nibble word of this lane
+    const bool rows_ok = g * 32 < N;
+    const uint64_t cb = lbq::refine_column_bytes(N);
+    if (warp < kApplyWarps) {
+        float acc[8];
 #pragma unroll
-    for (int b = 0; b < 8; ++b) acc[b] = 0.f;
-    // four columns per round, all their loads issued before any is used
-    constexpr int kU = 4;
-    for (int j0 = warp; j0 < nsel; j0 += kApplyWarps * kU) {
-        int col_i[kU];
+        for (int b = 0; b < 8; ++b) acc[b] = 0.f;
+        // four columns per round, all their loads issued before any is used
+        constexpr int kU = 4;
+        for (int j0 = warp; j0 < nsel; j0 += kApplyWarps * kU) {
+            int col_i[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int j = j0 + u * kApplyWarps;
-            col_i[u] = j < nsel ? idx[j] : -1;
-            if (j < nsel && (col_i[u] < 0 || col_i[u] >= K)) {
-                if (lane == 0) atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
-                col_i[u] = -1;
+            for (int u = 0; u < kU; ++u) {
+                const int j = j0 + u * kApplyWarps;
+                col_i[u] = j < nsel ? idx[j] : -1;
+                if (j < nsel && (col_i[u] < 0 || col_i[u] >= K)) {
+                    if (lane == 0) atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
+                    col_i[u] = -1;
+                }
+            }
+            float xi[kU], sc[kU], zf[kU];
+            uint32_t word[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                xi[u] = 0.f;
+                sc[u] = 0.f;
+                zf[u] = 0.f;
+                word[u] = 0u;
+                if (col_i[u] >= 0 && rows_ok) {
+                    const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(col_i[u]) * cb;
+                    xi[u] = __half2float(x[col_i[u]]);
+                    word[u] = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
+                    sc[u] = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
+                    const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
+                    zf[u] = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const float lo = (static_cast<float>((word[u] >> (8 * b)) & 15u) - zf[u]) * sc[u];      // row 4 wd + b
+                    const float hi = (static_cast<float>((word[u] >> (8 * b + 4)) & 15u) - zf[u]) * sc[u];  // row 16 + 4 wd + b
+                    acc[b] = fmaf(lo, xi[u], acc[b]);
+                    acc[4 + b] = fmaf(hi, xi[u], acc[4 + b]);
+                }
             }
         }
-        float xi[kU], sc[kU], zf[kU];
-        uint32_t word[kU];
+        const int rbase = (lane >> 2) * 32 + 4 * wd;
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            xi[u] = 0.f;
-            sc[u] = 0.f;
-            zf[u] = 0.f;
-            word[u] = 0u;
-            if (col_i[u] >= 0 && rows_ok) {
-                const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(col_i[u]) * cb;
-                xi[u] = __half2float(x[col_i[u]]);
-                word[u] = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
-                sc[u] = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
-                const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
-                zf[u] = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
-            }
+        for (int b = 0; b < 4; ++b) {
+            part[warp][rbase + b] = acc[b];
+            part[warp][rbase + 16 + b] = acc[4 + b];
         }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const float lo = (static_cast<float>((word[u] >> (8 * b)) & 15u) - zf[u]) * sc[u];      // row 4 wd + b
-                const float hi = (static_cast<float>((word[u] >> (8 * b + 4)) & 15u) - zf[u]) * sc[u];  // row 16 + 4 wd + b
-                acc[b] = fmaf(lo, xi[u], acc[b]);
-                acc[4 + b] = fmaf(hi, xi[u], acc[4 + b]);
-            }
-        }
-    }
-    const int rbase = (lane >> 2) * 32 + 4 * wd;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        part[warp][rbase + b] = acc[b];
-        part[warp][rbase + 16 + b] = acc[4 + b];
     }
     __syncthreads();
     const int n = row0 + tid;
-    if (n < N) {
+    if (tid < kApplyRows && n < N) {
         float tot = 0.f;
 #pragma unroll
         for (int w = 0; w < kApplyWarps; ++w) tot += part[w][tid];
@@ -206,6 +217,20 @@ __global__ void __launch_bounds__(kApplyRows) lbq_refine_apply_kernel(const uint
             yh[n] = __float2half_rn(__half2float(yh[n]) + tot);
         }
     }
+}
+
+// W = 8 warps for short selections, 32 for long ones (224 columns after a
+// K = 14336 projection: 18.2 -> 12.5 us measured)
+template <int W>
+__global__ void __launch_bounds__(W * 32) lbq_refine_apply_kernel(const uint8_t* __restrict__ blob, int N, int K,
+                                                                  const __half* __restrict__ x,
+                                                                  const int32_t* __restrict__ idx, int nsel, void* y,
+                                                                  int y_f32, unsigned* err) {
+    __shared__ float part[W][kApplyRows];
+    // launched with programmatic dependent launch: idx, x and y come from the kernels before
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    check_refine_header(blob, N, K, err);
+    apply_tile<W>(blob, N, K, x, idx, nsel, y, y_f32, err, part);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -293,7 +318,10 @@ lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void
     const lbq_status st = lbq::device_context(&err, &sms);
     if (st != LBQ_OK) return st;
     const unsigned grid = static_cast<unsigned>((N + kApplyRows - 1) / kApplyRows);
-    return launch_pdl(reinterpret_cast<const void*>(&lbq_refine_apply_kernel), grid, kApplyRows, stream,
+    const bool wide = n_sel > kApplyWideFrom;
+    return launch_pdl(wide ? reinterpret_cast<const void*>(&lbq_refine_apply_kernel<kApplyWarpsMax>)
+                           : reinterpret_cast<const void*>(&lbq_refine_apply_kernel<8>),
+                      grid, wide ? kApplyWarpsMax * 32 : 8 * 32, stream,
                       static_cast<const uint8_t*>(refine), static_cast<int>(N), static_cast<int>(K),
                       static_cast<const __half*>(x_f16), idx, static_cast<int>(n_sel), y, y_dtype == LBQ_F32 ? 1 : 0,
                       err);

@@ -44,7 +44,8 @@ def test_selection_of_zeros_and_signed_zero(lbq):
     assert np.array_equal(_select(lbq, x, 3), O.select_refine(x, 3))
 
 
-@pytest.mark.parametrize("N,K,k", [(64, 64, 1), (128, 1088, 7), (320, 2112, 64), (4096, 4096, 16)])
+@pytest.mark.parametrize("N,K,k", [(64, 64, 1), (128, 1088, 7), (320, 2112, 64), (4096, 4096, 16),
+                                   (320, 4096, 100), (256, 14336, 16)])   # the last two: > 128 columns, 32 warps
 @pytest.mark.parametrize("f32", [True, False])
 def test_apply_elementwise(lbq, N, K, k, f32):
     rng = np.random.default_rng(N + K + k)
@@ -109,3 +110,4 @@ def test_apply_reports_bad_index_and_header(lbq):
     lbq.refine_apply(to_dev(blob), N, K - 64, x, to_dev(np.array([1], np.int32)), 1, y)   # K differs from the blob
     assert lbq.device_error() == 6                                   # LBQ_ERR_FORMAT
     assert np.array_equal(y.cpu().numpy(), np.zeros(N, np.float32))    # a zero residual adds nothing
+
