@@ -48,9 +48,9 @@ SAMPLE_ROWS_MAX = 1024
 L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)
 # DRAM bytes (read + write) per grouped launch from ncu captures of the same
 # launches (profiles/); valid only for the kernel source they were taken on.
-TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "e9b27fb1ef1c9782",
-                   "traffic": {"w4_layer_sweep": 129298688, "w2_layer_sweep": 100333056,
-                               "w4_smallM_gate_down": 68173824}}
+TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "0dd2bd4338b36fff",
+                   "traffic": {"w4_layer_sweep": 129266944, "w2_layer_sweep": 100254720,
+                               "w4_smallM_gate_down": 68175104}}
 METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
 W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
 W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
@@ -340,8 +340,20 @@ def main():
     reps = []
     for r in range(REPLICAS):
         reps.append([torch.from_numpy(e["blob"]).to(dev) for e in layer])
-    xs = [torch.from_numpy(np.ascontiguousarray(e["x"])).to(dev) for e in layer]
-    ys = [torch.empty((e["M"], e["N"]), dtype=torch.float16, device=dev) for e in layer]
+    # the activations of all matrices in one device buffer, the outputs in another
+    # (views of 16-byte aligned slices), so a step's inputs and results cross the
+    # host link in one copy each
+    x_all = torch.from_numpy(np.concatenate([np.ascontiguousarray(e["x"], dtype=np.float16).reshape(-1)
+                                             for e in layer])).to(dev)
+    y_all = torch.empty(sum(e["M"] * e["N"] for e in layer), dtype=torch.float16, device=dev)
+    xs, ys, xo, yo = [], [], 0, 0
+    for e in layer:
+        n = int(np.asarray(e["x"]).size)
+        xs.append(x_all[xo:xo + n].view(np.asarray(e["x"]).shape))
+        ys.append(y_all[yo:yo + e["M"] * e["N"]].view(e["M"], e["N"]))
+        assert (xo * 2) % 16 == 0 and (yo * 2) % 16 == 0
+        xo += n
+        yo += e["M"] * e["N"]
     launches_per_step = sum(group_launch_count(lbq, layer, kind, reps[0], xs, ys) for _, kind in GROUPS)
 
     def step_launches(blobs):
@@ -440,20 +452,20 @@ def main():
     clocks.stop()
     assert lbq.device_error(stream) == 0
 
-    # e2e: host (pinned) activations in, outputs back to host, through the same graph
-    h_x = [torch.from_numpy(np.ascontiguousarray(e["x"])).pin_memory() for e in layer]
-    h_y = [torch.empty((e["M"], e["N"]), dtype=torch.float16).pin_memory() for e in layer]
-    h2d = sum(t.numel() * 2 for t in h_x)
-    d2h = sum(t.numel() * 2 for t in h_y)
+    # e2e: host (pinned) activations in, outputs back to host, through the same
+    # graph, one synchronisation per step (a decode step needs its result)
+    h_x = torch.from_numpy(np.concatenate([np.ascontiguousarray(e["x"], dtype=np.float16).reshape(-1)
+                                           for e in layer])).pin_memory()
+    h_y = torch.empty(y_all.numel(), dtype=torch.float16).pin_memory()
+    h2d = h_x.numel() * 2
+    d2h = h_y.numel() * 2
     e2e_steps = max(10, min(2000, args.steps // 10))
     with torch.cuda.stream(stream):
         t0 = time.perf_counter()
         for s in range(e2e_steps):
-            for i in range(len(layer)):
-                xs[i].copy_(h_x[i], non_blocking=True)
+            x_all.copy_(h_x, non_blocking=True)
             graphs[s % REPLICAS].replay()
-            for i in range(len(layer)):
-                h_y[i].copy_(ys[i], non_blocking=True)
+            h_y.copy_(y_all, non_blocking=True)
             stream.synchronize()
         e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     e2e_value = whole_job_gbs(step_bytes, world, e2e_steps, e2e_s)
