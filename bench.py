@@ -311,7 +311,8 @@ def main():
     ap.add_argument("--no-sweep70b", action="store_true", help="skip the Llama-3-70B weight sweep detail")
     ap.add_argument("--single", default=None,
                     help="kind:N:K:n_out:M - time one kernel configuration alone (profiling aid), "
-                         "kind in w4, w2, w4m")
+                         "kind in w4, w2, w4m; sweep:KIND (one grouped launch of the step); "
+                         "kv:ROWS:WIDTH (KV cache read); refine:N:K:k (select + apply)")
     args = ap.parse_args()
     if args.single:
         return run_single(args)
@@ -763,6 +764,8 @@ def run_single(args):
     from bit_weight_only_lbq_gb300 import lbq
     if args.single.startswith("sweep:"):
         return run_single_sweep(args, args.single.split(":")[1])
+    if args.single.startswith("kv:") or args.single.startswith("refine:"):
+        return run_single_row(args)
     kind, N, K, n_out, M = args.single.split(":")
     N, K, n_out, M = int(N), int(K), int(n_out), int(M)
     rng = np.random.default_rng(0)
@@ -788,6 +791,53 @@ def run_single(args):
     torch.cuda.synchronize()
     us = [a.elapsed_time(b) * 1e3 for a, b in ts]
     nbytes = algorithmic_bytes("w2" if kind == "w2" else "w4", N, K, n_out, M)
+    assert lbq.device_error() == 0
+    print(json.dumps({"single": args.single, "bytes": nbytes, "us_median": statistics.median(us),
+                      "GB_s": nbytes / (statistics.median(us) * 1e-6) / 1e9}), flush=True)
+    return 0
+
+
+def run_single_row(args):
+    """The KV cache read (kv:ROWS:WIDTH, after filling the cache) or the refinement
+    (refine:N:K:k, select + apply on a random residual), launched steps times after
+    warmup without graphs (for ncu captures)."""
+    import torch
+    from bit_weight_only_lbq_gb300 import lbq
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(0)
+    parts = args.single.split(":")
+    if parts[0] == "kv":
+        rows, width = int(parts[1]), int(parts[2])
+        cache = torch.zeros((rows, lbq.kv_record_bytes(width)), dtype=torch.uint8, device=dev)
+        states = torch.from_numpy(rng.standard_normal((rows, width)).astype(np.float16)).to(dev)
+        lbq.kv_quantize(states, rows, width, cache, 0)
+        out = torch.empty((rows, width), dtype=torch.float16, device=dev)
+        fn = lambda: lbq.kv_dequant(cache, 0, rows, width, out)
+        nbytes = rows * (lbq.kv_record_bytes(width) + 2 * width)
+    else:
+        N, K, k = int(parts[1]), int(parts[2]), int(parts[3])
+        blob = torch.from_numpy(lbq.pack_refine((rng.standard_normal((N, K)) * 1e-3).astype(np.float32))).to(dev)
+        x = torch.from_numpy(rng.standard_normal(K).astype(np.float16)).to(dev)
+        y = torch.zeros(N, dtype=torch.float32, device=dev)
+        n_sel = lbq.refine_selected_count(K, k)
+        idx = torch.empty(n_sel, dtype=torch.int32, device=dev)
+
+        def fn():
+            lbq.refine_select(x, K, k, idx)
+            lbq.refine_apply(blob, N, K, x, idx, n_sel, y)
+        nbytes = n_sel * (lbq.lib().lbq_refine_packed_bytes(N, 1) - 64) + 2 * K + 6 * n_sel + 8 * N
+    for _ in range(max(1, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in ts]
     assert lbq.device_error() == 0
     print(json.dumps({"single": args.single, "bytes": nbytes, "us_median": statistics.median(us),
                       "GB_s": nbytes / (statistics.median(us) * 1e-6) / 1e9}), flush=True)
