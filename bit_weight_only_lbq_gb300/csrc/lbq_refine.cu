@@ -33,6 +33,7 @@
 namespace {
 
 constexpr int kChunk = lbq::kRefineChunk;
+static_assert(kChunk == 1024, "the selection runs one thread per channel of a 1,024-channel chunk");
 
 // Index scratch of lbq_refine_noalloc: one array per device, shared by every
 // call.  64 chunks (K <= 65536) x 256 channels (k <= 256) = 16384 indices, 64 KB.
@@ -74,9 +75,11 @@ __device__ void find_bin(const unsigned* hist, int nbins, unsigned remaining, in
 
 __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half* __restrict__ x, int K, int k,
                                                                    int32_t* __restrict__ idx) {
-    __shared__ unsigned hist[512];
-    __shared__ int s_bin;
-    __shared__ unsigned s_above;
+    // one histogram and one (bin, count above) slot per pass, so no pass waits
+    // for the one before it to be done reading
+    __shared__ unsigned hist[512 + 256 + 256];
+    __shared__ int s_bin[3];
+    __shared__ unsigned s_above[3];
     __shared__ unsigned warp_cnt[kChunk / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     // launched with programmatic dependent launch: x may come from the kernel before
@@ -95,20 +98,21 @@ __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half*
     unsigned thr = 0;
     if (kk < len) {
         unsigned prefix = 0, remaining = static_cast<unsigned>(kk);
+        hist[t] = 0u;                                     // 1,024 counters, one per thread
+        __syncthreads();
         // digits: key bits 24..16 (512 bins), 15..8, 7..0 (256 bins each)
         for (int pass = 0; pass < 3; ++pass) {
             const int shift = pass == 0 ? 16 : pass == 1 ? 8 : 0;
             const int nbins = pass == 0 ? 512 : 256;
-            for (int b = t; b < 512; b += kChunk) hist[b] = 0u;
-            __syncthreads();
+            unsigned* h = hist + (pass == 0 ? 0 : pass == 1 ? 512 : 768);
             const bool cand = valid && (pass == 0 || (key >> (shift + 8)) == prefix);
-            if (cand) atomicAdd(&hist[(key >> shift) & (nbins - 1)], 1u);
+            if (cand) atomicAdd(&h[(key >> shift) & (nbins - 1)], 1u);
             __syncthreads();
-            if (warp == 0) find_bin(hist, nbins, remaining, lane, &s_bin, &s_above);
+            if (warp == 0) find_bin(h, nbins, remaining, lane, &s_bin[pass], &s_above[pass]);
             __syncthreads();
-            prefix = (pass == 0) ? static_cast<unsigned>(s_bin) : ((prefix << 8) | static_cast<unsigned>(s_bin));
-            remaining -= s_above;
-            __syncthreads();
+            prefix = (pass == 0) ? static_cast<unsigned>(s_bin[pass])
+                                 : ((prefix << 8) | static_cast<unsigned>(s_bin[pass]));
+            remaining -= s_above[pass];
         }
         thr = prefix;   // all 25 bits: unique keys, so exactly kk keys are >= thr
     }
@@ -155,44 +159,55 @@ __device__ __forceinline__ void apply_tile(const uint8_t* __restrict__ blob, int
         float acc[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc[b] = 0.f;
-        // four columns per round, all their loads issued before any is used
+        // the warp's columns are j = warp + W c; their indices are loaded 32 at a
+        // time (lane c holds column c's), then gathered four columns per round,
+        // all loads of a round issued before any is used
         constexpr int kU = 4;
-        for (int j0 = warp; j0 < nsel; j0 += kApplyWarps * kU) {
-            int col_i[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int j = j0 + u * kApplyWarps;
-                col_i[u] = j < nsel ? idx[j] : -1;
-                if (j < nsel && (col_i[u] < 0 || col_i[u] >= K)) {
-                    if (lane == 0) atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
-                    col_i[u] = -1;
+        for (int base = 0; base < nsel; base += kApplyWarps * 32) {
+            const int jl = base + warp + kApplyWarps * lane;
+            int mine = -1;
+            if (jl < nsel) {
+                mine = idx[jl];
+                if (mine < 0 || mine >= K) {
+                    atomicCAS(err, 0u, static_cast<unsigned>(LBQ_ERR_VALUE));
+                    mine = -1;
                 }
             }
-            float xi[kU], sc[kU], zf[kU];
-            uint32_t word[kU];
+            const int rest = nsel - base - warp;
+            const int ncols = rest <= 0 ? 0 : min(32, (rest + kApplyWarps - 1) / kApplyWarps);
+            for (int r0 = 0; r0 < ncols; r0 += kU) {
+                int col_i[kU];
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                xi[u] = 0.f;
-                sc[u] = 0.f;
-                zf[u] = 0.f;
-                word[u] = 0u;
-                if (col_i[u] >= 0 && rows_ok) {
-                    const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(col_i[u]) * cb;
-                    xi[u] = __half2float(x[col_i[u]]);
-                    word[u] = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
-                    sc[u] = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
-                    const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
-                    zf[u] = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+                for (int u = 0; u < kU; ++u) {
+                    const int c = __shfl_sync(0xffffffffu, mine, (r0 + u) & 31);
+                    col_i[u] = r0 + u < ncols ? c : -1;
                 }
-            }
+                float xi[kU], sc[kU], zf[kU];
+                uint32_t word[kU];
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
+                for (int u = 0; u < kU; ++u) {
+                    xi[u] = 0.f;
+                    sc[u] = 0.f;
+                    zf[u] = 0.f;
+                    word[u] = 0u;
+                    if (col_i[u] >= 0 && rows_ok) {
+                        const uint8_t* col = blob + lbq::kRefineHeader + static_cast<uint64_t>(col_i[u]) * cb;
+                        xi[u] = __half2float(x[col_i[u]]);
+                        word[u] = *reinterpret_cast<const uint32_t*>(col + g * 16 + wd * 4);
+                        sc[u] = __half2float(*reinterpret_cast<const __half*>(col + N / 2 + g * 2));
+                        const uint32_t zb = col[N / 2 + N / 16 + (g >> 1)];
+                        zf[u] = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+                    }
+                }
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const float lo = (static_cast<float>((word[u] >> (8 * b)) & 15u) - zf[u]) * sc[u];      // row 4 wd + b
-                    const float hi = (static_cast<float>((word[u] >> (8 * b + 4)) & 15u) - zf[u]) * sc[u];  // row 16 + 4 wd + b
-                    acc[b] = fmaf(lo, xi[u], acc[b]);
-                    acc[4 + b] = fmaf(hi, xi[u], acc[4 + b]);
+                for (int u = 0; u < kU; ++u) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        const float lo = (static_cast<float>((word[u] >> (8 * b)) & 15u) - zf[u]) * sc[u];      // row 4 wd + b
+                        const float hi = (static_cast<float>((word[u] >> (8 * b + 4)) & 15u) - zf[u]) * sc[u];  // row 16 + 4 wd + b
+                        acc[b] = fmaf(lo, xi[u], acc[b]);
+                        acc[4 + b] = fmaf(hi, xi[u], acc[4 + b]);
+                    }
                 }
             }
         }
