@@ -10,15 +10,16 @@
 // GB300 design:
 //  * selection: one CTA of 1,024 threads per chunk, one channel per thread.
 //    The key (|x| as its 15 FP16 magnitude bits, then 1023 - channel) is unique,
-//    so a most-significant-digit radix select (9 + 8 + 8 bits, shared-memory
-//    histograms, a warp-parallel scan of the bins) finds the k-th largest key
-//    exactly; ties in |x| go to the lower channel.  The selected channels are
-//    written in ascending order with a ballot prefix sum.
+//    so a most-significant-digit radix select (9 + 8 + 8 bits, one
+//    shared-memory histogram per pass, a warp-parallel scan of the bins) finds
+//    the k-th largest key exactly; ties in |x| go to the lower channel.  The
+//    selected channels are written in ascending order with a ballot prefix sum.
 //  * apply: one CTA per 256 output rows, W warps (8, or 32 for selections of
-//    more than 128 columns) taking every W-th selected column; a lane owns one
-//    32-bit nibble word (8 rows) of a group and accumulates x_i (q - z) s in
-//    FP32 ((q - z) s is exact in FP32); the W warps' partial rows are added in
-//    warp order (deterministic) and added to y.
+//    more than 128 columns) taking every W-th selected column, the indices of
+//    a warp's next 32 columns loaded at once; a lane owns one 32-bit nibble
+//    word (8 rows) of a group and accumulates x_i (q - z) s in FP32 ((q - z) s
+//    is exact in FP32); the W warps' partial rows are added in warp order
+//    (deterministic) and added to y.
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
