@@ -29,8 +29,9 @@
  *    code; they touch no GPU and are thread-safe.
  *  - Device entry points take device pointers (16-byte aligned where stated)
  *    and a stream (a cudaStream_t passed as void*, NULL = legacy default
- *    stream).  They validate arguments on the host, enqueue one kernel and
- *    return without synchronising.  They never allocate.
+ *    stream).  They validate arguments on the host, enqueue their kernels
+ *    (one for a single M = 1 call; a call states when it may enqueue more)
+ *    and return without synchronising.  They never allocate.
  *  - Errors: every entry point returns an lbq_status; nothing crosses the ABI
  *    as an exception.  A kernel never traps: a bounded wait that gives up, or
  *    a blob whose header does not match the call, records a code in a
@@ -185,7 +186,10 @@ lbq_status lbq_gemv_w2cb_outlier(const void* packed, int64_t N, int64_t K, int32
  * X_f16 : device, M rows of K FP16 with leading dimension ldx (elements),
  *         16-byte aligned base, ldx % 8 == 0, ldx >= K.
  * Y     : device, M rows of N values of y_dtype with leading dimension ldy >= N.
- * 1 <= M <= 64.  Errors as lbq_gemv_w4a16. */
+ * 1 <= M <= 64.  M < 16, or any M with n_out > 0: passes of 2, 4 or 8
+ * activation rows on the CUDA-core kernel (one kernel per pass); M >= 16
+ * with n_out == 0: one launch of the tensor-core (tcgen05) kernel.
+ * Errors as lbq_gemv_w4a16. */
 lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
                                  const void* X_f16, int64_t ldx, void* Y, int64_t ldy,
                                  lbq_dtype y_dtype, void* stream);
