@@ -27,6 +27,16 @@ def _states(rng, rows, width):
     X[0, :32] = np.float16(0.0)                                                   # a zero group
     if rows > 2:
         X[2, 32:64] = np.float16(-1.25)                                           # a constant group
+    if rows > 3:
+        # ties of w / s + z on .5 (s = 1 exactly): round half to even decides the codes
+        X[1, :32] = np.float16(0.0)
+        X[1, :6] = np.array([0.0, 15.0, 7.5, 2.5, 0.5, 13.5], np.float16)
+        # z itself on a tie: wmin = -7.5, s = 1, z = round(7.5) = 8
+        X[3, :32] = np.float16(1.0)
+        X[3, :4] = np.array([-7.5, 7.5, -2.5, 0.0], np.float16)
+        # FP16 subnormals and a negative zero
+        X[1, 32:64] = (np.arange(32) * 2.0 ** -24).astype(np.float16)
+        X[1, 40] = np.float16(-0.0)
     return X
 
 

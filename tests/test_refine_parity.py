@@ -45,7 +45,8 @@ def test_selection_of_zeros_and_signed_zero(lbq):
 
 
 @pytest.mark.parametrize("N,K,k", [(64, 64, 1), (128, 1088, 7), (320, 2112, 64), (4096, 4096, 16),
-                                   (320, 4096, 100), (256, 14336, 16)])   # the last two: > 128 columns, 32 warps
+                                   (320, 4096, 100), (256, 14336, 16),    # > 128 columns: 32 warps
+                                   (64, 8192, 256)])                      # > 1024 columns: two index blocks
 @pytest.mark.parametrize("f32", [True, False])
 def test_apply_elementwise(lbq, N, K, k, f32):
     rng = np.random.default_rng(N + K + k)
