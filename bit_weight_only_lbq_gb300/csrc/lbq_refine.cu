@@ -11,7 +11,8 @@
 //  * selection: one CTA of 1,024 threads per chunk, one channel per thread.
 //    The key (|x| as its 15 FP16 magnitude bits, then 1023 - channel) is unique,
 //    so a most-significant-digit radix select (9 + 8 + 8 bits, one
-//    shared-memory histogram per pass, a warp-parallel scan of the bins) finds
+//    shared-memory histogram per pass, a warp-parallel scan of the bins with
+//    16-byte loads) finds
 //    the k-th largest key exactly; ties in |x| go to the lower channel.  The
 //    selected channels are written in ascending order with a ballot prefix sum.
 //  * apply: one CTA per 256 output rows, W warps (8, or 32 for selections of
@@ -45,31 +46,49 @@ constexpr int kApplyWarpsMax = 32;
 constexpr int kApplyWideFrom = 128;   // selections longer than this use 32 warps
 
 // Warp-parallel search of the histogram from its top bin down: the bin in which
-// the running count reaches `remaining`; returns it and the count above it.
+// the running count reaches `remaining`; returns it and the count above it.  A
+// lane reads its 8 or 16 consecutive bins with 16-byte loads (a 2-way bank
+// conflict instead of 16-way for one bin per load); hist is 16-byte aligned.
 __device__ void find_bin(const unsigned* hist, int nbins, unsigned remaining, int lane, int* bin_out,
                          unsigned* above_out) {
-    const int per = nbins / 32;                       // bins per lane, lane 0 the highest
-    const int top = nbins - per * lane;               // lane covers [top - per, top)
+    const int per = nbins / 32;                       // 16 or 8 bins per lane, lane 0 the highest
+    const int lo = nbins - per * (lane + 1);          // lane covers [lo, lo + per)
+    unsigned v[16];
+    const uint4* hv = reinterpret_cast<const uint4*>(hist + lo);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = q * 4 < per ? hv[q] : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * q] = u.x;
+        v[4 * q + 1] = u.y;
+        v[4 * q + 2] = u.z;
+        v[4 * q + 3] = u.w;
+    }
     unsigned mine = 0;
-    for (int b = top - 1; b >= top - per; --b) mine += hist[b];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mine += v[i];
     unsigned incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const unsigned v2 = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v2;
     }
     const unsigned excl = incl - mine;
     const unsigned hit = __ballot_sync(0xffffffffu, incl >= remaining && excl < remaining);
     const int src = __ffs(hit) - 1;
     if (lane == src) {
         unsigned cum = excl;
-        for (int b = top - 1; b >= top - per; --b) {
-            if (cum + hist[b] >= remaining) {
-                *bin_out = b;
-                *above_out = cum;
-                break;
+        bool found = false;
+#pragma unroll
+        for (int i = 15; i >= 0; --i) {
+            if (i < per && !found) {
+                if (cum + v[i] >= remaining) {
+                    *bin_out = lo + i;
+                    *above_out = cum;
+                    found = true;
+                } else {
+                    cum += v[i];
+                }
             }
-            cum += hist[b];
         }
     }
 }
@@ -78,7 +97,7 @@ __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half*
                                                                    int32_t* __restrict__ idx) {
     // one histogram and one (bin, count above) slot per pass, so no pass waits
     // for the one before it to be done reading
-    __shared__ unsigned hist[512 + 256 + 256];
+    __shared__ __align__(16) unsigned hist[512 + 256 + 256];
     __shared__ int s_bin[3];
     __shared__ unsigned s_above[3];
     __shared__ unsigned warp_cnt[kChunk / 32];
