@@ -499,7 +499,8 @@ def main():
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp16 activations, fp32 accumulate (w4 / w2 weights)",
+        "vs_baseline": None, "dtype": "f32",
+        "dtype_detail": "4-/2-bit weights and fp16 activations in, exact fp16 products, fp32 accumulation",
         "data": "synthetic (seeded; shapes and distributions of the decode configs)",
         "config": config_dict(),
         "gpu_launches": launches_per_step * args.steps,
