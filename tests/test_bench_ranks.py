@@ -53,3 +53,16 @@ def test_reference_arm_other_ranks_exit_quietly(capsys):
         steps, warmup = 1, 0
     assert bench.run_reference(A(), rank=1, world=2) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_algorithmic_bytes_match_the_roofline_table():
+    """The bytes the roofline divides by, worked by hand from the layout: 4-bit
+    4 bits + an FP16 scale / 32 + a 4-bit zero / 32 per weight, 2-bit 2 bits +
+    FP16 S and Z / 32, outliers 4 B of index + 2 B per row, FP16 x in, FP16 y out."""
+    assert bench.algorithmic_bytes("w4", 4096, 4096, 0) == 4096 * 4096 * 37 // 64 + 2 * 4096 + 2 * 4096
+    assert bench.algorithmic_bytes("w4", 4096, 4096, 0) == 9715712
+    assert bench.algorithmic_bytes("w2", 4096, 4096, 143) == 4096 * 4096 * 3 // 8 + 143 * (4 + 2 * 4096) + 4 * 4096
+    assert bench.algorithmic_bytes("w4", 14336, 4096, 0, M=4) == 14336 * 4096 * 37 // 64 + 2 * 4096 * 4 + 2 * 14336 * 4
+    layer = sum(bench.algorithmic_bytes("w4", N, K, 0) for N, K in
+                ((4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (14336, 4096), (14336, 4096), (4096, 14336)))
+    assert layer == 126255104
