@@ -298,13 +298,19 @@ size_t lbq_kv_record_bytes(int64_t width);
 
 /* Device: quantise `rows` FP16 rows (x_f16, leading dimension ldx elements,
  * 16-byte aligned, ldx % 8 == 0) into records first_row .. first_row + rows - 1
- * of `cache` (16-byte aligned).  rows = 0 is a no-op. */
+ * of `cache` (16-byte aligned).  rows = 0 is a no-op.  The caller owns the
+ * cache and must size it for first_row + rows records of
+ * lbq_kv_record_bytes(width) bytes (the library cannot check it).  Writes
+ * touch only those records.  Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE (width,
+ * rows, first_row < 0, ldx < width), LBQ_ERR_ALIGN, LBQ_ERR_CUDA,
+ * LBQ_ERR_UNSUPPORTED (no sm_103a device). */
 lbq_status lbq_kv_quantize(const void* x_f16, int64_t ldx, int64_t rows, int64_t width, void* cache,
                            int64_t first_row, void* stream);
 
 /* Device: read records first_row .. first_row + rows - 1 back as FP16 rows
  * ((q - z) s rounded once) into out_f16 (leading dimension ldo, 16-byte
- * aligned, ldo % 8 == 0). */
+ * aligned, ldo % 8 == 0); columns past width of each output row are not
+ * written.  Errors as lbq_kv_quantize (ldo < width is LBQ_ERR_SHAPE). */
 lbq_status lbq_kv_dequant(const void* cache, int64_t first_row, int64_t rows, int64_t width, void* out_f16,
                           int64_t ldo, void* stream);
 
