@@ -355,13 +355,17 @@ size_t lbq_refine_packed_bytes(int64_t N, int64_t K);
 
 /* Host: quantise the N x K FP32 row-major matrix R column by column and write
  * the refinement blob into dst (caller-allocated host memory, dst_bytes >=
- * lbq_refine_packed_bytes).  LBQ_ERR_VALUE for non-finite input. */
+ * lbq_refine_packed_bytes).  Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE,
+ * LBQ_ERR_BUFFER_TOO_SMALL, LBQ_ERR_VALUE (non-finite input). */
 lbq_status lbq_pack_refine(const float* R, int64_t N, int64_t K, void* dst, size_t dst_bytes);
 
 /* Host: the matrix a resident blob applies, as N x K FP32 row-major: the
  * dequantised dense weights (4-bit (q - z) s, 2-bit S C[q] + Z, evaluated in
  * FP64 and rounded once to FP32) with each outlier column replaced by its
- * exact FP16 values.  packed: host copy of a blob of either kind. */
+ * exact FP16 values.  packed: host copy of a blob of either kind, of
+ * packed_bytes bytes; W_hat: N x K floats, caller-allocated.  Errors:
+ * LBQ_ERR_NULL, LBQ_ERR_BUFFER_TOO_SMALL (shorter than its header says),
+ * LBQ_ERR_FORMAT (not a blob of this library's format). */
 lbq_status lbq_dequant_host(const void* packed, size_t packed_bytes, float* W_hat);
 
 /* Number of channels lbq_refine_select writes for (K, k); 0 for bad arguments. */
