@@ -1263,15 +1263,19 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
     // M >= 16 without outlier columns: the tensor-core kernel, one launch per problem
     bool dense_only = true;
     for (int i = 0; i < count; ++i) dense_only = dense_only && P[i].n_out == 0;
-    if (kind == kW4 && M >= 16 && dense_only) {
+    if (M >= 16 && dense_only) {
         for (int i = 0; i < count; ++i) {
-            if (launches) {
+            const uint32_t fl = i == 0 ? flags : (flags | LBQ_FLAG_PDL);
+            if (kind == kW2) {
+                st = lbq::launch_w2_mma(P[i].packed, P[i].N, P[i].K, M, P[i].x, P[i].ldx, P[i].y, P[i].ldy, f32,
+                                        dev->err_word, dev->max_smem, stream, fl, launches);
+            } else if (launches) {
                 ++*launches;
-                continue;
+                st = LBQ_OK;
+            } else {
+                st = lbq::launch_w4_mma(P[i].packed, P[i].N, P[i].K, M, P[i].x, P[i].ldx, P[i].y, P[i].ldy, f32,
+                                        dev->err_word, dev->sms, dev->max_smem, stream, fl);
             }
-            st = lbq::launch_w4_mma(P[i].packed, P[i].N, P[i].K, M, P[i].x, P[i].ldx, P[i].y, P[i].ldy, f32,
-                                    dev->err_word, dev->sms, dev->max_smem, stream,
-                                    i == 0 ? flags : (flags | LBQ_FLAG_PDL));
             if (st != LBQ_OK) return st;
         }
         return LBQ_OK;

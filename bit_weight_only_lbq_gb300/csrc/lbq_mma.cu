@@ -1,43 +1,46 @@
-// 4-bit small-M GEMM on the 5th-generation tensor cores (tcgen05) for
-// M >= 16 activation rows, sm_103a.
+// Small-M GEMM (16 <= M <= 64 activation rows) of the 2-bit codebook format
+// on the 5th-generation tensor cores (tcgen05), sm_103a.  (The 4-bit format's
+// tensor-core kernel is lbq_mma_w4.cu.)
 //
-// Method (SPECTRA article, section 4.2 "Batched Tensor Core W4A16 GEMM with
-// In-Kernel Outlier Fusion"): at M >= 16 the product Y = X W_hat^T is a real
-// dense contraction, so the packed 4-bit weights are dequantised in the kernel
-// to FP16 tiles w_hat = s (q - z) and multiplied on the tensor cores with FP32
-// accumulation; the weights still cross HBM once, in their packed form.
+// Method (otf-llm 4.0.0, kernel description of its fused INT2 GEMM; SPECTRA
+// article, section 4.2 "Batched Tensor Core W4A16 GEMM"): at M >= 16 the
+// product Y = X W_hat^T is a real dense contraction, so the packed 2-bit codes
+// are dequantised in the kernel to FP16 tiles w_hat = S C[q] + Z (one FP16
+// fused multiply-add: one rounding, as the pages' dequantised tiles) and
+// multiplied on the tensor cores with FP32 accumulation; the codes cross HBM
+// once, in packed form.
 //
-// GB300 design:
-//  * a CTA owns a tile of 128 weight rows (32 row blocks of the blob) and a
-//    range of its 1024-k record blocks, walked in 256-k stages;
-//  * three tensor maps feed it through the Tensor Memory Accelerator: the
-//    nibbles of one stage for the 32 row blocks x 4 rows (16 KB, 128-byte
-//    swizzle, so the dequantising threads read shared memory without bank
-//    conflicts), the scales and zero points of a record block (10 KB), and
-//    the activations of the stage, written by the copy engine straight in the
-//    128-byte-swizzled K-major layout the tensor core reads (rows past M and
-//    columns past K arrive as zeros);
-//  * warp roles: one warp copies the weights (nibbles and metadata, which no
-//    earlier kernel writes, so it starts before the grid dependency resolves),
-//    one copies the activations, two issue tcgen05.mma (alternate stages, each
-//    into its own accumulator: a barrier wait holds the issuing thread until its
-//    earlier MMAs are taken, and the other warp issues meanwhile), sixteen
-//    dequantise - each thread owns one weight row (its tensor-memory lane) and
-//    2 groups per stage: 1024 + q from the nibble masked into the FP16 magic
-//    exponent, minus (1024 + z) exactly, times the FP16 scale (one rounding),
-//    stored into tensor memory with tcgen05.st (k in natural order).  A stays in
-//    tensor memory rather than shared memory: written and read there it would
-//    cost 128 KB of shared-memory traffic per stage;
-//  * every hand-off is an mbarrier: rings of 6-10 nibble stages, 2 metadata
-//    blocks, 3-4 activation stages, and 3 A stages in tensor memory (freed by
-//    tcgen05.commit when the tensor core has read them);
-//  * tcgen05.mma: A from tensor memory (128 rows), B from shared memory
-//    (N = 16..64 activation rows), K = 16, FP16 x FP16 -> FP32 in tensor
-//    memory; the two accumulators are added in a fixed order at the end;
-//  * when a tile's K is split over a cluster of CTAs, each CTA moves its FP32
-//    partial from tensor memory to shared memory and the cluster's rank 0 adds
-//    the partials in rank order through distributed shared memory
-//    (deterministic, no global workspace);
+// GB300 design.  On sm_103a a kind::f16 MMA with M = 128 and K = 16 takes the
+// same ~128 clocks for every N from 16 to 256 (measured), so the weights are
+// the N = 256 operand and the activations the M = 128 one: each MMA consumes
+// 4096 weights, twice what a 128-row weight operand would.
+//  * tile = 256 weight rows (64 row blocks of the blob); the work of a call is
+//    the sequence of (tile, 256-k chunk) units; a cluster of C CTAs takes a
+//    contiguous run of tiles and cuts its units into C contiguous ranges
+//    (split-K), so every SM gets the same number of chunks;
+//  * tensor memory holds two accumulators of 128 lanes x 256 FP32 columns: a
+//    CTA's range spans at most two tiles (taller matrices are cut into slabs
+//    of tiles launched one after another), each accumulated in its own D.  The
+//    A operand (activations) stays in shared memory: activation stores into
+//    tensor memory were measured to stall behind the MMAs' accumulator traffic;
+//  * warp roles: 8 dequantising warps (thread = weight row of the tile) load
+//    their row's 64 code bytes of each 256-k chunk and the chunk's S and Z
+//    straight into registers, one chunk ahead, prefetch their row's line ~8
+//    chunks ahead into L2, and turn the codes into the FP16 B stage (256 rows x
+//    64 k, the 128-byte swizzled K-major layout the tensor core reads); a copy
+//    warp brings each 64-k stage of X (M rows rounded to 8, zero-filled) into
+//    the A stage in the same layout (the MMA's 128-row A reads past it into
+//    rows whose products land in accumulator lanes that are never read); one
+//    thread issues the MMAs (4 per stage) and frees the stages with
+//    tcgen05.commit;
+//  * codes decode four at a time into a byte-permute selector, so the B stage
+//    holds each 16-k block in the order (0,4,8,12,1,5,...); 2 warps (thread =
+//    activation row) put the A stage in the same order in place, which leaves
+//    the contraction unchanged;
+//  * partial accumulators of a tile split over several CTAs go through shared
+//    memory; each contributing CTA adds one column slice of the tile from all
+//    contributors in rank order through distributed shared memory (fixed
+//    order: deterministic, no global workspace);
 //  * every wait is bounded (2 s of %globaltimer); a timeout records
 //    LBQ_ERR_TIMEOUT, makes every other wait of the CTA give up at once, and the
 //    CTA drains its copies and tensor-core work, frees its tensor memory and
@@ -56,38 +59,73 @@
 
 namespace {
 
-constexpr int kWorkerWarps = 16;             // dequantising warps: 4 per tensor-memory lane quarter
-constexpr int kWorkers = 32 * kWorkerWarps;
-// tensor-core issue is split over two warps taking alternate stages, each into
-// its own accumulator: a barrier wait holds its thread until the MMAs it issued
-// before have been taken by the tensor core, and the other warp issues meanwhile
-constexpr int kIssuers = 2;
-constexpr int kThreads = kWorkers + 64 + 32 * kIssuers;   // + weight-copy, activation-copy and MMA warps
-constexpr int kTileRows = 128;               // MMA M
-constexpr int kTileRb = kTileRows / 4;       // row blocks per tile
-constexpr int kRecBytes = 2368;              // 4-bit dense record
-constexpr int kMetaBytes = 320;              // its scales (256) and zero points (64)
-constexpr int kStageK = 256;                 // k per stage (8 groups)
-constexpr int kStagesPerBlock = 1024 / kStageK;
-constexpr int kGpw = 8 / (kWorkerWarps / 4);    // groups of a stage per dequantising warp
-constexpr int kCodeStage = kTileRb * 4 * 128;   // 16 KB: 8 groups x 16 B for 128 rows
-constexpr int kMetaBlock = kTileRb * kMetaBytes;  // 10 KB
-constexpr int kNA = 3;                       // A stages in tensor memory
-constexpr uint32_t kTmemCols = 512;          // accumulators in [0, 128), A stages from column 128
-constexpr uint32_t kAcol = 128;
+constexpr int kTileRows = 256;                 // weight rows per tile = MMA N
+constexpr int kTileRb = kTileRows / 4;         // row blocks per tile
+constexpr int kStageK = 64;                    // k per stage (4 MMAs of K = 16)
+constexpr int kChunkStages = 4;                // stages per copied chunk (256 k)
+constexpr int kChunksPerRec = 1024 / (kStageK * kChunkStages);
+constexpr int kDqWarps = 8;                    // dequantising warps: thread = weight row
+constexpr int kActWarps = 2;                   // 2-bit: warps ordering the A stage, thread = activation row
+// one thread issues the MMAs; it polls its barriers with mbarrier.test_wait:
+// a try_wait after MMAs was measured to hold the thread until its earlier MMAs
+// had drained (~1.3 k clocks a stage), a test_wait returns at once
+constexpr int kIssuers = 1;
+constexpr int kThreads = 32 * (kDqWarps + kActWarps + 1 + kIssuers);   // + X copy warp + MMA warps
+constexpr int kWarpAct = kDqWarps;             // first activation warp
+constexpr int kWarpXCopy = kDqWarps + kActWarps;  // activations
+constexpr int kWarpMma = kWarpXCopy + 1;          // first MMA warp
+constexpr int kNB = 4;                         // B stages (FP16 weights) in shared memory
+constexpr int kBStage = kTileRows * 128;       // 32 KB: 256 rows x 64 k x 2 B
+constexpr int kNA = 8;                         // A stages in shared memory (X copies run ahead: L2 latency)
+constexpr int kAStage = 64 * 128;              // 8 KB: 64 activation rows x 64 k x 2 B
+constexpr uint32_t kTmemCols = 512;            // D0 in [0, 256), D1 in [256, 512)
+constexpr int kPartStride = 1024 + 16;         // bytes per accumulator row of the partials (padded)
+constexpr int kMaxCluster = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// 2-bit record (1536 B): codes (4 rows x 256 B), FP16 S (4 x 32 groups, at 1024), FP16 Z (at 1280)
+struct Fmt {
+    static constexpr int kRecBytes = 1536;
+    static constexpr int kRowCodeBytes = 256;                        // codes of one row in a record
+    static constexpr int kChunkRowBytes = kRowCodeBytes / kChunksPerRec;   // 64: one row of a chunk
+    static constexpr int kCodeVecs = kChunkRowBytes / 16;            // 16-byte loads per row and chunk
+    static constexpr int kMeta0Off = 1024;                           // S
+    static constexpr int kMeta1Off = 1280;                           // Z
+    static constexpr int kPF = 8;                                    // chunks prefetched into L2 ahead
+    static constexpr uint32_t kMagicHi = 0x32334332u;                // "2C32"
+    // shared memory: A ring (first: the MMA's A reads run 8 KB past a stage, into
+    // the next one or the B ring), B ring, mbarriers, flags
+    static constexpr int kA = 0;
+    static constexpr int kB = kNA * kAStage;
+    static constexpr int kBars = kB + kNB * kBStage;
+    static constexpr int kNBars = 2 * kNB + 3 * kNA + 1;
+    static constexpr int kTotal = kBars + 8 * kNBars + 64 + 1024;   // + flags, 1024-byte alignment slack
+};
+
+struct Maps {
+    CUtensorMap x;
+};
 
 struct MmaArgs {
     const uint8_t* blob;
+    const uint8_t* area;    // row block 0
+    const __half* x;
     void* y;
     unsigned* err;
-    long long ldy;
+    long long ldx, ldy;
     long long N, K;
-    int recs;       // k-blocks
+    long long rb_bytes;
     int n_rb;
-    int M;          // activation rows (<= NM)
-    int S;          // k-splits per tile = cluster size
+    int T;                  // tiles
+    int U;                  // stages per tile
+    int Uc;                 // chunks per tile
+    int C;                  // CTAs per cluster
+    int G;                  // clusters
+    int M;                  // activation rows
+    int Mr;                 // rows of an X copy: M rounded up to 8
     int y_f32;
+    long long N_hdr;        // rows of the whole blob (a slab's launch checks the header against it)
+    uint32_t lut_lo, lut_hi;   // 2-bit codebook as FP16 byte tables
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -98,6 +136,18 @@ __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -147,124 +197,161 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
-__device__ __forceinline__ uint32_t u4w(const uint4& v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-
-// Word j (0..3) of a group's 16 qweight bytes (byte k = q_k | q_{k+16} << 4) as
-// 8 dequantised FP16 weights in natural order: lo[0] = (w_{4j}, w_{4j+1}),
-// lo[1] = (w_{4j+2}, w_{4j+3}), hi[0] = (w_{4j+16}, w_{4j+17}), hi[1] = (w_{4j+18}, w_{4j+19}).
-// 1024 + q is exact in FP16 (magic exponent), (1024 + q) - (1024 + z) = q - z
-// exactly, (1024 + 16 q) / 16 - (64 + z) = q - z exactly, then one rounding by s.
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t zlo2, uint32_t zhi2, uint32_t s2, uint32_t (&lo)[2],
-                                             uint32_t (&hi)[2]) {
-    const uint32_t sixteenth2 = 0x2C002C00u;   // FP16 1/16 in both halves
-    const uint32_t b01 = prmt(w, 0u, 0x4140u), b23 = prmt(w, 0u, 0x4342u);   // bytes 0,1 / 2,3 to the halves
-    lo[0] = hmul2(hsub2((b01 & 0x000F000Fu) | 0x64006400u, zlo2), s2);
-    lo[1] = hmul2(hsub2((b23 & 0x000F000Fu) | 0x64006400u, zlo2), s2);
-    hi[0] = hmul2(hfma2((b01 & 0x00F000F0u) | 0x64006400u, sixteenth2, zhi2), s2);
-    hi[1] = hmul2(hfma2((b23 & 0x00F000F0u) | 0x64006400u, sixteenth2, zhi2), s2);
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ uint4 ldg128(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t u4w(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-template <int NM>
-struct Geom {
-    // stages in flight within 227 KB of shared memory: nibbles (16 KB each; the
-    // deeper the better against DRAM latency) and activations (NM x 512 B each)
-    static constexpr int kNC = NM == 16 ? 10 : NM <= 48 ? 8 : 6;
-    static constexpr int kNB = NM <= 32 ? 4 : 3;
-    static constexpr int kBBox = NM * 128;                         // one 64-k box of NM rows
-    static constexpr int kBStage = 4 * kBBox;
-    static constexpr int code = 0;                                 // kNC x 16 KB (1024-aligned)
-    static constexpr int b = code + kNC * kCodeStage;              // kNB activation stages
-    static constexpr int meta = b + kNB * kBStage;                 // 2 x 10 KB
-    static constexpr int bars = meta + 2 * kMetaBlock;
-    static constexpr int nbars = 2 * kNC + 2 * 2 + 2 * kNB + 2 * kNA + 1;
-    static constexpr int total = bars + 8 * nbars + 32 + 1024;    // + flags, alignment
-};
+// Word v of a row's 2-bit codes (16 codes, byte i = codes of k = 4i..4i+3) as
+// 16 dequantised FP16 weights S C[q] + Z (one rounding), in the stage order
+// slot p <-> k = 4 (p % 4) + p / 4: out[2 sh] = (w_{sh}, w_{4+sh}),
+// out[2 sh + 1] = (w_{8+sh}, w_{12+sh}).
+__device__ __forceinline__ void w2_word(uint32_t w, uint32_t S2, uint32_t Z2, uint32_t lut_lo, uint32_t lut_hi,
+                                        uint32_t (&out)[8]) {
+#pragma unroll
+    for (int sh = 0; sh < 4; ++sh) {
+        const uint32_t t = (w >> (2 * sh)) & 0x03030303u;
+        const uint32_t sel = t * 0x11u + 0x40404040u;   // nibbles (c, c + 4) per code
+        out[2 * sh] = hfma2(prmt(lut_lo, lut_hi, sel), S2, Z2);
+        out[2 * sh + 1] = hfma2(prmt(lut_lo, lut_hi, sel >> 16), S2, Z2);
+    }
+}
 
-struct Maps {
-    CUtensorMap codes, meta, x;
-};
+// 16 activations of one 16-k block (natural pairs n[0..7]) in the 2-bit stage
+// order: pairs (0,4) (8,12) (1,5) (9,13) (2,6) (10,14) (3,7) (11,15).
+__device__ __forceinline__ void w2_order(const uint32_t (&n)[8], uint32_t (&o)[8]) {
+    o[0] = prmt(n[0], n[2], 0x5410u);
+    o[1] = prmt(n[4], n[6], 0x5410u);
+    o[2] = prmt(n[0], n[2], 0x7632u);
+    o[3] = prmt(n[4], n[6], 0x7632u);
+    o[4] = prmt(n[1], n[3], 0x5410u);
+    o[5] = prmt(n[5], n[7], 0x5410u);
+    o[6] = prmt(n[1], n[3], 0x7632u);
+    o[7] = prmt(n[5], n[7], 0x7632u);
+}
 
-template <int NM>
+// Units of cluster c: tiles [t0, t1) x Uc chunks; rank r takes [u0, u1).
+__host__ __device__ inline void cluster_tiles(int T, int G, int c, int* t0, int* t1) {
+    *t0 = static_cast<int>(static_cast<long long>(T) * c / G);
+    *t1 = static_cast<int>(static_cast<long long>(T) * (c + 1) / G);
+}
+__host__ __device__ inline void rank_range(long long units, int C, int r, long long* u0, long long* u1) {
+    *u0 = units * r / C;
+    *u1 = units * (r + 1) / C;
+}
+// The rank whose range holds unit u (ranges are contiguous and ascending).
+__host__ __device__ inline int rank_of(long long units, int C, long long u) {
+    int r = static_cast<int>((u * C) / (units > 0 ? units : 1));
+    if (r > C - 1) r = C - 1;
+    while (r > 0 && units * r / C > u) --r;
+    while (r + 1 < C && units * (r + 1) / C <= u) ++r;
+    return r;
+}
+
+}  // namespace
+
+namespace {
+
 __global__ void __launch_bounds__(kThreads, 1)
-    lbq_w4_mma_kernel(const __grid_constant__ MmaArgs a, const __grid_constant__ Maps maps) {
-    using G = Geom<NM>;
-    constexpr int kNB = G::kNB;
-    constexpr int kNC = G::kNC;
-    constexpr uint32_t kIdesc = idesc_f16(kTileRows, NM);
+    lbq_w2_mma_kernel(const __grid_constant__ MmaArgs a, const __grid_constant__ Maps maps) {
+    using F = Fmt;
+    constexpr uint32_t kIdesc = idesc_f16(128, kTileRows);
+    static_assert(128 * kPartStride <= F::kBars, "the partial accumulators reuse the stage rings");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::bars);
-    // mbarriers: code full/empty [kNC], meta full/empty [2], b full/empty [kNB], a full/empty [kNA], last
-    const uint32_t cfull = smem_u32(bars), cempty = cfull + 8 * kNC, mfull = cempty + 8 * kNC, mempty = mfull + 16,
-                   bfull = mempty + 16, bempty = bfull + 8 * kNB, afull = bempty + 8 * kNB, aempty = afull + 8 * kNA,
-                   last_bar = aempty + 8 * kNA;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + G::nbars);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + G::nbars) + 1;
-    // stages (nibbles, activations) and record blocks (metadata) whose copies were issued
-    volatile int* issued = reinterpret_cast<volatile int*>(bars + G::nbars) + 2;
+    const uint32_t sb = smem_u32(smem);
+    // mbarriers: B full/empty [kNB], X copied [kNA], A ready [kNA] (reordered), A
+    // empty [kNA], accumulators done
+    const uint32_t bfull = sb + F::kBars, bempty = bfull + 8 * kNB, xfull = bempty + 8 * kNB,
+                   afull = xfull + 8 * kNA, aempty = afull + 8 * kNA, dfull = aempty + 8 * kNA;
+    uint32_t* flags = reinterpret_cast<uint32_t*>(smem + F::kBars + 8 * F::kNBars);
+    volatile uint32_t* abort_flag = flags + 1;
+    volatile int* xissued = reinterpret_cast<volatile int*>(flags + 4);  // X stages whose copies were issued
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int S = a.S;
-    const int rank = static_cast<int>(blockIdx.x) % S;         // rank in the cluster (cluster = S consecutive CTAs)
-    const int tile = static_cast<int>(blockIdx.x) / S;
-    const int kb0 = rank * a.recs / S, kb1 = (rank + 1) * a.recs / S;
-    const int nkb = kb1 - kb0;
-    const int nstages = nkb * kStagesPerBlock;
-    const int rb0 = tile * kTileRb;
+    const int C = a.C, U = a.U, Uc = a.Uc;
+    const int cl = static_cast<int>(blockIdx.x) / C, rank = static_cast<int>(blockIdx.x) % C;
+    int t0, t1;
+    cluster_tiles(a.T, a.G, cl, &t0, &t1);
+    const long long units = static_cast<long long>(t1 - t0) * Uc;
+    long long lu0, lu1;
+    rank_range(units, C, rank, &lu0, &lu1);
+    const int u0 = static_cast<int>(lu0), u1 = static_cast<int>(lu1);   // this CTA's chunk units
+    const int ncu = u1 - u0;
+    auto chunk_stages = [&](int u) { const int c = u % Uc; return min(kChunkStages, U - kChunkStages * c); };
+    int nst = 0;
+    for (int u = u0; u < u1; ++u) nst += chunk_stages(u);
+    const int first_tile = t0 + (ncu > 0 ? u0 / Uc : 0);
+    const int nbands = ncu > 0 ? (u1 - 1) / Uc - u0 / Uc + 1 : 0;   // tiles touched (<= 2)
 
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(flags)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     if (tid == 32) {
-        for (int i = 0; i < G::nbars; ++i) {
-            const uint32_t bar = cfull + 8 * i;
-            // arrivals: copies (1, with the byte count), the dequantising warps,
-            // one tensor-core commit, or one commit per MMA warp (the last)
-            const bool workers = (bar >= cempty && bar < mfull) || (bar >= mempty && bar < bfull) ||
-                                 (bar >= afull && bar < aempty);
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar),
-                         "r"(workers ? kWorkerWarps : bar == last_bar ? kIssuers : 1)
-                         : "memory");
+        for (int i = 0; i < F::kNBars; ++i) {
+            const uint32_t bar = bfull + 8 * i;
+            // arrivals: the dequantising warps, the reordering warps, a copy (1, with
+            // the byte count), one tensor-core commit, or one per MMA warp
+            const uint32_t count = bar < bempty                     ? kDqWarps
+                                   : (bar >= afull && bar < aempty) ? kActWarps
+                                   : bar == dfull                   ? kIssuers
+                                                                    : 1;
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
         }
         *abort_flag = 0;
-        issued[0] = issued[1] = issued[2] = 0;
+        *xissued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = flags[0];
+    if (warp < 4) {
+        // clear both accumulators (every MMA accumulates): warp w zeroes lane quarter w
+#pragma unroll 1
+        for (int c0 = 0; c0 < static_cast<int>(kTmemCols); c0 += 32)
+            asm volatile(
+                "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, "
+                "%1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1, %1};" ::"r"(
+                    tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0)),
+                "r"(0u)
+                : "memory");
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // bounded wait that gives up at once after any thread of the CTA gave up
     auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-        // no sleep between polls: try_wait suspends the thread until the phase
-        // completes or a short hardware limit passes, and a sleep would only add
-        // wake-up latency to every hand-off
         if (mbar_try_wait(bar, parity)) return true;
-        const uint64_t t0 = global_ns();
+        const uint64_t w0 = global_ns();
         while (!mbar_try_wait(bar, parity)) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - w0 > kWaitLimitNs) {
                 *abort_flag = 1;
                 atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
                 return false;
@@ -275,256 +362,352 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto arrive = [&](uint32_t bar) {
         asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
     };
-    auto expect = [&](uint32_t bar, uint32_t bytes) {
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-    };
-
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     auto commit = [&](uint32_t bar) {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                      : "memory");
     };
-    if (warp == kWorkerWarps) {
-        // ------------------------------------------------------------------ weight copies
-        // the packed weights are not written by earlier kernels: no wait on them
-        if (lane == 0) {
-            int s = 0;
-            for (; s < nstages; ++s) {
-                const int kb = kb0 + s / kStagesPerBlock, sl = s % kStagesPerBlock, blk = s / kStagesPerBlock;
-                if (sl == 0) {
-                    const int m = blk & 1;
-                    if (blk >= 2 && !wait(mempty + 8 * m, ((blk - 2) >> 1) & 1)) break;
-                    expect(mfull + 8 * m, kMetaBlock);
-                    asm volatile(
-                        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem + G::meta + m * kMetaBlock)),
-                        "l"(&maps.meta), "r"(0), "r"(kb), "r"(rb0), "r"(mfull + 8 * m)
-                        : "memory");
-                    issued[2] = blk + 1;
-                }
-                const int c = s % kNC;
-                if (s >= kNC && !wait(cempty + 8 * c, ((s - kNC) / kNC) & 1)) break;
-                expect(cfull + 8 * c, kCodeStage);
-                asm volatile(
-                    "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                    " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem + G::code + c * kCodeStage)),
-                    "l"(&maps.codes), "r"(128 * sl), "r"(0), "r"(kb), "r"(rb0), "r"(cfull + 8 * c)
-                    : "memory");
-            }
-            issued[0] = s;
-        }
+    // lane 0 waits for the warp; the others follow after __syncwarp
+    auto warp_wait = [&](uint32_t bar, uint32_t parity, bool cond) -> bool {
+        bool ok = true;
+        if (lane == 0 && cond) ok = wait(bar, parity);
         __syncwarp();
-    } else if (warp == kWorkerWarps + 1) {
+        return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    };
+
+    if (warp == kWarpXCopy) {
         // ------------------------------------------------------------------ activation copies
         if (lane == 0) {
-            asm volatile("griddepcontrol.wait;" ::: "memory");   // x may be written by the previous kernel
-            int s = 0;
-            for (; s < nstages; ++s) {
-                const int kb = kb0 + s / kStagesPerBlock, sl = s % kStagesPerBlock;
-                const int bs = s % kNB;
-                if (s >= kNB && !wait(bempty + 8 * bs, ((s - kNB) / kNB) & 1)) break;
-                expect(bfull + 8 * bs, G::kBStage);
-                const int k0 = kb * 1024 + sl * kStageK;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    asm volatile(
-                        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem + G::b + bs * G::kBStage + j * G::kBBox)),
-                        "l"(&maps.x), "r"(k0 + 64 * j), "r"(0), "r"(bfull + 8 * bs)
-                        : "memory");
+            asm volatile("griddepcontrol.wait;" ::: "memory");   // X may be written by the previous kernel
+            int i = 0, cu = u0, cj = 0;
+            for (; i < nst; ++i) {
+                const int s = kChunkStages * (cu % Uc) + cj;
+                if (++cj == chunk_stages(cu)) {
+                    cj = 0;
+                    ++cu;
+                }
+                const int as = i % kNA;
+                if (i >= kNA && !wait(aempty + 8 * as, ((i - kNA) / kNA) & 1)) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(xfull + 8 * as),
+                             "r"(static_cast<uint32_t>(a.Mr * 128))
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                    " [%0], [%1, {%2, %3}], [%4];" ::"r"(sb + F::kA + as * kAStage),
+                    "l"(&maps.x), "r"(s * kStageK), "r"(0), "r"(xfull + 8 * as)
+                    : "memory");
             }
-            issued[1] = s;
+            *xissued = i;
         }
         __syncwarp();
-    } else if (warp >= kWorkerWarps + 2) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ tensor-core issue
-        // MMA warp iw takes stages iw, iw + kIssuers, ... into accumulator iw
-        const int iw = warp - (kWorkerWarps + 2);
+        // one thread, stages in order (D sums them in a fixed order); its waits poll
+        // with test_wait, bounded like every other wait
+        auto poll = [&](uint32_t bar, uint32_t parity) -> bool {
+            if (mbar_test_wait(bar, parity)) return true;
+            const uint64_t w0 = global_ns();
+            while (!mbar_test_wait(bar, parity)) {
+                if (*abort_flag) return false;
+                if (global_ns() - w0 > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
+                    return false;
+                }
+            }
+            return true;
+        };
         if (lane == 0) {
-            for (int s = iw; s < nstages; s += kIssuers) {
-                const int as = s % kNA, bs = s % kNB;
-                const bool ok = wait(afull + 8 * as, (s / kNA) & 1) && wait(bfull + 8 * bs, (s / kNB) & 1);
+            int cu = u0, cj = 0;   // chunk unit and stage of stage i
+            for (int i = 0; i < nst; ++i) {
+                const int t = t0 + cu / Uc;
+                if (++cj == chunk_stages(cu)) {
+                    cj = 0;
+                    ++cu;
+                }
+                const int as = i % kNA, bs = i % kNB;
+                bool ok = poll(afull + 8 * as, (i / kNA) & 1) &&
+                          poll(bfull + 8 * bs, (i / kNB) & 1);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 if (ok && !*abort_flag) {
-                    const uint32_t b0 = smem_u32(smem + G::b + bs * G::kBStage);
+                    const uint32_t a0 = sb + F::kA + as * kAStage, b0 = sb + F::kB + bs * kBStage;
+                    const uint32_t d = tmem + (t == first_tile ? 0u : static_cast<uint32_t>(kTileRows));
 #pragma unroll
-                    for (int ks = 0; ks < kStageK / 16; ++ks) {
-                        const uint64_t db = smem_desc_sw128(b0 + (ks >> 2) * G::kBBox + (ks & 3) * 32);
-                        const uint32_t acc = (s >= kIssuers || ks > 0) ? 1u : 0u;
+                    for (int ks = 0; ks < kStageK / 16; ++ks)
                         asm volatile(
-                            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + NM * iw),
-                            "r"(tmem + kAcol + 128u * as + 8u * ks), "l"(db), "r"(kIdesc), "r"(acc)
+                            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                            "l"(smem_desc_sw128(a0 + 32 * ks)), "l"(smem_desc_sw128(b0 + 32 * ks)), "r"(kIdesc)
                             : "memory");
-                    }
                 }
                 // always commit, so that every wait on these stages completes
-                commit(aempty + 8 * as);
                 commit(bempty + 8 * bs);
+                commit(aempty + 8 * as);
             }
-            commit(last_bar);   // tracks every tensor-core operation this thread issued
+            if (nst > 0) commit(dfull);   // tracks every tensor-core operation of the CTA
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------------ dequantisation
-        // thread owns tensor-memory lane m = 32 (warp % 4) + lane = weight row
-        // 4 rb + r of the tile, rb = 8 (warp % 4) + 2 (lane / 8) + (lane / 4) % 2,
-        // r = lane % 4: the 8 lanes of a quarter warp read 8 different 16-byte
-        // bank groups of the swizzled nibble stage; groups kGpw (warp / 4) .. + kGpw - 1
-        const int qd = warp & 3, gh = warp >> 2;
-        const int rb = 8 * qd + 2 * (lane >> 3) + ((lane >> 2) & 1), r = lane & 3;
-        const int row128 = rb * 4 + r;                              // 128-byte row of the nibble stage
-        const uint32_t tlane = static_cast<uint32_t>(32 * qd) << 16;
-        for (int s = 0; s < nstages; ++s) {
-            const int sl = s % kStagesPerBlock, blk = s / kStagesPerBlock;
-            const int c = s % kNC, as = s % kNA, m = blk & 1;
-            // lane 0 polls for the warp; __syncwarp then orders the other lanes
-            // after its acquire
-            bool ok = true;
-            if (lane == 0) {
-                if (sl == 0) ok = wait(mfull + 8 * m, (blk >> 1) & 1) && ok;
-                ok = wait(cfull + 8 * c, (s / kNC) & 1) && ok;
-                if (s >= kNA) ok = wait(aempty + 8 * as, ((s - kNA) / kNA) & 1) && ok;
-            }
-            __syncwarp();
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (ok && !*abort_flag) {
-                const uint8_t* cs = smem + G::code + c * kCodeStage + row128 * 128;
-                const uint8_t* ms = smem + G::meta + m * kMetaBlock + rb * kMetaBytes;
-                const int g0 = 8 * sl + kGpw * gh;                  // first of this thread's groups in the record
-                static_assert(kGpw == 2, "scale and zero-point loads below are for two groups per warp");
-                const uint32_t sc = *reinterpret_cast<const uint32_t*>(ms + r * 64 + g0 * 2);   // 2 FP16 scales
-                const uint32_t zw = ms[256 + r * 16 + g0 / 2];                                   // 2 zero points
+    } else if (warp >= kWarpAct) {
+        // ------------------------------------------------------------------ A stage in decode order
+        {
+            const int m = 32 * (warp - kWarpAct) + lane;   // A row: 128 bytes at its swizzled place
+            const uint32_t arow = static_cast<uint32_t>((m >> 3) * 1024 + (m & 7) * 128), asw = static_cast<uint32_t>(m & 7);
+            for (int i = 0; i < nst; ++i) {
+                const int as = i % kNA;
+                const bool ok = warp_wait(xfull + 8 * as, (i / kNA) & 1, true);
+                if (ok && !*abort_flag && m < a.Mr) {
+                    const uint32_t row = sb + F::kA + as * kAStage + arow;
+                    uint32_t w[32];
 #pragma unroll
-                for (int t = 0; t < kGpw; ++t) {
-                    const int g8 = kGpw * gh + t;                   // group of the stage
-                    const uint4 q = *reinterpret_cast<const uint4*>(cs + ((g8 ^ (row128 & 7)) << 4));
-                    const uint32_t z = (zw >> (4 * t)) & 15u;
-                    const uint32_t sb = sc >> (16 * t) & 0xFFFFu;
-                    const uint32_t zlo2 = (0x6400u | z) * 0x00010001u;           // 1024 + z
-                    const uint32_t zhi2 = (0xD400u | (z << 4)) * 0x00010001u;    // -(64 + z)
-                    const uint32_t s2 = sb * 0x00010001u;
-                    uint32_t v[16];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t lo[2], hi[2];
-                        dequant_word(u4w(q, j), zlo2, zhi2, s2, lo, hi);
-                        v[2 * j] = lo[0];
-                        v[2 * j + 1] = lo[1];
-                        v[8 + 2 * j] = hi[0];
-                        v[9 + 2 * j] = hi[1];
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 v = lds128(row + ((j ^ asw) << 4));
+                        w[4 * j] = v.x;
+                        w[4 * j + 1] = v.y;
+                        w[4 * j + 2] = v.z;
+                        w[4 * j + 3] = v.w;
                     }
-                    asm volatile(
-                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                        "%12, %13, %14, %15, %16};" ::"r"(tmem + tlane + kAcol + 128u * as + 16u * g8),
-                        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-                        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-                        : "memory");
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        uint32_t nat[8], o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) nat[e] = w[8 * blk + e];
+                        w2_order(nat, o);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w[8 * blk + e] = o[e];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sts128(row + ((j ^ asw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor core
                 }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-                arrive(cempty + 8 * c);                                 // this warp is done with the nibbles
-                if (sl == kStagesPerBlock - 1) arrive(mempty + 8 * m);  // and with the block's metadata
-                arrive(afull + 8 * as);
+                __syncwarp();
+                if (lane == 0) arrive(afull + 8 * as);
             }
         }
+    } else {
+        // ------------------------------------------------------------------ dequantisation -> B stages
+        // thread = weight row n of the tile (row block n / 4, row n % 4); its codes and
+        // metadata come straight from global memory into registers, one chunk ahead
+        const int n = tid, rbl = n >> 2, r = n & 3;
+        const uint32_t brow = static_cast<uint32_t>((n >> 3) * 1024 + (n & 7) * 128);   // row n of a B stage
+        const uint32_t sw = static_cast<uint32_t>(n & 7);                               // its 128-byte swizzle
+        const uint32_t lut_lo = a.lut_lo, lut_hi = a.lut_hi;
+        constexpr int CV = F::kCodeVecs;
+        // row n's record of chunk unit u (nullptr past the matrix: zero codes and metadata)
+        auto rec_of = [&](int u, int* cc) -> const uint8_t* {
+            const int t = t0 + u / Uc, c = u % Uc, rb = t * kTileRb + rbl;
+            *cc = c % kChunksPerRec;
+            if (rb >= a.n_rb) return nullptr;
+            return a.area + static_cast<long long>(rb) * a.rb_bytes +
+                   static_cast<long long>(c / kChunksPerRec) * F::kRecBytes;
+        };
+        // the chunk's codes (CV x 16 B) and metadata words: 4 S words + 4 Z words
+        auto load_chunk = [&](int u, uint4 (&q)[CV], uint4& m0, uint4& m1) {
+            int cc;
+            const uint8_t* rec = rec_of(u, &cc);
+            if (rec) {
+                const uint8_t* codes = rec + r * F::kRowCodeBytes + cc * F::kChunkRowBytes;
+#pragma unroll
+                for (int v = 0; v < CV; ++v) q[v] = ldg128(codes + 16 * v);
+                m0 = ldg128(rec + F::kMeta0Off + r * 64 + 16 * cc);
+                m1 = ldg128(rec + F::kMeta1Off + r * 64 + 16 * cc);
+            } else {
+#pragma unroll
+                for (int v = 0; v < CV; ++v) q[v] = make_uint4(0u, 0u, 0u, 0u);
+                m0 = m1 = make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        auto prefetch_chunk = [&](int u) {
+            int cc;
+            const uint8_t* rec = rec_of(u, &cc);
+            if (rec) {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + r * F::kRowCodeBytes + cc * F::kChunkRowBytes));
+                if (cc == 0 && r == 0) {
+                    // the row block's S and Z lines of the record (512 B)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 128));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 256));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 384));
+                }
+            }
+        };
+        uint4 q[CV], qn[CV], m0, m1, m0n, m1n;
+        if (ncu > 0) load_chunk(u0, qn, m0n, m1n);   // ahead of the prefetches in the memory queues
+        for (int j = 1; j < F::kPF && j < ncu; ++j) prefetch_chunk(u0 + j);
+        int ist = 0;   // stage index of the chunk's first stage
+        for (int j = 0; j < ncu; ++j) {
+            const int u = u0 + j, nsc = chunk_stages(u);
+#pragma unroll
+            for (int v = 0; v < CV; ++v) q[v] = qn[v];
+            m0 = m0n;
+            m1 = m1n;
+            if (j + 1 < ncu) load_chunk(u + 1, qn, m0n, m1n);
+            if (j + F::kPF < ncu) prefetch_chunk(u + F::kPF);
+#pragma unroll
+            for (int jj = 0; jj < kChunkStages; ++jj) {
+                if (jj >= nsc) break;
+                const int is = ist + jj, bs = is % kNB;
+                const bool ok = warp_wait(bempty + 8 * bs, ((is - kNB) / kNB) & 1, is >= kNB);
+                const uint32_t bst = sb + F::kB + bs * kBStage + brow;
+                if (ok && !*abort_flag) {
+                    const uint4 qs = q[jj];
+                    const uint32_t Sw = u4w(m0, jj), Zw = u4w(m1, jj);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int g = v >> 1;   // group of the stage
+                        const uint32_t S2 = ((Sw >> (16 * g)) & 0xFFFFu) * 0x00010001u;
+                        const uint32_t Z2 = ((Zw >> (16 * g)) & 0xFFFFu) * 0x00010001u;
+                        uint32_t o[8];
+                        w2_word(u4w(qs, v), S2, Z2, lut_lo, lut_hi, o);
+                        sts128(bst + (((2 * v) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+                        sts128(bst + (((2 * v + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+                    }
+                }
+                // the B stage is read by the tensor core (async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) arrive(bfull + 8 * bs);
+            }
+            ist += nsc;
+        }
     }
+
+    // ---------------------------------------------------------------------- epilogue
     // the accumulator is complete once the last commit has arrived
-    const bool got = nstages == 0 || mbar_wait(last_bar, 0, kWaitLimitNs);
+    const bool got = nst == 0 || mbar_wait(dfull, 0, kWaitLimitNs);
     if (!got && tid == 0) atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
     __syncthreads();
     const bool bad = *abort_flag != 0 || !got;
-    // after an abort, the last copies issued may still be in flight: wait for them
-    // (a stage the copy warps never issued is not waited for)
-    if (bad && tid == kWorkers) {
-        const int ic = issued[0], ix = issued[1], im = issued[2];
-        for (int s = ic > kNC ? ic - kNC : 0; s < ic; ++s)
-            mbar_wait(cfull + 8 * (s % kNC), (s / kNC) & 1, kWaitLimitNs / 64);
-        for (int s = ix > kNB ? ix - kNB : 0; s < ix; ++s)
-            mbar_wait(bfull + 8 * (s % kNB), (s / kNB) & 1, kWaitLimitNs / 64);
-        for (int blk = im > 2 ? im - 2 : 0; blk < im; ++blk)
-            mbar_wait(mfull + 8 * (blk & 1), (blk >> 1) & 1, kWaitLimitNs / 64);
+    // after an abort the last code copies issued may still be in flight: wait for them
+    if (bad && tid == 32 * kWarpXCopy) {
+        const int ix = *xissued;
+        for (int i = ix > kNA ? ix - kNA : 0; i < ix; ++i)
+            mbar_wait(xfull + 8 * (i % kNA), (i / kNA) & 1, kWaitLimitNs / 64);
     }
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // epilogue: warp w reads accumulator lanes 32 (w % 4) .. + 31 (its rows) and
-    // columns 16 (w / 4) .. + 15 (activation rows), so up to 16 warps share it
-    constexpr int kChunks = NM / 16;
-    const int qd = warp & 3, cc = warp >> 2;
-    const bool ep = warp < 4 * kChunks;
-    const int m = 32 * qd + lane;
-    const int erb = 8 * qd + 2 * (lane >> 3) + ((lane >> 2) & 1), er = lane & 3;
-    const long long n = static_cast<long long>(rb0 + erb) * 4 + er;
-    float d[16];
-    if (ep) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) d[i] = 0.f;
-#pragma unroll
-        for (int acc = 0; acc < kIssuers; ++acc) {   // the accumulators, added in a fixed order
-            uint32_t v[16];
-            asm volatile(
-                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-                "%13, %14, %15}, [%16];"
-                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                : "r"(tmem + (static_cast<uint32_t>(32 * qd) << 16) + NM * acc + 16 * cc));
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-            for (int i = 0; i < 16; ++i) d[i] += (nstages > 0 && !bad) ? __uint_as_float(v[i]) : 0.f;
-        }
-    }
-    auto write_y = [&]() {
-        asm volatile("griddepcontrol.wait;" ::: "memory");   // the previous kernel is done with y
-        if (n < a.N && !bad) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int row = 16 * cc + i;
-                if (row < a.M) {
-                    if (a.y_f32)
-                        reinterpret_cast<float*>(a.y)[row * a.ldy + n] = d[i];
-                    else
-                        reinterpret_cast<__half*>(a.y)[row * a.ldy + n] = __float2half_rn(d[i]);
-                }
-            }
-        }
+    // contributors of tile t: the ranks whose ranges hold its first and last chunk
+    auto contributors = [&](int t, int* rlo, int* rhi) {
+        *rlo = rank_of(units, C, static_cast<long long>(t - t0) * Uc);
+        *rhi = rank_of(units, C, static_cast<long long>(t - t0 + 1) * Uc - 1);
     };
-    if (S == 1) {
-        if (ep) write_y();
-    } else {
-        // split K: partials through distributed shared memory, added in rank order by rank 0
-        float* part = reinterpret_cast<float*>(smem + G::code);   // NM x 128 FP32 over the (idle) nibble ring
-        if (ep)
+    auto store_y = [&](int m, long long n, float v) {
+        if (a.y_f32)
+            reinterpret_cast<float*>(a.y)[m * a.ldy + n] = v;
+        else
+            reinterpret_cast<__half*>(a.y)[m * a.ldy + n] = __float2half_rn(v);
+    };
+    // D -> shared memory: warps 0, 1, 4, 5 read lane quarter warp % 4 (activation
+    // rows 32 (warp % 4) ..) and columns 128 (warp / 4) .. + 127 of each accumulator
+    // into row 64 b + m of the partials (padded rows: conflict-free 16-byte stores)
+    if (warp < kDqWarps && (warp & 3) < 2 && 32 * (warp & 3) < a.M && !bad) {
+        const int q = warp & 3, h = warp >> 2;
+        const int m = 32 * q + lane;
+        for (int b = 0; b < nbands; ++b) {
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col0 = 128 * h + 32 * cc;
+                uint32_t v[32];
+                __syncwarp();   // tcgen05.ld is warp-collective
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+                    "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+                    "[%32];"
+                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                      "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                      "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                      "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                      "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                    : "r"(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(kTileRows * b + col0)));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (m < a.M) {
+                    const uint32_t p = sb + static_cast<uint32_t>((64 * b + m) * kPartStride + col0 * 4);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) part[(16 * cc + i) * kTileRows + m] = d[i];
-        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-        if (rank == 0 && ep) {
-            for (int p = 1; p < S; ++p) {
-                uint32_t remote;
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(part)), "r"(p));
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float v;
-                    asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                                 : "=f"(v)
-                                 : "r"(remote + 4u * ((16 * cc + i) * kTileRows + m)));
-                    d[i] += v;
+                    for (int j = 0; j < 32; j += 4) sts128(p + 4 * j, v[j], v[j + 1], v[j + 2], v[j + 3]);
                 }
             }
-            write_y();
         }
-        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
+    // every CTA's partials are in place; a tile is summed over its contributors in
+    // rank order, each contributor taking one column slice, and written along the
+    // columns (4 columns a thread, consecutive threads consecutive columns)
+    if (C > 1)
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    else
+        __syncthreads();
+    if (!bad) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the previous kernel is done with y
+        for (int b = 0; b < nbands; ++b) {
+            const int t = first_tile + b;
+            int rlo, rhi;
+            contributors(t, &rlo, &rhi);
+            const int nc = rhi - rlo + 1, ci = rank - rlo;
+            const int c0 = 4 * ((64 * ci) / nc), c1 = 4 * ((64 * (ci + 1)) / nc);
+            const int w4 = (c1 - c0) / 4;
+            if (w4 <= 0) continue;
+            // the contributors' band of this tile: 0, except for the first contributor
+            // when its range starts in the tile before
+            const int bp_lo = t0 + static_cast<int>((units * rlo / C) / Uc) < t ? 1 : 0;
+            const int ne = a.M * w4;
+            for (int e0 = tid; e0 < ne; e0 += 2 * kThreads) {
+                // two elements a thread, every load of both in flight, then the sums in rank order
+                float4 pv[2][kMaxCluster];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e = e0 + h * kThreads;
+                    if (e >= ne) break;
+                    const int m = e / w4, cq = e - m * w4;
+#pragma unroll
+                    for (int k = 0; k < kMaxCluster; ++k) {
+                        if (k >= nc) break;
+                        const int bp = k == 0 ? bp_lo : 0;
+                        const uint32_t local =
+                            sb + static_cast<uint32_t>((64 * bp + m) * kPartStride + (c0 + 4 * cq) * 4);
+                        if (C > 1) {
+                            uint32_t remote;
+                            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rlo + k));
+                            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(pv[h][k].x), "=f"(pv[h][k].y), "=f"(pv[h][k].z), "=f"(pv[h][k].w)
+                                         : "r"(remote));
+                        } else {
+                            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(pv[h][k].x), "=f"(pv[h][k].y), "=f"(pv[h][k].z), "=f"(pv[h][k].w)
+                                         : "r"(local));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int e = e0 + h * kThreads;
+                    if (e >= ne) break;
+                    const int m = e / w4, cq = e - m * w4;
+                    float4 sum = pv[h][0];
+#pragma unroll
+                    for (int k = 1; k < kMaxCluster; ++k) {
+                        if (k >= nc) break;
+                        sum.x += pv[h][k].x;
+                        sum.y += pv[h][k].y;
+                        sum.z += pv[h][k].z;
+                        sum.w += pv[h][k].w;
+                    }
+                    const long long n = static_cast<long long>(t) * kTileRows + c0 + 4 * cq;
+                    if (n < a.N) store_y(m, n, sum.x);
+                    if (n + 1 < a.N) store_y(m, n + 1, sum.y);
+                    if (n + 2 < a.N) store_y(m, n + 2, sum.z);
+                    if (n + 3 < a.N) store_y(m, n + 3, sum.w);
+                }
+            }
+        }
+    }
+    // no CTA leaves while another may still read its shared memory
+    if (C > 1)
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     if (blockIdx.x == 0 && tid == 0) {
-        const uint4* h = reinterpret_cast<const uint4*>(a.blob);
-        const uint4 h0 = h[0], h1 = h[1], h2 = h[2];
+        const uint4* hp = reinterpret_cast<const uint4*>(a.blob);
+        const uint4 h0 = hp[0], h1 = hp[1], h2 = hp[2];
         const long long n_hdr = (static_cast<long long>(h1.y) << 32) | h1.x;
         const long long k_hdr = (static_cast<long long>(h1.w) << 32) | h1.z;
-        if (h0.x != 0x5751424Cu || h0.y != 0x32334734u || h0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != a.N ||
+        if (h0.x != 0x5751424Cu || h0.y != F::kMagicHi || h0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != a.N_hdr ||
             k_hdr != a.K || h2.x != 0u)
             atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_FORMAT));
     }
@@ -534,16 +717,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
-}
-
-template <int NM>
-const void* kernel_fn() {
-    return reinterpret_cast<const void*>(&lbq_w4_mma_kernel<NM>);
-}
-
-template <int NM>
-int smem_bytes() {
-    return Geom<NM>::total;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
@@ -561,107 +734,202 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+const void* kernel_fn() { return reinterpret_cast<const void*>(&lbq_w2_mma_kernel); }
+
+// Clusters of each size that fit the device at once (0: that size cannot be
+// launched), per device and kind, looked up once.
+constexpr int kMaxDev = 64;
+std::mutex g_plan_mu;
+int g_active[kMaxDev][kMaxCluster + 1];
+bool g_active_init[kMaxDev];
+
+lbq_status active_clusters(int max_smem, const int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return LBQ_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (!g_active_init[dev]) {
+        const void* fn = kernel_fn();
+        const int smem = Fmt::kTotal;
+        if (smem > max_smem) return LBQ_ERR_SHAPE;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return LBQ_ERR_CUDA;
+        }
+        for (int c = 1; c <= kMaxCluster; ++c) {
+            cudaLaunchConfig_t cfg;
+            std::memset(&cfg, 0, sizeof(cfg));
+            cfg.gridDim = dim3(static_cast<unsigned>(c));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(c);
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+                (void)cudaGetLastError();
+                n = 0;
+            }
+            g_active[dev][c] = n;
+        }
+        g_active_init[dev] = true;
+    }
+    *out = g_active[dev];
+    return LBQ_OK;
+}
+
 }  // namespace
 
 namespace lbq {
 
-int mma_padded_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 : 64; }
+// Work plan of the tensor-core kernel over T tiles of Uc chunks: the cluster
+// size C and cluster count G that give the fewest chunks to the busiest CTA,
+// with every CTA's range spanning at most as many tiles as the accumulator has
+// lane bands.  False when no cluster size fits.
+bool mma_plan(int T, int Uc, int bands, const int* active, int* C_out, int* G_out, int* load_out) {
+    int bestC = 0, bestG = 0;
+    long long best = -1;
+    for (int c = 1; c <= kMaxCluster; ++c) {
+        int g = active[c];
+        if (g <= 0) continue;
+        if (g > T) g = T;
+        long long load = 0;
+        bool fits = true;
+        for (int cl = 0; cl < g && fits; ++cl) {
+            int t0, t1;
+            cluster_tiles(T, g, cl, &t0, &t1);
+            const long long units = static_cast<long long>(t1 - t0) * Uc;
+            for (int r = 0; r < c; ++r) {
+                long long u0, u1;
+                rank_range(units, c, r, &u0, &u1);
+                if (u1 - u0 > load) load = u1 - u0;
+                if (u1 > u0 && (u1 - 1) / Uc - u0 / Uc + 1 > bands) fits = false;
+            }
+        }
+        // fewer chunks per CTA wins; on a tie the smaller cluster (less reduction)
+        if (fits && (best < 0 || load < best)) {
+            best = load;
+            bestC = c;
+            bestG = g;
+        }
+    }
+    if (best < 0) return false;
+    *C_out = bestC;
+    *G_out = bestG;
+    *load_out = static_cast<int>(best);
+    return true;
+}
 
-// Launch the tensor-core 4-bit GEMM for one problem (16 <= M <= 64, no outlier
-// columns).  Tiles of 128 rows; K split over a cluster of S CTAs so that tiles
-// x S fills the SMs.  Returns LBQ_ERR_SHAPE when it does not fit.
-lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
-                         int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
-                         uint32_t flags) {
+// Launch the tensor-core GEMM for one problem (16 <= M <= 64, no outlier
+// columns): one launch per slab of tiles, each slab small enough that every
+// CTA's range spans at most two tiles.  With `launches` set, only counts the
+// launches.  Returns LBQ_ERR_SHAPE when the problem does not fit the kernel.
+lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
+                         int64_t ldy, bool y_f32, unsigned* err_word, int max_smem, void* stream, uint32_t flags,
+                         int* launches) {
     if (M < 16 || M > 64) return LBQ_ERR_SHAPE;
     lbq_layout L;
-    lbq_status st = lbq_blob_layout(LBQ_KIND_W4, N, K, 0, &L);
+    lbq_status st = lbq_blob_layout(LBQ_KIND_W2CB, N, K, 0, &L);
     if (st != LBQ_OK) return st;
-    const int NM = mma_padded_rows(M);
-    const int smem = NM == 16 ? smem_bytes<16>() : NM == 32 ? smem_bytes<32>() : NM == 48 ? smem_bytes<48>()
-                                                                                         : smem_bytes<64>();
-    if (smem > max_smem) return LBQ_ERR_SHAPE;
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return LBQ_ERR_CUDA;
-    MmaArgs a;
-    std::memset(&a, 0, sizeof(a));
+    const int* active = nullptr;
+    st = active_clusters(max_smem, &active);
+    if (st != LBQ_OK) return st;
+    const int T = static_cast<int>((N + kTileRows - 1) / kTileRows);
+    const int U = static_cast<int>(K / kStageK), Uc = (U + kChunkStages - 1) / kChunkStages;
+    int slab = T, C = 0, G = 0, load = 0;
+    while (slab > 1 && !mma_plan(slab, Uc, 2, active, &C, &G, &load)) slab = (slab + 1) / 2;
+    if (!mma_plan(slab, Uc, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
+    if (launches) {
+        *launches += (T + slab - 1) / slab;
+        return LBQ_OK;
+    }
+    // 2-bit codebook as FP16 byte tables for PRMT (otf-llm section 2, rounded once)
+    uint32_t lut_lo = 0, lut_hi = 0;
+    const double cb[4] = {-1.52, -0.45, 0.45, 1.52};
+    for (int c = 0; c < 4; ++c) {
+        const uint16_t h = lbq::host_f64_to_f16(cb[c]);
+        lut_lo |= uint32_t(h & 0xFF) << (8 * c);
+        lut_hi |= uint32_t(h >> 8) << (8 * c);
+    }
+    const void* fn = kernel_fn();
+    const int smem = Fmt::kTotal;
     uint8_t* b = static_cast<uint8_t*>(const_cast<void*>(packed));
-    a.blob = b;
-    a.y = y;
-    a.err = err_word;
-    a.ldy = ldy;
-    a.N = N;
-    a.K = K;
-    a.recs = static_cast<int>(L.records);
-    a.n_rb = static_cast<int>((N + 3) / 4);
-    a.M = M;
-    a.y_f32 = y_f32 ? 1 : 0;
-    // tensor maps: nibbles (byte of a row's codes, row, record block, row block),
-    // metadata (u16 of a record's scales + zeros, record block, row block),
-    // activations (k, activation row)
-    static thread_local Maps maps;
-    std::memset(&maps, 0, sizeof(maps));
-    const cuuint32_t one[4] = {1, 1, 1, 1};
-    {
-        const cuuint64_t dims[4] = {512, 4, static_cast<cuuint64_t>(a.recs), static_cast<cuuint64_t>(a.n_rb)};
-        const cuuint64_t strides[3] = {512, static_cast<cuuint64_t>(kRecBytes), L.row_block_bytes};
-        const cuuint32_t box[4] = {128, 4, 1, static_cast<cuuint32_t>(kTileRb)};
-        if (encode(&maps.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, b + L.area_offset, dims, strides, box, one,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return LBQ_ERR_CUDA;
-    }
-    {
-        const cuuint64_t dims[3] = {kMetaBytes / 2, static_cast<cuuint64_t>(a.recs), static_cast<cuuint64_t>(a.n_rb)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kRecBytes), L.row_block_bytes};
-        const cuuint32_t box[3] = {kMetaBytes / 2, 1, static_cast<cuuint32_t>(kTileRb)};
-        if (encode(&maps.meta, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, b + L.area_offset + 2048, dims, strides, box, one,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return LBQ_ERR_CUDA;
-    }
-    {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(NM)};
-        if (encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, one,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return LBQ_ERR_CUDA;
-    }
-    const int tiles = (a.n_rb + kTileRb - 1) / kTileRb;
-    int S = sms / tiles;
-    if (S < 1) S = 1;
-    if (S > 8) S = 8;
-    if (S > a.recs) S = a.recs;
-    a.S = S;
-    const void* fn = NM == 16 ? kernel_fn<16>() : NM == 32 ? kernel_fn<32>() : NM == 48 ? kernel_fn<48>()
-                                                                                      : kernel_fn<64>();
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return LBQ_ERR_CUDA;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * S));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = static_cast<unsigned>(S);
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-    if (flags & LBQ_FLAG_PDL) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
+    for (int ts = 0; ts < T; ts += slab) {
+        const int tiles = T - ts < slab ? T - ts : slab;
+        if (!mma_plan(tiles, Uc, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
+        const long long n0 = static_cast<long long>(ts) * kTileRows;
+        const long long Ns = N - n0 < static_cast<long long>(tiles) * kTileRows ? N - n0
+                                                                                 : static_cast<long long>(tiles) * kTileRows;
+        MmaArgs a;
+        std::memset(&a, 0, sizeof(a));
+        a.blob = b;
+        a.area = b + L.area_offset + (n0 / 4) * static_cast<long long>(L.row_block_bytes);
+        a.x = static_cast<const __half*>(x);
+        a.y = static_cast<uint8_t*>(y) + n0 * (y_f32 ? 4 : 2);
+        a.err = err_word;
+        a.ldx = ldx;
+        a.ldy = ldy;
+        a.N = Ns;
+        a.K = K;
+        a.N_hdr = N;
+        a.rb_bytes = static_cast<long long>(L.row_block_bytes);
+        a.n_rb = static_cast<int>((Ns + 3) / 4);
+        a.T = tiles;
+        a.U = U;
+        a.Uc = Uc;
+        a.C = C;
+        a.G = G;
+        a.M = M;
+        a.Mr = (M + 7) / 8 * 8;
+        a.y_f32 = y_f32 ? 1 : 0;
+        a.lut_lo = lut_lo;
+        a.lut_hi = lut_hi;
+        // tensor map of X: (k, activation row), 64-k x Mr-row boxes in the MMA's swizzled layout
+        Maps maps;
+        std::memset(&maps, 0, sizeof(maps));
+        const cuuint32_t one[2] = {1, 1};
+        bool enc = true;
+        {
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
+            const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(a.Mr)};
+            enc = enc && encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+                                one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+        if (!enc) return LBQ_ERR_CUDA;
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(static_cast<unsigned>(C * G));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cudaLaunchAttribute attr[2];
+        int na = 0;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(C);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
         ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    void* args[] = {&a, &maps};
-    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return LBQ_ERR_CUDA;
+        // later slabs follow a slab of this same call, which never writes the weights or x
+        if ((flags & LBQ_FLAG_PDL) || ts > 0) {
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = na;
+        void* args[] = {&a, &maps};
+        if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return LBQ_ERR_CUDA;
+        }
     }
     return LBQ_OK;
 }

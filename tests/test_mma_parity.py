@@ -1,7 +1,14 @@
-"""GPU parity of the tensor-core small-M 4-bit GEMM (16 <= M <= 64, no outlier
-columns) against the FP64 oracle, element by element: ragged row tiles (N not a
-multiple of 128), partial 1024-k blocks, K split over clusters of 1..8 CTAs,
-activation rows padded to the MMA width, leading dimensions, FP16 output.
+"""GPU parity of the tensor-core small-M GEMMs (16 <= M <= 64, no outlier
+columns) against the FP64 oracle, element by element, for both weight formats:
+4-bit (weights dequantised into tensor memory, 128-row tiles, K split over a
+cluster) and 2-bit codebook (weights as the 256-wide operand in shared memory,
+256-row tiles and 256-k chunks split over a cluster, each CTA's range spanning
+at most two tiles with one accumulator each; taller matrices go in slabs of
+tiles, one launch each).  The shapes cover: N ragged against both tile sizes
+(and smaller than one row block), K with a partial 1024-k record and a partial
+chunk, M from 16 to 64, CTA ranges that span two tiles, a single tile whose K is
+split over a whole cluster, two slabs, leading dimensions, FP16 output,
+repeatable bits.
 The weights are dequantised to FP16 before the FP32-accumulating product, so
 each weight carries one FP16 rounding; the bound stays the oracle tolerance."""
 import numpy as np
@@ -14,6 +21,8 @@ from gpu_util import assert_close, to_dev
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
+NONE = np.zeros(0, np.int32)
+
 
 def _case(seed, M, N, K):
     rng = np.random.default_rng(seed)
@@ -24,50 +33,60 @@ def _case(seed, M, N, K):
     return W, X
 
 
-def _run(lbq, blob, M, N, K, X, ldx=None, ldy=None, f32=True):
+def _pack(lbq, kind, W):
+    return (lbq.pack_w4(W), O.pack_w4(W)) if kind == "w4" else (lbq.pack_w2cb(W, NONE), O.pack_w2cb(W, NONE))
+
+
+def _run(lbq, kind, blob, M, N, K, X, ldx=None, ldy=None, f32=True):
     ldx = ldx or K
     ldy = ldy or N
     Xp = np.zeros((M, ldx), np.float16)
     Xp[:, :K] = X
     Y = torch.full((M, ldy), float("nan"), dtype=torch.float32 if f32 else torch.float16, device="cuda:0")
-    lbq.gemm_w4a16_smallM(to_dev(blob), M, N, K, 0, to_dev(Xp), ldx, Y, ldy)
+    f = lbq.gemm_w4a16_smallM if kind == "w4" else lbq.gemm_w2cb_outlier_smallM
+    f(to_dev(blob), M, N, K, 0, to_dev(Xp), ldx, Y, ldy)
     torch.cuda.synchronize()
     assert lbq.device_error() == 0
     return Y.float().cpu().numpy()
 
 
-# (M, N, K): N ragged against the 128-row tile; K with partial k-blocks; the
-# cluster size is min(8, SMs // tiles, k-blocks), so small N spreads K over 8 CTAs
-SHAPES = [(16, 128, 1024), (16, 1, 64), (17, 70, 1088), (32, 129, 3072), (33, 300, 2112), (48, 257, 4096),
-          (64, 1000, 1024), (64, 128, 8192), (40, 600, 7168), (16, 4100, 1024)]
+# (M, N, K): ragged tiles, partial records, one tile split over a cluster, many
+# tiles (CTA ranges that span two tiles: both accumulators in use), and more
+# tiles than one launch takes (two slabs of tiles)
+SHAPES = [(16, 256, 1024), (16, 1, 64), (17, 70, 1088), (32, 257, 3072), (33, 300, 2112), (48, 513, 4096),
+          (64, 1000, 1024), (64, 256, 8192), (40, 600, 7168), (16, 4100, 1024), (24, 9000, 2048),
+          (64, 14336, 1024), (20, 4096, 4096), (16, 80000, 64)]
 
 
+@pytest.mark.parametrize("kind", ["w4", "w2"])
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_elementwise(lbq, M, N, K):
+def test_elementwise(lbq, kind, M, N, K):
     W, X = _case(M * 7 + N + K, M, N, K)
-    blob = lbq.pack_w4(W)
-    ref = O.gemm(O.pack_w4(W), X)
-    assert_close(_run(lbq, blob, M, N, K, X), ref, what="mma M=%d N=%d K=%d" % (M, N, K))
+    blob, ref_blob = _pack(lbq, kind, W)
+    ref = O.gemm(ref_blob, X)
+    assert_close(_run(lbq, kind, blob, M, N, K, X), ref, what="mma %s M=%d N=%d K=%d" % (kind, M, N, K))
 
 
-def test_fp16_output_and_leading_dimensions(lbq):
+@pytest.mark.parametrize("kind", ["w4", "w2"])
+def test_fp16_output_and_leading_dimensions(lbq, kind):
     M, N, K = 24, 200, 2048
     W, X = _case(5, M, N, K)
-    blob = lbq.pack_w4(W)
-    ref = O.gemm(O.pack_w4(W), X)
-    Y = _run(lbq, blob, M, N, K, X, ldx=K + 40, ldy=N + 5, f32=False)
-    assert_close(Y[:, :N], ref, fp16_out=True, what="mma f16 ld")
+    blob, ref_blob = _pack(lbq, kind, W)
+    ref = O.gemm(ref_blob, X)
+    Y = _run(lbq, kind, blob, M, N, K, X, ldx=K + 40, ldy=N + 5, f32=False)
+    assert_close(Y[:, :N], ref, fp16_out=True, what="mma %s f16 ld" % kind)
     assert np.isnan(Y[:, N:]).all()
 
 
-def test_deterministic_across_calls(lbq):
+@pytest.mark.parametrize("kind", ["w4", "w2"])
+def test_deterministic_across_calls(lbq, kind):
     """Split-K partials are added in rank order: identical bits on every call."""
     M, N, K = 64, 256, 8192
     W, X = _case(9, M, N, K)
-    blob = lbq.pack_w4(W)
-    a = _run(lbq, blob, M, N, K, X)
+    blob, _ = _pack(lbq, kind, W)
+    a = _run(lbq, kind, blob, M, N, K, X)
     for _ in range(3):
-        assert np.array_equal(_run(lbq, blob, M, N, K, X), a)
+        assert np.array_equal(_run(lbq, kind, blob, M, N, K, X), a)
 
 
 def test_grouped_and_launch_count(lbq):
@@ -79,6 +98,8 @@ def test_grouped_and_launch_count(lbq):
         probs.append((to_dev(lbq.pack_w4(W)), N, K, 0, to_dev(X), K, Y, N))
         checks.append((Y, O.gemm(O.pack_w4(W), X)))
     assert lbq.gemv_grouped_launches(lbq.LBQ_KIND_W4, probs, M=M) == 2
+    big = [(probs[0][0], 80000, 64, 0, probs[0][4], 64, probs[0][6], 80000)]
+    assert lbq.gemv_grouped_launches(lbq.LBQ_KIND_W2CB, big, M=16) == 2   # 2-bit: two slabs of tiles
     lbq.gemv_grouped(lbq.LBQ_KIND_W4, probs, M=M)
     torch.cuda.synchronize()
     assert lbq.device_error() == 0
