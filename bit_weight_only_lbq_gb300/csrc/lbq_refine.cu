@@ -40,6 +40,8 @@ static_assert(kChunk == 1024, "the selection runs one thread per channel of a 1,
 // Index scratch of lbq_refine_noalloc: one array per device, shared by every
 // call.  64 chunks (K <= 65536) x 256 channels (k <= 256) = 16384 indices, 64 KB.
 constexpr int kNoAllocIdxMax = (lbq::kMaxK / lbq::kRefineChunk) * lbq::kRefineMaxK;
+static_assert(kNoAllocIdxMax >= ((lbq::kMaxK + lbq::kRefineChunk - 1) / lbq::kRefineChunk) * lbq::kRefineMaxK,
+              "the scratch holds the selection of every valid (K, k)");
 __device__ __align__(256) int32_t g_refine_idx_scratch[kNoAllocIdxMax];
 constexpr int kApplyRows = 256;
 constexpr int kApplyWarpsMax = 32;
@@ -364,13 +366,19 @@ lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void
 
 lbq_status lbq_refine_noalloc(const void* refine, int64_t N, int64_t K, int32_t k, const void* x_f16, void* y,
                              lbq_dtype y_dtype, void* stream) {
+    // every check of the two-call form first, so that an error leaves nothing enqueued
     if (!refine || !x_f16 || !y) return LBQ_ERR_NULL;
     if (N < 64 || N % 64 || N > INT32_MAX || K < 1 || K > lbq::kMaxK || k < 1 || k > lbq::kRefineMaxK)
         return LBQ_ERR_SHAPE;
-    const int64_t n_sel = lbq_refine_selected_count(K, k);
-    if (n_sel < 1 || n_sel > kNoAllocIdxMax) return LBQ_ERR_SHAPE;   // larger than the static scratch
+    if (y_dtype != LBQ_F16 && y_dtype != LBQ_F32) return LBQ_ERR_UNSUPPORTED;
+    if (!aligned(refine, 16) || !aligned(x_f16, 2) || !aligned(y, y_dtype == LBQ_F32 ? 4 : 2)) return LBQ_ERR_ALIGN;
+    unsigned* err = nullptr;
+    int sms = 0;
+    lbq_status st = lbq::device_context(&err, &sms);
+    if (st != LBQ_OK) return st;
+    const int64_t n_sel = lbq_refine_selected_count(K, k);   // <= kNoAllocIdxMax for every valid (K, k)
     int32_t* idx = nullptr;
-    lbq_status st = refine_scratch(&idx);
+    st = refine_scratch(&idx);
     if (st != LBQ_OK) return st;
     // the selection writes every index the apply reads: nothing to clear
     st = lbq_refine_select(x_f16, K, k, idx, stream);

@@ -373,7 +373,10 @@ int64_t lbq_refine_selected_count(int64_t K, int32_t k);
 
 /* Device: S(x) of a K-vector of FP16 activations, written to idx (device,
  * lbq_refine_selected_count(K, k) int32): chunk c's channels at [c k, ...),
- * ascending.  One CTA per chunk.  Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE,
+ * ascending.  |x_i| is ranked by the 15 magnitude bits of its FP16 encoding:
+ * the order of |x_i| for finite values, with an infinity above every finite
+ * value and a NaN above an infinity (ties, including +inf/-inf, go to the
+ * lower channel).  One CTA per chunk.  Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE,
  * LBQ_ERR_ALIGN (x 2-byte, idx 4-byte aligned), LBQ_ERR_UNSUPPORTED,
  * LBQ_ERR_CUDA. */
 lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* idx, void* stream);
@@ -389,10 +392,11 @@ lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void
 
 /* lbq_refine_select followed by lbq_refine_apply with no caller-provided index
  * buffer: the selected channels go to a static device array inside the
- * library (16384 int32 = 64 KB per device, enough for K <= 65536 with
- * k <= 256; a larger selection would be rejected with LBQ_ERR_SHAPE).  The
- * pages have no counterpart of this entry point: it is a convenience of this
- * library, with the same results as the two-call form.
+ * library (16384 int32 = 64 KB per device: the selection of every valid K and
+ * k, K <= 65536 and k <= 256).  The pages have no counterpart of this entry
+ * point: it is a convenience of this library, with the same results as the
+ * two-call form.  All argument checks run before anything is enqueued, so an
+ * error return leaves the stream untouched.
  * Nothing in the scratch needs clearing: the selection writes every index the
  * apply reads.  Races: the scratch is shared by all calls on a device, so two
  * calls must not overlap in time - issue them on one stream, or order them

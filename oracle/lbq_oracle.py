@@ -603,8 +603,13 @@ def unpack_refine(blob: np.ndarray, cols=None) -> np.ndarray:
 
 def select_refine(x: np.ndarray, k: int) -> np.ndarray:
     """S(x): per chunk of 1,024 channels the min(k, chunk length) largest |x_i|,
-    ties to the lower index; ascending channel indices."""
-    a = np.abs(np.asarray(x, dtype=np.float16).astype(F64).reshape(-1))
+    ties to the lower index; ascending channel indices.
+
+    |x_i| is ranked by the magnitude field of x_i's FP16 encoding (the 15 bits
+    below the sign): for finite values that order is the order of |x_i|, and it
+    also places the non-finite values, which the pages leave open: an infinity
+    ranks above every finite value and a NaN above an infinity."""
+    a = (np.asarray(x, dtype=np.float16).reshape(-1).view(np.uint16) & 0x7FFF).astype(F64)
     out = []
     for c0 in range(0, a.size, REFINE_CHUNK):
         chunk = a[c0:c0 + REFINE_CHUNK]

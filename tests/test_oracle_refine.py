@@ -63,6 +63,23 @@ def test_selection_matches_rank_counting(K, k):
     assert O.select_refine(x, k).tolist() == _rank_select(x, k)
 
 
+def test_selection_ranks_non_finite_values_above_finite():
+    """NaN above infinity above every finite |x| (the FP16 magnitude field's order);
+    +inf and -inf tie, the lower channel first; finite values keep the |x| order."""
+    x = np.zeros(2048, np.float16)
+    x[10] = np.float16(60000.0)            # the largest finite magnitude present
+    x[700] = np.float16(np.inf)
+    x[33] = np.float16(-np.inf)
+    x[900] = np.float16(np.nan)
+    x[1500] = np.float16(-np.nan)
+    x[1024 + 5] = np.float16(-3.0)
+    x[1024 + 6] = np.float16(2.0)
+    assert O.select_refine(x, 1).tolist() == [900, 1500]
+    assert O.select_refine(x, 2).tolist() == [33, 900, 1029, 1500]
+    assert O.select_refine(x, 3).tolist() == [33, 700, 900, 1029, 1030, 1500]
+    assert O.select_refine(x, 4).tolist() == [10, 33, 700, 900, 1024, 1029, 1030, 1500]
+
+
 def test_zero_residual_gives_zero_refinement():
     R = np.zeros((128, 5), np.float32)
     C = O.unpack_refine(O.pack_refine(R))

@@ -37,6 +37,14 @@ def test_selection_bitexact(lbq, K, k):
     assert np.array_equal(_select(lbq, x, k), O.select_refine(x, k))
 
 
+def test_selection_of_non_finite_values(lbq):
+    x = (np.random.default_rng(5).standard_normal(3000) * 2).astype(np.float16)
+    x[17], x[400] = np.float16(np.inf), np.float16(-np.inf)
+    x[900], x[2100] = np.float16(np.nan), np.float16(65504.0)
+    for k in (1, 2, 3, 8):
+        assert np.array_equal(_select(lbq, x, k), O.select_refine(x, k))
+
+
 def test_selection_of_zeros_and_signed_zero(lbq):
     x = np.zeros(3000, np.float16)
     x[1500] = np.float16(-0.0)
