@@ -135,9 +135,20 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=2)
 
-    def summary(self, t0: float, t1: float) -> dict:
+    def wait_first(self, timeout: float = 5.0):
+        """Block until the sampler has produced its first line (or timeout)."""
+        t = time.time()
+        while self.proc is not None and not self.samples and time.time() - t < timeout:
+            time.sleep(0.02)
+
+    def summary(self, t0: float, t1: float, w0: float = None, w1: float = None) -> dict:
+        """Clock record of the timed region [t0, t1] and of the measurement window
+        [w0, w1] around it (warm-up, timed region and the per-launch timing passes,
+        all under the same load).  The median and the reasons come from the window
+        when the timed region is too short to hold a 200 ms sample."""
         inside = [s for t, s in self.samples if t0 <= t <= t1]
-        used = inside if inside else [s for _, s in self.samples[-3:]]
+        window = [s for t, s in self.samples if (w0 if w0 is not None else t0) <= t <= (w1 if w1 is not None else t1)]
+        used = inside if inside else (window if window else [s for _, s in self.samples[-3:]])
         sm = [float(s[1]) for s in used if len(s) > 8 and s[1].replace(".", "").isdigit()]
         mx = [float(s[2]) for s in used if len(s) > 8 and s[2].replace(".", "").isdigit()]
         reasons = set()
@@ -148,7 +159,9 @@ class ClockSampler:
                     if s[5 + i].lower() == "active":
                         reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples_in_region": len(inside)}
+                "reasons": sorted(reasons), "samples_in_region": len(inside), "samples_in_window": len(window),
+                "source": "timed region" if inside else "measurement window (warm-up, timed steps, per-launch "
+                                                         "timing passes)"}
 
 
 # ---------------------------------------------------------------------------
@@ -227,6 +240,30 @@ def launch(lbq, e, blob, x, y, pdl):
 # reference arm: the FP64 CPU oracle
 # ---------------------------------------------------------------------------
 
+def oracle_workload(rows: int):
+    """The step's 16 matrices built with the oracle alone (no native code): the
+    first `rows` rows of each seeded weight matrix, the 2-bit outlier columns
+    chosen by the oracle's impact-score selection over the whole matrix, and the
+    activations.  Entries as make_workload's, with W_head holding the rows."""
+    from oracle import lbq_oracle as O
+    layer = []
+    for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
+        W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li)
+        layer.append(dict(kind="w4", name=name, N=N, K=K, n_out=0, M=1, W_head=W[:rows].copy(),
+                          idx=np.zeros(0, np.int32), x=synth.activations(1, K, config_id=2, layer_id=li)[0]))
+    for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
+        W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
+        idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=3, layer_id=li))
+        layer.append(dict(kind="w2", name=name, N=N, K=K, n_out=len(idx), M=1, W_head=W[:rows].copy(), idx=idx,
+                          x=synth.activations(1, K, config_id=3, layer_id=li)[0]))
+    for li in (4, 6):
+        name, N, K = synth.LLAMA3_8B_LINEARS[li]
+        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
+        layer.append(dict(kind="w4m", name=name, N=N, K=K, n_out=0, M=SMALL_M, W_head=W[:rows].copy(),
+                          idx=np.zeros(0, np.int32), x=synth.activations(SMALL_M, K, config_id=4, layer_id=li)))
+    return layer
+
+
 def oracle_sample(layer, rows_per_matrix: int):
     """A step of the oracle over the first rows of every matrix of the step.  The
     oracle packs its own blob of those rows (untimed); the returned step times
@@ -244,24 +281,78 @@ def oracle_sample(layer, rows_per_matrix: int):
             O.gemm(blob, e["x"])
             nbytes += algorithmic_bytes("w4" if e["kind"] != "w2" else "w2", R, e["K"], e["n_out"], e["M"])
         return nbytes
-    return step
+    return step, prepared
+
+
+def oracle_figures(layer, rows: int, reps: int) -> dict:
+    """The three CPU figures of the oracle over a row sample of the step (each
+    scaled to GB/s of the sample's algorithmic bytes): (i) packing (quantise +
+    pack, FP64), (ii) dequantise-from-bytes + matvec, (iii) matvec alone on the
+    cached FP64 matrix the blob applies."""
+    from oracle import lbq_oracle as O
+    t = time.perf_counter()
+    step, prepared = oracle_sample(layer, rows)
+    t_pack = time.perf_counter() - t
+    nbytes = step()
+    t = time.perf_counter()
+    for _ in range(reps):
+        step()
+    t_step = (time.perf_counter() - t) / reps
+    cached = [(e, O.dequant_eff(blob), np.asarray(e["x"], np.float16).astype(np.float64)) for e, _, blob in prepared]
+    t = time.perf_counter()
+    for _ in range(reps):
+        for e, Wh, x in cached:
+            Wh @ x.T
+    t_mv = (time.perf_counter() - t) / reps
+    weights = sum(R * e["K"] for e, R, _ in prepared)
+    return {"rows": rows, "bytes": nbytes, "weights": weights,
+            "pack": {"s": round(t_pack, 4), "weights_per_s": round(weights / t_pack, 1)},
+            "dequant_matvec": {"s": round(t_step, 5), "GB_s": round(nbytes / t_step / 1e9, 6)},
+            "matvec_cached": {"s": round(t_mv, 5), "GB_s": round(nbytes / t_mv / 1e9, 6)}}
+
+
+def oracle_70b_extrapolated(rows: int = 8) -> dict:
+    """Config 5 on the host: one sample of `rows` rows of each Llama-3-70B linear
+    shape and of the lm_head, oracle dequantise-from-bytes + matvec, scaled by
+    each shape's rows and count to one token's 80 x 7 + 1 matrices.  Extrapolated,
+    never run whole (the oracle would hold 69.5 G FP64 weights)."""
+    from oracle import lbq_oracle as O
+    total = 0.0
+    parts = []
+    shapes = [(n, N, K, synth.LLAMA3_70B_LAYERS) for (n, N, K) in synth.LLAMA3_70B_LINEARS]
+    hn, hN, hK = synth.LLAMA3_70B_LM_HEAD
+    shapes.append((hn, hN, hK, 1))
+    for name, N, K, count in shapes:
+        W = synth.weights_heavy_cols(rows, K, config_id=5, layer_id=len(parts))
+        blob = O.pack_w4(W)
+        x = synth.activations(1, K, config_id=5, layer_id=K)[0]
+        t = time.perf_counter()
+        O.gemm(blob, x)
+        dt = time.perf_counter() - t
+        s_shape = dt / rows * N * count
+        total += s_shape
+        parts.append({"linear": name, "N": N, "K": K, "count": count, "s_per_token": round(s_shape, 3)})
+    nbytes = sum(algorithmic_bytes("w4", N, K, 0) * c for (_, N, K, c) in shapes)
+    return {"label": "extrapolated from %d-row samples" % rows, "s_per_token": round(total, 2),
+            "GB_s": round(nbytes / total / 1e9, 6), "per_shape": parts}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the FP64 oracle as it stands, on the host cores, over a
+    bounded row sample of the step, with inputs built by the oracle alone."""
     if rank != 0:
         return 0
-    from bit_weight_only_lbq_gb300 import lbq
-    layer = make_workload(lbq, 0)
     budget_s = 120.0
     rows = 64
-    step = oracle_sample(layer, rows)
+    layer = oracle_workload(rows)
+    step, _ = oracle_sample(layer, rows)
     t = time.perf_counter()
     step()
     one = time.perf_counter() - t
     per_step_budget = budget_s / max(1, args.steps + args.warmup)
     while rows > 1 and one > per_step_budget:
         rows //= 2
-        step = oracle_sample(layer, rows)
+        step, _ = oracle_sample(layer, rows)
         t = time.perf_counter()
         step()
         one = time.perf_counter() - t
@@ -281,7 +372,8 @@ def run_reference(args, rank, world):
         "config": config_dict(),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": "first %d rows of each of the step's 16 matrices per step (FP64 NumPy "
-                                   "dequantise-from-bytes + matvec)" % rows},
+                                   "dequantise-from-bytes + matvec; inputs and outlier columns from the oracle)"
+                                   % rows},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -309,6 +401,7 @@ def main():
     ap.add_argument("--impl", default="lbq", choices=["lbq", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep70b", action="store_true", help="skip the Llama-3-70B weight sweep detail")
+    ap.add_argument("--no-smallm-sweep", action="store_true", help="skip the small-M (M = 2..64) detail")
     ap.add_argument("--single", default=None,
                     help="kind:N:K:n_out:M - time one kernel configuration alone (profiling aid), "
                          "kind in w4, w2, w4m; sweep:KIND (one grouped launch of the step); "
@@ -376,9 +469,17 @@ def main():
 
     clocks = ClockSampler(local_rank)
     clocks.start()
+    clocks.wait_first()
+    w_wall0 = time.time()
     with torch.cuda.stream(stream):
-        for s in range(max(3, args.warmup)):
+        # at least W warm-up steps, and at least 0.5 s of them, so the clocks have
+        # settled under load and the sampler has seen it
+        s = 0
+        while s < max(3, args.warmup) or time.time() - w_wall0 < 0.5:
             graphs[s % REPLICAS].replay()
+            s += 1
+            if s % 200 == 0:
+                stream.synchronize()
         stream.synchronize()
         if dist:
             dist.barrier()
@@ -396,7 +497,6 @@ def main():
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     if dist:
         dist.barrier()
-    clk = clocks.summary(t_wall0, t_wall1)
 
     # timing of one launch kind on its own: back to back over rotating copies
     # inside a CUDA graph (chained with programmatic dependent launch, as in
@@ -447,6 +547,9 @@ def main():
         del g, extra
     refinement = run_refinement(lbq, layer, dev, stream)
     kv_cache = time_kv_cache(lbq, dev, stream)
+    decode_sweep = run_decode_sweep(lbq, layer, copies, ncopy, xs, ys, stream, replays)
+    small_m = None if args.no_smallm_sweep else run_smallm_sweep(lbq, dev, stream)
+    clk = clocks.summary(t_wall0, t_wall1, w_wall0, time.time())
     sweep70b = None
     if not args.no_sweep70b:
         sweep70b = run_sweep70b(lbq, dev, stream)
@@ -522,10 +625,11 @@ def main():
                            1.0 / (32 * sum(statistics.median(per_call[i]) for i, e in enumerate(layer)
                                            if e["kind"] == "w4") * 1e-3), 1)},
                    "w4_layer_bytes": w4_bytes, "w2_layer_bytes": w2_bytes,
+                   "decode_sweep_dependent_launches": decode_sweep, "small_m": small_m,
                    "llama3_70b_sweep": sweep70b, "selective_refinement": refinement, "kv_cache_4bit": kv_cache},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(layer)
+        line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -601,6 +705,132 @@ def run_refinement(lbq, layer, dev, stream, replays=20):
     return out
 
 
+# a decode step can only group linears whose inputs are ready together:
+# {q, k, v} (the layer input), o (after attention), {gate, up} (after o), down
+# (after gate and up)
+DECODE_STAGES = (("q_proj", "k_proj", "v_proj"), ("o_proj",), ("gate_proj", "up_proj"), ("down_proj",))
+
+
+def run_decode_sweep(lbq, layer, copies, ncopy, xs, ys, stream, replays):
+    """The layer sweep as a real decode step issues it: 4 grouped launches a layer
+    (DECODE_STAGES), each depending on the one before (programmatic dependent
+    launch: a launch's prologue overlaps the previous one, its activations are
+    read after it completes), for the 4-bit and the 2-bit layer, over rotating
+    copies of the weights in a CUDA graph."""
+    import torch
+    out = {}
+    for kind in ("w4", "w2"):
+        lk = lbq.LBQ_KIND_W2CB if kind == "w2" else lbq.LBQ_KIND_W4
+        stages = [[i for i, e in enumerate(layer) if e["kind"] == kind and e["name"] in names] for names in DECODE_STAGES]
+        n = ncopy[kind]
+
+        def sweep():
+            for r in range(n):
+                for members in stages:
+                    lbq.gemv_grouped(lk, group_args(lbq, layer, members, copies[r], xs, ys), M=1, pdl=True)
+        with torch.cuda.stream(stream):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                sweep()
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(replays):
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_) * 1e3 / n)
+        del g
+        us = statistics.median(ts)
+        nbytes = sum(layer[i]["bytes"] for st in stages for i in st)
+        out[kind] = {"launches_per_layer": len(stages), "us_per_layer": round(us, 3), "bytes": nbytes,
+                     "GB_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                     "implied_tokens_per_s_32_layers": round(1.0 / (32 * us * 1e-6), 1)}
+    assert lbq.device_error(stream) == 0
+    return out
+
+
+FMA_PEAK = 152 * 128 * 2.07e9       # FP32 FMA lanes of a GB300 (152 SMs x 128 a clock) at the 2.07 GHz maximum
+
+
+def run_smallm_sweep(lbq, dev, stream, replays=5):
+    """Config 4 across M: the 4-bit gate (14336 x 4096) and down (4096 x 14336)
+    projections at M = 2..64 (CUDA cores below 16, tensor cores from 16), the
+    2-bit ones with 3.5 % outlier columns (CUDA cores at every M) and without
+    outlier columns at M >= 16 (tensor cores).  Each configuration chained over
+    rotating copies (>= 512 MB) in a CUDA graph.  Next to the HBM fraction: the
+    FP32-FMA fraction below M = 16 (one FMA per weight and activation row) and
+    the dense FP16 tensor fraction from M = 16."""
+    import torch
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        with open(pp) as f:
+            peaks = json.load(f)
+    tc_peak = float(peaks.get("bf16_tflops", 1900.0)) * 1e12   # FP16 and BF16 dense rates are equal
+    hbm_peak, _ = load_peaks()
+    cases = []
+    for li in (4, 6):
+        name, N, K = synth.LLAMA3_8B_LINEARS[li]
+        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
+        b4 = lbq.pack_w4(W)
+        for M in (2, 4, 8, 16, 32, 64):
+            cases.append(("w4", name, N, K, M, 0, b4))
+        W2 = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
+        idx = lbq.select_outliers_impact(W2, synth.profile_vectors(K, config_id=3, layer_id=li), 0.035)
+        b2o = lbq.pack_w2cb(W2, idx)
+        for M in (2, 4, 8, 16):
+            cases.append(("w2", name, N, K, M, len(idx), b2o))
+        b2 = lbq.pack_w2cb(W2, np.zeros(0, np.int32))
+        for M in (16, 64):
+            cases.append(("w2", name, N, K, M, 0, b2))
+        del W, W2
+    rows = []
+    for kind, name, N, K, M, n_out, blob in cases:
+        n = max(REPLICAS, -(-L2_ROTATION_BYTES // blob.size))
+        d0 = torch.from_numpy(blob).to(dev)
+        cps = [d0] + [d0.clone() for _ in range(n - 1)]
+        X = torch.from_numpy(synth.activations(M, K, config_id=4, layer_id=0)).to(dev)
+        Y = torch.empty((M, N), dtype=torch.float16, device=dev)
+        f = lbq.gemm_w4a16_smallM if kind == "w4" else lbq.gemm_w2cb_outlier_smallM
+        with torch.cuda.stream(stream):
+            for c in cps[:2]:
+                f(c, M, N, K, n_out, X, K, Y, N, stream=stream, pdl=True)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in cps:
+                    f(c, M, N, K, n_out, X, K, Y, N, stream=stream, pdl=True)
+            g.replay()
+            stream.synchronize()
+            ts = []
+            for _ in range(replays):
+                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+                b_.synchronize()
+                ts.append(a_.elapsed_time(b_) * 1e3 / n)
+        del g, cps, d0
+        us = statistics.median(ts)
+        nbytes = algorithmic_bytes(kind, N, K, n_out, M)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        row = {"kind": kind, "linear": name, "N": N, "K": K, "M": M, "n_out": n_out,
+               "path": "tensor cores" if (M >= 16 and n_out == 0) else "CUDA cores",
+               "us_per_call": round(us, 3), "GB_s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
+        macs = M * N * K
+        if row["path"] == "CUDA cores":
+            row["frac_of_fp32_fma"] = round(macs / (us * 1e-6) / FMA_PEAK, 4)
+        else:
+            row["frac_of_fp16_tensor"] = round(2 * macs / (us * 1e-6) / tc_peak, 4)
+        rows.append(row)
+    assert lbq.device_error(stream) == 0
+    torch.cuda.empty_cache()
+    return {"cases": rows, "fp32_fma_peak": FMA_PEAK, "fp16_tensor_peak_flops": tc_peak}
+
+
 def run_sweep70b(lbq, dev, stream, replays=5):
     """Config 5: one decode token through every linear of a Llama-3-70B-shaped
     model (80 layers x 7 linears + lm_head, W4A16 G32, M = 1): 40.2 GB of packed
@@ -642,11 +872,22 @@ def run_sweep70b(lbq, dev, stream, replays=5):
                 lbq.gemv_w4a16(blobs[i], N, K, 0, xs[K], ys[i], pdl=True)
         lbq.gemv_w4a16(head, hN, hK, 0, xs[hK], yh, pdl=True)
 
+    stages = [[i for i, (name, _, _, _) in enumerate(layer) if name in names] for names in DECODE_STAGES]
+
+    def token_dependent():
+        # what a decode step can group: {q, k, v} | o | {gate, up} | down, in order
+        for blobs in layers:
+            for members in stages:
+                lbq.gemv_grouped(lbq.LBQ_KIND_W4, [(blobs[i], layer[i][1], layer[i][2], 0, xs[layer[i][2]], ys[i])
+                                                   for i in members], pdl=True)
+        lbq.gemv_w4a16(head, hN, hK, 0, xs[hK], yh, pdl=True)
+
     out = {"workload": "llama3_70b decode weight sweep: 80 x (q 8192x8192, k/v 1024x8192, o 8192x8192, gate/up "
                        "28672x8192, down 8192x28672) + lm_head 128256x8192, W4A16 G32, M=1, one token",
            "bytes_per_token": total, "host_pack_s": round(t_pack, 1),
            "note": "one packed layer replicated 80x in HBM (each layer streams its own copy)"}
     for label, fn, launches in (("fused_layer_sweeps", token_grouped, synth.LLAMA3_70B_LAYERS + 1),
+                                ("dependent_launches", token_dependent, synth.LLAMA3_70B_LAYERS * 4 + 1),
                                 ("per_call", token_per_call, synth.LLAMA3_70B_LAYERS * 7 + 1)):
         with torch.cuda.stream(stream):
             fn()
@@ -876,30 +1117,24 @@ def run_single_sweep(args, kind):
     return 0
 
 
-def cpu_baseline(layer):
-    """The oracle as it stands on the host cores: FP64 dequantise-from-bytes + matvec
-    over a row sample of every matrix of the step, scaled to the step's bytes."""
-    step = None
-    rows = 256
-    t_budget = 15.0
-    while True:
-        step = oracle_sample(layer, rows)
-        t = time.perf_counter()
-        nbytes = step()
-        dt = time.perf_counter() - t
-        if dt > 0.5 or rows >= 4096:
-            break
-        rows *= 2
-    reps = max(1, int(t_budget / max(dt, 1e-3)))
-    reps = min(reps, 20)
+def cpu_baseline() -> dict:
+    """The oracle as it stands on the host cores, with inputs built by the oracle
+    alone: (ii) dequantise-from-bytes + matvec over a row sample of every matrix of
+    the step (the headline value, GB/s of algorithmic bytes), with (i) packing and
+    (iii) matvec on the cached matrix beside it, and config 5 extrapolated."""
+    rows = 128
+    layer = oracle_workload(rows)
+    step, _ = oracle_sample(layer, rows)
     t = time.perf_counter()
-    for _ in range(reps):
-        step()
-    dt = (time.perf_counter() - t) / reps
-    return {"value": round(nbytes / dt / 1e9, 6), "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
+    step()
+    dt = time.perf_counter() - t
+    reps = max(1, min(20, int(10.0 / max(dt, 1e-3))))
+    fig = oracle_figures(layer, rows, reps)
+    return {"value": fig["dequant_matvec"]["GB_s"], "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle",
-            "sample": "first %d rows of each of the step's 16 matrices, %d repetitions (FP64 NumPy "
-                      "dequantise-from-bytes + matvec)" % (rows, reps)}
+            "sample": "first %d rows of each of the step's 16 matrices, %d repetitions (FP64 NumPy; inputs and "
+                      "outlier columns from the oracle)" % (rows, reps),
+            "figures": fig, "llama3_70b_extrapolated": oracle_70b_extrapolated()}
 
 
 if __name__ == "__main__":
