@@ -47,12 +47,13 @@ uint16_t host_f64_to_f16(double v);
 lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
                          int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
                          uint32_t flags);
-// Tensor-core 2-bit codebook GEMM for 16 <= M <= 64 without outlier columns
-// (lbq_mma.cu).  One launch per slab of 256-row tiles; with `launches` set it
-// only adds the number of launches.  LBQ_ERR_SHAPE when the problem does not fit.
-lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
-                         int64_t ldy, bool y_f32, unsigned* err_word, int max_smem, void* stream, uint32_t flags,
-                         int* launches);
+// Tensor-core 2-bit codebook GEMM for 16 <= M <= 64 with its exact FP16
+// outlier columns (lbq_mma.cu).  One launch per slab of 256-row tiles; with
+// `launches` set it only adds the number of launches.  LBQ_ERR_SHAPE when the
+// problem does not fit.
+lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int32_t n_out, int M, const void* x, int64_t ldx,
+                         void* y, int64_t ldy, bool y_f32, unsigned* err_word, int max_smem, void* stream,
+                         uint32_t flags, int* launches);
 double host_f16_to_f64(uint16_t h);
 
 }  // namespace lbq

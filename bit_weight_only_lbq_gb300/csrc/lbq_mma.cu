@@ -37,6 +37,13 @@
 //    holds each 16-k block in the order (0,4,8,12,1,5,...); 2 warps (thread =
 //    activation row) put the A stage in the same order in place, which leaves
 //    the contraction unchanged;
+//  * outlier columns (otf-llm's exact FP16 outlier path, in the same kernel as
+//    SPECTRA section 4.2's in-kernel outlier fusion) are extra stages of 64
+//    columns after a tile's dense chunks: their B stage is the FP16 outlier
+//    values of the tile's 256 rows, copied straight into the swizzled B layout
+//    by one tensor copy, their A stage x[idx] gathered by the activation warps;
+//    the dense A stages carry x~ (the outlier channels zeroed), so every term
+//    of y = W_hat x~ + W_out x[idx] lands in the same FP32 accumulator;
 //  * partial accumulators of a tile split over several CTAs go through shared
 //    memory; each contributing CTA adds one column slice of the tile from all
 //    contributors in rank order through distributed shared memory (fixed
@@ -97,13 +104,16 @@ struct Fmt {
     // the next one or the B ring), B ring, mbarriers, flags
     static constexpr int kA = 0;
     static constexpr int kB = kNA * kAStage;
-    static constexpr int kBars = kB + kNB * kBStage;
-    static constexpr int kNBars = 2 * kNB + 3 * kNA + 1;
+    static constexpr int kMask = kB + kNB * kBStage;                 // outlier-channel bitmask (K bits)
+    static constexpr int kBars = kMask + static_cast<int>(lbq::kMaxK / 8);
+    static constexpr int kNBars = 2 * kNB + 3 * kNA + 2;
     static constexpr int kTotal = kBars + 8 * kNBars + 64 + 1024;   // + flags, 1024-byte alignment slack
 };
 
 struct Maps {
     CUtensorMap x;
+    CUtensorMap out_full;   // outlier records but the last: (column, row, record, row block)
+    CUtensorMap out_last;   // the last outlier record of a row block: (column, row, row block)
 };
 
 struct MmaArgs {
@@ -117,8 +127,15 @@ struct MmaArgs {
     long long rb_bytes;
     int n_rb;
     int T;                  // tiles
-    int U;                  // stages per tile
-    int Uc;                 // chunks per tile
+    int U;                  // dense stages per tile (K / 64)
+    int Ud;                 // dense chunks per tile
+    int OS;                 // outlier stages per tile (64 columns each)
+    int Uc;                 // chunk units per tile: dense chunks, then outlier chunks (<= 4 stages each)
+    int n_out;              // outlier columns
+    int OT;                 // outlier records per row block
+    int recs;               // dense records per row block
+    int cols_last;          // columns of the last outlier record (a multiple of 8)
+    const int32_t* idx;     // outlier channel indices (device, in the blob)
     int C;                  // CTAs per cluster
     int G;                  // clusters
     int M;                  // activation rows
@@ -282,13 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // mbarriers: B full/empty [kNB], X copied [kNA], A ready [kNA] (reordered), A
     // empty [kNA], accumulators done
     const uint32_t bfull = sb + F::kBars, bempty = bfull + 8 * kNB, xfull = bempty + 8 * kNB,
-                   afull = xfull + 8 * kNA, aempty = afull + 8 * kNA, dfull = aempty + 8 * kNA;
+                   afull = xfull + 8 * kNA, aempty = afull + 8 * kNA, dfull = aempty + 8 * kNA,
+                   ocopy = dfull + 8;
     uint32_t* flags = reinterpret_cast<uint32_t*>(smem + F::kBars + 8 * F::kNBars);
     volatile uint32_t* abort_flag = flags + 1;
     volatile int* xissued = reinterpret_cast<volatile int*>(flags + 4);  // X stages whose copies were issued
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int C = a.C, U = a.U, Uc = a.Uc;
+    const int C = a.C, U = a.U, Uc = a.Uc, Ud = a.Ud;
     const int cl = static_cast<int>(blockIdx.x) / C, rank = static_cast<int>(blockIdx.x) % C;
     int t0, t1;
     cluster_tiles(a.T, a.G, cl, &t0, &t1);
@@ -297,7 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     rank_range(units, C, rank, &lu0, &lu1);
     const int u0 = static_cast<int>(lu0), u1 = static_cast<int>(lu1);   // this CTA's chunk units
     const int ncu = u1 - u0;
-    auto chunk_stages = [&](int u) { const int c = u % Uc; return min(kChunkStages, U - kChunkStages * c); };
+    // stages of chunk unit u: dense chunks cover K in 256-k steps, outlier chunks
+    // the outlier columns in 256-column steps
+    auto chunk_stages = [&](int u) {
+        const int c = u % Uc;
+        return c < Ud ? min(kChunkStages, U - kChunkStages * c) : min(kChunkStages, a.OS - kChunkStages * (c - Ud));
+    };
     int nst = 0;
     for (int u = u0; u < u1; ++u) nst += chunk_stages(u);
     const int first_tile = t0 + (ncu > 0 ? u0 / Uc : 0);
@@ -309,6 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    uint32_t* omask = reinterpret_cast<uint32_t*>(smem + F::kMask);   // bit k: channel k is an outlier
+    if (a.n_out > 0)
+        for (int i = tid; i < static_cast<int>((a.K + 31) / 32); i += kThreads) omask[i] = 0u;
     if (tid == 32) {
         for (int i = 0; i < F::kNBars; ++i) {
             const uint32_t bar = bfull + 8 * i;
@@ -328,6 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = flags[0];
+    for (int i = tid; i < a.n_out; i += kThreads) {
+        const int k = a.idx[i];
+        if (k >= 0 && k < a.K)
+            atomicOr(&omask[k >> 5], 1u << (k & 31));
+        else
+            atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_OUTLIER_IDX));   // corrupted blob: never index outside x
+    }
     if (warp < 4) {
         // clear both accumulators (every MMA accumulates): warp w zeroes lane quarter w
 #pragma unroll 1
@@ -380,21 +413,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             asm volatile("griddepcontrol.wait;" ::: "memory");   // X may be written by the previous kernel
             int i = 0, cu = u0, cj = 0;
             for (; i < nst; ++i) {
-                const int s = kChunkStages * (cu % Uc) + cj;
+                const int c = cu % Uc, s = kChunkStages * c + cj;
                 if (++cj == chunk_stages(cu)) {
                     cj = 0;
                     ++cu;
                 }
                 const int as = i % kNA;
                 if (i >= kNA && !wait(aempty + 8 * as, ((i - kNA) / kNA) & 1)) break;
-                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(xfull + 8 * as),
-                             "r"(static_cast<uint32_t>(a.Mr * 128))
-                             : "memory");
-                asm volatile(
-                    "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-                    " [%0], [%1, {%2, %3}], [%4];" ::"r"(sb + F::kA + as * kAStage),
-                    "l"(&maps.x), "r"(s * kStageK), "r"(0), "r"(xfull + 8 * as)
-                    : "memory");
+                if (c < Ud) {
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(xfull + 8 * as),
+                                 "r"(static_cast<uint32_t>(a.Mr * 128))
+                                 : "memory");
+                    asm volatile(
+                        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                        " [%0], [%1, {%2, %3}], [%4];" ::"r"(sb + F::kA + as * kAStage),
+                        "l"(&maps.x), "r"(s * kStageK), "r"(0), "r"(xfull + 8 * as)
+                        : "memory");
+                } else {
+                    // outlier stage: the activation warps gather its A stage; the slot is free
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(xfull + 8 * as) : "memory");
+                }
             }
             *xissued = i;
         }
@@ -447,32 +485,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp >= kWarpAct) {
-        // ------------------------------------------------------------------ A stage in decode order
+        // ------------------------------------------------------------------ A stages: order, mask, gather
+        // dense stage: the copied X in the codes' decode order, outlier channels
+        // zeroed (x~); outlier stage: x[idx_j] of its 64 outlier columns, in order
         {
             const int m = 32 * (warp - kWarpAct) + lane;   // A row: 128 bytes at its swizzled place
             const uint32_t arow = static_cast<uint32_t>((m >> 3) * 1024 + (m & 7) * 128), asw = static_cast<uint32_t>(m & 7);
+            int cu = u0, cj = 0;
             for (int i = 0; i < nst; ++i) {
+                const int c = cu % Uc, jj = cj;
+                if (++cj == chunk_stages(cu)) {
+                    cj = 0;
+                    ++cu;
+                }
                 const int as = i % kNA;
                 const bool ok = warp_wait(xfull + 8 * as, (i / kNA) & 1, true);
                 if (ok && !*abort_flag && m < a.Mr) {
                     const uint32_t row = sb + F::kA + as * kAStage + arow;
                     uint32_t w[32];
+                    if (c < Ud) {
+                        const int s = kChunkStages * c + jj;   // k in [64 s, 64 s + 64)
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint4 v = lds128(row + ((j ^ asw) << 4));
-                        w[4 * j] = v.x;
-                        w[4 * j + 1] = v.y;
-                        w[4 * j + 2] = v.z;
-                        w[4 * j + 3] = v.w;
-                    }
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 v = lds128(row + ((j ^ asw) << 4));
+                            w[4 * j] = v.x;
+                            w[4 * j + 1] = v.y;
+                            w[4 * j + 2] = v.z;
+                            w[4 * j + 3] = v.w;
+                        }
+                        if (a.n_out > 0) {
+                            const uint32_t mk[2] = {omask[2 * s], omask[2 * s + 1]};
+                            if (mk[0] | mk[1]) {
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk) {
-                        uint32_t nat[8], o[8];
+                                for (int e = 0; e < 32; ++e) {
+                                    const uint32_t bits = (mk[e >> 4] >> (2 * (e & 15))) & 3u;
+                                    w[e] &= ((bits & 1u) ? 0xFFFF0000u : 0xFFFFFFFFu) & ((bits & 2u) ? 0x0000FFFFu : 0xFFFFFFFFu);
+                                }
+                            }
+                        }
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) nat[e] = w[8 * blk + e];
-                        w2_order(nat, o);
+                        for (int blk = 0; blk < 4; ++blk) {
+                            uint32_t nat[8], o[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) w[8 * blk + e] = o[e];
+                            for (int e = 0; e < 8; ++e) nat[e] = w[8 * blk + e];
+                            w2_order(nat, o);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[8 * blk + e] = o[e];
+                        }
+                    } else {
+                        const int j0 = kStageK * (kChunkStages * (c - Ud) + jj);   // first outlier column
+                        const unsigned short* xr = reinterpret_cast<const unsigned short*>(a.x) + m * a.ldx;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            uint32_t lo = 0u, hi = 0u;
+                            if (m < a.M) {
+                                const int j = j0 + 2 * e;
+                                if (j < a.n_out) {
+                                    const int k = __ldg(a.idx + j);
+                                    if (k >= 0 && k < a.K) lo = __ldg(xr + k);
+                                }
+                                if (j + 1 < a.n_out) {
+                                    const int k = __ldg(a.idx + j + 1);
+                                    if (k >= 0 && k < a.K) hi = __ldg(xr + k);
+                                }
+                            }
+                            w[e] = lo | (hi << 16);
+                        }
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
@@ -492,11 +570,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sw = static_cast<uint32_t>(n & 7);                               // its 128-byte swizzle
         const uint32_t lut_lo = a.lut_lo, lut_hi = a.lut_hi;
         constexpr int CV = F::kCodeVecs;
-        // row n's record of chunk unit u (nullptr past the matrix: zero codes and metadata)
+        // row n's record of dense chunk unit u (nullptr past the matrix, and for
+        // outlier chunks: zero codes and metadata)
         auto rec_of = [&](int u, int* cc) -> const uint8_t* {
             const int t = t0 + u / Uc, c = u % Uc, rb = t * kTileRb + rbl;
             *cc = c % kChunksPerRec;
-            if (rb >= a.n_rb) return nullptr;
+            if (rb >= a.n_rb || c >= Ud) return nullptr;
             return a.area + static_cast<long long>(rb) * a.rb_bytes +
                    static_cast<long long>(c / kChunksPerRec) * F::kRecBytes;
         };
@@ -516,9 +595,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m0 = m1 = make_uint4(0u, 0u, 0u, 0u);
             }
         };
+        // row n's FP16 outlier values of outlier stage os (64 columns) and where they sit
+        auto out_row = [&](int t, int os) -> const uint8_t* {
+            const int rb = t * kTileRb + rbl, j0 = kStageK * os, o = j0 / lbq::kOutlierCols;
+            if (rb >= a.n_rb) return nullptr;
+            const int cols = o + 1 < a.OT ? lbq::kOutlierCols : a.cols_last;
+            return a.area + static_cast<long long>(rb) * a.rb_bytes + static_cast<long long>(a.recs) * F::kRecBytes +
+                   static_cast<long long>(o) * (lbq::kOutlierCols * lbq::kRowsPerBlock * 2) + r * cols * 2 +
+                   (j0 % lbq::kOutlierCols) * 2;
+        };
         auto prefetch_chunk = [&](int u) {
             int cc;
             const uint8_t* rec = rec_of(u, &cc);
+            if (u % Uc >= Ud) {
+                const int t = t0 + u / Uc, os0 = kChunkStages * (u % Uc - Ud);
+                for (int jj = 0; jj < chunk_stages(u); ++jj) {
+                    const uint8_t* p = out_row(t, os0 + jj);
+                    if (p) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+                }
+            }
             if (rec) {
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + r * F::kRowCodeBytes + cc * F::kChunkRowBytes));
                 if (cc == 0 && r == 0) {
@@ -533,7 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 q[CV], qn[CV], m0, m1, m0n, m1n;
         if (ncu > 0) load_chunk(u0, qn, m0n, m1n);   // ahead of the prefetches in the memory queues
         for (int j = 1; j < F::kPF && j < ncu; ++j) prefetch_chunk(u0 + j);
-        int ist = 0;   // stage index of the chunk's first stage
+        int ist = 0;        // stage index of the chunk's first stage
+        int n_copies = 0;   // outlier copies issued (warp 0, lane 0)
         for (int j = 0; j < ncu; ++j) {
             const int u = u0 + j, nsc = chunk_stages(u);
 #pragma unroll
@@ -548,6 +644,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int is = ist + jj, bs = is % kNB;
                 const bool ok = warp_wait(bempty + 8 * bs, ((is - kNB) / kNB) & 1, is >= kNB);
                 const uint32_t bst = sb + F::kB + bs * kBStage + brow;
+                if (u % Uc >= Ud) {
+                    // outlier stage: the tile's 256 rows x 64 FP16 outlier values go straight
+                    // into the B stage (the copy writes the swizzled layout); warp 0 issues the
+                    // copy and waits for it to land before its arrival, so that no copy is in
+                    // flight when the CTA ends, whatever happened
+                    if (lane == 0 && warp == 0 && ok && !*abort_flag) {
+                        const int t = t0 + u / Uc, j0 = kStageK * (kChunkStages * (u % Uc - Ud) + jj);
+                        const int o = j0 / lbq::kOutlierCols, col = j0 % lbq::kOutlierCols;
+                        const uint32_t dst = sb + F::kB + bs * kBStage;
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(ocopy), "r"(kBStage)
+                                     : "memory");
+                        if (o + 1 < a.OT)
+                            asm volatile(
+                                "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+                                "l"(&maps.out_full), "r"(col), "r"(0), "r"(o), "r"(t * kTileRb), "r"(ocopy)
+                                : "memory");
+                        else
+                            asm volatile(
+                                "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                                " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+                                "l"(&maps.out_last), "r"(col), "r"(0), "r"(t * kTileRb), "r"(ocopy)
+                                : "memory");
+                        if (!mbar_wait(ocopy, n_copies & 1, kWaitLimitNs)) {
+                            *abort_flag = 1;
+                            atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_TIMEOUT));
+                        }
+                        ++n_copies;
+                    }
+                    __syncwarp();
+                    if (lane == 0) arrive(bfull + 8 * bs);
+                    continue;
+                }
                 if (ok && !*abort_flag) {
                     const uint4 qs = q[jj];
                     const uint32_t Sw = u4w(m0, jj), Zw = u4w(m1, jj);
@@ -708,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long n_hdr = (static_cast<long long>(h1.y) << 32) | h1.x;
         const long long k_hdr = (static_cast<long long>(h1.w) << 32) | h1.z;
         if (h0.x != 0x5751424Cu || h0.y != F::kMagicHi || h0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != a.N_hdr ||
-            k_hdr != a.K || h2.x != 0u)
+            k_hdr != a.K || static_cast<int>(h2.x) != a.n_out)
             atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_FORMAT));
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -824,16 +953,16 @@ bool mma_plan(int T, int Uc, int bands, const int* active, int* C_out, int* G_ou
     return true;
 }
 
-// Launch the tensor-core GEMM for one problem (16 <= M <= 64, no outlier
-// columns): one launch per slab of tiles, each slab small enough that every
-// CTA's range spans at most two tiles.  With `launches` set, only counts the
-// launches.  Returns LBQ_ERR_SHAPE when the problem does not fit the kernel.
-lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
-                         int64_t ldy, bool y_f32, unsigned* err_word, int max_smem, void* stream, uint32_t flags,
-                         int* launches) {
+// Launch the tensor-core GEMM for one problem (16 <= M <= 64, any number of
+// outlier columns): one launch per slab of tiles, each slab small enough that
+// every CTA's range spans at most two tiles.  With `launches` set, only counts
+// the launches.  Returns LBQ_ERR_SHAPE when the problem does not fit the kernel.
+lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int32_t n_out, int M, const void* x, int64_t ldx,
+                         void* y, int64_t ldy, bool y_f32, unsigned* err_word, int max_smem, void* stream,
+                         uint32_t flags, int* launches) {
     if (M < 16 || M > 64) return LBQ_ERR_SHAPE;
     lbq_layout L;
-    lbq_status st = lbq_blob_layout(LBQ_KIND_W2CB, N, K, 0, &L);
+    lbq_status st = lbq_blob_layout(LBQ_KIND_W2CB, N, K, n_out, &L);
     if (st != LBQ_OK) return st;
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return LBQ_ERR_CUDA;
@@ -841,7 +970,14 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int M, const 
     st = active_clusters(max_smem, &active);
     if (st != LBQ_OK) return st;
     const int T = static_cast<int>((N + kTileRows - 1) / kTileRows);
-    const int U = static_cast<int>(K / kStageK), Uc = (U + kChunkStages - 1) / kChunkStages;
+    // chunk units of a tile: the dense chunks (256 k each), then the outlier chunks
+    // (256 outlier columns each, in 64-column stages)
+    const int U = static_cast<int>(K / kStageK), Ud = (U + kChunkStages - 1) / kChunkStages;
+    const int OS = (n_out + kStageK - 1) / kStageK, Uc = Ud + (OS + kChunkStages - 1) / kChunkStages;
+    const int OT = static_cast<int>(L.outlier_records);
+    const int cols_last = n_out > 0 ? (n_out + lbq::kOutlierColAlign - 1) / lbq::kOutlierColAlign *
+                                              lbq::kOutlierColAlign - (OT - 1) * lbq::kOutlierCols
+                                    : 0;
     int slab = T, C = 0, G = 0, load = 0;
     while (slab > 1 && !mma_plan(slab, Uc, 2, active, &C, &G, &load)) slab = (slab + 1) / 2;
     if (!mma_plan(slab, Uc, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
@@ -882,7 +1018,14 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int M, const 
         a.n_rb = static_cast<int>((Ns + 3) / 4);
         a.T = tiles;
         a.U = U;
+        a.Ud = Ud;
+        a.OS = OS;
         a.Uc = Uc;
+        a.n_out = n_out;
+        a.OT = OT;
+        a.recs = static_cast<int>(L.records);
+        a.cols_last = cols_last;
+        a.idx = n_out > 0 ? reinterpret_cast<const int32_t*>(b + L.idx_offset) : nullptr;
         a.C = C;
         a.G = G;
         a.M = M;
@@ -901,6 +1044,33 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int M, const 
             const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(a.Mr)};
             enc = enc && encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box,
                                 one, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+        // tensor maps of the outlier values, FP16 (column, row, [record,] row block):
+        // 64-column x 256-row boxes in the MMA's swizzled layout; columns past the
+        // last record's width and row blocks past the slab read as zero
+        if (n_out > 0) {
+            uint8_t* out0 = b + L.area_offset + (n0 / 4) * static_cast<long long>(L.row_block_bytes) +
+                            L.records * L.record_bytes;
+            const cuuint32_t one4[4] = {1, 1, 1, 1};
+            if (OT > 1) {
+                const cuuint64_t dims[4] = {static_cast<cuuint64_t>(lbq::kOutlierCols), 4,
+                                            static_cast<cuuint64_t>(OT - 1), static_cast<cuuint64_t>(a.n_rb)};
+                const cuuint64_t strides[3] = {static_cast<cuuint64_t>(lbq::kOutlierCols) * 2,
+                                               static_cast<cuuint64_t>(L.outlier_record_bytes),
+                                               static_cast<cuuint64_t>(L.row_block_bytes)};
+                const cuuint32_t box[4] = {static_cast<cuuint32_t>(kStageK), 4, 1, static_cast<cuuint32_t>(kTileRb)};
+                enc = enc && encode(&maps.out_full, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, out0, dims, strides, box, one4,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            }
+            const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols_last), 4, static_cast<cuuint64_t>(a.n_rb)};
+            const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols_last) * 2,
+                                           static_cast<cuuint64_t>(L.row_block_bytes)};
+            const cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), 4, static_cast<cuuint32_t>(kTileRb)};
+            enc = enc && encode(&maps.out_last, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                                out0 + static_cast<long long>(OT - 1) * L.outlier_record_bytes, dims, strides, box,
+                                one4, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
         }
         if (!enc) return LBQ_ERR_CUDA;

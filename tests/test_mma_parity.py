@@ -1,14 +1,18 @@
-"""GPU parity of the tensor-core small-M GEMMs (16 <= M <= 64, no outlier
-columns) against the FP64 oracle, element by element, for both weight formats:
-4-bit (weights dequantised into tensor memory, 128-row tiles, K split over a
-cluster) and 2-bit codebook (weights as the 256-wide operand in shared memory,
-256-row tiles and 256-k chunks split over a cluster, each CTA's range spanning
-at most two tiles with one accumulator each; taller matrices go in slabs of
-tiles, one launch each).  The shapes cover: N ragged against both tile sizes
-(and smaller than one row block), K with a partial 1024-k record and a partial
-chunk, M from 16 to 64, CTA ranges that span two tiles, a single tile whose K is
-split over a whole cluster, two slabs, leading dimensions, FP16 output,
-repeatable bits.
+"""GPU parity of the tensor-core small-M GEMMs (16 <= M <= 64) against the FP64
+oracle, element by element, for both weight formats: 4-bit (weights dequantised
+into tensor memory, 128-row tiles, K split over a cluster; no outlier columns)
+and 2-bit codebook (weights as the 256-wide operand in shared memory, 256-row
+tiles and 256-k chunks split over a cluster, each CTA's range spanning at most
+two tiles with one accumulator each; taller matrices go in slabs of tiles, one
+launch each; the exact FP16 outlier columns are extra 64-column stages of the
+same accumulation, their values copied straight into the operand stage and the
+activations gathered by index).  The shapes cover: N ragged against both tile
+sizes (and smaller than one row block), K with a partial 1024-k record and a
+partial chunk, M from 16 to 64, CTA ranges that span two tiles, a single tile
+whose K is split over a whole cluster, two slabs, leading dimensions, FP16
+output, repeatable bits; with outliers: one column, a trimmed last outlier
+record (8 columns wide), exactly one full record, two and four records, every
+column an outlier, the first and last channel.
 The weights are dequantised to FP16 before the FP32-accumulating product, so
 each weight carries one FP16 rounding; the bound stays the oracle tolerance."""
 import numpy as np
@@ -105,3 +109,59 @@ def test_grouped_and_launch_count(lbq):
     assert lbq.device_error() == 0
     for Y, ref in checks:
         assert_close(Y.cpu().numpy(), ref, what="mma grouped")
+
+
+def _idx(seed, K, n_out):
+    rng = np.random.default_rng(seed)
+    if n_out >= 2:   # the first and the last channel are always among them
+        rest = rng.choice(np.arange(1, K - 1), size=n_out - 2, replace=False)
+        return np.sort(np.concatenate([[0, K - 1], rest])).astype(np.int32)
+    return np.sort(rng.choice(K, size=n_out, replace=False)).astype(np.int32)
+
+
+def _run_out(lbq, blob, M, N, K, n_out, X, f32=True):
+    Y = torch.full((M, N), float("nan"), dtype=torch.float32 if f32 else torch.float16, device="cuda:0")
+    lbq.gemm_w2cb_outlier_smallM(to_dev(blob), M, N, K, n_out, to_dev(X), K, Y, N)
+    torch.cuda.synchronize()
+    assert lbq.device_error() == 0
+    return Y.float().cpu().numpy()
+
+
+# (M, N, K, n_out): one outlier column; 77 (a trimmed last record, two 64-column
+# stages); 256 (one full record); 257 (a full record and an 8-column one); 501 over
+# two records at K = 14336; 1000 (four records, four outlier chunks); every column
+# an outlier; outliers with two tiles per CTA range and with two slabs
+OUT_SHAPES = [(16, 300, 1024, 1), (17, 70, 2112, 77), (32, 513, 4096, 256), (64, 257, 2048, 257),
+              (16, 512, 14336, 501), (40, 1000, 4096, 1000), (24, 100, 128, 128), (48, 9000, 2048, 61),
+              (16, 80000, 64, 9)]
+
+
+@pytest.mark.parametrize("M,N,K,n_out", OUT_SHAPES)
+def test_w2_outliers_elementwise(lbq, M, N, K, n_out):
+    W, X = _case(M * 5 + N + K + n_out, M, N, K)
+    idx = _idx(n_out + K, K, n_out)
+    X[:, idx[: max(1, n_out // 3)]] *= 30   # large activations on outlier channels too
+    ref = O.gemm(O.pack_w2cb(W, idx), X)
+    blob = lbq.pack_w2cb(W, idx)
+    assert_close(_run_out(lbq, blob, M, N, K, n_out, X), ref, what="mma w2 M=%d N=%d K=%d n_out=%d" % (M, N, K, n_out))
+
+
+def test_w2_outliers_fp16_output_and_repeatable(lbq):
+    M, N, K, n_out = 33, 700, 3072, 143
+    W, X = _case(77, M, N, K)
+    idx = _idx(78, K, n_out)
+    blob = lbq.pack_w2cb(W, idx)
+    ref = O.gemm(O.pack_w2cb(W, idx), X)
+    assert_close(_run_out(lbq, blob, M, N, K, n_out, X, f32=False), ref, fp16_out=True, what="mma w2 outliers f16")
+    a = _run_out(lbq, blob, M, N, K, n_out, X)
+    for _ in range(2):
+        assert np.array_equal(_run_out(lbq, blob, M, N, K, n_out, X), a)
+
+
+def test_w2_outliers_launch_count(lbq):
+    """Outlier stages add chunks to every tile but no launches."""
+    W, X = _case(3, 16, 80000, 64)
+    idx = _idx(4, 64, 9)
+    big = [(to_dev(lbq.pack_w2cb(W, idx)), 80000, 64, 9, to_dev(X), 64,
+            torch.empty((16, 80000), dtype=torch.float32, device="cuda:0"), 80000)]
+    assert lbq.gemv_grouped_launches(lbq.LBQ_KIND_W2CB, big, M=16) == 2
