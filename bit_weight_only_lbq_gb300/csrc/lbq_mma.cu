@@ -73,17 +73,20 @@ constexpr int kChunkStages = 4;                // stages per copied chunk (256 k
 constexpr int kChunksPerRec = 1024 / (kStageK * kChunkStages);
 constexpr int kDqWarps = 8;                    // dequantising warps: thread = weight row
 constexpr int kActWarps = 2;                   // 2-bit: warps ordering the A stage, thread = activation row
-// one thread issues the MMAs; it polls its barriers with mbarrier.test_wait:
-// a try_wait after MMAs was measured to hold the thread until its earlier MMAs
-// had drained (~1.3 k clocks a stage), a test_wait returns at once
-constexpr int kIssuers = 1;
+constexpr int kIssuers = 1;                    // one thread issues the MMAs
 constexpr int kThreads = 32 * (kDqWarps + kActWarps + 1 + kIssuers);   // + X copy warp + MMA warps
-constexpr int kWarpAct = kDqWarps;             // first activation warp
-constexpr int kWarpXCopy = kDqWarps + kActWarps;  // activations
-constexpr int kWarpMma = kWarpXCopy + 1;          // first MMA warp
-constexpr int kNB = 4;                         // B stages (FP16 weights) in shared memory
+// warp roles: a warp's scheduler is warp % 4; the issuing warp's scheduler hosts
+// only the two activation warps (the single issuing thread was measured to be
+// starved of issue slots next to dequantising warps: ~1000 clocks a stage)
+constexpr int kWarpMma = 3;                    // issues the MMAs
+constexpr int kWarpAct = 7;                    // activation warps 7 and 11
+constexpr int kWarpXCopy = 10;                 // activation copies
+// dequantising warps 0, 1, 2, 4, 5, 6, 8, 9 -> index 0..7
+__device__ __forceinline__ int dq_index(int warp) { return warp - (warp >= 4) - (warp >= 8); }
+constexpr int kNB = 3;                         // B stages (FP16 weights) in shared memory
 constexpr int kBStage = kTileRows * 128;       // 32 KB: 256 rows x 64 k x 2 B
-constexpr int kNA = 8;                         // A stages in shared memory (X copies run ahead: L2 latency)
+constexpr int kNA = 6;                         // A stages in shared memory (X copies run ahead: L2 latency)
+constexpr int kNR = 3;                         // raw chunks (codes, S, Z) in shared memory: 2 in flight
 constexpr int kAStage = 64 * 128;              // 8 KB: 64 activation rows x 64 k x 2 B
 constexpr uint32_t kTmemCols = 512;            // D0 in [0, 256), D1 in [256, 512)
 constexpr int kPartStride = 1024 + 16;         // bytes per accumulator row of the partials (padded)
@@ -104,10 +107,15 @@ struct Fmt {
     // the next one or the B ring), B ring, mbarriers, flags
     static constexpr int kA = 0;
     static constexpr int kB = kNA * kAStage;
-    static constexpr int kMask = kB + kNB * kBStage;                 // outlier-channel bitmask (K bits)
+    // raw chunk: codes of 256 rows x 64 B (each row's four 16-byte parts rotated by
+    // row / 2: conflict-free 16-byte reads), then S and Z, 16 B per row
+    static constexpr int kRaw = kB + kNB * kBStage;
+    static constexpr int kRawS = kTileRows * 64, kRawZ = kRawS + kTileRows * 16;
+    static constexpr int kRawStage = kRawZ + kTileRows * 16;         // 24 KB
+    static constexpr int kMask = kRaw + kNR * kRawStage;             // outlier-channel bitmask (K bits)
     static constexpr int kBars = kMask + static_cast<int>(lbq::kMaxK / 8);
-    static constexpr int kNBars = 2 * kNB + 3 * kNA + 2;
-    static constexpr int kTotal = kBars + 8 * kNBars + 64 + 1024;   // + flags, 1024-byte alignment slack
+    static constexpr int kNBars = kNB + 2 * kNA + 2;
+    static constexpr int kTotal = kBars + 8 * kNBars + 64 + 4 * (kNB + kNA) + 1024;   // + flags, counters, alignment slack
 };
 
 struct Maps {
@@ -128,9 +136,9 @@ struct MmaArgs {
     int n_rb;
     int T;                  // tiles
     int U;                  // dense stages per tile (K / 64)
-    int Ud;                 // dense chunks per tile
+    int Ud;                 // dense chunks per tile (256 k each; the last may be short)
     int OS;                 // outlier stages per tile (64 columns each)
-    int Uc;                 // chunk units per tile: dense chunks, then outlier chunks (<= 4 stages each)
+    int Ut;                 // stages per tile: U dense, then OS outlier stages
     int n_out;              // outlier columns
     int OT;                 // outlier records per row block
     int recs;               // dense records per row block
@@ -155,17 +163,6 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -227,11 +224,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
-__device__ __forceinline__ uint4 ldg128(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+// 16-byte copy global -> shared that completes asynchronously (zero fill when
+// src_bytes is 0; the source is then not read)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t u4w(const uint4& v, int i) {
@@ -266,7 +271,7 @@ __device__ __forceinline__ void w2_order(const uint32_t (&n)[8], uint32_t (&o)[8
     o[7] = prmt(n[5], n[7], 0x7632u);
 }
 
-// Units of cluster c: tiles [t0, t1) x Uc chunks; rank r takes [u0, u1).
+// Units of cluster c: tiles [t0, t1) x Ut stages; rank r takes [u0, u1).
 __host__ __device__ inline void cluster_tiles(int T, int G, int c, int* t0, int* t1) {
     *t0 = static_cast<int>(static_cast<long long>(T) * c / G);
     *t1 = static_cast<int>(static_cast<long long>(T) * (c + 1) / G);
@@ -293,38 +298,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     using F = Fmt;
     constexpr uint32_t kIdesc = idesc_f16(128, kTileRows);
     static_assert(128 * kPartStride <= F::kBars, "the partial accumulators reuse the stage rings");
+    static_assert(F::kTotal <= 232448, "shared memory of one CTA");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
-    // mbarriers: B full/empty [kNB], X copied [kNA], A ready [kNA] (reordered), A
-    // empty [kNA], accumulators done
-    const uint32_t bfull = sb + F::kBars, bempty = bfull + 8 * kNB, xfull = bempty + 8 * kNB,
-                   afull = xfull + 8 * kNA, aempty = afull + 8 * kNA, dfull = aempty + 8 * kNA,
-                   ocopy = dfull + 8;
+    // mbarriers (one arrival each: a tensor-core commit or a copy's issuing thread):
+    // B stage free [kNB], X copied [kNA], A stage free [kNA], accumulators done,
+    // outlier copy landed
+    const uint32_t bempty = sb + F::kBars, xfull = bempty + 8 * kNB, aempty = xfull + 8 * kNA,
+                   dfull = aempty + 8 * kNA, ocopy = dfull + 8;
     uint32_t* flags = reinterpret_cast<uint32_t*>(smem + F::kBars + 8 * F::kNBars);
     volatile uint32_t* abort_flag = flags + 1;
+    // per ring slot, the arrivals of the warps that fill it (dequantising warps for a
+    // B slot, activation warps for an A slot), counted over the slot's rounds: round
+    // r of a slot is ready at (r + 1) x warps (no warp reaches the next round before
+    // the MMAs of this one have freed the slot).  The issuing thread polls these with
+    // plain acquire loads: an mbarrier wait right after its commits was measured to
+    // hold it until the tensor core had drained (the MMAs ran ~30 % of the time)
+    const uint32_t bready = smem_u32(flags + 16), aready = bready + 4 * kNB;
     volatile int* xissued = reinterpret_cast<volatile int*>(flags + 4);  // X stages whose copies were issued
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int C = a.C, U = a.U, Uc = a.Uc, Ud = a.Ud;
+    const int C = a.C, U = a.U, Ut = a.Ut;
     const int cl = static_cast<int>(blockIdx.x) / C, rank = static_cast<int>(blockIdx.x) % C;
     int t0, t1;
     cluster_tiles(a.T, a.G, cl, &t0, &t1);
-    const long long units = static_cast<long long>(t1 - t0) * Uc;
+    const long long units = static_cast<long long>(t1 - t0) * Ut;
     long long lu0, lu1;
     rank_range(units, C, rank, &lu0, &lu1);
-    const int u0 = static_cast<int>(lu0), u1 = static_cast<int>(lu1);   // this CTA's chunk units
-    const int ncu = u1 - u0;
-    // stages of chunk unit u: dense chunks cover K in 256-k steps, outlier chunks
-    // the outlier columns in 256-column steps
-    auto chunk_stages = [&](int u) {
-        const int c = u % Uc;
-        return c < Ud ? min(kChunkStages, U - kChunkStages * c) : min(kChunkStages, a.OS - kChunkStages * (c - Ud));
-    };
-    int nst = 0;
-    for (int u = u0; u < u1; ++u) nst += chunk_stages(u);
-    const int first_tile = t0 + (ncu > 0 ? u0 / Uc : 0);
-    const int nbands = ncu > 0 ? (u1 - 1) / Uc - u0 / Uc + 1 : 0;   // tiles touched (<= 2)
+    // this CTA's stages: units [u0, u1) of the cluster, unit u = stage u % Ut of tile
+    // t0 + u / Ut (stage c < U: k in [64 c, 64 c + 64); c >= U: outlier columns
+    // [64 (c - U), 64 (c - U) + 64))
+    const int u0 = static_cast<int>(lu0), u1 = static_cast<int>(lu1);
+    const int nst = u1 - u0;
+    const int first_tile = t0 + (nst > 0 ? u0 / Ut : 0);
+    const int nbands = nst > 0 ? (u1 - 1) / Ut - u0 / Ut + 1 : 0;   // tiles touched (<= 2)
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(flags)),
@@ -336,17 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.n_out > 0)
         for (int i = tid; i < static_cast<int>((a.K + 31) / 32); i += kThreads) omask[i] = 0u;
     if (tid == 32) {
-        for (int i = 0; i < F::kNBars; ++i) {
-            const uint32_t bar = bfull + 8 * i;
-            // arrivals: the dequantising warps, the reordering warps, a copy (1, with
-            // the byte count), one tensor-core commit, or one per MMA warp
-            const uint32_t count = bar < bempty                     ? kDqWarps
-                                   : (bar >= afull && bar < aempty) ? kActWarps
-                                   : bar == dfull                   ? kIssuers
-                                                                    : 1;
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-        }
+        for (int i = 0; i < F::kNBars; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bempty + 8 * i) : "memory");
         *abort_flag = 0;
+        for (int i = 0; i < kNB + kNA; ++i) flags[16 + i] = 0u;
         *xissued = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -392,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
     };
-    auto arrive = [&](uint32_t bar) {
-        asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    auto count_up = [&](uint32_t counter) {
+        asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(counter) : "memory");
     };
     auto commit = [&](uint32_t bar) {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -411,23 +412,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ activation copies
         if (lane == 0) {
             asm volatile("griddepcontrol.wait;" ::: "memory");   // X may be written by the previous kernel
-            int i = 0, cu = u0, cj = 0;
-            for (; i < nst; ++i) {
-                const int c = cu % Uc, s = kChunkStages * c + cj;
-                if (++cj == chunk_stages(cu)) {
-                    cj = 0;
-                    ++cu;
-                }
+            int i = 0, c = u0 % Ut;
+            for (; i < nst; ++i, c = c + 1 == Ut ? 0 : c + 1) {
                 const int as = i % kNA;
                 if (i >= kNA && !wait(aempty + 8 * as, ((i - kNA) / kNA) & 1)) break;
-                if (c < Ud) {
+                if (c < U) {
                     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(xfull + 8 * as),
                                  "r"(static_cast<uint32_t>(a.Mr * 128))
                                  : "memory");
                     asm volatile(
                         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
                         " [%0], [%1, {%2, %3}], [%4];" ::"r"(sb + F::kA + as * kAStage),
-                        "l"(&maps.x), "r"(s * kStageK), "r"(0), "r"(xfull + 8 * as)
+                        "l"(&maps.x), "r"(c * kStageK), "r"(0), "r"(xfull + 8 * as)
                         : "memory");
                 } else {
                     // outlier stage: the activation warps gather its A stage; the slot is free
@@ -440,11 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------------ tensor-core issue
         // one thread, stages in order (D sums them in a fixed order); its waits poll
-        // with test_wait, bounded like every other wait
-        auto poll = [&](uint32_t bar, uint32_t parity) -> bool {
-            if (mbar_test_wait(bar, parity)) return true;
+        // the ready counters, bounded like every other wait
+        auto poll = [&](uint32_t counter, uint32_t target) -> bool {
+            if (ld_acquire_u32(counter) >= target) return true;
             const uint64_t w0 = global_ns();
-            while (!mbar_test_wait(bar, parity)) {
+            while (ld_acquire_u32(counter) < target) {
                 if (*abort_flag) return false;
                 if (global_ns() - w0 > kWaitLimitNs) {
                     *abort_flag = 1;
@@ -455,56 +451,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         if (lane == 0) {
-            int cu = u0, cj = 0;   // chunk unit and stage of stage i
-            for (int i = 0; i < nst; ++i) {
-                const int t = t0 + cu / Uc;
-                if (++cj == chunk_stages(cu)) {
-                    cj = 0;
-                    ++cu;
-                }
-                const int as = i % kNA, bs = i % kNB;
-                bool ok = poll(afull + 8 * as, (i / kNA) & 1) &&
-                          poll(bfull + 8 * bs, (i / kNB) & 1);
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                if (ok && !*abort_flag) {
-                    const uint32_t a0 = sb + F::kA + as * kAStage, b0 = sb + F::kB + bs * kBStage;
-                    const uint32_t d = tmem + (t == first_tile ? 0u : static_cast<uint32_t>(kTileRows));
+            int i = 0, as = 0, bs = 0;          // stage, its A and B slots
+            uint32_t ra = kActWarps, rb = kDqWarps;   // arrivals that make slots as, bs ready
+            for (int c = u0 % Ut, t = first_tile; i < nst; ++i, c = c + 1 == Ut ? 0 : c + 1) {
+                if (c == 0 && i > 0) ++t;
+                const uint32_t d = tmem + (t == first_tile ? 0u : static_cast<uint32_t>(kTileRows));
+                {
+                    bool ok = poll(aready + 4 * as, ra) && poll(bready + 4 * bs, rb);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    if (ok) {
+                        const uint64_t da = smem_desc_sw128(sb + F::kA + as * kAStage),
+                                       db = smem_desc_sw128(sb + F::kB + bs * kBStage);
 #pragma unroll
-                    for (int ks = 0; ks < kStageK / 16; ++ks)
-                        asm volatile(
-                            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-                            "l"(smem_desc_sw128(a0 + 32 * ks)), "l"(smem_desc_sw128(b0 + 32 * ks)), "r"(kIdesc)
-                            : "memory");
+                        for (int ks = 0; ks < kStageK / 16; ++ks)   // +32 bytes of K per MMA
+                            asm volatile(
+                                "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                                "l"(da + 2 * ks), "l"(db + 2 * ks), "r"(kIdesc)
+                                : "memory");
+                    }
+                    // always commit, so that every wait on these stages completes
+                    commit(bempty + 8 * bs);
+                    commit(aempty + 8 * as);
+                    if (++as == kNA) {
+                        as = 0;
+                        ra += kActWarps;
+                    }
+                    if (++bs == kNB) {
+                        bs = 0;
+                        rb += kDqWarps;
+                    }
                 }
-                // always commit, so that every wait on these stages completes
-                commit(bempty + 8 * bs);
-                commit(aempty + 8 * as);
             }
             if (nst > 0) commit(dfull);   // tracks every tensor-core operation of the CTA
         }
         __syncwarp();
-    } else if (warp >= kWarpAct) {
+    } else if ((warp & 3) == 3) {
         // ------------------------------------------------------------------ A stages: order, mask, gather
         // dense stage: the copied X in the codes' decode order, outlier channels
         // zeroed (x~); outlier stage: x[idx_j] of its 64 outlier columns, in order
         {
-            const int m = 32 * (warp - kWarpAct) + lane;   // A row: 128 bytes at its swizzled place
+            const int m = 32 * (warp == kWarpAct ? 0 : 1) + lane;   // A row: 128 bytes at its swizzled place
             const uint32_t arow = static_cast<uint32_t>((m >> 3) * 1024 + (m & 7) * 128), asw = static_cast<uint32_t>(m & 7);
-            int cu = u0, cj = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int c = cu % Uc, jj = cj;
-                if (++cj == chunk_stages(cu)) {
-                    cj = 0;
-                    ++cu;
-                }
+            for (int i = 0, c = u0 % Ut; i < nst; ++i, c = c + 1 == Ut ? 0 : c + 1) {
                 const int as = i % kNA;
                 const bool ok = warp_wait(xfull + 8 * as, (i / kNA) & 1, true);
                 if (ok && !*abort_flag && m < a.Mr) {
                     const uint32_t row = sb + F::kA + as * kAStage + arow;
                     uint32_t w[32];
-                    if (c < Ud) {
-                        const int s = kChunkStages * c + jj;   // k in [64 s, 64 s + 64)
+                    if (c < U) {
+                        const int s = c;   // k in [64 s, 64 s + 64)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const uint4 v = lds128(row + ((j ^ asw) << 4));
@@ -533,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 8; ++e) w[8 * blk + e] = o[e];
                         }
                     } else {
-                        const int j0 = kStageK * (kChunkStages * (c - Ud) + jj);   // first outlier column
+                        const int j0 = kStageK * (c - U);   // first outlier column
                         const unsigned short* xr = reinterpret_cast<const unsigned short*>(a.x) + m * a.ldx;
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
@@ -558,42 +554,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor core
                 }
                 __syncwarp();
-                if (lane == 0) arrive(afull + 8 * as);
+                if (lane == 0) count_up(aready + 4 * as);
             }
         }
     } else {
         // ------------------------------------------------------------------ dequantisation -> B stages
         // thread = weight row n of the tile (row block n / 4, row n % 4); its codes and
         // metadata come straight from global memory into registers, one chunk ahead
-        const int n = tid, rbl = n >> 2, r = n & 3;
+        const int dw = dq_index(warp), n = 32 * dw + lane, rbl = n >> 2, r = n & 3;
         const uint32_t brow = static_cast<uint32_t>((n >> 3) * 1024 + (n & 7) * 128);   // row n of a B stage
         const uint32_t sw = static_cast<uint32_t>(n & 7);                               // its 128-byte swizzle
         const uint32_t lut_lo = a.lut_lo, lut_hi = a.lut_hi;
         constexpr int CV = F::kCodeVecs;
-        // row n's record of dense chunk unit u (nullptr past the matrix, and for
-        // outlier chunks: zero codes and metadata)
-        auto rec_of = [&](int u, int* cc) -> const uint8_t* {
-            const int t = t0 + u / Uc, c = u % Uc, rb = t * kTileRb + rbl;
-            *cc = c % kChunksPerRec;
-            if (rb >= a.n_rb || c >= Ud) return nullptr;
-            return a.area + static_cast<long long>(rb) * a.rb_bytes +
-                   static_cast<long long>(c / kChunksPerRec) * F::kRecBytes;
+        // The stages are consumed in groups: a group is the CTA's run of stages inside
+        // one chunk (4 dense stages = 256 k, or 4 outlier stages = 256 columns).  Group
+        // starting at unit g ends where the chunk does (or at u1):
+        auto group_end = [&](int g) -> int {
+            const int c = g % Ut;
+            const int ce = c < U ? min(c - c % kChunkStages + kChunkStages, U)
+                                 : U + min(c - U - (c - U) % kChunkStages + kChunkStages, Ut - U);
+            return min(g + (ce - c), u1);
         };
-        // the chunk's codes (CV x 16 B) and metadata words: 4 S words + 4 Z words
-        auto load_chunk = [&](int u, uint4 (&q)[CV], uint4& m0, uint4& m1) {
-            int cc;
-            const uint8_t* rec = rec_of(u, &cc);
-            if (rec) {
-                const uint8_t* codes = rec + r * F::kRowCodeBytes + cc * F::kChunkRowBytes;
+        // copies of the dense group at unit g into raw slot `slot`: of the chunk, the
+        // codes of the group's stages (16 B a row and stage; 4 lanes a row: whole 32-byte
+        // sectors) and the chunk's S and Z (lane = row)
+        auto copy_group = [&](int g, int slot_i) {
+            const int t = t0 + g / Ut, c = g % Ut;
+            if (c >= U) return;
+            const int p0 = c % kChunkStages, p1 = p0 + (group_end(g) - g);   // parts (stages) to copy
+            const uint32_t slot = sb + F::kRaw + slot_i * F::kRawStage;
+            const int cc = (c / kChunkStages) % kChunksPerRec;
+            const long long rec_off = static_cast<long long>(c / (kChunkStages * kChunksPerRec)) * F::kRecBytes;
 #pragma unroll
-                for (int v = 0; v < CV; ++v) q[v] = ldg128(codes + 16 * v);
-                m0 = ldg128(rec + F::kMeta0Off + r * 64 + 16 * cc);
-                m1 = ldg128(rec + F::kMeta1Off + r * 64 + 16 * cc);
-            } else {
-#pragma unroll
-                for (int v = 0; v < CV; ++v) q[v] = make_uint4(0u, 0u, 0u, 0u);
-                m0 = m1 = make_uint4(0u, 0u, 0u, 0u);
+            for (int v = 0; v < F::kCodeVecs; ++v) {
+                const int rw = 8 * v + (lane >> 2), part = lane & 3, nr = 32 * dw + rw;
+                const int rb = t * kTileRb + (nr >> 2);
+                if (rb < a.n_rb && part >= p0 && part < p1)
+                    cp_async16(slot + nr * 64 + (((part + (rw >> 1)) & 3) << 4),
+                               a.area + static_cast<long long>(rb) * a.rb_bytes + rec_off +
+                                   (nr & 3) * F::kRowCodeBytes + cc * F::kChunkRowBytes + 16 * part,
+                               16u);
             }
+            const int rb = t * kTileRb + rbl;
+            const bool in = rb < a.n_rb;   // rows past the matrix: zero S and Z, so zero weights
+            const uint8_t* rec = a.area + (in ? static_cast<long long>(rb) * a.rb_bytes + rec_off + r * 64 + 16 * cc : 0);
+            cp_async16(slot + F::kRawS + 16 * n, rec + (in ? F::kMeta0Off : 0), in ? 16u : 0u);
+            cp_async16(slot + F::kRawZ + 16 * n, rec + (in ? F::kMeta1Off : 0), in ? 16u : 0u);
         };
         // row n's FP16 outlier values of outlier stage os (64 columns) and where they sit
         auto out_row = [&](int t, int os) -> const uint8_t* {
@@ -604,53 +610,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                    static_cast<long long>(o) * (lbq::kOutlierCols * lbq::kRowsPerBlock * 2) + r * cols * 2 +
                    (j0 % lbq::kOutlierCols) * 2;
         };
-        auto prefetch_chunk = [&](int u) {
-            int cc;
-            const uint8_t* rec = rec_of(u, &cc);
-            if (u % Uc >= Ud) {
-                const int t = t0 + u / Uc, os0 = kChunkStages * (u % Uc - Ud);
-                for (int jj = 0; jj < chunk_stages(u); ++jj) {
-                    const uint8_t* p = out_row(t, os0 + jj);
+        // L2 prefetch of the group at unit g: row n's lines
+        auto prefetch_group = [&](int g) {
+            const int t = t0 + g / Ut, c = g % Ut, rb = t * kTileRb + rbl;
+            if (rb >= a.n_rb) return;
+            if (c >= U) {
+                for (int e = g; e < group_end(g); ++e) {
+                    const uint8_t* p = out_row(t, c - U + (e - g));
                     if (p) asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
                 }
+                return;
             }
-            if (rec) {
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + r * F::kRowCodeBytes + cc * F::kChunkRowBytes));
-                if (cc == 0 && r == 0) {
-                    // the row block's S and Z lines of the record (512 B)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 128));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 256));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 384));
-                }
+            const int cc = (c / kChunkStages) % kChunksPerRec;
+            const uint8_t* rec = a.area + static_cast<long long>(rb) * a.rb_bytes +
+                                 static_cast<long long>(c / (kChunkStages * kChunksPerRec)) * F::kRecBytes;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + r * F::kRowCodeBytes + cc * F::kChunkRowBytes));
+            if (r == 0 && (cc == 0 || g == u0)) {
+                // the row block's S and Z lines of the record (512 B)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 128));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 256));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(rec + F::kMeta0Off + 384));
             }
         };
-        uint4 q[CV], qn[CV], m0, m1, m0n, m1n;
-        if (ncu > 0) load_chunk(u0, qn, m0n, m1n);   // ahead of the prefetches in the memory queues
-        for (int j = 1; j < F::kPF && j < ncu; ++j) prefetch_chunk(u0 + j);
-        int ist = 0;        // stage index of the chunk's first stage
+        int gc = u0;   // next group to copy
+        for (int j = 0; j < kNR - 1; ++j) {
+            if (gc < u1) {
+                copy_group(gc, j);
+                gc = group_end(gc);
+            }
+            cp_async_commit();
+        }
+        int gp = u0;   // next group to prefetch into L2
+        for (int j = 0; j < F::kPF && gp < u1; ++j) {
+            if (j > 0) prefetch_group(gp);
+            gp = group_end(gp);
+        }
+        int is = 0;         // stage index
         int n_copies = 0;   // outlier copies issued (warp 0, lane 0)
-        for (int j = 0; j < ncu; ++j) {
-            const int u = u0 + j, nsc = chunk_stages(u);
+        for (int g = u0, j = 0; g < u1; ++j) {
+            const int ge = group_end(g), t = t0 + g / Ut, c0 = g % Ut;
+            __syncwarp();   // every lane has read the slot that the next copies refill
+            if (gc < u1) {
+                copy_group(gc, (j + kNR - 1) % kNR);
+                gc = group_end(gc);
+            }
+            cp_async_commit();
+            if (gp < u1) {
+                prefetch_group(gp);
+                gp = group_end(gp);
+            }
+            cp_async_wait<kNR - 1>();   // this lane's copies of group j have landed
+            __syncwarp();               // and every lane's
+            uint4 q[CV], m0, m1;
+            {
+                const uint32_t slot = sb + F::kRaw + (j % kNR) * F::kRawStage;
 #pragma unroll
-            for (int v = 0; v < CV; ++v) q[v] = qn[v];
-            m0 = m0n;
-            m1 = m1n;
-            if (j + 1 < ncu) load_chunk(u + 1, qn, m0n, m1n);
-            if (j + F::kPF < ncu) prefetch_chunk(u + F::kPF);
+                for (int v = 0; v < CV; ++v) q[v] = lds128(slot + n * 64 + (((v + (n >> 1)) & 3) << 4));
+                m0 = lds128(slot + F::kRawS + 16 * n);
+                m1 = lds128(slot + F::kRawZ + 16 * n);
+            }
+            const int jj0 = c0 < U ? c0 % kChunkStages : (c0 - U) % kChunkStages;   // first stage in the chunk
 #pragma unroll
             for (int jj = 0; jj < kChunkStages; ++jj) {
-                if (jj >= nsc) break;
-                const int is = ist + jj, bs = is % kNB;
+                if (jj < jj0 || jj >= jj0 + (ge - g)) continue;
+                const int bs = is % kNB;
                 const bool ok = warp_wait(bempty + 8 * bs, ((is - kNB) / kNB) & 1, is >= kNB);
                 const uint32_t bst = sb + F::kB + bs * kBStage + brow;
-                if (u % Uc >= Ud) {
+                if (c0 >= U) {
                     // outlier stage: the tile's 256 rows x 64 FP16 outlier values go straight
                     // into the B stage (the copy writes the swizzled layout); warp 0 issues the
                     // copy and waits for it to land before its arrival, so that no copy is in
                     // flight when the CTA ends, whatever happened
                     if (lane == 0 && warp == 0 && ok && !*abort_flag) {
-                        const int t = t0 + u / Uc, j0 = kStageK * (kChunkStages * (u % Uc - Ud) + jj);
+                        const int j0 = kStageK * (c0 - U - jj0 + jj);
                         const int o = j0 / lbq::kOutlierCols, col = j0 % lbq::kOutlierCols;
                         const uint32_t dst = sb + F::kB + bs * kBStage;
                         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(ocopy), "r"(kBStage)
@@ -674,7 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ++n_copies;
                     }
                     __syncwarp();
-                    if (lane == 0) arrive(bfull + 8 * bs);
+                    if (lane == 0) count_up(bready + 4 * bs);
+                    ++is;
                     continue;
                 }
                 if (ok && !*abort_flag) {
@@ -682,9 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t Sw = u4w(m0, jj), Zw = u4w(m1, jj);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const int g = v >> 1;   // group of the stage
-                        const uint32_t S2 = ((Sw >> (16 * g)) & 0xFFFFu) * 0x00010001u;
-                        const uint32_t Z2 = ((Zw >> (16 * g)) & 0xFFFFu) * 0x00010001u;
+                        const int qg = v >> 1;   // 32-k quantisation group of the stage
+                        const uint32_t S2 = ((Sw >> (16 * qg)) & 0xFFFFu) * 0x00010001u;
+                        const uint32_t Z2 = ((Zw >> (16 * qg)) & 0xFFFFu) * 0x00010001u;
                         uint32_t o[8];
                         w2_word(u4w(qs, v), S2, Z2, lut_lo, lut_hi, o);
                         sts128(bst + (((2 * v) ^ sw) << 4), o[0], o[1], o[2], o[3]);
@@ -694,10 +728,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the B stage is read by the tensor core (async proxy)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) arrive(bfull + 8 * bs);
+                if (lane == 0) count_up(bready + 4 * bs);
+                ++is;
             }
-            ist += nsc;
+            g = ge;
         }
+        cp_async_wait<0>();   // no copy outlives the loop, whatever happened
     }
 
     // ---------------------------------------------------------------------- epilogue
@@ -715,10 +751,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    // contributors of tile t: the ranks whose ranges hold its first and last chunk
+    // contributors of tile t: the ranks whose ranges hold its first and last stage
     auto contributors = [&](int t, int* rlo, int* rhi) {
-        *rlo = rank_of(units, C, static_cast<long long>(t - t0) * Uc);
-        *rhi = rank_of(units, C, static_cast<long long>(t - t0 + 1) * Uc - 1);
+        *rlo = rank_of(units, C, static_cast<long long>(t - t0) * Ut);
+        *rhi = rank_of(units, C, static_cast<long long>(t - t0 + 1) * Ut - 1);
     };
     auto store_y = [&](int m, long long n, float v) {
         if (a.y_f32)
@@ -776,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (w4 <= 0) continue;
             // the contributors' band of this tile: 0, except for the first contributor
             // when its range starts in the tile before
-            const int bp_lo = t0 + static_cast<int>((units * rlo / C) / Uc) < t ? 1 : 0;
+            const int bp_lo = t0 + static_cast<int>((units * rlo / C) / Ut) < t ? 1 : 0;
             const int ne = a.M * w4;
             for (int e0 = tid; e0 < ne; e0 += 2 * kThreads) {
                 // two elements a thread, every load of both in flight, then the sums in rank order
@@ -915,11 +951,11 @@ lbq_status active_clusters(int max_smem, const int** out) {
 
 namespace lbq {
 
-// Work plan of the tensor-core kernel over T tiles of Uc chunks: the cluster
+// Work plan of the tensor-core kernel over T tiles of Ut stages: the cluster
 // size C and cluster count G that give the fewest chunks to the busiest CTA,
 // with every CTA's range spanning at most as many tiles as the accumulator has
 // lane bands.  False when no cluster size fits.
-bool mma_plan(int T, int Uc, int bands, const int* active, int* C_out, int* G_out, int* load_out) {
+bool mma_plan(int T, int Ut, int bands, const int* active, int* C_out, int* G_out, int* load_out) {
     int bestC = 0, bestG = 0;
     long long best = -1;
     for (int c = 1; c <= kMaxCluster; ++c) {
@@ -931,12 +967,12 @@ bool mma_plan(int T, int Uc, int bands, const int* active, int* C_out, int* G_ou
         for (int cl = 0; cl < g && fits; ++cl) {
             int t0, t1;
             cluster_tiles(T, g, cl, &t0, &t1);
-            const long long units = static_cast<long long>(t1 - t0) * Uc;
+            const long long units = static_cast<long long>(t1 - t0) * Ut;
             for (int r = 0; r < c; ++r) {
                 long long u0, u1;
                 rank_range(units, c, r, &u0, &u1);
                 if (u1 - u0 > load) load = u1 - u0;
-                if (u1 > u0 && (u1 - 1) / Uc - u0 / Uc + 1 > bands) fits = false;
+                if (u1 > u0 && (u1 - 1) / Ut - u0 / Ut + 1 > bands) fits = false;
             }
         }
         // fewer chunks per CTA wins; on a tie the smaller cluster (less reduction)
@@ -973,14 +1009,14 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int32_t n_out
     // chunk units of a tile: the dense chunks (256 k each), then the outlier chunks
     // (256 outlier columns each, in 64-column stages)
     const int U = static_cast<int>(K / kStageK), Ud = (U + kChunkStages - 1) / kChunkStages;
-    const int OS = (n_out + kStageK - 1) / kStageK, Uc = Ud + (OS + kChunkStages - 1) / kChunkStages;
+    const int OS = (n_out + kStageK - 1) / kStageK, Ut = U + OS;
     const int OT = static_cast<int>(L.outlier_records);
     const int cols_last = n_out > 0 ? (n_out + lbq::kOutlierColAlign - 1) / lbq::kOutlierColAlign *
                                               lbq::kOutlierColAlign - (OT - 1) * lbq::kOutlierCols
                                     : 0;
     int slab = T, C = 0, G = 0, load = 0;
-    while (slab > 1 && !mma_plan(slab, Uc, 2, active, &C, &G, &load)) slab = (slab + 1) / 2;
-    if (!mma_plan(slab, Uc, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
+    while (slab > 1 && !mma_plan(slab, Ut, 2, active, &C, &G, &load)) slab = (slab + 1) / 2;
+    if (!mma_plan(slab, Ut, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
     if (launches) {
         *launches += (T + slab - 1) / slab;
         return LBQ_OK;
@@ -998,7 +1034,7 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int32_t n_out
     uint8_t* b = static_cast<uint8_t*>(const_cast<void*>(packed));
     for (int ts = 0; ts < T; ts += slab) {
         const int tiles = T - ts < slab ? T - ts : slab;
-        if (!mma_plan(tiles, Uc, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
+        if (!mma_plan(tiles, Ut, 2, active, &C, &G, &load)) return LBQ_ERR_SHAPE;
         const long long n0 = static_cast<long long>(ts) * kTileRows;
         const long long Ns = N - n0 < static_cast<long long>(tiles) * kTileRows ? N - n0
                                                                                  : static_cast<long long>(tiles) * kTileRows;
@@ -1020,7 +1056,7 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int32_t n_out
         a.U = U;
         a.Ud = Ud;
         a.OS = OS;
-        a.Uc = Uc;
+        a.Ut = Ut;
         a.n_out = n_out;
         a.OT = OT;
         a.recs = static_cast<int>(L.records);
