@@ -496,10 +496,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0, c = u0 % Ut; i < nst; ++i, c = c + 1 == Ut ? 0 : c + 1) {
                 const int as = i % kNA;
                 const bool ok = warp_wait(xfull + 8 * as, (i / kNA) & 1, true);
-                if (ok && !*abort_flag && m < a.Mr) {
+                if (ok && !*abort_flag) {
                     const uint32_t row = sb + F::kA + as * kAStage + arow;
                     uint32_t w[32];
-                    if (c < U) {
+                    if (c >= U) {
+                        // outlier stage: the warp's lanes load the stage's 64 indices (2 each),
+                        // pass them round by shuffles, and every lane has all 64 of its row's
+                        // loads in flight at once (clamped addresses; invalid ones give 0)
+                        const int j0 = kStageK * (c - U);   // first outlier column
+                        const int ja = j0 + lane, jb = j0 + 32 + lane;
+                        const int ka = ja < a.n_out ? __ldg(a.idx + ja) : -1;
+                        const int kb = jb < a.n_out ? __ldg(a.idx + jb) : -1;
+                        const unsigned short* xr = reinterpret_cast<const unsigned short*>(a.x) + (m < a.M ? m : 0) * a.ldx;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int klo = __shfl_sync(0xffffffffu, e < 16 ? ka : kb, (2 * e) & 31);
+                            const int khi = __shfl_sync(0xffffffffu, e < 16 ? ka : kb, (2 * e + 1) & 31);
+                            const bool vlo = m < a.M && klo >= 0 && klo < a.K, vhi = m < a.M && khi >= 0 && khi < a.K;
+                            const uint32_t lo = __ldg(xr + (vlo ? klo : 0)), hi = __ldg(xr + (vhi ? khi : 0));
+                            w[e] = (vlo ? lo : 0u) | ((vhi ? hi : 0u) << 16);
+                        }
+                    } else if (m < a.Mr) {
                         const int s = c;   // k in [64 s, 64 s + 64)
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
@@ -528,30 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 8; ++e) w[8 * blk + e] = o[e];
                         }
-                    } else {
-                        const int j0 = kStageK * (c - U);   // first outlier column
-                        const unsigned short* xr = reinterpret_cast<const unsigned short*>(a.x) + m * a.ldx;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            uint32_t lo = 0u, hi = 0u;
-                            if (m < a.M) {
-                                const int j = j0 + 2 * e;
-                                if (j < a.n_out) {
-                                    const int k = __ldg(a.idx + j);
-                                    if (k >= 0 && k < a.K) lo = __ldg(xr + k);
-                                }
-                                if (j + 1 < a.n_out) {
-                                    const int k = __ldg(a.idx + j + 1);
-                                    if (k >= 0 && k < a.K) hi = __ldg(xr + k);
-                                }
-                            }
-                            w[e] = lo | (hi << 16);
-                        }
                     }
+                    if (m < a.Mr) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        sts128(row + ((j ^ asw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor core
+                        for (int j = 0; j < 8; ++j)
+                            sts128(row + ((j ^ asw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor core
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) count_up(aready + 4 * as);
