@@ -1,7 +1,8 @@
 """GPU parity of grouped launches (several independent problems in one kernel)
 against the FP64 oracle, through the C ABI: ragged mixed shapes element by
-element, the Llama-3-8B layer sweeps on sampled rows, small M, and a group too
-wide for one launch (split into back-to-back launches)."""
+element, small M, and a group too wide for one launch (split into back-to-back
+launches).  The full-size layer sweeps are checked on every row in
+test_fullsize_parity.py."""
 import numpy as np
 import pytest
 
@@ -49,31 +50,6 @@ def test_mixed_group_elementwise(lbq, kind, f32):
     assert lbq.device_error() == 0
     for (N, K, n_out), y, ref in zip(MIXED, ys, refs):
         assert_close(y.float().cpu().numpy(), ref, fp16_out=not f32, what="%s group %dx%d/%d" % (kind, N, K, n_out))
-
-
-@pytest.mark.parametrize("kind", ["w4", "w2"])
-def test_llama8b_layer_sweep_sampled(lbq, kind):
-    """One launch over the seven linears of a Llama-3-8B layer (configs 2 / 3)."""
-    cfg = 2 if kind == "w4" else 3
-    probs, checks = [], []
-    for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
-        W = synth.weights_heavy_cols(N, K, config_id=cfg, layer_id=li)
-        x = synth.activations(1, K, config_id=cfg, layer_id=li)[0]
-        if kind == "w4":
-            idx = np.zeros(0, np.int32)
-            blob, ob = lbq.pack_w4(W, idx), O.pack_w4
-        else:
-            idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=cfg, layer_id=li))
-            blob, ob = lbq.pack_w2cb(W, idx), O.pack_w2cb
-        y = torch.empty(N, dtype=torch.float32, device="cuda:0")
-        probs.append((to_dev(blob), N, K, len(idx), to_dev(x), y))
-        rows = _sampled_rows(N, np.random.default_rng(200 + li))
-        checks.append((name, y, rows, O.gemv(ob(W[rows], idx), x)))
-    lbq.gemv_grouped(lbq.LBQ_KIND_W4 if kind == "w4" else lbq.LBQ_KIND_W2CB, probs)
-    torch.cuda.synchronize()
-    assert lbq.device_error() == 0
-    for name, y, rows, ref in checks:
-        assert_close(y.cpu().numpy()[rows], ref, what="%s sweep %s" % (kind, name))
 
 
 @pytest.mark.parametrize("M", [2, 3, 8, 13])

@@ -115,3 +115,20 @@ def test_tolerance_function():
     assert O.fp16_ulp(np.array([1.0, 1024.0, 2.0 ** -20]))[0] == 2.0 ** -10
     assert O.fp16_ulp(np.array([1024.0]))[0] == 1.0
     assert O.fp16_ulp(np.array([2.0 ** -20]))[0] == 2.0 ** -24
+
+
+def test_row_chunks_equal_whole_matrix():
+    """The every-row parity tests compute the oracle over row chunks in worker
+    processes; rows are independent in the blob format, so the chunks'
+    products concatenate to the whole matrix's, bit for bit (both formats,
+    with outliers, a ragged last chunk)."""
+    import oracle_rows
+    rng = np.random.default_rng(5)
+    N, K = 70, 1088
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    X = rng.standard_normal((3, K)).astype(np.float16)
+    idx = np.sort(rng.choice(K, size=21, replace=False)).astype(np.int32)
+    with oracle_rows.pool(2) as ex:
+        for kind, pack in (("w4", O.pack_w4), ("w2", O.pack_w2cb)):
+            whole = O.gemm(pack(W, idx), X)
+            assert np.array_equal(oracle_rows.collect(oracle_rows.submit(ex, kind, W, idx, X, chunk=24)), whole)
