@@ -93,6 +93,11 @@ struct ProbArg {
     int out_last;          // bytes of the last one (4 rows x its columns, rounded up to 8, x 2 B)
     int n_out;
     int ub;                // index of its first row block in the launch's sequence
+    // selective refinement (M = 1): blob of (N, K), its n_sel chosen channels, column bytes
+    const uint8_t* rblob;  // or nullptr
+    const int32_t* ridx;
+    int nsel;
+    long long rcb;
 };
 
 struct GroupArgs {
@@ -890,6 +895,65 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
     }
     __syncthreads();
 
+    // selective refinement (M = 1; StrataFlux section 3, Eq. 2): the corrections
+    // sum_j x[idx_j] C[n, idx_j] of the CTA's rows, in FP32, each row's columns
+    // split over S slices of threads (columns j = s, s + S, ...: a fixed order);
+    // the combine below adds the slices in order.  The selection kernel before
+    // this one prefetched the columns into L2.
+    float* rcorr = reinterpret_cast<float*>(smem + P.ring);   // the stage ring is free now
+    const int RR = R * kTR, RT = RR < kThreads ? RR : kThreads, S = RR > 0 ? kThreads / RT : 0;
+    bool refined = false;
+    if (MB == 1 && R > 0)
+        for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) refined = refined || a.p[q].nsel > 0;
+    if (refined && S * RR * 4 > P.yacc - P.ring) {   // the host keeps row ranges within the ring
+        if (tid == 0) record_error(LBQ_ERR_SHAPE);
+        refined = false;
+    }
+    if (refined) {
+        const int sl = tid / RT;
+        for (int rl = tid % RT; rl < RR && sl < S; rl += RT) {
+            const int u = u0 + rl / kTR;
+            int q = qf;
+            while (q + 1 < a.count && a.p[q + 1].ub <= u) ++q;
+            const ProbArg& pa = a.p[q];
+            const long long n = static_cast<long long>(u - pa.ub) * kTR + rl % kTR;
+            float corr = 0.f;
+            if (pa.nsel > 0 && n < pa.N) {
+                const int g = static_cast<int>(n >> 5), b = static_cast<int>(n & 15), hi = static_cast<int>((n >> 4) & 1);
+                const long long sc_off = pa.N / 2 + 2 * g, z_off = pa.N / 2 + pa.N / 16 + (g >> 1);
+                const uint8_t* cols = pa.rblob + lbq::kRefineHeader;
+#pragma unroll 4
+                for (int j = sl; j < pa.nsel; j += S) {
+                    int c = pa.ridx[j];
+                    const bool ok_c = c >= 0 && c < pa.K;
+                    if (!ok_c) {
+                        record_error(LBQ_ERR_VALUE);
+                        c = 0;
+                    }
+                    const uint8_t* col = cols + static_cast<long long>(c) * pa.rcb;
+                    const uint32_t qb = col[g * 16 + b];
+                    const float sc = __half2float(*reinterpret_cast<const __half*>(col + sc_off));
+                    const uint32_t zb = col[z_off];
+                    const float xv = ok_c ? __half2float(pa.x[c]) : 0.f;
+                    const float qv = static_cast<float>(hi ? (qb >> 4) : (qb & 15u));
+                    const float zf = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
+                    corr = fmaf((qv - zf) * sc, xv, corr);   // (q - z) s is exact in FP32
+                }
+            }
+            rcorr[sl * RR + rl] = corr;
+        }
+        if (static_cast<int>(blockIdx.x) < a.count && tid == 32 && a.p[blockIdx.x].nsel > 0) {
+            const ProbArg& pa = a.p[blockIdx.x];
+            const unsigned* h = reinterpret_cast<const unsigned*>(pa.rblob);
+            const long long n_hdr = *reinterpret_cast<const long long*>(pa.rblob + 16);
+            const long long k_hdr = *reinterpret_cast<const long long*>(pa.rblob + 24);
+            if (h[0] != 0x5251424Cu || h[1] != 0x43345746u || h[2] != lbq::kRefineVersion || n_hdr != pa.N ||
+                k_hdr != pa.K)
+                record_error(LBQ_ERR_FORMAT);
+        }
+        __syncthreads();
+    }
+
     if (check_hdr) {
         const ProbArg& pa = a.p[blockIdx.x];
         const long long n_hdr = (static_cast<long long>(hdr1.y) << 32) | hdr1.x;
@@ -916,6 +980,8 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
         const long long n = static_cast<long long>(u - pa.ub) * kTR + r;
         if (n < pa.N && m < mrows) {
             y *= 1.f / kUnit;
+            if (refined && pa.nsel > 0)
+                for (int sl = 0; sl < S; ++sl) y += rcorr[sl * RR + rr];
             if (a.y_f32)
                 reinterpret_cast<float*>(pa.y)[m * pa.ldy + n] = y;
             else
@@ -1027,6 +1093,9 @@ struct HostProblem {
     int64_t ldx;
     void* y;
     int64_t ldy;
+    const void* refine = nullptr;   // selective refinement (M = 1)
+    const int32_t* ridx = nullptr;
+    int32_t nsel = 0;
 };
 
 // Fill the launch arguments of a group (without the partition).
@@ -1057,6 +1126,12 @@ lbq_status prepare_group(int kind, const HostProblem* P, int count, GroupArgs* a
                               : 0;
         p.n_out = P[i].n_out;
         p.ub = static_cast<int>(ub);
+        if (P[i].refine && P[i].nsel > 0) {
+            p.rblob = static_cast<const uint8_t*>(P[i].refine);
+            p.ridx = P[i].ridx;
+            p.nsel = P[i].nsel;
+            p.rcb = static_cast<long long>(lbq_refine_packed_bytes(P[i].N, 1)) - lbq::kRefineHeader;
+        }
         ub += (P[i].N + kTR - 1) / kTR;
         if (ub > INT32_MAX / 2) return LBQ_ERR_SHAPE;
     }
@@ -1306,8 +1381,8 @@ lbq_status run_one(int kind, const void* packed, int32_t M, int64_t N, int64_t K
     return run(kind, &p, 1, M, y_dtype, stream, flags, nullptr);
 }
 
-lbq_status grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M, lbq_dtype y_dtype,
-                   void* stream, uint32_t flags, int* launches) {
+lbq_status grouped(lbq_kind kind, const lbq_problem* problems, const lbq_refinement* refinements, int32_t count,
+                   int32_t M, lbq_dtype y_dtype, void* stream, uint32_t flags, int* launches) {
     if (!problems) return LBQ_ERR_NULL;
     if (kind != LBQ_KIND_W4 && kind != LBQ_KIND_W2CB) return LBQ_ERR_UNSUPPORTED;
     if (count < 1 || count > kMaxGroup) return LBQ_ERR_SHAPE;
@@ -1316,6 +1391,15 @@ lbq_status grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, in
         const lbq_problem& q = problems[i];
         if (q.reserved != 0) return LBQ_ERR_SHAPE;
         P[i] = HostProblem{q.packed, q.N, q.K, q.n_out, q.x, q.ldx, q.y, q.ldy};
+        if (refinements && refinements[i].refine) {
+            const lbq_refinement& r = refinements[i];
+            if (r.reserved != 0 || M != 1 || q.N % 64 || r.n_sel < 0 || r.n_sel > q.K) return LBQ_ERR_SHAPE;
+            if (r.n_sel > 0 && !r.idx) return LBQ_ERR_NULL;
+            if (!aligned(r.refine, 16) || (r.idx && !aligned(r.idx, 4))) return LBQ_ERR_ALIGN;
+            P[i].refine = r.refine;
+            P[i].ridx = r.idx;
+            P[i].nsel = r.n_sel;
+        }
     }
     return run(kind == LBQ_KIND_W4 ? kW4 : kW2, P, count, M, y_dtype, stream, flags, launches);
 }
@@ -1382,14 +1466,20 @@ lbq_status lbq_gemm_w2cb_outlier_smallM(const void* packed, int32_t M, int64_t N
 
 lbq_status lbq_gemv_grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
                             lbq_dtype y_dtype, void* stream, uint32_t flags) {
-    return grouped(kind, problems, count, M, y_dtype, stream, flags, nullptr);
+    return grouped(kind, problems, nullptr, count, M, y_dtype, stream, flags, nullptr);
+}
+
+lbq_status lbq_gemv_grouped_refined(lbq_kind kind, const lbq_problem* problems, const lbq_refinement* refinements,
+                                    int32_t count, lbq_dtype y_dtype, void* stream, uint32_t flags) {
+    if (!refinements) return LBQ_ERR_NULL;
+    return grouped(kind, problems, refinements, count, 1, y_dtype, stream, flags, nullptr);
 }
 
 lbq_status lbq_gemv_grouped_launches(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
                                      lbq_dtype y_dtype, int32_t* launches) {
     if (!launches) return LBQ_ERR_NULL;
     int n = 0;
-    const lbq_status st = grouped(kind, problems, count, M, y_dtype, nullptr, 0u, &n);
+    const lbq_status st = grouped(kind, problems, nullptr, count, M, y_dtype, nullptr, 0u, &n);
     *launches = st == LBQ_OK ? n : 0;
     return st;
 }

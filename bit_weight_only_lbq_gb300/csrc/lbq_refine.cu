@@ -95,8 +95,11 @@ __device__ void find_bin(const unsigned* hist, int nbins, unsigned remaining, in
     }
 }
 
-__global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half* __restrict__ x, int K, int k,
-                                                                   int32_t* __restrict__ idx) {
+// Selection of chunk `chunk` of x (the CTA's 1,024 threads, one channel each);
+// the chosen channels go to idx[chunk k ...] ascending and, when `sel_list` is
+// given, to sel_list[0 .. count) in shared memory.  Returns the count.
+__device__ int select_chunk(const __half* __restrict__ x, int K, int k, int32_t* __restrict__ idx, int chunk,
+                            int* sel_list) {
     // one histogram and one (bin, count above) slot per pass, so no pass waits
     // for the one before it to be done reading
     __shared__ __align__(16) unsigned hist[512 + 256 + 256];
@@ -104,10 +107,7 @@ __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half*
     __shared__ unsigned s_above[3];
     __shared__ unsigned warp_cnt[kChunk / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    // launched with programmatic dependent launch: x may come from the kernel before
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int base = blockIdx.x * kChunk;
+    const int base = chunk * kChunk;
     const int len = min(kChunk, K - base);
     const int kk = min(k, len);
     const bool valid = t < len;
@@ -146,7 +146,53 @@ __global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half*
     if (sel) {
         unsigned off = __popc(bal & ((1u << lane) - 1u));
         for (int w = 0; w < warp; ++w) off += warp_cnt[w];
-        idx[static_cast<long long>(blockIdx.x) * k + off] = base + t;
+        idx[static_cast<long long>(chunk) * k + off] = base + t;
+        if (sel_list) sel_list[off] = base + t;
+    }
+    return kk;
+}
+
+__global__ void __launch_bounds__(kChunk) lbq_refine_select_kernel(const __half* __restrict__ x, int K, int k,
+                                                                   int32_t* __restrict__ idx) {
+    // launched with programmatic dependent launch: x may come from the kernel before
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    (void)select_chunk(x, K, k, idx, blockIdx.x, nullptr);
+}
+
+// Several selections in one launch (a layer's activation vectors): CTA b takes
+// chunk b - chunk_ub[q] of problem q.  With a refinement blob, the CTA then
+// prefetches the chosen columns' records into L2, so that the GEMV that applies
+// them (lbq_gemv_grouped_refined, launched next) finds them there.
+struct SelectProb {
+    const __half* x;
+    int32_t* idx;
+    const uint8_t* refine;   // or nullptr
+    int K, k;
+    long long cb;            // refinement column bytes
+};
+struct SelectGroup {
+    int count;
+    int chunk_ub[LBQ_MAX_GROUP + 1];
+    SelectProb p[LBQ_MAX_GROUP];
+};
+
+__global__ void __launch_bounds__(kChunk) lbq_refine_select_grouped_kernel(const __grid_constant__ SelectGroup g) {
+    __shared__ int sel_list[lbq::kRefineMaxK];
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    int q = 0;
+    while (q + 1 < g.count && g.chunk_ub[q + 1] <= static_cast<int>(blockIdx.x)) ++q;
+    const SelectProb& pr = g.p[q];
+    const int kk = select_chunk(pr.x, pr.K, pr.k, pr.idx, blockIdx.x - g.chunk_ub[q], sel_list);
+    if (pr.refine) {
+        __syncthreads();
+        const int lines = static_cast<int>((pr.cb + 127) / 128);
+        for (int i = threadIdx.x; i < kk * lines; i += kChunk) {
+            const int c = sel_list[i / lines];
+            const uint8_t* p = pr.refine + lbq::kRefineHeader + static_cast<long long>(c) * pr.cb + 128ll * (i % lines);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
     }
 }
 
@@ -339,6 +385,38 @@ lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* i
     const unsigned grid = static_cast<unsigned>((K + kChunk - 1) / kChunk);
     return launch_pdl(reinterpret_cast<const void*>(&lbq_refine_select_kernel), grid, kChunk, stream,
                       static_cast<const __half*>(x_f16), static_cast<int>(K), k, idx);
+}
+
+lbq_status lbq_refine_select_grouped(const lbq_refine_select_problem* problems, int32_t count, void* stream) {
+    if (!problems) return LBQ_ERR_NULL;
+    if (count < 1 || count > LBQ_MAX_GROUP) return LBQ_ERR_SHAPE;
+    SelectGroup g;
+    memset(&g, 0, sizeof(g));
+    g.count = count;
+    int chunks = 0;
+    for (int i = 0; i < count; ++i) {
+        const lbq_refine_select_problem& q = problems[i];
+        if (!q.x || !q.idx) return LBQ_ERR_NULL;
+        if (q.reserved != 0 || q.K < 1 || q.K > lbq::kMaxK || q.k < 1 || q.k > lbq::kRefineMaxK) return LBQ_ERR_SHAPE;
+        if (q.refine && (q.N < 64 || q.N % 64 || q.N > INT32_MAX)) return LBQ_ERR_SHAPE;
+        if (!aligned(q.x, 2) || !aligned(q.idx, 4) || (q.refine && !aligned(q.refine, 16))) return LBQ_ERR_ALIGN;
+        SelectProb& p = g.p[i];
+        p.x = static_cast<const __half*>(q.x);
+        p.idx = q.idx;
+        p.refine = static_cast<const uint8_t*>(q.refine);
+        p.K = static_cast<int>(q.K);
+        p.k = q.k;
+        p.cb = q.refine ? static_cast<long long>(lbq_refine_packed_bytes(q.N, 1)) - lbq::kRefineHeader : 0;
+        g.chunk_ub[i] = chunks;
+        chunks += static_cast<int>((q.K + kChunk - 1) / kChunk);
+    }
+    g.chunk_ub[count] = chunks;
+    unsigned* err = nullptr;
+    int sms = 0;
+    const lbq_status st = lbq::device_context(&err, &sms);
+    if (st != LBQ_OK) return st;
+    return launch_pdl(reinterpret_cast<const void*>(&lbq_refine_select_grouped_kernel), static_cast<unsigned>(chunks),
+                      kChunk, stream, g);
 }
 
 lbq_status lbq_refine_apply(const void* refine, int64_t N, int64_t K, const void* x_f16, const int32_t* idx,

@@ -41,6 +41,7 @@ EXPORTS = (
     "lbq_selftest_wait_timeout", "lbq_device_error", "lbq_refine_packed_bytes", "lbq_pack_refine",
     "lbq_dequant_host", "lbq_refine_selected_count", "lbq_refine_select", "lbq_refine_apply",
     "lbq_refine_noalloc", "lbq_embed_gather", "lbq_kv_record_bytes", "lbq_kv_quantize", "lbq_kv_dequant",
+    "lbq_refine_select_grouped", "lbq_gemv_grouped_refined",
 )
 
 
@@ -55,6 +56,16 @@ class Layout(ctypes.Structure):
                 ("record_bytes", ctypes.c_uint64), ("records", ctypes.c_uint64),
                 ("outlier_record_bytes", ctypes.c_uint64), ("outlier_records", ctypes.c_uint64),
                 ("idx_offset", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64)]
+
+
+class SelectProblem(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("K", ctypes.c_int64), ("k", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("idx", ctypes.c_void_p), ("refine", ctypes.c_void_p), ("N", ctypes.c_int64)]
+
+
+class Refinement(ctypes.Structure):
+    _fields_ = [("refine", ctypes.c_void_p), ("idx", ctypes.c_void_p), ("n_sel", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class Problem(ctypes.Structure):
@@ -125,6 +136,9 @@ def lib():
             "lbq_kv_record_bytes": (c_sz, [c_i64]),
             "lbq_kv_quantize": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_vp]),
             "lbq_kv_dequant": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_vp]),
+            "lbq_refine_select_grouped": (ctypes.c_int, [ctypes.POINTER(SelectProblem), c_i32, c_vp]),
+            "lbq_gemv_grouped_refined": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(Problem),
+                                                        ctypes.POINTER(Refinement), c_i32, ctypes.c_int, c_vp, c_u32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -305,6 +319,31 @@ def refine_apply(refine, N: int, K: int, x, idx, n_sel: int, y, stream=None, y_d
     yd = _ydtype(y) if y_dtype is None else y_dtype
     _check(lib().lbq_refine_apply(_dev_ptr(refine), N, K, _dev_ptr(x), _dev_ptr(idx) if n_sel else None, n_sel,
                                   _dev_ptr(y), yd, _stream(stream)), "lbq_refine_apply")
+
+
+def refine_select_grouped(problems, stream=None):
+    """Several selections in one launch.  problems: sequence of (x, K, k, idx) or
+    (x, K, k, idx, refine, N) (refine: blob whose chosen columns are prefetched
+    into L2); device buffers."""
+    arr = (SelectProblem * len(problems))()
+    for i, p in enumerate(problems):
+        x, K, k, idx = p[:4]
+        refine, N = (p[4], p[5]) if len(p) > 4 else (None, 0)
+        arr[i] = SelectProblem(_dev_ptr(x), K, k, 0, _dev_ptr(idx), _dev_ptr(refine) if refine is not None else None, N)
+    _check(lib().lbq_refine_select_grouped(arr, len(problems), _stream(stream)), "lbq_refine_select_grouped")
+
+
+def gemv_grouped_refined(kind: int, problems, refinements, stream=None, pdl: bool = False,
+                         y_dtype: int | None = None):
+    """gemv_grouped (M = 1) with selective refinement in the same kernel.
+    refinements: one entry per problem, None or (refine, idx, n_sel) device buffers."""
+    arr, yd = _problems(problems, y_dtype)
+    ref = (Refinement * len(problems))()
+    for i, r in enumerate(refinements):
+        if r is not None:
+            ref[i] = Refinement(_dev_ptr(r[0]), _dev_ptr(r[1]) if r[2] else None, r[2], 0)
+    _check(lib().lbq_gemv_grouped_refined(kind, arr, ref, len(problems), yd, _stream(stream),
+                                          LBQ_FLAG_PDL if pdl else 0), "lbq_gemv_grouped_refined")
 
 
 def refine_noalloc(refine, N: int, K: int, k: int, x, y, stream=None, y_dtype: int | None = None):

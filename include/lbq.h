@@ -262,6 +262,29 @@ typedef struct {
 lbq_status lbq_gemv_grouped(lbq_kind kind, const lbq_problem* problems, int32_t count, int32_t M,
                             lbq_dtype y_dtype, void* stream, uint32_t flags);
 
+/* Grouped GEMV (M = 1) with selective refinement applied in the same kernel
+ * (StrataFlux paper, section 3 "Weight Refinement", Eq. 2):
+ *     y[n] = (the lbq_gemv_grouped result of the problem)[n] + sum_{j < n_sel} x[idx_j] C[n, idx_j]
+ * with the sum over j in FP32 and y rounded once to y_dtype.  refinements:
+ * host array parallel to problems (read during the call only); an entry with
+ * refine == NULL leaves its problem unrefined.  refine: device refinement blob
+ * of the problem's (N, K) (lbq_pack_refine, N % 64 == 0), 16-byte aligned;
+ * idx: device, n_sel channels in [0, K), written by an earlier kernel on the
+ * stream (lbq_refine_select / lbq_refine_select_grouped).  Each CTA adds the
+ * corrections of the rows it computes, so the refinement needs no launch of
+ * its own.  Errors: as lbq_gemv_grouped with M = 1; LBQ_ERR_SHAPE for N % 64,
+ * n_sel outside [0, K] or reserved != 0; an index outside [0, K) is skipped
+ * and reported as LBQ_ERR_VALUE, a refinement header mismatch as
+ * LBQ_ERR_FORMAT, both through lbq_device_error. */
+typedef struct {
+    const void* refine;   /* device refinement blob of the problem's (N, K), or NULL */
+    const int32_t* idx;   /* device, n_sel selected channels */
+    int32_t n_sel;
+    int32_t reserved;     /* must be 0 */
+} lbq_refinement;
+lbq_status lbq_gemv_grouped_refined(lbq_kind kind, const lbq_problem* problems, const lbq_refinement* refinements,
+                                    int32_t count, lbq_dtype y_dtype, void* stream, uint32_t flags);
+
 /* How many kernels lbq_gemv_grouped would launch for these arguments (1 when
  * the group fits one launch).  Validates exactly as lbq_gemv_grouped and reads
  * the current device's attributes, but launches nothing.
@@ -380,6 +403,26 @@ int64_t lbq_refine_selected_count(int64_t K, int32_t k);
  * LBQ_ERR_ALIGN (x 2-byte, idx 4-byte aligned), LBQ_ERR_UNSUPPORTED,
  * LBQ_ERR_CUDA. */
 lbq_status lbq_refine_select(const void* x_f16, int64_t K, int32_t k, int32_t* idx, void* stream);
+
+/* Device: several selections in ONE launch (a decode layer's activation
+ * vectors), each exactly lbq_refine_select of its (x, K, k, idx).  With a
+ * refinement blob `refine` of shape (N, K) given, the records of the chosen
+ * columns are also prefetched into L2 for the GEMV that applies them
+ * (lbq_gemv_grouped_refined, issued next on the stream).
+ * problems: host array of count descriptors (1 <= count <= LBQ_MAX_GROUP),
+ * read during the call only; device pointers with the alignment of
+ * lbq_refine_select (refine 16-byte aligned); reserved must be 0.
+ * Errors: LBQ_ERR_NULL, LBQ_ERR_SHAPE, LBQ_ERR_ALIGN, LBQ_ERR_CUDA. */
+typedef struct {
+    const void* x;        /* device, K FP16 */
+    int64_t K;
+    int32_t k;            /* channels per 1,024-channel chunk, 1..256 */
+    int32_t reserved;     /* must be 0 */
+    int32_t* idx;         /* device, lbq_refine_selected_count(K, k) int32 */
+    const void* refine;   /* device refinement blob of (N, K) to prefetch from, or NULL */
+    int64_t N;            /* rows of refine; ignored without it */
+} lbq_refine_select_problem;
+lbq_status lbq_refine_select_grouped(const lbq_refine_select_problem* problems, int32_t count, void* stream);
 
 /* Device: y[n] += sum_{j < n_sel} x[idx_j] C[n, idx_j] for the refinement blob
  * `refine` (device, 16-byte aligned) of shape (N, K); y (device, N values of
