@@ -672,12 +672,14 @@ def run_refinement(lbq, layer, dev, stream, replays=20):
         del g
         return statistics.median(ts)
 
+    rblobs = []
     for e in layer:
         if e["kind"] != "w4":
             continue
         N, K = e["N"], e["K"]
         R = (synth.weights_heavy_cols(N, K, config_id=2, layer_id=e["li"]) - lbq.dequant_host(e["blob"]))
         rblob = lbq.pack_refine(R.astype(np.float32))
+        rblobs.append(rblob)
         del R
         n_sel = lbq.refine_selected_count(K, REFINE_K)
         ncopy = max(2, min(64, -(-L2_ROTATION_BYTES // rblob.size)))
@@ -702,7 +704,55 @@ def run_refinement(lbq, layer, dev, stream, replays=20):
     assert lbq.device_error(stream) == 0
     torch.cuda.empty_cache()
     out["layer_us"] = round(total_us, 2)
+    out["fused_layer"] = run_refined_sweep(lbq, [e for e in layer if e["kind"] == "w4"], rblobs, dev, stream, timed)
     return out
+
+
+def run_refined_sweep(lbq, w4, rblobs, dev, stream, timed):
+    """The 4-bit layer sweep with refinement fused: one grouped selection launch
+    (the 7 activation vectors; chosen columns prefetched into L2) and one grouped
+    GEMV launch that adds each row's correction (lbq_gemv_grouped_refined),
+    against the plain grouped sweep, both over rotating copies of the weights and
+    refinement blobs (>= 512 MB) in a CUDA graph."""
+    import torch
+    ncp = max(2, -(-L2_ROTATION_BYTES // sum(len(e["blob"]) + len(r) for e, r in zip(w4, rblobs))))
+    blobs = [[torch.from_numpy(e["blob"]).to(dev) for e in w4] for _ in range(ncp)]
+    rbs = [[torch.from_numpy(r).to(dev) for r in rblobs] for _ in range(ncp)]
+    xs = [torch.from_numpy(np.ascontiguousarray(e["x"]).reshape(-1)).to(dev) for e in w4]
+    ys = [torch.empty(e["N"], dtype=torch.float32, device=dev) for e in w4]
+    nsel = [lbq.refine_selected_count(e["K"], REFINE_K) for e in w4]
+    idxs = [torch.empty(n, dtype=torch.int32, device=dev) for n in nsel]
+
+    def probs(c):
+        return [(blobs[c][i], e["N"], e["K"], 0, xs[i], ys[i]) for i, e in enumerate(w4)]
+
+    def plain(c):
+        lbq.gemv_grouped(lbq.LBQ_KIND_W4, probs(c), pdl=True, stream=stream)
+
+    def fused(c):
+        lbq.refine_select_grouped([(xs[i], e["K"], REFINE_K, idxs[i], rbs[c][i], e["N"]) for i, e in enumerate(w4)],
+                                  stream=stream)
+        lbq.gemv_grouped_refined(lbq.LBQ_KIND_W4, probs(c), [(rbs[c][i], idxs[i], nsel[i]) for i in range(len(w4))],
+                                 pdl=True, stream=stream)
+
+    def select_only(c):
+        lbq.refine_select_grouped([(xs[i], e["K"], REFINE_K, idxs[i], rbs[c][i], e["N"]) for i, e in enumerate(w4)],
+                                  stream=stream)
+
+    def gemv_only(c):
+        lbq.gemv_grouped_refined(lbq.LBQ_KIND_W4, probs(c), [(rbs[c][i], idxs[i], nsel[i]) for i in range(len(w4))],
+                                 pdl=True, stream=stream)
+
+    us_plain = timed(plain, list(range(ncp)))
+    us_fused = timed(fused, list(range(ncp)))
+    us_sel = timed(select_only, list(range(ncp)))
+    us_gemv = timed(gemv_only, list(range(ncp)))
+    assert lbq.device_error(stream) == 0
+    del blobs, rbs
+    torch.cuda.empty_cache()
+    return {"launches": 2, "us_plain_sweep": round(us_plain, 3), "us_refined_sweep": round(us_fused, 3),
+            "retained_throughput": round(us_plain / us_fused, 4), "copies": ncp,
+            "us_selection_alone": round(us_sel, 3), "us_refined_gemv_alone": round(us_gemv, 3)}
 
 
 # a decode step can only group linears whose inputs are ready together:
@@ -758,8 +808,9 @@ FMA_PEAK = 152 * 128 * 2.07e9       # FP32 FMA lanes of a GB300 (152 SMs x 128 a
 def run_smallm_sweep(lbq, dev, stream, replays=5):
     """Config 4 across M: the 4-bit gate (14336 x 4096) and down (4096 x 14336)
     projections at M = 2..64 (CUDA cores below 16, tensor cores from 16), the
-    2-bit ones with 3.5 % outlier columns (CUDA cores at every M) and without
-    outlier columns at M >= 16 (tensor cores).  Each configuration chained over
+    2-bit ones with 3.5 % outlier columns (CUDA cores below 16, tensor cores
+    from 16) and without outlier columns at M >= 16 (tensor cores).  Each
+    configuration chained over
     rotating copies (>= 512 MB) in a CUDA graph.  Next to the HBM fraction: the
     FP32-FMA fraction below M = 16 (one FMA per weight and activation row) and
     the dense FP16 tensor fraction from M = 16."""
@@ -781,7 +832,7 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
         W2 = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
         idx = lbq.select_outliers_impact(W2, synth.profile_vectors(K, config_id=3, layer_id=li), 0.035)
         b2o = lbq.pack_w2cb(W2, idx)
-        for M in (2, 4, 8, 16):
+        for M in (2, 4, 8, 16, 32, 64):
             cases.append(("w2", name, N, K, M, len(idx), b2o))
         b2 = lbq.pack_w2cb(W2, np.zeros(0, np.int32))
         for M in (16, 64):
@@ -818,7 +869,7 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
         nbytes = algorithmic_bytes(kind, N, K, n_out, M)
         gbs = nbytes / (us * 1e-6) / 1e9
         row = {"kind": kind, "linear": name, "N": N, "K": K, "M": M, "n_out": n_out,
-               "path": "tensor cores" if (M >= 16 and n_out == 0) else "CUDA cores",
+               "path": "tensor cores" if (M >= 16 and (n_out == 0 or kind == "w2")) else "CUDA cores",
                "us_per_call": round(us, 3), "GB_s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
         macs = M * N * K
         if row["path"] == "CUDA cores":

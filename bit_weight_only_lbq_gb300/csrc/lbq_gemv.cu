@@ -60,6 +60,7 @@ constexpr int kStagesM1 = 2, kStagesMB = 4;
 constexpr int kMaxGroup = LBQ_MAX_GROUP;               // problems per launch
 constexpr int kMaxGrid = 192;                          // CTAs per launch (>= SMs of a GB300)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kRefineBatchMax = 512;                   // refinement columns staged at once per CTA
 
 enum Kind { kW4 = 0, kW2 = 1 };
 
@@ -107,6 +108,7 @@ struct GroupArgs {
     int y_f32;
     int SPW;               // stages per warp
     int rb_cap;            // most row blocks any CTA owns
+    int rearly;            // refinement pieces staged before the main loop (after the CTA's staging)
     uint32_t lut_lo, lut_hi;   // 2-bit codebook: low / high bytes of the FP16 centroids
     int cta_ub[kMaxGrid + 1];  // CTA c owns row blocks [cta_ub[c], cta_ub[c + 1])
     ProbArg p[kMaxGroup];
@@ -283,6 +285,32 @@ __host__ __device__ inline FixedPlan fixed_plan(int NW, int stage, int SPW, int 
 __host__ __device__ inline int staging_bytes(int MB, int recs, int OT) {
     const int ng = recs * 32;
     return MB * ng * 64 + MB * ng * 4 + ng * 4 + MB * OT * kOutCols * 2;
+}
+
+// Selective refinement pieces of one column that cover rows [n0, n1) of an
+// N-row refinement blob, as 16-byte-aligned ranges from the column start: the
+// nibble bytes of groups g0 .. g0 + ng - 1 (16 B each), their FP16 scales
+// [s_lo, s_lo + ls) and their zero-point bytes [z_lo, z_lo + lz).
+struct RefPieces {
+    int g0, ng, ln, ls, lz;
+    long long s_lo, z_lo;
+    __host__ __device__ int bytes() const { return ln + ls + lz; }
+};
+__host__ __device__ inline RefPieces ref_pieces(long long N, long long n0, long long n1) {
+    RefPieces r;
+    r.g0 = static_cast<int>(n0 >> 5);
+    r.ng = static_cast<int>((n1 - 1) >> 5) - r.g0 + 1;
+    r.ln = 16 * r.ng;
+    r.s_lo = (N / 2 + 2 * r.g0) & ~15ll;
+    r.ls = static_cast<int>(((N / 2 + 2 * (r.g0 + r.ng) + 15) & ~15ll) - r.s_lo);
+    r.z_lo = (N / 2 + N / 16 + r.g0 / 2) & ~15ll;
+    r.lz = static_cast<int>(((N / 2 + N / 16 + (r.g0 + r.ng - 1) / 2 + 1 + 15) & ~15ll) - r.z_lo);
+    return r;
+}
+// Bytes of the early refinement area of a problem for rows [n0, n1):
+// channels (int), x pairs (u32), then the columns' pieces.
+__host__ __device__ inline int ref_area_bytes(long long N, long long n0, long long n1, int nsel) {
+    return round_up(8 * nsel, 16) + nsel * ref_pieces(N, n0, n1).bytes();
 }
 
 // ----------------------------------------------------------- item math
@@ -510,37 +538,46 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
     const int R = u1 - u0;
 
     // problems this CTA touches: qf .. qf + np - 1; its items (records and
-    // outlier records of its row blocks, in memory order)
-    int qf = 0;
-    while (qf + 1 < a.count && a.p[qf + 1].ub <= u0) ++qf;
-    int np = 0, n_items = 0;
-    if (R > 0)
-        for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) {
-            const int lo = max(u0, a.p[q].ub), hi = min(u1, unit_end(a, q));
-            n_items += (hi - lo) * ((a.p[q].recs + RPI - 1) / RPI + a.p[q].OT);
-            ++np;
+    // outlier records of its row blocks, in memory order).  Lane l of every warp
+    // reads problem l's scalars (at most 32 problems), so the launch parameters
+    // are fetched in one round instead of a chain of dependent reads (measured:
+    // ~1.8 us of prologue before), and the loops over problems become ballots and
+    // warp scans.
+    const bool lp = lane < a.count;
+    const int p_ub = lp ? a.p[lane].ub : INT_MAX;
+    const int p_end = lp ? (lane + 1 < a.count ? a.p[lane + 1].ub : a.nunits) : INT_MAX;
+    const int p_recs = lp ? a.p[lane].recs : 0, p_OT = lp ? a.p[lane].OT : 0;
+    const int qf = __popc(__ballot_sync(0xffffffffu, p_ub <= u0)) - 1;   // ub ascending, ub[0] = 0
+    const bool in_cta = R > 0 && lp && lane >= qf && p_ub < u1;
+    const int np = __popc(__ballot_sync(0xffffffffu, in_cta));
+    const int p_tpr = (p_recs + RPI - 1) / RPI + p_OT;                    // items per row block
+    const int p_items = in_cta ? (min(u1, p_end) - max(u0, p_ub)) * p_tpr : 0;
+    const int p_stg = in_cta ? staging_bytes(MB, p_recs, p_OT) : 0;
+    int items_incl = p_items, stg_incl = p_stg;                           // inclusive warp scans
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int vi = __shfl_up_sync(0xffffffffu, items_incl, d), vs = __shfl_up_sync(0xffffffffu, stg_incl, d);
+        if (lane >= d) {
+            items_incl += vi;
+            stg_incl += vs;
         }
+    }
+    const int n_items = __shfl_sync(0xffffffffu, items_incl, 31);
     // this warp's contiguous share of the items, and where it starts
     const int ib = static_cast<int>((static_cast<long long>(warp) * n_items) / NW);
     const int ie = static_cast<int>((static_cast<long long>(warp + 1) * n_items) / NW);
     const int my_items = ie - ib;
     int s_q = qf, s_stg = 0, s_u = u0, s_kk = 0;
     if (my_items > 0) {
-        int before = 0;
-        for (;;) {
-            const int lo = max(u0, a.p[s_q].ub), hi = min(u1, unit_end(a, s_q));
-            const int TPR = (a.p[s_q].recs + RPI - 1) / RPI + a.p[s_q].OT;
-            const int items = (hi - lo) * TPR;
-            if (ib < before + items) {
-                const int j = ib - before;
-                s_u = lo + j / TPR;
-                s_kk = j - (j / TPR) * TPR;
-                break;
-            }
-            before += items;
-            s_stg += staging_bytes(MB, a.p[s_q].recs, a.p[s_q].OT);
-            ++s_q;
-        }
+        // the problem whose items hold ib: the first lane whose inclusive count exceeds ib
+        const int sl = __ffs(__ballot_sync(0xffffffffu, in_cta && items_incl > ib)) - 1;
+        const int before = __shfl_sync(0xffffffffu, items_incl - p_items, sl);
+        const int tpr = __shfl_sync(0xffffffffu, p_tpr, sl), lo = __shfl_sync(0xffffffffu, max(u0, p_ub), sl);
+        s_q = sl;
+        s_stg = __shfl_sync(0xffffffffu, stg_incl - p_stg, sl);
+        const int j = ib - before;
+        s_u = lo + j / tpr;
+        s_kk = j - (j / tpr) * tpr;
     }
     uint64_t* my_bars = reinterpret_cast<uint64_t*>(smem + P.bars) + warp * SPW;
     uint8_t* my_ring = smem + P.ring + warp * SPW * kStage;
@@ -590,13 +627,20 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
     }
     // blob header of problem blockIdx.x: loaded now, compared after the main
     // loop, so the check never delays this CTA's prologue
-    uint4 hdr0 = make_uint4(0u, 0u, 0u, 0u), hdr1 = hdr0, hdr2 = hdr0;
+    uint4 hdr0 = make_uint4(0u, 0u, 0u, 0u), hdr1 = hdr0, hdr2 = hdr0, rhdr0 = hdr0, rhdr1 = hdr0;
     const bool check_hdr = static_cast<int>(blockIdx.x) < a.count && tid == 0;
     if (check_hdr) {
         const uint4* h = reinterpret_cast<const uint4*>(a.p[blockIdx.x].blob);
         hdr0 = h[0];
         hdr1 = h[1];
         hdr2 = h[2];
+    }
+    // and its refinement blob's header (magic, version, N, K)
+    const bool check_rhdr = MB == 1 && static_cast<int>(blockIdx.x) < a.count && tid == 32 && a.p[blockIdx.x].nsel > 0;
+    if (check_rhdr) {
+        const uint4* h = reinterpret_cast<const uint4*>(a.p[blockIdx.x].rblob);
+        rhdr0 = h[0];
+        rhdr1 = h[1];
     }
     // outlier-channel bitmasks and the row accumulators (no dependence on the previous grid)
     bool any_out = false;
@@ -635,6 +679,32 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
     }
     __syncthreads();
     pdl_wait();
+
+    // selective refinement, early staging (M = 1): the area after the CTA's
+    // staging holds, per refined problem, its chosen channels, their x pairs and
+    // the chosen columns' pieces covering the CTA's rows.  The channels are copied
+    // now (asynchronously, while x is staged), the pieces right before the main
+    // loop, so that they land while the weights stream.
+    uint8_t* rarea = nullptr;
+    if (MB == 1 && a.rearly && R > 0) {
+        int off = 0;
+        for (int j = 0, q = qf; j < np; ++j, ++q) off += staging_bytes(MB, a.p[q].recs, a.p[q].OT);
+        rarea = stg + off;
+        int aoff = 0;
+        for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) {
+            const ProbArg& pa = a.p[q];
+            const int lo = max(u0, pa.ub), hi = min(u1, unit_end(a, q));
+            const long long n0 = static_cast<long long>(lo - pa.ub) * kTR;
+            const long long n1 = min(pa.N, static_cast<long long>(hi - pa.ub) * kTR);
+            if (pa.nsel <= 0 || n1 <= n0) continue;
+            for (int jj = tid; jj < pa.nsel; jj += kThreads)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(rarea + aoff + 4 * jj)),
+                             "l"(pa.ridx + jj)
+                             : "memory");
+            aoff += ref_area_bytes(pa.N, n0, n1, pa.nsel);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
 
     // stage x of every problem: a thread takes whole groups (four 16-byte loads),
     // zeroes outlier channels, writes the permuted chunks and the group sum X~_g
@@ -713,6 +783,43 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
         }
     }
     __syncthreads();
+    if (rarea) {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();   // every thread's channel copies have landed
+        int aoff = 0;
+        for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) {
+            const ProbArg& pa = a.p[q];
+            const int lo = max(u0, pa.ub), hi = min(u1, unit_end(a, q));
+            const long long n0 = static_cast<long long>(lo - pa.ub) * kTR;
+            const long long n1 = min(pa.N, static_cast<long long>(hi - pa.ub) * kTR);
+            if (pa.nsel <= 0 || n1 <= n0) continue;
+            const RefPieces rp = ref_pieces(pa.N, n0, n1);
+            const int lc = rp.bytes(), pieces = lc / 16;
+            const int* rs = reinterpret_cast<const int*>(rarea + aoff);
+            uint8_t* raw = rarea + aoff + round_up(8 * pa.nsel, 16);
+            const uint8_t* cols = pa.rblob + lbq::kRefineHeader;
+            for (int pi = tid; pi < pa.nsel * pieces; pi += kThreads) {
+                const int jj = pi / pieces, k = pi - jj * pieces;
+                const int c = rs[jj] >= 0 && rs[jj] < pa.K ? rs[jj] : 0;   // a bad channel is reported later
+                const uint8_t* col = cols + static_cast<long long>(c) * pa.rcb;
+                const uint8_t* src = k * 16 < rp.ln           ? col + 16 * rp.g0 + 16 * k
+                                     : k * 16 < rp.ln + rp.ls ? col + rp.s_lo + (16 * k - rp.ln)
+                                                              : col + rp.z_lo + (16 * k - rp.ln - rp.ls);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(raw + jj * lc + 16 * k)),
+                             "l"(src)
+                             : "memory");
+            }
+            // the 4-byte pair of x holding x[c]
+            for (int jj = tid; jj < pa.nsel; jj += kThreads) {
+                const int c = rs[jj] >= 0 && rs[jj] < pa.K ? rs[jj] : 0;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(rarea + aoff + 4 * pa.nsel + 4 * jj)),
+                             "l"(pa.x + (c & ~1))
+                             : "memory");
+            }
+            aoff += ref_area_bytes(pa.N, n0, n1, pa.nsel);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
 
     // main loop: this warp's items through its ring, one segment (a run of
     // items of one row block: its dense records, then its outlier records) at a time
@@ -896,62 +1003,154 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
     __syncthreads();
 
     // selective refinement (M = 1; StrataFlux section 3, Eq. 2): the corrections
-    // sum_j x[idx_j] C[n, idx_j] of the CTA's rows, in FP32, each row's columns
-    // split over S slices of threads (columns j = s, s + S, ...: a fixed order);
-    // the combine below adds the slices in order.  The selection kernel before
-    // this one prefetched the columns into L2.
-    float* rcorr = reinterpret_cast<float*>(smem + P.ring);   // the stage ring is free now
-    const int RR = R * kTR, RT = RR < kThreads ? RR : kThreads, S = RR > 0 ? kThreads / RT : 0;
+    // sum_j x[idx_j] C[n, idx_j] of the CTA's rows, in FP32.  The chosen columns'
+    // pieces that cover the CTA's rows (nibble bytes of its 32-row groups, their
+    // scales and zero points) are in the early area (staged while the weights
+    // streamed), or, when that did not fit in shared memory, are copied now into
+    // the free stage ring, all in flight at once (the selection kernel before
+    // this one prefetched them into L2), in batches that fit.  A thread then
+    // takes one 32-bit nibble word (8 rows of a group) and one slice of the
+    // columns (column j in slice j % WS, ascending); the slices' partial rows are
+    // added in slice order into rfin (a fixed order), which the combine below
+    // adds to y.
+    // ring: [rfin: RR floats][channels, x values: batch][word partials][columns]
+    const int RR = R * kTR;
+    float* rfin = reinterpret_cast<float*>(smem + P.ring);
+    const int fin_bytes = round_up(RR * 4, 16);
+    int* rsel_b = reinterpret_cast<int*>(smem + P.ring + fin_bytes);
+    float* rx_b = reinterpret_cast<float*>(rsel_b + kRefineBatchMax);
+    float* wpart = rx_b + kRefineBatchMax;
+    const int fixed_bytes = fin_bytes + 8 * kRefineBatchMax;
     bool refined = false;
     if (MB == 1 && R > 0)
         for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) refined = refined || a.p[q].nsel > 0;
-    if (refined && S * RR * 4 > P.yacc - P.ring) {   // the host keeps row ranges within the ring
-        if (tid == 0) record_error(LBQ_ERR_SHAPE);
-        refined = false;
-    }
     if (refined) {
-        const int sl = tid / RT;
-        for (int rl = tid % RT; rl < RR && sl < S; rl += RT) {
-            const int u = u0 + rl / kTR;
-            int q = qf;
-            while (q + 1 < a.count && a.p[q + 1].ub <= u) ++q;
+        if (rarea) asm volatile("cp.async.wait_group 0;" ::: "memory");   // this thread's early pieces
+        for (int i = tid; i < RR; i += kThreads) rfin[i] = 0.f;
+        int aoff = 0;
+        for (int q = qf; q < a.count && a.p[q].ub < u1; ++q) {
             const ProbArg& pa = a.p[q];
-            const long long n = static_cast<long long>(u - pa.ub) * kTR + rl % kTR;
-            float corr = 0.f;
-            if (pa.nsel > 0 && n < pa.N) {
-                const int g = static_cast<int>(n >> 5), b = static_cast<int>(n & 15), hi = static_cast<int>((n >> 4) & 1);
-                const long long sc_off = pa.N / 2 + 2 * g, z_off = pa.N / 2 + pa.N / 16 + (g >> 1);
-                const uint8_t* cols = pa.rblob + lbq::kRefineHeader;
-#pragma unroll 4
-                for (int j = sl; j < pa.nsel; j += S) {
-                    int c = pa.ridx[j];
-                    const bool ok_c = c >= 0 && c < pa.K;
-                    if (!ok_c) {
-                        record_error(LBQ_ERR_VALUE);
-                        c = 0;
+            if (pa.nsel <= 0) continue;
+            const int lo = max(u0, pa.ub), hi = min(u1, unit_end(a, q));
+            const long long n0 = static_cast<long long>(lo - pa.ub) * kTR;
+            const long long n1 = min(pa.N, static_cast<long long>(hi - pa.ub) * kTR);
+            if (n1 <= n0) continue;
+            const int rl0 = (lo - u0) * kTR;                 // CTA-local row of n0
+            const RefPieces rp = ref_pieces(pa.N, n0, n1);
+            const int g0 = rp.g0, ng = rp.ng, ln = rp.ln, ls = rp.ls;
+            const int lc = rp.bytes(), pieces = lc / 16;
+            // words of the CTA's groups; word threads and column slices
+            const int nw = 4 * ng, WT = nw < kThreads ? nw : kThreads, WS = kThreads / WT;
+            const int wt = tid % WT, ws = tid / WT;
+            const int wbytes = 32 * WS * nw;                  // 8 row partials per (slice, word)
+            __syncthreads();   // the previous problem's partials have been read (and the early pieces landed)
+            for (int i = tid; i < 8 * WS * nw; i += kThreads) wpart[i] = 0.f;
+            // one batch of columns j0 .. j0 + nb - 1: pieces at raw, x values at rx
+            auto accumulate = [&](const uint8_t* raw, const float* rx, int j0, int nb) {
+                if (ws >= WS) return;
+                for (int wi = wt; wi < nw; wi += WT) {
+                    const int g = wi >> 2, w = wi & 3;
+                    const int so = static_cast<int>(pa.N / 2 + 2 * (g0 + g) - rp.s_lo);
+                    const int zo = static_cast<int>(pa.N / 2 + pa.N / 16 + (g0 + g) / 2 - rp.z_lo);
+                    const int zsh = ((g0 + g) & 1) ? 4 : 0;
+                    float* wp = wpart + (ws * nw + wi) * 8;
+                    float acc[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = wp[e];
+                    for (int jj = (ws - j0 % WS + WS) % WS; jj < nb; jj += WS) {   // (j0 + jj) % WS == ws
+                        const uint8_t* cp = raw + jj * lc;
+                        const uint32_t word = *reinterpret_cast<const uint32_t*>(cp + 16 * g + 4 * w);
+                        const float sc = __half2float(*reinterpret_cast<const __half*>(cp + ln + so));
+                        const float zf = static_cast<float>((cp[ln + ls + zo] >> zsh) & 15u);
+                        const float xs = rx[jj];
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            // rows 32 g + 4 w + b (low nibble), 32 g + 16 + 4 w + b (high);
+                            // (q - z) s is exact in FP32
+                            acc[b] = fmaf((static_cast<float>((word >> (8 * b)) & 15u) - zf) * sc, xs, acc[b]);
+                            acc[4 + b] =
+                                fmaf((static_cast<float>((word >> (8 * b + 4)) & 15u) - zf) * sc, xs, acc[4 + b]);
+                        }
                     }
-                    const uint8_t* col = cols + static_cast<long long>(c) * pa.rcb;
-                    const uint32_t qb = col[g * 16 + b];
-                    const float sc = __half2float(*reinterpret_cast<const __half*>(col + sc_off));
-                    const uint32_t zb = col[z_off];
-                    const float xv = ok_c ? __half2float(pa.x[c]) : 0.f;
-                    const float qv = static_cast<float>(hi ? (qb >> 4) : (qb & 15u));
-                    const float zf = static_cast<float>((g & 1) ? (zb >> 4) : (zb & 15u));
-                    corr = fmaf((qv - zf) * sc, xv, corr);   // (q - z) s is exact in FP32
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) wp[e] = acc[e];
+                }
+            };
+            if (rarea) {
+                // early area: channels, x pairs -> x values in place, pieces
+                int* rs = reinterpret_cast<int*>(rarea + aoff);
+                uint32_t* xp = reinterpret_cast<uint32_t*>(rarea + aoff + 4 * pa.nsel);
+                for (int jj = tid; jj < pa.nsel; jj += kThreads) {
+                    const int c = rs[jj];
+                    float xv = 0.f;
+                    if (c >= 0 && c < pa.K)
+                        xv = __half2float(__ushort_as_half(static_cast<unsigned short>(xp[jj] >> (16 * (c & 1)))));
+                    else
+                        record_error(LBQ_ERR_VALUE);   // skipped: its x counts as 0
+                    reinterpret_cast<float*>(xp)[jj] = xv;
+                }
+                __syncthreads();
+                accumulate(rarea + aoff + round_up(8 * pa.nsel, 16), reinterpret_cast<const float*>(xp), 0, pa.nsel);
+                aoff += ref_area_bytes(pa.N, n0, n1, pa.nsel);
+            } else {
+                uint8_t* raw = smem + P.ring + fixed_bytes + wbytes;
+                int per = (P.yacc - P.ring - fixed_bytes - wbytes) / lc;
+                per = per < kRefineBatchMax ? per : kRefineBatchMax;
+                if (per < 1) {   // row ranges this long are not planned with a refinement
+                    if (tid == 0) record_error(LBQ_ERR_SHAPE);
+                    break;
+                }
+                const uint8_t* cols = pa.rblob + lbq::kRefineHeader;
+                for (int j0 = 0; j0 < pa.nsel; j0 += per) {
+                    const int nb = min(per, pa.nsel - j0);
+                    __syncthreads();   // the previous batch has been read
+                    for (int jj = tid; jj < nb; jj += kThreads) {
+                        const int c = pa.ridx[j0 + jj];
+                        rsel_b[jj] = c >= 0 && c < pa.K ? c : -1;
+                    }
+                    __syncthreads();
+                    for (int pi = tid; pi < nb * pieces; pi += kThreads) {
+                        const int jj = pi / pieces, k = pi - jj * pieces;
+                        const uint8_t* col = cols + static_cast<long long>(rsel_b[jj] >= 0 ? rsel_b[jj] : 0) * pa.rcb;
+                        const uint8_t* src = k * 16 < ln        ? col + 16 * g0 + 16 * k
+                                             : k * 16 < ln + ls ? col + rp.s_lo + (16 * k - ln)
+                                                                : col + rp.z_lo + (16 * k - ln - ls);
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(raw + jj * lc + 16 * k)),
+                                     "l"(src)
+                                     : "memory");
+                    }
+                    // the x values load while the column copies are in flight
+                    for (int jj = tid; jj < nb; jj += kThreads) {
+                        const int c = rsel_b[jj];
+                        if (c < 0) record_error(LBQ_ERR_VALUE);   // skipped: its x counts as 0
+                        rx_b[jj] = c >= 0 ? __half2float(pa.x[c]) : 0.f;
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    asm volatile("cp.async.wait_group 0;" ::: "memory");
+                    __syncthreads();
+                    accumulate(raw, rx_b, j0, nb);
                 }
             }
-            rcorr[sl * RR + rl] = corr;
-        }
-        if (static_cast<int>(blockIdx.x) < a.count && tid == 32 && a.p[blockIdx.x].nsel > 0) {
-            const ProbArg& pa = a.p[blockIdx.x];
-            const unsigned* h = reinterpret_cast<const unsigned*>(pa.rblob);
-            const long long n_hdr = *reinterpret_cast<const long long*>(pa.rblob + 16);
-            const long long k_hdr = *reinterpret_cast<const long long*>(pa.rblob + 24);
-            if (h[0] != 0x5251424Cu || h[1] != 0x43345746u || h[2] != lbq::kRefineVersion || n_hdr != pa.N ||
-                k_hdr != pa.K)
-                record_error(LBQ_ERR_FORMAT);
+            // each row of this problem: its word's partials, in slice order
+            __syncthreads();
+            for (int rl = rl0 + tid; rl < rl0 + static_cast<int>(n1 - n0); rl += kThreads) {
+                const long long n = n0 + (rl - rl0);
+                const int wi = (static_cast<int>(n >> 5) - g0) * 4 + static_cast<int>((n >> 2) & 3);
+                const int e = static_cast<int>(n & 3) + (((n >> 4) & 1) ? 4 : 0);
+                float tot = 0.f;
+                for (int s2 = 0; s2 < WS; ++s2) tot += wpart[(s2 * nw + wi) * 8 + e];
+                rfin[rl] = tot;
+            }
         }
         __syncthreads();
+    }
+    if (check_rhdr) {
+        const ProbArg& pa = a.p[blockIdx.x];
+        const long long n_hdr = (static_cast<long long>(rhdr1.y) << 32) | rhdr1.x;
+        const long long k_hdr = (static_cast<long long>(rhdr1.w) << 32) | rhdr1.z;
+        if (rhdr0.x != 0x5251424Cu || rhdr0.y != 0x43345746u || rhdr0.z != lbq::kRefineVersion || n_hdr != pa.N ||
+            k_hdr != pa.K)
+            record_error(LBQ_ERR_FORMAT);
     }
 
     if (check_hdr) {
@@ -981,7 +1180,7 @@ __global__ void __launch_bounds__(NW * 32, (MB == 1 && NW == 8) ? 2 : 1) lbq_gem
         if (n < pa.N && m < mrows) {
             y *= 1.f / kUnit;
             if (refined && pa.nsel > 0)
-                for (int sl = 0; sl < S; ++sl) y += rcorr[sl * RR + rr];
+                y += rfin[rr];
             if (a.y_f32)
                 reinterpret_cast<float*>(pa.y)[m * pa.ldy + n] = y;
             else
@@ -1150,8 +1349,9 @@ int unit_end_host(const GroupArgs& a, int q) { return q + 1 < a.count ? a.p[q + 
 
 // Persistent grid of <= one CTA per SM; CTA c owns a contiguous run of row
 // blocks whose bytes are about 1/grid of the total.  Returns the largest
-// staging area any CTA needs; sets grid, cta_ub and rb_cap.
-int partition(const DeviceInfo* dev, int MB, GroupArgs& a, int* grid) {
+// staging area any CTA needs, and in *stg_ref_max the largest with the early
+// refinement area added (M = 1); sets grid, cta_ub and rb_cap.
+int partition(const DeviceInfo* dev, int MB, GroupArgs& a, int* grid, int* stg_ref_max) {
     long long total = 0;
     for (int q = 0; q < a.count; ++q) total += static_cast<long long>(unit_end_host(a, q) - a.p[q].ub) * a.p[q].rb_bytes;
     int G = dev->sms < kMaxGrid ? dev->sms : kMaxGrid;
@@ -1174,15 +1374,27 @@ int partition(const DeviceInfo* dev, int MB, GroupArgs& a, int* grid) {
     }
     a.cta_ub[G] = a.nunits;
     int rb_cap = 1, stg_max = 0;
+    long long ref_max = 0;
     for (int c = 0; c < G; ++c) {
         const int u0 = a.cta_ub[c], u1 = a.cta_ub[c + 1];
         if (u1 - u0 > rb_cap) rb_cap = u1 - u0;
         int s = 0;
+        long long r = 0;
         if (u1 > u0)
             for (int p = 0; p < a.count; ++p)
-                if (a.p[p].ub < u1 && unit_end_host(a, p) > u0) s += staging_bytes(MB, a.p[p].recs, a.p[p].OT);
+                if (a.p[p].ub < u1 && unit_end_host(a, p) > u0) {
+                    s += staging_bytes(MB, a.p[p].recs, a.p[p].OT);
+                    const int lo = u0 > a.p[p].ub ? u0 : a.p[p].ub;
+                    const int hi = u1 < unit_end_host(a, p) ? u1 : unit_end_host(a, p);
+                    const long long n0 = static_cast<long long>(lo - a.p[p].ub) * kTR;
+                    long long n1 = static_cast<long long>(hi - a.p[p].ub) * kTR;
+                    if (n1 > a.p[p].N) n1 = a.p[p].N;
+                    if (MB == 1 && a.p[p].nsel > 0 && n1 > n0) r += ref_area_bytes(a.p[p].N, n0, n1, a.p[p].nsel);
+                }
         if (s > stg_max) stg_max = s;
+        if (s + r > ref_max) ref_max = s + r;
     }
+    *stg_ref_max = ref_max > INT32_MAX / 2 ? INT32_MAX / 2 : static_cast<int>(ref_max);
     a.rb_cap = rb_cap;
     *grid = G;
     return stg_max;
@@ -1200,7 +1412,14 @@ int stages_per_warp(const DeviceInfo* dev, const Variant& V, int rb_cap, int stg
 // Plan one launch of variant vi over the group; LBQ_ERR_SHAPE when it does not fit.
 lbq_status plan_group(const DeviceInfo* dev, int vi, GroupArgs& a, int* grid, size_t* smem) {
     const Variant& V = variant(vi);
-    const int stg_max = partition(dev, V.MB, a, grid);
+    int stg_ref = 0;
+    int stg_max = partition(dev, V.MB, a, grid, &stg_ref);
+    // the early refinement area when it fits with the full ring, else the ring path
+    a.rearly = 0;
+    if (stg_ref > stg_max && stages_per_warp(dev, V, a.rb_cap, stg_ref) >= (V.MB == 1 ? kStagesM1 : kStagesMB)) {
+        a.rearly = 1;
+        stg_max = stg_ref;
+    }
     const int spw = stages_per_warp(dev, V, a.rb_cap, stg_max);
     if (spw < 2) return LBQ_ERR_SHAPE;
     a.SPW = spw;

@@ -60,18 +60,25 @@ def _run(lbq, kind, specs, f32=True, seed=0):
     return [(y.float().cpu().numpy(), ref, None if d is None else d.cpu().numpy(), r) for y, ref, d, r in out]
 
 
+# the chosen columns' pieces fit in shared memory next to the staging: they are
+# copied while the weights stream
 MIXED = [(64, 64, 0, 1), (320, 1088, 5, 100), (128, 2112, 0, None), (4096, 4096, 41, 16), (256, 14336, 0, 16),
-         (64, 8192, 64, 256), (1024, 3072, 0, 256)]
+         (1024, 3072, 0, 256)]
+# thousands of chosen columns: the pieces do not fit, they are copied after the
+# main loop into the stage ring, in batches
+MANY = [(64, 8192, 64, 256), (128, 16384, 0, 256), (200 - 200 % 64, 2048, 0, 16)]
 
 
+@pytest.mark.parametrize("specs", ["MIXED", "MANY"])
 @pytest.mark.parametrize("kind", ["w4", "w2"])
 @pytest.mark.parametrize("f32", [True, False])
-def test_fused_refinement_elementwise(lbq, kind, f32):
-    for i, (y, ref, gidx, oidx) in enumerate(_run(lbq, kind, MIXED, f32=f32, seed=3 if kind == "w4" else 4)):
-        N, K, n_out, k = MIXED[i]
+def test_fused_refinement_elementwise(lbq, specs, kind, f32):
+    sp = MIXED if specs == "MIXED" else MANY
+    for i, (y, ref, gidx, oidx) in enumerate(_run(lbq, kind, sp, f32=f32, seed=3 if kind == "w4" else 4)):
+        N, K, n_out, k = sp[i]
         if gidx is not None:
             assert np.array_equal(gidx, oidx), "grouped selection %d" % i
-        assert_close(y, ref, fp16_out=not f32, what="fused refine %s N=%d K=%d k=%s" % (kind, N, K, k))
+        assert_close(y, ref, fp16_out=not f32, what="fused refine %s %s N=%d K=%d k=%s" % (specs, kind, N, K, k))
 
 
 def test_fused_refinement_llama8b_layer_every_row(lbq):
