@@ -48,9 +48,9 @@ SAMPLE_ROWS_MAX = 1024
 L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)
 # DRAM bytes (read + write) per grouped launch from ncu captures of the same
 # launches (profiles/); valid only for the kernel source they were taken on.
-TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "0dd2bd4338b36fff",
-                   "traffic": {"w4_layer_sweep": 129266944, "w2_layer_sweep": 100254720,
-                               "w4_smallM_gate_down": 68175104}}
+TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "95359677cbaefb8b",
+                   "traffic": {"w4_layer_sweep": 129320960, "w2_layer_sweep": 100127232,
+                               "w4_smallM_gate_down": 68189184}}
 METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
 W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
 W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
@@ -228,12 +228,15 @@ def group_launch_count(lbq, layer, kind, blobs, xs, ys):
 
 
 def launch(lbq, e, blob, x, y, pdl):
-    if e["kind"] == "w4":
-        lbq.gemv_w4a16(blob, e["N"], e["K"], e["n_out"], x, y, pdl=pdl)
+    M = e.get("M", 1)
+    if e["kind"] == "w2" and M > 1:
+        lbq.gemm_w2cb_outlier_smallM(blob, M, e["N"], e["K"], e["n_out"], x, e["K"], y, e["N"], pdl=pdl)
     elif e["kind"] == "w2":
         lbq.gemv_w2cb_outlier(blob, e["N"], e["K"], e["n_out"], x, y, pdl=pdl)
+    elif e["kind"] == "w4" and M == 1:
+        lbq.gemv_w4a16(blob, e["N"], e["K"], e["n_out"], x, y, pdl=pdl)
     else:
-        lbq.gemm_w4a16_smallM(blob, e["M"], e["N"], e["K"], e["n_out"], x, e["K"], y, e["N"], pdl=pdl)
+        lbq.gemm_w4a16_smallM(blob, M, e["N"], e["K"], e["n_out"], x, e["K"], y, e["N"], pdl=pdl)
 
 
 # ---------------------------------------------------------------------------
