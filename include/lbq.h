@@ -200,8 +200,10 @@ lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64
  * states the M = 1 kernel):
  *     Y[m, n] = sum_g [ S_{n,g} sum_{k in g} C[q_{n,k}] X~[m,k] + Z_{n,g} sum_{k in g} X~[m,k] ]
  *               + sum_j vals[n,j] X[m, idx_j],  0 <= m < M
- * Arguments, layouts and errors as lbq_gemm_w4a16_smallM, with a 2-bit blob;
- * every M runs on the CUDA-core kernel (passes of 2, 4 or 8 activation rows). */
+ * Arguments, layouts and errors as lbq_gemm_w4a16_smallM, with a 2-bit blob.
+ * M < 16: passes of 2, 4 or 8 activation rows on the CUDA-core kernel;
+ * M >= 16: the tensor-core (tcgen05) kernel, with the outlier columns as extra
+ * stages of the same FP32 accumulation (one launch per slab of 256-row tiles). */
 lbq_status lbq_gemm_w2cb_outlier_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
                                         const void* X_f16, int64_t ldx, void* Y, int64_t ldy,
                                         lbq_dtype y_dtype, void* stream);
