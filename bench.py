@@ -810,9 +810,10 @@ FMA_PEAK = 152 * 128 * 2.07e9       # FP32 FMA lanes of a GB300 (152 SMs x 128 a
 
 def run_smallm_sweep(lbq, dev, stream, replays=5):
     """Config 4 across M: the 4-bit gate (14336 x 4096) and down (4096 x 14336)
-    projections at M = 2..64 (CUDA cores below 16, tensor cores from 16), the
-    2-bit ones with 3.5 % outlier columns (CUDA cores below 16, tensor cores
-    from 16) and without outlier columns at M >= 16 (tensor cores).  Each
+    projections at M = 2..64 (CUDA cores below 16, tensor cores from 16) and
+    with their saliency-selected outlier columns at M = 16 / 64, the 2-bit ones
+    with 3.5 % outlier columns (CUDA cores below 16, tensor cores from 16) and
+    without outlier columns at M >= 16 (tensor cores).  Each
     configuration chained over
     rotating copies (>= 512 MB) in a CUDA graph.  Next to the HBM fraction: the
     FP32-FMA fraction below M = 16 (one FMA per weight and activation row) and
@@ -832,6 +833,10 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
         b4 = lbq.pack_w4(W)
         for M in (2, 4, 8, 16, 32, 64):
             cases.append(("w4", name, N, K, M, 0, b4))
+        idx4 = lbq.select_outliers_w4(W)                   # SPECTRA 3.2-3.3 saliency + kurtosis ratio
+        b4o = lbq.pack_w4(W, idx4)
+        for M in (16, 64):
+            cases.append(("w4", name, N, K, M, len(idx4), b4o))
         W2 = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
         idx = lbq.select_outliers_impact(W2, synth.profile_vectors(K, config_id=3, layer_id=li), 0.035)
         b2o = lbq.pack_w2cb(W2, idx)
@@ -872,7 +877,7 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
         nbytes = algorithmic_bytes(kind, N, K, n_out, M)
         gbs = nbytes / (us * 1e-6) / 1e9
         row = {"kind": kind, "linear": name, "N": N, "K": K, "M": M, "n_out": n_out,
-               "path": "tensor cores" if (M >= 16 and (n_out == 0 or kind == "w2")) else "CUDA cores",
+               "path": "tensor cores" if M >= 16 else "CUDA cores",
                "us_per_call": round(us, 3), "GB_s": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
         macs = M * N * K
         if row["path"] == "CUDA cores":

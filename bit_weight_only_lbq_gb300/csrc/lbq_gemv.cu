@@ -1554,11 +1554,8 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
         const int v0 = dual ? (kind == kW4 ? kVarW4Narrow : kVarW2Narrow) : one ? fallback_variant(vi) : vi;
         return launch_pass(dev, kind, v0, true, P, count, 1, f32, stream, flags, launches);
     }
-    // M >= 16: the tensor-core kernels, one launch per problem (the 4-bit one takes
-    // no outlier columns: 4-bit problems with outliers stay on the CUDA cores)
-    bool tc = true;
-    for (int i = 0; i < count; ++i) tc = tc && (kind == kW2 || P[i].n_out == 0);
-    if (M >= 16 && tc) {
+    // M >= 16: the tensor-core kernels, one launch per problem
+    if (M >= 16) {
         for (int i = 0; i < count; ++i) {
             const uint32_t fl = i == 0 ? flags : (flags | LBQ_FLAG_PDL);
             if (kind == kW2) {
@@ -1568,8 +1565,8 @@ lbq_status run(int kind, const HostProblem* P, int count, int M, lbq_dtype y_dty
                 ++*launches;
                 st = LBQ_OK;
             } else {
-                st = lbq::launch_w4_mma(P[i].packed, P[i].N, P[i].K, M, P[i].x, P[i].ldx, P[i].y, P[i].ldy, f32,
-                                        dev->err_word, dev->sms, dev->max_smem, stream, fl);
+                st = lbq::launch_w4_mma(P[i].packed, P[i].N, P[i].K, P[i].n_out, M, P[i].x, P[i].ldx, P[i].y,
+                                        P[i].ldy, f32, dev->err_word, dev->sms, dev->max_smem, stream, fl);
             }
             if (st != LBQ_OK) return st;
         }

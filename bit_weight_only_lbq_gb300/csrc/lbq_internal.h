@@ -42,10 +42,10 @@ lbq_status device_context(unsigned** err_word, int* sms);
 
 uint16_t host_f64_to_f16(double v);
 
-// Tensor-core 4-bit GEMM for 16 <= M <= 64 without outlier columns
-// (lbq_mma_w4.cu); err_word is the device error word of the library.
-lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
-                         int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
+// Tensor-core 4-bit GEMM for 16 <= M <= 64, outlier columns added in its
+// epilogue (lbq_mma_w4.cu); err_word is the device error word of the library.
+lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int32_t n_out, int M, const void* x, int64_t ldx,
+                         void* y, int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
                          uint32_t flags);
 // Tensor-core 2-bit codebook GEMM for 16 <= M <= 64 with its exact FP16
 // outlier columns (lbq_mma.cu).  One launch per slab of 256-row tiles; with

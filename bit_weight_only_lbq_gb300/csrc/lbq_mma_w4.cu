@@ -88,6 +88,16 @@ struct MmaArgs {
     int M;          // activation rows (<= NM)
     int S;          // k-splits per tile = cluster size
     int y_f32;
+    // outlier columns, added in the epilogue: X (row-major, ldx), their channels,
+    // and the outlier records (after the dense records of each row block)
+    const __half* x;
+    long long ldx;
+    const int32_t* idx;
+    int n_out;
+    int OT;                 // outlier records per row block
+    int cols_last;          // columns of the last one (a multiple of 8)
+    long long rb_bytes;
+    const uint8_t* out0;    // outlier records of row block 0
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -493,7 +503,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     };
+    // exact FP16 outlier columns (SPECTRA section 4.2, in-kernel outlier fusion):
+    // d[i] += sum_j X[16 cc + i][idx_j] Wout[n][j], in FP32, columns in order, by the
+    // CTA that writes y.  In chunks of 64 columns: the chunk's X[:, idx] (NM rows,
+    // zero past M) staged once in the idle activation ring as FP32, each thread's
+    // 64 outlier values of row n read from its row block's outlier record.
+    auto add_outliers = [&]() {
+        if (a.n_out <= 0 || bad) return;
+        float* xo = reinterpret_cast<float*>(smem + G::b);
+        const int rbn = static_cast<int>(n >> 2), rn = static_cast<int>(n & 3);
+        for (int j0 = 0; j0 < a.n_out; j0 += 64) {
+            __syncthreads();   // the previous chunk has been read
+            for (int e = tid; e < NM * 64; e += kThreads) {
+                const int row = e >> 6, j = j0 + (e & 63);
+                float v = 0.f;
+                if (row < a.M && j < a.n_out) {
+                    const int k = a.idx[j];
+                    if (k >= 0 && k < a.K)
+                        v = __half2float(a.x[row * a.ldx + k]);
+                    else
+                        atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_OUTLIER_IDX));
+                }
+                xo[e] = v;
+            }
+            __syncthreads();
+            if (ep && n < a.N) {
+                const int o = j0 / lbq::kOutlierCols, width = o + 1 < a.OT ? lbq::kOutlierCols : a.cols_last;
+                const int nj = min(64, a.n_out - j0);
+                const uint4* wrow = reinterpret_cast<const uint4*>(
+                    a.out0 + static_cast<long long>(rbn) * a.rb_bytes +
+                    static_cast<long long>(o) * (lbq::kOutlierCols * lbq::kRowsPerBlock * 2) +
+                    (static_cast<long long>(rn) * width + j0 % lbq::kOutlierCols) * 2);
+                const float4* xo4 = reinterpret_cast<const float4*>(xo + 16 * cc * 64);
+#pragma unroll 1
+                for (int j8 = 0; j8 < nj; j8 += 8) {
+                    const uint4 wv = wrow[j8 / 8];   // 8 FP16 outlier values (past n_out: zero padding)
+                    const float2 w0 = __half22float2(*reinterpret_cast<const __half2*>(&wv.x));
+                    const float2 w1 = __half22float2(*reinterpret_cast<const __half2*>(&wv.y));
+                    const float2 w2 = __half22float2(*reinterpret_cast<const __half2*>(&wv.z));
+                    const float2 w3 = __half22float2(*reinterpret_cast<const __half2*>(&wv.w));
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float4 xa = xo4[i * 16 + j8 / 4], xb = xo4[i * 16 + j8 / 4 + 1];
+                        float t = d[i];
+                        t = fmaf(w0.x, xa.x, t);
+                        t = fmaf(w0.y, xa.y, t);
+                        t = fmaf(w1.x, xa.z, t);
+                        t = fmaf(w1.y, xa.w, t);
+                        t = fmaf(w2.x, xb.x, t);
+                        t = fmaf(w2.y, xb.y, t);
+                        t = fmaf(w3.x, xb.z, t);
+                        t = fmaf(w3.y, xb.w, t);
+                        d[i] = t;
+                    }
+                }
+            }
+        }
+    };
     if (S == 1) {
+        add_outliers();
         if (ep) write_y();
     } else {
         // split K: partials through distributed shared memory, added in rank order by rank 0
@@ -502,20 +570,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) part[(16 * cc + i) * kTileRows + m] = d[i];
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-        if (rank == 0 && ep) {
-            for (int p = 1; p < S; ++p) {
-                uint32_t remote;
-                asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(part)), "r"(p));
+        if (rank == 0) {
+            if (ep)
+                for (int p = 1; p < S; ++p) {
+                    uint32_t remote;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(part)), "r"(p));
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float v;
-                    asm volatile("ld.shared::cluster.f32 %0, [%1];"
-                                 : "=f"(v)
-                                 : "r"(remote + 4u * ((16 * cc + i) * kTileRows + m)));
-                    d[i] += v;
+                    for (int i = 0; i < 16; ++i) {
+                        float v;
+                        asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                                     : "=f"(v)
+                                     : "r"(remote + 4u * ((16 * cc + i) * kTileRows + m)));
+                        d[i] += v;
+                    }
                 }
-            }
-            write_y();
+            add_outliers();
+            if (ep) write_y();
         }
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
@@ -525,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long n_hdr = (static_cast<long long>(h1.y) << 32) | h1.x;
         const long long k_hdr = (static_cast<long long>(h1.w) << 32) | h1.z;
         if (h0.x != 0x5751424Cu || h0.y != 0x32334734u || h0.z != LBQ_FORMAT_VERSION_NUM || n_hdr != a.N ||
-            k_hdr != a.K || h2.x != 0u)
+            k_hdr != a.K || static_cast<int>(h2.x) != a.n_out)
             atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_FORMAT));
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -570,12 +640,12 @@ int mma_padded_rows(int M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 48 ? 48 :
 // Launch the tensor-core 4-bit GEMM for one problem (16 <= M <= 64, no outlier
 // columns).  Tiles of 128 rows; K split over a cluster of S CTAs so that tiles
 // x S fills the SMs.  Returns LBQ_ERR_SHAPE when it does not fit.
-lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const void* x, int64_t ldx, void* y,
-                         int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
+lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int32_t n_out, int M, const void* x, int64_t ldx,
+                         void* y, int64_t ldy, bool y_f32, unsigned* err_word, int sms, int max_smem, void* stream,
                          uint32_t flags) {
     if (M < 16 || M > 64) return LBQ_ERR_SHAPE;
     lbq_layout L;
-    lbq_status st = lbq_blob_layout(LBQ_KIND_W4, N, K, 0, &L);
+    lbq_status st = lbq_blob_layout(LBQ_KIND_W4, N, K, n_out, &L);
     if (st != LBQ_OK) return st;
     const int NM = mma_padded_rows(M);
     const int smem = NM == 16 ? smem_bytes<16>() : NM == 32 ? smem_bytes<32>() : NM == 48 ? smem_bytes<48>()
@@ -596,6 +666,17 @@ lbq_status launch_w4_mma(const void* packed, int64_t N, int64_t K, int M, const 
     a.n_rb = static_cast<int>((N + 3) / 4);
     a.M = M;
     a.y_f32 = y_f32 ? 1 : 0;
+    a.x = static_cast<const __half*>(x);
+    a.ldx = ldx;
+    a.n_out = n_out;
+    if (n_out > 0) {
+        a.idx = reinterpret_cast<const int32_t*>(b + L.idx_offset);
+        a.OT = static_cast<int>(L.outlier_records);
+        a.cols_last = (n_out + lbq::kOutlierColAlign - 1) / lbq::kOutlierColAlign * lbq::kOutlierColAlign -
+                      (a.OT - 1) * lbq::kOutlierCols;
+        a.rb_bytes = static_cast<long long>(L.row_block_bytes);
+        a.out0 = b + L.area_offset + L.records * L.record_bytes;
+    }
     // tensor maps: nibbles (byte of a row's codes, row, record block, row block),
     // metadata (u16 of a record's scales + zeros, record block, row block),
     // activations (k, activation row)

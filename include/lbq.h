@@ -186,9 +186,9 @@ lbq_status lbq_gemv_w2cb_outlier(const void* packed, int64_t N, int64_t K, int32
  * X_f16 : device, M rows of K FP16 with leading dimension ldx (elements),
  *         16-byte aligned base, ldx % 8 == 0, ldx >= K.
  * Y     : device, M rows of N values of y_dtype with leading dimension ldy >= N.
- * 1 <= M <= 64.  M < 16, or any M with n_out > 0: passes of 2, 4 or 8
- * activation rows on the CUDA-core kernel (one kernel per pass); M >= 16
- * with n_out == 0: one launch of the tensor-core (tcgen05) kernel.
+ * 1 <= M <= 64.  M < 16: passes of 2, 4 or 8 activation rows on the CUDA-core
+ * kernel (one kernel per pass); M >= 16: one launch of the tensor-core
+ * (tcgen05) kernel, whose epilogue adds the outlier columns in FP32.
  * Errors as lbq_gemv_w4a16. */
 lbq_status lbq_gemm_w4a16_smallM(const void* packed, int32_t M, int64_t N, int64_t K, int32_t n_out,
                                  const void* X_f16, int64_t ldx, void* Y, int64_t ldy,

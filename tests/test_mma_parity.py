@@ -6,7 +6,9 @@ tiles and 256-k chunks split over a cluster, each CTA's range spanning at most
 two tiles with one accumulator each; taller matrices go in slabs of tiles, one
 launch each; the exact FP16 outlier columns are extra 64-column stages of the
 same accumulation, their values copied straight into the operand stage and the
-activations gathered by index).  The shapes cover: N ragged against both tile
+activations gathered by index).  The 4-bit kernel adds the outlier columns
+in its epilogue (FP32 FMAs on the CUDA cores, by the CTA that writes y).  The
+shapes cover: N ragged against both tile
 sizes (and smaller than one row block), K with a partial 1024-k record and a
 partial chunk, M from 16 to 64, CTA ranges that span two tiles, a single tile
 whose K is split over a whole cluster, two slabs, leading dimensions, FP16
@@ -119,9 +121,10 @@ def _idx(seed, K, n_out):
     return np.sort(rng.choice(K, size=n_out, replace=False)).astype(np.int32)
 
 
-def _run_out(lbq, blob, M, N, K, n_out, X, f32=True):
+def _run_out(lbq, blob, M, N, K, n_out, X, f32=True, kind="w2"):
     Y = torch.full((M, N), float("nan"), dtype=torch.float32 if f32 else torch.float16, device="cuda:0")
-    lbq.gemm_w2cb_outlier_smallM(to_dev(blob), M, N, K, n_out, to_dev(X), K, Y, N)
+    f = lbq.gemm_w4a16_smallM if kind == "w4" else lbq.gemm_w2cb_outlier_smallM
+    f(to_dev(blob), M, N, K, n_out, to_dev(X), K, Y, N)
     torch.cuda.synchronize()
     assert lbq.device_error() == 0
     return Y.float().cpu().numpy()
@@ -136,26 +139,34 @@ OUT_SHAPES = [(16, 300, 1024, 1), (17, 70, 2112, 77), (32, 513, 4096, 256), (64,
               (16, 80000, 64, 9)]
 
 
+@pytest.mark.parametrize("kind", ["w2", "w4"])
 @pytest.mark.parametrize("M,N,K,n_out", OUT_SHAPES)
-def test_w2_outliers_elementwise(lbq, M, N, K, n_out):
+def test_outliers_elementwise(lbq, kind, M, N, K, n_out):
+    """2-bit: outlier stages of the tensor-core accumulation; 4-bit: outlier
+    columns added in the tensor-core kernel's epilogue (both one launch per slab
+    or problem)."""
     W, X = _case(M * 5 + N + K + n_out, M, N, K)
     idx = _idx(n_out + K, K, n_out)
     X[:, idx[: max(1, n_out // 3)]] *= 30   # large activations on outlier channels too
-    ref = O.gemm(O.pack_w2cb(W, idx), X)
-    blob = lbq.pack_w2cb(W, idx)
-    assert_close(_run_out(lbq, blob, M, N, K, n_out, X), ref, what="mma w2 M=%d N=%d K=%d n_out=%d" % (M, N, K, n_out))
+    pack, opack = (lbq.pack_w4, O.pack_w4) if kind == "w4" else (lbq.pack_w2cb, O.pack_w2cb)
+    ref = O.gemm(opack(W, idx), X)
+    y = _run_out(lbq, pack(W, idx), M, N, K, n_out, X, kind=kind)
+    assert_close(y, ref, what="mma %s M=%d N=%d K=%d n_out=%d" % (kind, M, N, K, n_out))
 
 
-def test_w2_outliers_fp16_output_and_repeatable(lbq):
+@pytest.mark.parametrize("kind", ["w2", "w4"])
+def test_outliers_fp16_output_and_repeatable(lbq, kind):
     M, N, K, n_out = 33, 700, 3072, 143
     W, X = _case(77, M, N, K)
     idx = _idx(78, K, n_out)
-    blob = lbq.pack_w2cb(W, idx)
-    ref = O.gemm(O.pack_w2cb(W, idx), X)
-    assert_close(_run_out(lbq, blob, M, N, K, n_out, X, f32=False), ref, fp16_out=True, what="mma w2 outliers f16")
-    a = _run_out(lbq, blob, M, N, K, n_out, X)
+    pack, opack = (lbq.pack_w4, O.pack_w4) if kind == "w4" else (lbq.pack_w2cb, O.pack_w2cb)
+    blob = pack(W, idx)
+    ref = O.gemm(opack(W, idx), X)
+    assert_close(_run_out(lbq, blob, M, N, K, n_out, X, f32=False, kind=kind), ref, fp16_out=True,
+                 what="mma %s outliers f16" % kind)
+    a = _run_out(lbq, blob, M, N, K, n_out, X, kind=kind)
     for _ in range(2):
-        assert np.array_equal(_run_out(lbq, blob, M, N, K, n_out, X), a)
+        assert np.array_equal(_run_out(lbq, blob, M, N, K, n_out, X, kind=kind), a)
 
 
 def test_w2_outliers_launch_count(lbq):
