@@ -48,9 +48,9 @@ SAMPLE_ROWS_MAX = 1024
 L2_ROTATION_BYTES = 512 << 20  # distinct weight bytes one timing pass rotates through (4x L2)
 # DRAM bytes (read + write) per grouped launch from ncu captures of the same
 # launches (profiles/); valid only for the kernel source they were taken on.
-TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "95359677cbaefb8b",
-                   "traffic": {"w4_layer_sweep": 129320960, "w2_layer_sweep": 100127232,
-                               "w4_smallM_gate_down": 68189184}}
+TRAFFIC_CAPTURE = {"kernel_sha256_prefix": "22be62a830ce8505",
+                   "traffic": {"w4_layer_sweep": 129267712, "w2_layer_sweep": 100116736,
+                               "w4_smallM_gate_down": 68175872}}
 METRIC = "W4/W2 decode GEMV µs/call and HBM GB/s (% of GB300 roofline); implied tokens/s"
 W4_BYTES_PER_WEIGHT = 0.578125      # 4 bits + FP16 scale / 32 + 4-bit zero / 32
 W2_BYTES_PER_WEIGHT = 0.375         # 2 bits + FP16 S / 32 + FP16 Z / 32
