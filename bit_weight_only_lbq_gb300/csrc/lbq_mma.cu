@@ -675,9 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < kChunkStages; ++jj) {
                 if (jj < jj0 || jj >= jj0 + (ge - g)) continue;
                 const int bs = is % kNB;
-                const bool ok = warp_wait(bempty + 8 * bs, ((is - kNB) / kNB) & 1, is >= kNB);
                 const uint32_t bst = sb + F::kB + bs * kBStage + brow;
                 if (c0 >= U) {
+                    const bool ok = warp_wait(bempty + 8 * bs, ((is - kNB) / kNB) & 1, is >= kNB);
                     // outlier stage: the tile's 256 rows x 64 FP16 outlier values go straight
                     // into the B stage (the copy writes the swizzled layout); warp 0 issues the
                     // copy and waits for it to land before its arrival, so that no copy is in
@@ -711,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++is;
                     continue;
                 }
-                if (ok && !*abort_flag) {
+                // dense stage: decode first (it needs no slot), then wait for the slot and store
+                uint32_t o[4][8];
+                {
                     const uint4 qs = q[jj];
                     const uint32_t Sw = u4w(m0, jj), Zw = u4w(m1, jj);
 #pragma unroll
@@ -719,10 +721,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int qg = v >> 1;   // 32-k quantisation group of the stage
                         const uint32_t S2 = ((Sw >> (16 * qg)) & 0xFFFFu) * 0x00010001u;
                         const uint32_t Z2 = ((Zw >> (16 * qg)) & 0xFFFFu) * 0x00010001u;
-                        uint32_t o[8];
-                        w2_word(u4w(qs, v), S2, Z2, lut_lo, lut_hi, o);
-                        sts128(bst + (((2 * v) ^ sw) << 4), o[0], o[1], o[2], o[3]);
-                        sts128(bst + (((2 * v + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+                        w2_word(u4w(qs, v), S2, Z2, lut_lo, lut_hi, o[v]);
+                    }
+                }
+                const bool ok = warp_wait(bempty + 8 * bs, ((is - kNB) / kNB) & 1, is >= kNB);
+                if (ok && !*abort_flag) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        sts128(bst + (((2 * v) ^ sw) << 4), o[v][0], o[v][1], o[v][2], o[v][3]);
+                        sts128(bst + (((2 * v + 1) ^ sw) << 4), o[v][4], o[v][5], o[v][6], o[v][7]);
                     }
                 }
                 // the B stage is read by the tensor core (async proxy)
