@@ -98,3 +98,29 @@ def test_grouped_entry_point_rejects_bad_args_without_gpu(lbq):
     assert L.lbq_gemv_grouped(0, bad, 2, 1, 0, None, 0) == 1
     bad = (P * 2)(good, P(16, 8, 64, 0, 0, 16, 64, 16, 4))             # ldy < N
     assert L.lbq_gemv_grouped(0, bad, 2, 1, 0, None, 0) == 2
+
+
+def test_grouped_selection_and_refined_sweep_argument_errors(lbq):
+    """lbq_refine_select_grouped and lbq_gemv_grouped_refined validate every
+    descriptor on the host before touching a device (fake device addresses)."""
+    L = lbq.lib()
+    SP, RF, PB = lbq.SelectProblem, lbq.Refinement, lbq.Problem
+    x, idx, rb = 0x10000, 0x20000, 0x30000
+    ok = SP(x, 4096, 16, 0, idx, rb, 4096)
+    assert L.lbq_refine_select_grouped(None, 1, None) == 1                         # NULL array
+    assert L.lbq_refine_select_grouped((SP * 1)(ok), 0, None) == 2                 # count
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(0, 4096, 16, 0, idx, rb, 4096)), 1, None) == 1
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(x, 4096, 0, 0, idx, rb, 4096)), 1, None) == 2    # k
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(x, 4096, 257, 0, idx, rb, 4096)), 1, None) == 2  # k > 256
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(x, 4096, 16, 1, idx, rb, 4096)), 1, None) == 2   # reserved
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(x, 4096, 16, 0, idx, rb, 100)), 1, None) == 2    # N % 64
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(x + 1, 4096, 16, 0, idx, rb, 4096)), 1, None) == 3  # x align
+    assert L.lbq_refine_select_grouped((SP * 1)(SP(x, 4096, 16, 0, idx, rb + 8, 4096)), 1, None) == 3  # blob align
+    prob = (PB * 1)(PB(0x40000, 128, 1024, 0, 0, x, 1024, 0x50000, 128))
+    assert L.lbq_gemv_grouped_refined(0, prob, None, 1, 1, None, 0) == 1            # no refinement array
+    assert L.lbq_gemv_grouped_refined(0, prob, (RF * 1)(RF(rb, idx, 1025, 0)), 1, 1, None, 0) == 2  # n_sel > K
+    assert L.lbq_gemv_grouped_refined(0, prob, (RF * 1)(RF(rb, idx, 4, 1)), 1, 1, None, 0) == 2     # reserved
+    assert L.lbq_gemv_grouped_refined(0, prob, (RF * 1)(RF(rb, None, 4, 0)), 1, 1, None, 0) == 1    # idx
+    assert L.lbq_gemv_grouped_refined(0, prob, (RF * 1)(RF(rb + 8, idx, 4, 0)), 1, 1, None, 0) == 3  # blob align
+    odd = (PB * 1)(PB(0x40000, 100, 1024, 0, 0, x, 1024, 0x50000, 100))
+    assert L.lbq_gemv_grouped_refined(0, odd, (RF * 1)(RF(rb, idx, 4, 0)), 1, 1, None, 0) == 2     # N % 64
