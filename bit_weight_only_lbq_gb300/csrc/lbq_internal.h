@@ -56,4 +56,32 @@ lbq_status launch_w2_mma(const void* packed, int64_t N, int64_t K, int32_t n_out
                          uint32_t flags, int* launches);
 double host_f16_to_f64(uint16_t h);
 
+// Work split of the tensor-core kernels: T tiles of Ut stages each are cut into
+// G clusters of consecutive tiles (cluster c: tiles [t0, t1)), and a cluster's
+// units = (t1 - t0) x Ut stages into C contiguous ranges (rank r: [u0, u1)).
+// 32-bit arithmetic (the planner keeps T x Ut x C below 2^31): the kernels
+// evaluate these in their prologue and epilogue, where 64-bit divisions cost
+// microseconds.
+LBQ_HOST_DEVICE inline void cluster_tiles(int T, int G, int c, int* t0, int* t1) {
+    *t0 = T * c / G;
+    *t1 = T * (c + 1) / G;
+}
+LBQ_HOST_DEVICE inline void rank_range(int units, int C, int r, int* u0, int* u1) {
+    *u0 = units * r / C;
+    *u1 = units * (r + 1) / C;
+}
+// The rank whose range holds stage u (ranges are contiguous and ascending).
+LBQ_HOST_DEVICE inline int rank_of(int units, int C, int u) {
+    int r = (u * C) / (units > 0 ? units : 1);
+    if (r > C - 1) r = C - 1;
+    while (r > 0 && units * r / C > u) --r;
+    while (r + 1 < C && units * (r + 1) / C <= u) ++r;
+    return r;
+}
+// The cluster size C and cluster count G that give the fewest stages to the
+// busiest CTA, every CTA's range spanning at most `bands` tiles; active[c] is
+// the number of clusters of size c that fit the device at once (0: none).
+// False when no cluster size fits (lbq_mma.cu).
+bool mma_plan(int T, int Ut, int bands, const int* active, int* C_out, int* G_out, int* load_out);
+
 }  // namespace lbq

@@ -271,24 +271,6 @@ __device__ __forceinline__ void w2_order(const uint32_t (&n)[8], uint32_t (&o)[8
     o[7] = prmt(n[5], n[7], 0x7632u);
 }
 
-// Units of cluster c: tiles [t0, t1) x Ut stages; rank r takes [u0, u1).
-__host__ __device__ inline void cluster_tiles(int T, int G, int c, int* t0, int* t1) {
-    *t0 = static_cast<int>(static_cast<long long>(T) * c / G);
-    *t1 = static_cast<int>(static_cast<long long>(T) * (c + 1) / G);
-}
-__host__ __device__ inline void rank_range(long long units, int C, int r, long long* u0, long long* u1) {
-    *u0 = units * r / C;
-    *u1 = units * (r + 1) / C;
-}
-// The rank whose range holds unit u (ranges are contiguous and ascending).
-__host__ __device__ inline int rank_of(long long units, int C, long long u) {
-    int r = static_cast<int>((u * C) / (units > 0 ? units : 1));
-    if (r > C - 1) r = C - 1;
-    while (r > 0 && units * r / C > u) --r;
-    while (r + 1 < C && units * (r + 1) / C <= u) ++r;
-    return r;
-}
-
 }  // namespace
 
 namespace {
@@ -322,14 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int C = a.C, U = a.U, Ut = a.Ut;
     const int cl = static_cast<int>(blockIdx.x) / C, rank = static_cast<int>(blockIdx.x) % C;
     int t0, t1;
-    cluster_tiles(a.T, a.G, cl, &t0, &t1);
-    const long long units = static_cast<long long>(t1 - t0) * Ut;
-    long long lu0, lu1;
-    rank_range(units, C, rank, &lu0, &lu1);
+    lbq::cluster_tiles(a.T, a.G, cl, &t0, &t1);
+    const int units = (t1 - t0) * Ut;
+    int lu0, lu1;
+    lbq::rank_range(units, C, rank, &lu0, &lu1);
     // this CTA's stages: units [u0, u1) of the cluster, unit u = stage u % Ut of tile
     // t0 + u / Ut (stage c < U: k in [64 c, 64 c + 64); c >= U: outlier columns
     // [64 (c - U), 64 (c - U) + 64))
-    const int u0 = static_cast<int>(lu0), u1 = static_cast<int>(lu1);
+    const int u0 = lu0, u1 = lu1;
     const int nst = u1 - u0;
     const int first_tile = t0 + (nst > 0 ? u0 / Ut : 0);
     const int nbands = nst > 0 ? (u1 - 1) / Ut - u0 / Ut + 1 : 0;   // tiles touched (<= 2)
@@ -760,8 +742,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // contributors of tile t: the ranks whose ranges hold its first and last stage
     auto contributors = [&](int t, int* rlo, int* rhi) {
-        *rlo = rank_of(units, C, static_cast<long long>(t - t0) * Ut);
-        *rhi = rank_of(units, C, static_cast<long long>(t - t0 + 1) * Ut - 1);
+        *rlo = lbq::rank_of(units, C, (t - t0) * Ut);
+        *rhi = lbq::rank_of(units, C, (t - t0 + 1) * Ut - 1);
     };
     auto store_y = [&](int m, long long n, float v) {
         if (a.y_f32)
@@ -819,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (w4 <= 0) continue;
             // the contributors' band of this tile: 0, except for the first contributor
             // when its range starts in the tile before
-            const int bp_lo = t0 + static_cast<int>((units * rlo / C) / Ut) < t ? 1 : 0;
+            const int bp_lo = t0 + (units * rlo / C) / Ut < t ? 1 : 0;
             const int ne = a.M * w4;
             for (int e0 = tid; e0 < ne; e0 += 2 * kThreads) {
                 // two elements a thread, every load of both in flight, then the sums in rank order
@@ -963,6 +945,8 @@ namespace lbq {
 // with every CTA's range spanning at most as many tiles as the accumulator has
 // lane bands.  False when no cluster size fits.
 bool mma_plan(int T, int Ut, int bands, const int* active, int* C_out, int* G_out, int* load_out) {
+    // the split is evaluated in 32-bit arithmetic on the device
+    if (T < 1 || Ut < 1 || T > 32768 || static_cast<long long>(T) * Ut * kMaxCluster >= (1ll << 31)) return false;
     int bestC = 0, bestG = 0;
     long long best = -1;
     for (int c = 1; c <= kMaxCluster; ++c) {
@@ -974,9 +958,9 @@ bool mma_plan(int T, int Ut, int bands, const int* active, int* C_out, int* G_ou
         for (int cl = 0; cl < g && fits; ++cl) {
             int t0, t1;
             cluster_tiles(T, g, cl, &t0, &t1);
-            const long long units = static_cast<long long>(t1 - t0) * Ut;
+            const int units = (t1 - t0) * Ut;
             for (int r = 0; r < c; ++r) {
-                long long u0, u1;
+                int u0, u1;
                 rank_range(units, c, r, &u0, &u1);
                 if (u1 - u0 > load) load = u1 - u0;
                 if (u1 > u0 && (u1 - 1) / Ut - u0 / Ut + 1 > bands) fits = false;

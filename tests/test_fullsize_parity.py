@@ -2,7 +2,8 @@
 times: the Llama-3-8B layer sweep of seven 4-bit linears (one grouped launch),
 the same layer in the 2-bit codebook format with its 3.5 % profile-selected
 outlier columns (one grouped launch), the 4-bit gate + down projections at
-M = 4 activation rows (one grouped launch), and the Llama-3-70B layer (one
+M = 4 activation rows (one grouped launch) and on the tensor cores at M = 16
+and 32, and the Llama-3-70B layer (one
 grouped launch) and lm_head (one call).  Inputs are the bench's own seeded
 synthetic weights and activations (rank 0).  The oracle is computed over row
 chunks by worker processes (exact: rows are independent in the blob format).
@@ -67,6 +68,25 @@ def test_w2_layer_sweep_every_row(lbq, ex):
 
 def test_w4_small_m_gate_down_every_row(lbq, ex):
     _sweep(lbq, ex, "w4", [(li, synth.LLAMA3_8B_LINEARS[li]) for li in (4, 6)], cfg=4, M=4)
+
+
+@pytest.mark.parametrize("M", [16, 32])
+def test_w4_tensor_core_gate_down_every_row(lbq, ex, M):
+    """The 4-bit tensor-core kernel at full size: gate (112 tiles, a CTA each)
+    and down (K split over clusters of 4), every row."""
+    for li in (4, 6):
+        name, N, K = synth.LLAMA3_8B_LINEARS[li]
+        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
+        X = synth.activations(M, K, config_id=4, layer_id=li)
+        fut = oracle_rows.submit(ex, "w4", W, np.zeros(0, np.int32), X)
+        blob = lbq.pack_w4(W)
+        del W
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda:0")
+        b, x = to_dev(blob), to_dev(X)
+        lbq.gemm_w4a16_smallM(b, M, N, K, 0, x, K, y, N)
+        torch.cuda.synchronize()
+        assert lbq.device_error() == 0
+        assert_close(y.cpu().numpy(), oracle_rows.collect(fut), what="w4 tensor cores %s M=%d every row" % (name, M))
 
 
 def test_70b_layer_every_row(lbq, ex):

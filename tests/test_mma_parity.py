@@ -1,7 +1,7 @@
 """GPU parity of the tensor-core small-M GEMMs (16 <= M <= 64) against the FP64
 oracle, element by element, for both weight formats: 4-bit (weights dequantised
-into tensor memory, 128-row tiles, K split over a cluster; no outlier columns)
-and 2-bit codebook (weights as the 256-wide operand in shared memory, 256-row
+into tensor memory, 128-row tiles, K split over a cluster when the tiles leave
+SMs idle) and 2-bit codebook (weights as the 256-wide operand in shared memory, 256-row
 tiles and 256-k chunks split over a cluster, each CTA's range spanning at most
 two tiles with one accumulator each; taller matrices go in slabs of tiles, one
 launch each; the exact FP16 outlier columns are extra 64-column stages of the
@@ -57,11 +57,11 @@ def _run(lbq, kind, blob, M, N, K, X, ldx=None, ldy=None, f32=True):
 
 
 # (M, N, K): ragged tiles, partial records, one tile split over a cluster, many
-# tiles (CTA ranges that span two tiles: both accumulators in use), and more
-# tiles than one launch takes (two slabs of tiles)
+# tiles (2-bit: CTA ranges that span two tiles, both accumulators in use; 4-bit:
+# a CTA per tile, 80-112 tiles), and more tiles than one launch takes (two slabs)
 SHAPES = [(16, 256, 1024), (16, 1, 64), (17, 70, 1088), (32, 257, 3072), (33, 300, 2112), (48, 513, 4096),
           (64, 1000, 1024), (64, 256, 8192), (40, 600, 7168), (16, 4100, 1024), (24, 9000, 2048),
-          (64, 14336, 1024), (20, 4096, 4096), (16, 80000, 64)]
+          (64, 14336, 1024), (20, 4096, 4096), (16, 80000, 64), (16, 14336, 1024), (32, 10000, 2048)]
 
 
 @pytest.mark.parametrize("kind", ["w4", "w2"])
@@ -133,10 +133,11 @@ def _run_out(lbq, blob, M, N, K, n_out, X, f32=True, kind="w2"):
 # (M, N, K, n_out): one outlier column; 77 (a trimmed last record, two 64-column
 # stages); 256 (one full record); 257 (a full record and an 8-column one); 501 over
 # two records at K = 14336; 1000 (four records, four outlier chunks); every column
-# an outlier; outliers with two tiles per CTA range and with two slabs
+# an outlier; outliers with two tiles per CTA range (2-bit at 9000 and 10000
+# rows) and with two slabs
 OUT_SHAPES = [(16, 300, 1024, 1), (17, 70, 2112, 77), (32, 513, 4096, 256), (64, 257, 2048, 257),
               (16, 512, 14336, 501), (40, 1000, 4096, 1000), (24, 100, 128, 128), (48, 9000, 2048, 61),
-              (16, 80000, 64, 9)]
+              (16, 80000, 64, 9), (32, 10000, 2048, 61)]
 
 
 @pytest.mark.parametrize("kind", ["w2", "w4"])
