@@ -505,46 +505,72 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // exact FP16 outlier columns (SPECTRA section 4.2, in-kernel outlier fusion):
     // d[i] += sum_j X[16 cc + i][idx_j] Wout[n][j], in FP32, columns in order, by the
-    // CTA that writes y.  In chunks of 64 columns: the chunk's X[:, idx] (NM rows,
-    // zero past M) staged once in the idle activation ring as FP32, each thread's
-    // 64 outlier values of row n read from its row block's outlier record.
-    auto add_outliers = [&]() {
+    // CTA's partial.  In chunks of 64 columns (chunks c0, c0 + cs, ...: with K
+    // split over a cluster every rank adds its share of the chunks to its own
+    // partial, which the rank-order reduction then sums): the chunk's X[:, idx] (NM rows,
+    // zero past M) and the tile's outlier values of the chunk are staged in shared
+    // memory by the whole CTA with every load in flight (one round trip to memory
+    // per chunk), then each thread adds its row's 64 columns.
+    auto add_outliers = [&](int c0, int cs) {
         if (a.n_out <= 0 || bad) return;
+        // staging areas over the idle rings: the chunk's activations X[:, idx] as FP32
+        // (activation ring), the outlier channels (once) and the tile's 128 rows x 64
+        // FP16 outlier values of the chunk (nibble ring, past the split-K partials;
+        // rows padded to 144 bytes: conflict-free 16-byte reads by row)
         float* xo = reinterpret_cast<float*>(smem + G::b);
-        const int rbn = static_cast<int>(n >> 2), rn = static_cast<int>(n & 3);
-        for (int j0 = 0; j0 < a.n_out; j0 += 64) {
-            __syncthreads();   // the previous chunk has been read
+        int* ids = reinterpret_cast<int*>(smem + G::code + 32768);
+        uint8_t* wo = smem + G::code + 32768 + 4 * lbq::kMaxOutliers;
+        constexpr int kWoRow = 144;
+        static_assert(G::kNC * kCodeStage >= 32768 + 4 * lbq::kMaxOutliers + kTileRows * kWoRow,
+                      "outlier staging fits the nibble ring");
+        __syncthreads();   // every thread is past the partials' reads
+        for (int j = tid; j < a.n_out; j += kThreads) {
+            const int k = a.idx[j];
+            const bool ok_k = k >= 0 && k < a.K;
+            if (!ok_k) atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_OUTLIER_IDX));   // corrupted blob
+            ids[j] = ok_k ? k : -1;
+        }
+        const int nrow = static_cast<int>(n - static_cast<long long>(rb0) * 4);   // this thread's tile row
+        for (int j0 = 64 * c0; j0 < a.n_out; j0 += 64 * cs) {
+            const int nj = min(64, a.n_out - j0);
+            const int o = j0 / lbq::kOutlierCols, width = o + 1 < a.OT ? lbq::kOutlierCols : a.cols_last;
+            __syncthreads();   // the channels are staged, the previous chunk has been read
+            // the tile's outlier values of the chunk: 128 rows x 8 loads of 16 bytes, every
+            // load in flight at once (zero padding past n_out within a record)
+            for (int e = tid; e < kTileRows * 8; e += kThreads) {
+                const int row = e >> 3, u = e & 7, rb = rb0 + (row >> 2);
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (rb < a.n_rb && 8 * u < nj)
+                    v = *reinterpret_cast<const uint4*>(
+                        a.out0 + static_cast<long long>(rb) * a.rb_bytes +
+                        static_cast<long long>(o) * (lbq::kOutlierCols * lbq::kRowsPerBlock * 2) +
+                        (static_cast<long long>(row & 3) * width + j0 % lbq::kOutlierCols + 8 * u) * 2);
+                *reinterpret_cast<uint4*>(wo + row * kWoRow + 16 * u) = v;
+            }
             for (int e = tid; e < NM * 64; e += kThreads) {
                 const int row = e >> 6, j = j0 + (e & 63);
                 float v = 0.f;
                 if (row < a.M && j < a.n_out) {
-                    const int k = a.idx[j];
-                    if (k >= 0 && k < a.K)
-                        v = __half2float(a.x[row * a.ldx + k]);
-                    else
-                        atomicCAS(a.err, 0u, static_cast<unsigned>(LBQ_ERR_OUTLIER_IDX));
+                    const int k = ids[j];
+                    if (k >= 0) v = __half2float(a.x[row * a.ldx + k]);
                 }
                 xo[e] = v;
             }
             __syncthreads();
             if (ep && n < a.N) {
-                const int o = j0 / lbq::kOutlierCols, width = o + 1 < a.OT ? lbq::kOutlierCols : a.cols_last;
-                const int nj = min(64, a.n_out - j0);
-                const uint4* wrow = reinterpret_cast<const uint4*>(
-                    a.out0 + static_cast<long long>(rbn) * a.rb_bytes +
-                    static_cast<long long>(o) * (lbq::kOutlierCols * lbq::kRowsPerBlock * 2) +
-                    (static_cast<long long>(rn) * width + j0 % lbq::kOutlierCols) * 2);
                 const float4* xo4 = reinterpret_cast<const float4*>(xo + 16 * cc * 64);
+                const uint8_t* wr = wo + nrow * kWoRow;
 #pragma unroll 1
-                for (int j8 = 0; j8 < nj; j8 += 8) {
-                    const uint4 wv = wrow[j8 / 8];   // 8 FP16 outlier values (past n_out: zero padding)
+                for (int u = 0; u < 8; ++u) {
+                    if (8 * u >= nj) break;
+                    const uint4 wv = *reinterpret_cast<const uint4*>(wr + 16 * u);   // 8 FP16 outlier values
                     const float2 w0 = __half22float2(*reinterpret_cast<const __half2*>(&wv.x));
                     const float2 w1 = __half22float2(*reinterpret_cast<const __half2*>(&wv.y));
                     const float2 w2 = __half22float2(*reinterpret_cast<const __half2*>(&wv.z));
                     const float2 w3 = __half22float2(*reinterpret_cast<const __half2*>(&wv.w));
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float4 xa = xo4[i * 16 + j8 / 4], xb = xo4[i * 16 + j8 / 4 + 1];
+                        const float4 xa = xo4[i * 16 + 2 * u], xb = xo4[i * 16 + 2 * u + 1];
                         float t = d[i];
                         t = fmaf(w0.x, xa.x, t);
                         t = fmaf(w0.y, xa.y, t);
@@ -561,9 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
     if (S == 1) {
-        add_outliers();
+        add_outliers(0, 1);
         if (ep) write_y();
     } else {
+        add_outliers(rank, S);
         // split K: partials through distributed shared memory, added in rank order by rank 0
         float* part = reinterpret_cast<float*>(smem + G::code);   // NM x 128 FP32 over the (idle) nibble ring
         if (ep)
@@ -584,7 +611,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         d[i] += v;
                     }
                 }
-            add_outliers();
             if (ep) write_y();
         }
         asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
