@@ -3,7 +3,8 @@ times: the Llama-3-8B layer sweep of seven 4-bit linears (one grouped launch),
 the same layer in the 2-bit codebook format with its 3.5 % profile-selected
 outlier columns (one grouped launch), the 4-bit gate + down projections at
 M = 4 activation rows (one grouped launch) and on the tensor cores at M = 16
-and 32, and the Llama-3-70B layer (one
+and 32, the 2-bit gate with its outlier columns on the tensor cores at M = 16,
+and the Llama-3-70B layer (one
 grouped launch) and lm_head (one call).  Inputs are the bench's own seeded
 synthetic weights and activations (rank 0).  The oracle is computed over row
 chunks by worker processes (exact: rows are independent in the blob format).
@@ -87,6 +88,26 @@ def test_w4_tensor_core_gate_down_every_row(lbq, ex, M):
         torch.cuda.synchronize()
         assert lbq.device_error() == 0
         assert_close(y.cpu().numpy(), oracle_rows.collect(fut), what="w4 tensor cores %s M=%d every row" % (name, M))
+
+
+def test_w2_tensor_core_gate_with_outliers_every_row(lbq, ex):
+    """The 2-bit tensor-core kernel at full size with its profile-selected 3.5 %
+    outlier columns (gate projection, M = 16: CTA ranges over two tiles, outlier
+    stages at every tile's end), every row."""
+    M = 16
+    li = 4
+    name, N, K = synth.LLAMA3_8B_LINEARS[li]
+    W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
+    idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=3, layer_id=li))
+    X = synth.activations(M, K, config_id=3, layer_id=li)
+    fut = oracle_rows.submit(ex, "w2", W, idx, X)
+    blob = lbq.pack_w2cb(W, idx)
+    del W
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda:0")
+    lbq.gemm_w2cb_outlier_smallM(to_dev(blob), M, N, K, len(idx), to_dev(X), K, y, N)
+    torch.cuda.synchronize()
+    assert lbq.device_error() == 0
+    assert_close(y.cpu().numpy(), oracle_rows.collect(fut), what="w2 tensor cores %s M=%d every row" % (name, M))
 
 
 def test_70b_layer_every_row(lbq, ex):
