@@ -481,14 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && !*abort_flag) {
                     const uint32_t row = sb + F::kA + as * kAStage + arow;
                     uint32_t w[32];
-                    // outlier stage, x[idx_j] of its 64 outlier columns in order: up to 16 rows,
-                    // lane l gathers columns l and 32 + l of every row; more rows, lane = row
-                    // (each with every load in flight)
-                    const bool tgather = a.Mr <= 16;
-                    if (c >= U && tgather) {
-                        // lane l: columns l and 32 + l for the warp's rows (rows past M and
-                        // invalid channels give 0), stored in place, 2 bytes each, at their
-                        // swizzled positions
+                    if (c >= U) {
+                        // outlier stage: x[idx_j] of its 64 outlier columns, in order.  Lane l
+                        // gathers columns l and 32 + l of 16-row batches - activation warp w
+                        // takes rows 16 w .. 16 w + 15 and 32 + 16 w .. 32 + 16 w + 15 - with
+                        // every load of a batch in flight (rows past M and invalid channels
+                        // give 0), and stores them in place, 2 bytes each, at their swizzled
+                        // positions
                         const int j0 = kStageK * (c - U);   // first outlier column
                         const int ja = j0 + lane, jb = j0 + 32 + lane;
                         const int ka = ja < a.n_out ? __ldg(a.idx + ja) : -1;
@@ -497,8 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const unsigned short* xs = reinterpret_cast<const unsigned short*>(a.x);
                         const uint32_t abase = sb + F::kA + as * kAStage;
                         const uint32_t ca = static_cast<uint32_t>(lane >> 3), off = static_cast<uint32_t>((lane & 7) * 2);
-                        const int r0 = m - lane;   // the warp's first row
-                        for (int mb = r0; mb < r0 + 32 && mb < a.Mr; mb += 16) {
+                        auto gather_rows = [&](int mb) {
                             unsigned short va[16], vb[16];
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
@@ -519,25 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  : "memory");
                                 }
                             }
-                        }
+                        };
+#pragma unroll 1
+                        for (int mb = m - lane == 0 ? 0 : 16; mb < a.Mr; mb += 32) gather_rows(mb);   // this warp's batches
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // read by the tensor core
-                    } else if (c >= U) {
-                        // lane = row: the warp's lanes load the stage's 64 indices (2 each), pass
-                        // them round by shuffles, and every lane has all 64 of its row's loads in
-                        // flight at once (clamped addresses; invalid ones give 0)
-                        const int j0 = kStageK * (c - U);
-                        const int ja = j0 + lane, jb = j0 + 32 + lane;
-                        const int ka = ja < a.n_out ? __ldg(a.idx + ja) : -1;
-                        const int kb = jb < a.n_out ? __ldg(a.idx + jb) : -1;
-                        const unsigned short* xr = reinterpret_cast<const unsigned short*>(a.x) + (m < a.M ? m : 0) * a.ldx;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int klo = __shfl_sync(0xffffffffu, e < 16 ? ka : kb, (2 * e) & 31);
-                            const int khi = __shfl_sync(0xffffffffu, e < 16 ? ka : kb, (2 * e + 1) & 31);
-                            const bool vlo = m < a.M && klo >= 0 && klo < a.K, vhi = m < a.M && khi >= 0 && khi < a.K;
-                            const uint32_t lo = __ldg(xr + (vlo ? klo : 0)), hi = __ldg(xr + (vhi ? khi : 0));
-                            w[e] = (vlo ? lo : 0u) | ((vhi ? hi : 0u) << 16);
-                        }
                     } else if (m < a.Mr) {
                         const int s = c;   // k in [64 s, 64 s + 64)
 #pragma unroll
@@ -568,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 8; ++e) w[8 * blk + e] = o[e];
                         }
                     }
-                    if ((c < U || !tgather) && m < a.Mr) {
+                    if (c < U && m < a.Mr) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             sts128(row + ((j ^ asw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
