@@ -172,21 +172,21 @@ def make_workload(lbq, rank: int):
     """Pack the step's 16 matrices on the host (C++ packers) and return host data."""
     layer = []
     for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
-        W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li + 100 * rank)
-        x = synth.activations(1, K, config_id=2, layer_id=li)[0]
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W4, layer_id=li + 100 * rank)
+        x = synth.activations(1, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)[0]
         layer.append(dict(kind="w4", name=name, N=N, K=K, n_out=0, M=1, blob=lbq.pack_w4(W), x=x,
                           W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=np.zeros(0, np.int32), li=li + 100 * rank))
     for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
-        W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li + 100 * rank)
-        prof = synth.profile_vectors(K, config_id=3, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W2, layer_id=li + 100 * rank)
+        prof = synth.profile_vectors(K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
         idx = lbq.select_outliers_impact(W, prof, 0.035)
-        x = synth.activations(1, K, config_id=3, layer_id=li)[0]
+        x = synth.activations(1, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)[0]
         layer.append(dict(kind="w2", name=name, N=N, K=K, n_out=len(idx), M=1, blob=lbq.pack_w2cb(W, idx), x=x,
                           W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=idx))
     for li in (4, 6):
         name, N, K = synth.LLAMA3_8B_LINEARS[li]
-        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li + 100 * rank)
-        X = synth.activations(SMALL_M, K, config_id=4, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_SMALL_M, layer_id=li + 100 * rank)
+        X = synth.activations(SMALL_M, K, workload=synth.WL_SMALL_M, layer_id=li)
         layer.append(dict(kind="w4m", name=name, N=N, K=K, n_out=0, M=SMALL_M, blob=lbq.pack_w4(W), x=X,
                           W_head=W[:SAMPLE_ROWS_MAX].copy(), idx=np.zeros(0, np.int32)))
     for e in layer:
@@ -251,19 +251,19 @@ def oracle_workload(rows: int):
     from oracle import lbq_oracle as O
     layer = []
     for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
-        W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)
         layer.append(dict(kind="w4", name=name, N=N, K=K, n_out=0, M=1, W_head=W[:rows].copy(),
-                          idx=np.zeros(0, np.int32), x=synth.activations(1, K, config_id=2, layer_id=li)[0]))
+                          idx=np.zeros(0, np.int32), x=synth.activations(1, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)[0]))
     for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
-        W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
-        idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=3, layer_id=li))
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
+        idx = O.select_outliers_impact(W, synth.profile_vectors(K, workload=synth.WL_LLAMA8B_W2, layer_id=li))
         layer.append(dict(kind="w2", name=name, N=N, K=K, n_out=len(idx), M=1, W_head=W[:rows].copy(), idx=idx,
-                          x=synth.activations(1, K, config_id=3, layer_id=li)[0]))
+                          x=synth.activations(1, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)[0]))
     for li in (4, 6):
         name, N, K = synth.LLAMA3_8B_LINEARS[li]
-        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_SMALL_M, layer_id=li)
         layer.append(dict(kind="w4m", name=name, N=N, K=K, n_out=0, M=SMALL_M, W_head=W[:rows].copy(),
-                          idx=np.zeros(0, np.int32), x=synth.activations(SMALL_M, K, config_id=4, layer_id=li)))
+                          idx=np.zeros(0, np.int32), x=synth.activations(SMALL_M, K, workload=synth.WL_SMALL_M, layer_id=li)))
     return layer
 
 
@@ -315,7 +315,7 @@ def oracle_figures(layer, rows: int, reps: int) -> dict:
 
 
 def oracle_70b_extrapolated(rows: int = 8) -> dict:
-    """Config 5 on the host: one sample of `rows` rows of each Llama-3-70B linear
+    """The Llama-3-70B decode weight sweep on the host: one sample of `rows` rows of each Llama-3-70B linear
     shape and of the lm_head, oracle dequantise-from-bytes + matvec, scaled by
     each shape's rows and count to one token's 80 x 7 + 1 matrices.  Extrapolated,
     never run whole (the oracle would hold 69.5 G FP64 weights)."""
@@ -326,9 +326,9 @@ def oracle_70b_extrapolated(rows: int = 8) -> dict:
     hn, hN, hK = synth.LLAMA3_70B_LM_HEAD
     shapes.append((hn, hN, hK, 1))
     for name, N, K, count in shapes:
-        W = synth.weights_heavy_cols(rows, K, config_id=5, layer_id=len(parts))
+        W = synth.weights_heavy_cols(rows, K, workload=synth.WL_LLAMA70B, layer_id=len(parts))
         blob = O.pack_w4(W)
-        x = synth.activations(1, K, config_id=5, layer_id=K)[0]
+        x = synth.activations(1, K, workload=synth.WL_LLAMA70B, layer_id=K)[0]
         t = time.perf_counter()
         O.gemm(blob, x)
         dt = time.perf_counter() - t
@@ -384,8 +384,8 @@ def run_reference(args, rank, world):
 
 
 def config_dict():
-    return {"workload": "llama3_8b_layer_decode: 7 linears W4A16 G32 (cfg2) + 7 linears W2 Lloyd-Max G32 with "
-                        "top-3.5% FP16 outliers (cfg3) + W4 gate/down small-M M=4 (cfg4), one token; each row "
+    return {"workload": "llama3_8b_layer_decode: 7 linears W4A16 G32 + 7 linears W2 Lloyd-Max G32 with "
+                        "top-3.5% FP16 outliers + W4 gate/down small-M M=4, one token; each row "
                         "one fused sweep (grouped launch) over its matrices",
             "linears": [list(x) for x in synth.LLAMA3_8B_LINEARS], "small_m": SMALL_M,
             "l2": "inputs larger than L2: 3 rotating replicas of the 291 MB step",
@@ -680,7 +680,7 @@ def run_refinement(lbq, layer, dev, stream, replays=20):
         if e["kind"] != "w4":
             continue
         N, K = e["N"], e["K"]
-        R = (synth.weights_heavy_cols(N, K, config_id=2, layer_id=e["li"]) - lbq.dequant_host(e["blob"]))
+        R = (synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W4, layer_id=e["li"]) - lbq.dequant_host(e["blob"]))
         rblob = lbq.pack_refine(R.astype(np.float32))
         rblobs.append(rblob)
         del R
@@ -809,7 +809,7 @@ FMA_PEAK = 152 * 128 * 2.07e9       # FP32 FMA lanes of a GB300 (152 SMs x 128 a
 
 
 def run_smallm_sweep(lbq, dev, stream, replays=5):
-    """Config 4 across M: the 4-bit gate (14336 x 4096) and down (4096 x 14336)
+    """The batched 4-bit GEMM across M: the 4-bit gate (14336 x 4096) and down (4096 x 14336)
     projections at M = 2..64 (CUDA cores below 16, tensor cores from 16) and
     with their saliency-selected outlier columns at M = 16 / 64, the 2-bit ones
     with 3.5 % outlier columns (CUDA cores below 16, tensor cores from 16) and
@@ -829,7 +829,7 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
     cases = []
     for li in (4, 6):
         name, N, K = synth.LLAMA3_8B_LINEARS[li]
-        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_SMALL_M, layer_id=li)
         b4 = lbq.pack_w4(W)
         for M in (2, 4, 8, 16, 32, 64):
             cases.append(("w4", name, N, K, M, 0, b4))
@@ -837,8 +837,8 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
         b4o = lbq.pack_w4(W, idx4)
         for M in (16, 64):
             cases.append(("w4", name, N, K, M, len(idx4), b4o))
-        W2 = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
-        idx = lbq.select_outliers_impact(W2, synth.profile_vectors(K, config_id=3, layer_id=li), 0.035)
+        W2 = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
+        idx = lbq.select_outliers_impact(W2, synth.profile_vectors(K, workload=synth.WL_LLAMA8B_W2, layer_id=li), 0.035)
         b2o = lbq.pack_w2cb(W2, idx)
         for M in (2, 4, 8, 16, 32, 64):
             cases.append(("w2", name, N, K, M, len(idx), b2o))
@@ -851,7 +851,7 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
         n = max(REPLICAS, -(-L2_ROTATION_BYTES // blob.size))
         d0 = torch.from_numpy(blob).to(dev)
         cps = [d0] + [d0.clone() for _ in range(n - 1)]
-        X = torch.from_numpy(synth.activations(M, K, config_id=4, layer_id=0)).to(dev)
+        X = torch.from_numpy(synth.activations(M, K, workload=synth.WL_SMALL_M, layer_id=0)).to(dev)
         Y = torch.empty((M, N), dtype=torch.float16, device=dev)
         f = lbq.gemm_w4a16_smallM if kind == "w4" else lbq.gemm_w2cb_outlier_smallM
         with torch.cuda.stream(stream):
@@ -891,7 +891,7 @@ def run_smallm_sweep(lbq, dev, stream, replays=5):
 
 
 def run_sweep70b(lbq, dev, stream, replays=5):
-    """Config 5: one decode token through every linear of a Llama-3-70B-shaped
+    """The Llama-3-70B decode weight sweep: one decode token through every linear of a Llama-3-70B-shaped
     model (80 layers x 7 linears + lm_head, W4A16 G32, M = 1): 40.2 GB of packed
     weights streamed per token.  One layer is packed on the host (seeded, config
     5 distribution) and replicated 80 times in device memory, so every layer
@@ -902,17 +902,17 @@ def run_sweep70b(lbq, dev, stream, replays=5):
     t_pack = time.time()
     layer = []
     for li, (name, N, K) in enumerate(synth.LLAMA3_70B_LINEARS):
-        W = synth.weights_heavy_cols(N, K, config_id=5, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA70B, layer_id=li)
         layer.append((name, N, K, torch.from_numpy(lbq.pack_w4(W)).to(dev)))
         del W
     hn, hN, hK = synth.LLAMA3_70B_LM_HEAD
-    W = synth.weights_heavy_cols(hN, hK, config_id=5, layer_id=99)
+    W = synth.weights_heavy_cols(hN, hK, workload=synth.WL_LLAMA70B, layer_id=99)
     head = torch.from_numpy(lbq.pack_w4(W)).to(dev)
     del W
     t_pack = time.time() - t_pack
     layers = [[b for (_, _, _, b) in layer]] + [[b.clone() for (_, _, _, b) in layer]
                                                 for _ in range(synth.LLAMA3_70B_LAYERS - 1)]
-    xs = {K: torch.from_numpy(synth.activations(1, K, config_id=5, layer_id=K)[0]).to(dev)
+    xs = {K: torch.from_numpy(synth.activations(1, K, workload=synth.WL_LLAMA70B, layer_id=K)[0]).to(dev)
           for K in sorted({K for (_, _, K, _) in layer} | {hK})}
     ys = [torch.empty(N, dtype=torch.float16, device=dev) for (_, N, _, _) in layer]
     yh = torch.empty(hN, dtype=torch.float16, device=dev)
@@ -1180,7 +1180,7 @@ def cpu_baseline() -> dict:
     """The oracle as it stands on the host cores, with inputs built by the oracle
     alone: (ii) dequantise-from-bytes + matvec over a row sample of every matrix of
     the step (the headline value, GB/s of algorithmic bytes), with (i) packing and
-    (iii) matvec on the cached matrix beside it, and config 5 extrapolated."""
+    (iii) matvec on the cached matrix beside it, and the Llama-3-70B sweep extrapolated."""
     rows = 128
     layer = oracle_workload(rows)
     step, _ = oracle_sample(layer, rows)

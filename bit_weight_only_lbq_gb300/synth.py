@@ -7,19 +7,20 @@ be fed from it without sharing any of the method's code.
 
 Distributions follow the synthetic workloads of the SPECTRA article (wpnews.pro,
 "Compress any LLM 3x ...", section 5.7 "Experiment A": Gaussian 2048x2048
-matrices) and the five decode configurations this library is measured on:
+matrices) and the five decode workloads this library is measured on (the
+WL_* ids below):
 
 * weights  W ~ N(0, 0.02^2), FP32, N x K row-major (one output per row);
-  cfg 1 additionally scales each row's std by U(0.5, 2);
-  cfgs 2/3/4/5 scale floor(0.01 K) randomly chosen input columns by 20;
+  the single 4096 x 4096 GEMV additionally scales each row's std by U(0.5, 2);
+  the others scale floor(0.01 K) randomly chosen input columns by 20;
 * activations x ~ N(0, 1) rounded to FP16, with floor(0.005 K) fixed
   "spike" channels multiplied by 100 (the emergent activation spikes the
   otf-llm page, section 4 "Profile-Guided Activation Outliers", describes);
 * the otf-llm calibration profile is replaced by 64 seeded vectors drawn
   like x, sharing the same spike channels.
 
-Seeds: numpy PCG64 through ``SeedSequence([config_id, layer_id, role_id])``,
-except config 1's weight matrix, which uses plain seed 0.
+Seeds: numpy PCG64 through ``SeedSequence([workload, layer_id, role_id])``,
+except the single 4096 x 4096 GEMV's weight matrix, which uses plain seed 0.
 """
 from __future__ import annotations
 
@@ -32,6 +33,13 @@ ROLE_SPIKES = 2
 ROLE_HEAVY_COLS = 3
 ROLE_PROFILE = 4
 ROLE_ROWSCALE = 5
+
+# workload ids (the first word of every seed)
+WL_SINGLE_4096 = 1      # one W4A16 GEMV, 4096 x 4096, M = 1
+WL_LLAMA8B_W4 = 2       # the seven Llama-3-8B decode linears, 4-bit, M = 1
+WL_LLAMA8B_W2 = 3       # the same shapes, 2-bit codebook with 3.5 % FP16 outlier columns
+WL_SMALL_M = 4          # batched 4-bit gate and down projections, M = 2..64
+WL_LLAMA70B = 5         # the Llama-3-70B full-model decode weight sweep
 
 W_STD = 0.02
 SPIKE_FRAC = 0.005
@@ -66,8 +74,8 @@ LLAMA3_70B_LM_HEAD = ("lm_head", 128256, 8192)
 SMALL_M_VALUES = (2, 4, 8, 16, 32, 64)
 
 
-def rng(config_id: int, layer_id: int, role_id: int) -> np.random.Generator:
-    return np.random.default_rng(np.random.SeedSequence([config_id, layer_id, role_id]))
+def rng(workload: int, layer_id: int, role_id: int) -> np.random.Generator:
+    return np.random.default_rng(np.random.SeedSequence([workload, layer_id, role_id]))
 
 
 def gaussian_weights(N: int, K: int, g: np.random.Generator, std: float = W_STD) -> np.ndarray:
@@ -77,48 +85,49 @@ def gaussian_weights(N: int, K: int, g: np.random.Generator, std: float = W_STD)
     return W
 
 
-def weights_cfg1(N: int = 4096, K: int = 4096) -> np.ndarray:
-    """Config 1: N(0, 0.02^2), seed 0, each row's std scaled by U(0.5, 2)."""
+def weights_row_scaled(N: int = 4096, K: int = 4096) -> np.ndarray:
+    """The single 4096 x 4096 GEMV's matrix: N(0, 0.02^2), seed 0, each row's std
+    scaled by U(0.5, 2)."""
     g = np.random.default_rng(0)
     W = gaussian_weights(N, K, g)
-    row_scale = rng(1, 0, ROLE_ROWSCALE).uniform(0.5, 2.0, size=(N, 1)).astype(np.float32)
+    row_scale = rng(WL_SINGLE_4096, 0, ROLE_ROWSCALE).uniform(0.5, 2.0, size=(N, 1)).astype(np.float32)
     W *= row_scale
     return W
 
 
-def heavy_columns(K: int, config_id: int, layer_id: int) -> np.ndarray:
+def heavy_columns(K: int, workload: int, layer_id: int) -> np.ndarray:
     n = int(HEAVY_COL_FRAC * K)
-    cols = rng(config_id, layer_id, ROLE_HEAVY_COLS).choice(K, size=n, replace=False)
+    cols = rng(workload, layer_id, ROLE_HEAVY_COLS).choice(K, size=n, replace=False)
     return np.sort(cols).astype(np.int64)
 
 
-def weights_heavy_cols(N: int, K: int, config_id: int, layer_id: int) -> np.ndarray:
+def weights_heavy_cols(N: int, K: int, workload: int, layer_id: int) -> np.ndarray:
     """N(0, 0.02^2) with floor(0.01 K) input columns multiplied by 20."""
-    W = gaussian_weights(N, K, rng(config_id, layer_id, ROLE_WEIGHT))
-    W[:, heavy_columns(K, config_id, layer_id)] *= np.float32(HEAVY_COL_MULT)
+    W = gaussian_weights(N, K, rng(workload, layer_id, ROLE_WEIGHT))
+    W[:, heavy_columns(K, workload, layer_id)] *= np.float32(HEAVY_COL_MULT)
     return W
 
 
-def spike_channels(K: int, config_id: int) -> np.ndarray:
+def spike_channels(K: int, workload: int) -> np.ndarray:
     """floor(0.005 K) fixed activation spike channels for a given width K."""
     n = int(SPIKE_FRAC * K)
-    ch = rng(config_id, K, ROLE_SPIKES).choice(K, size=n, replace=False)
+    ch = rng(workload, K, ROLE_SPIKES).choice(K, size=n, replace=False)
     return np.sort(ch).astype(np.int64)
 
 
-def activations(M: int, K: int, config_id: int, layer_id: int, stream: int = 0) -> np.ndarray:
+def activations(M: int, K: int, workload: int, layer_id: int, stream: int = 0) -> np.ndarray:
     """M x K float16: N(0,1) with the fixed spike channels scaled by 100."""
-    g = rng(config_id, layer_id, ROLE_X * 1000 + stream)
+    g = rng(workload, layer_id, ROLE_X * 1000 + stream)
     X = g.standard_normal((M, K))
-    X[:, spike_channels(K, config_id)] *= SPIKE_MULT
+    X[:, spike_channels(K, workload)] *= SPIKE_MULT
     return X.astype(np.float16)
 
 
-def profile_vectors(K: int, config_id: int, layer_id: int, P: int = PROFILE_VECTORS) -> np.ndarray:
+def profile_vectors(K: int, workload: int, layer_id: int, P: int = PROFILE_VECTORS) -> np.ndarray:
     """P x K float16 calibration stand-in, drawn like the activations."""
-    g = rng(config_id, layer_id, ROLE_PROFILE)
+    g = rng(workload, layer_id, ROLE_PROFILE)
     X = g.standard_normal((P, K))
-    X[:, spike_channels(K, config_id)] *= SPIKE_MULT
+    X[:, spike_channels(K, workload)] *= SPIKE_MULT
     return X.astype(np.float16)
 
 

@@ -28,16 +28,16 @@ def ex():
         yield e
 
 
-def _sweep(lbq, ex, kind, linears, cfg, M=1, fp16_out=False):
+def _sweep(lbq, ex, kind, linears, wl, M=1, fp16_out=False):
     probs, checks, keep = [], [], []
     for li, (name, N, K) in linears:
-        W = synth.weights_heavy_cols(N, K, config_id=cfg, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=wl, layer_id=li)
         if M == 1:
-            X = synth.activations(1, K, config_id=cfg, layer_id=li)
+            X = synth.activations(1, K, workload=wl, layer_id=li)
         else:
-            X = synth.activations(M, K, config_id=cfg, layer_id=li)
+            X = synth.activations(M, K, workload=wl, layer_id=li)
         if kind == "w2":
-            idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=cfg, layer_id=li))
+            idx = O.select_outliers_impact(W, synth.profile_vectors(K, workload=wl, layer_id=li))
             blob = lbq.pack_w2cb(W, idx)
         else:
             idx = np.zeros(0, np.int32)
@@ -60,15 +60,15 @@ def _sweep(lbq, ex, kind, linears, cfg, M=1, fp16_out=False):
 
 
 def test_w4_layer_sweep_every_row(lbq, ex):
-    _sweep(lbq, ex, "w4", list(enumerate(synth.LLAMA3_8B_LINEARS)), cfg=2)
+    _sweep(lbq, ex, "w4", list(enumerate(synth.LLAMA3_8B_LINEARS)), wl=synth.WL_LLAMA8B_W4)
 
 
 def test_w2_layer_sweep_every_row(lbq, ex):
-    _sweep(lbq, ex, "w2", list(enumerate(synth.LLAMA3_8B_LINEARS)), cfg=3)
+    _sweep(lbq, ex, "w2", list(enumerate(synth.LLAMA3_8B_LINEARS)), wl=synth.WL_LLAMA8B_W2)
 
 
 def test_w4_small_m_gate_down_every_row(lbq, ex):
-    _sweep(lbq, ex, "w4", [(li, synth.LLAMA3_8B_LINEARS[li]) for li in (4, 6)], cfg=4, M=4)
+    _sweep(lbq, ex, "w4", [(li, synth.LLAMA3_8B_LINEARS[li]) for li in (4, 6)], wl=synth.WL_SMALL_M, M=4)
 
 
 @pytest.mark.parametrize("M", [16, 32])
@@ -77,8 +77,8 @@ def test_w4_tensor_core_gate_down_every_row(lbq, ex, M):
     and down (K split over clusters of 4), every row."""
     for li in (4, 6):
         name, N, K = synth.LLAMA3_8B_LINEARS[li]
-        W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
-        X = synth.activations(M, K, config_id=4, layer_id=li)
+        W = synth.weights_heavy_cols(N, K, workload=synth.WL_SMALL_M, layer_id=li)
+        X = synth.activations(M, K, workload=synth.WL_SMALL_M, layer_id=li)
         fut = oracle_rows.submit(ex, "w4", W, np.zeros(0, np.int32), X)
         blob = lbq.pack_w4(W)
         del W
@@ -97,9 +97,9 @@ def test_w2_tensor_core_gate_with_outliers_every_row(lbq, ex):
     M = 16
     li = 4
     name, N, K = synth.LLAMA3_8B_LINEARS[li]
-    W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
-    idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=3, layer_id=li))
-    X = synth.activations(M, K, config_id=3, layer_id=li)
+    W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
+    idx = O.select_outliers_impact(W, synth.profile_vectors(K, workload=synth.WL_LLAMA8B_W2, layer_id=li))
+    X = synth.activations(M, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
     fut = oracle_rows.submit(ex, "w2", W, idx, X)
     blob = lbq.pack_w2cb(W, idx)
     del W
@@ -111,13 +111,13 @@ def test_w2_tensor_core_gate_with_outliers_every_row(lbq, ex):
 
 
 def test_70b_layer_every_row(lbq, ex):
-    _sweep(lbq, ex, "w4", list(enumerate(synth.LLAMA3_70B_LINEARS)), cfg=5, fp16_out=True)
+    _sweep(lbq, ex, "w4", list(enumerate(synth.LLAMA3_70B_LINEARS)), wl=synth.WL_LLAMA70B, fp16_out=True)
 
 
 def test_70b_lm_head_every_row(lbq, ex):
     name, N, K = synth.LLAMA3_70B_LM_HEAD
-    W = synth.weights_heavy_cols(N, K, config_id=5, layer_id=99)
-    x = synth.activations(1, K, config_id=5, layer_id=K)
+    W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA70B, layer_id=99)
+    x = synth.activations(1, K, workload=synth.WL_LLAMA70B, layer_id=K)
     fut = oracle_rows.submit(ex, "w4", W, np.zeros(0, np.int32), x, chunk=4096)
     blob = to_dev(lbq.pack_w4(W))
     del W

@@ -49,46 +49,46 @@ def _sampled_rows(N, rng, n=192):
     return rows[(rows >= 0) & (rows < N)]
 
 
-def _cfg_layer(cfg, N, K, layer):
-    if cfg == 1:
-        return synth.weights_cfg1(N, K)
-    return synth.weights_heavy_cols(N, K, config_id=cfg, layer_id=layer)
+def _layer_weights(wl, N, K, layer):
+    if wl == synth.WL_SINGLE_4096:
+        return synth.weights_row_scaled(N, K)
+    return synth.weights_heavy_cols(N, K, workload=wl, layer_id=layer)
 
 
 @pytest.mark.parametrize("li", range(len(synth.LLAMA3_8B_LINEARS)))
-def test_cfg2_llama8b_w4_sampled(lbq, li):
+def test_llama8b_w4_linears_sampled(lbq, li):
     name, N, K = synth.LLAMA3_8B_LINEARS[li]
-    W = _cfg_layer(2, N, K, li)
-    x = synth.activations(1, K, config_id=2, layer_id=li)[0]
+    W = _layer_weights(synth.WL_LLAMA8B_W4, N, K, li)
+    x = synth.activations(1, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)[0]
     rng = np.random.default_rng(li)
     rows = _sampled_rows(N, rng)
     for with_outliers in (False, True):
         idx = O.select_outliers_w4(W) if with_outliers else np.zeros(0, np.int32)
         y = _run(lbq, "w4", lbq.pack_w4(W, idx), N, K, len(idx), x)
         ref = O.gemv(O.pack_w4(W[rows], idx), x)
-        assert_close(y[rows], ref, what="cfg2 %s outliers=%s" % (name, with_outliers))
+        assert_close(y[rows], ref, what="llama8b w4 %s outliers=%s" % (name, with_outliers))
 
 
 @pytest.mark.parametrize("li", range(len(synth.LLAMA3_8B_LINEARS)))
-def test_cfg3_llama8b_w2_sampled(lbq, li):
+def test_llama8b_w2_linears_sampled(lbq, li):
     name, N, K = synth.LLAMA3_8B_LINEARS[li]
-    W = _cfg_layer(3, N, K, li)
-    x = synth.activations(1, K, config_id=3, layer_id=li)[0]
-    prof = synth.profile_vectors(K, config_id=3, layer_id=li)
+    W = _layer_weights(synth.WL_LLAMA8B_W2, N, K, li)
+    x = synth.activations(1, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)[0]
+    prof = synth.profile_vectors(K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
     idx = O.select_outliers_impact(W, prof)
     assert len(idx) == int(0.035 * K)
     rows = _sampled_rows(N, np.random.default_rng(100 + li))
     y = _run(lbq, "w2", lbq.pack_w2cb(W, idx), N, K, len(idx), x)
-    assert_close(y[rows], O.gemv(O.pack_w2cb(W[rows], idx), x), what="cfg3 %s" % name)
+    assert_close(y[rows], O.gemv(O.pack_w2cb(W[rows], idx), x), what="llama8b w2 %s" % name)
 
 
-def test_cfg1_full_elementwise(lbq):
-    W = synth.weights_cfg1()
-    x = synth.activations(1, 4096, config_id=1, layer_id=0)[0]
+def test_single_4096_full_elementwise(lbq):
+    W = synth.weights_row_scaled()
+    x = synth.activations(1, 4096, workload=synth.WL_SINGLE_4096, layer_id=0)[0]
     blob = lbq.pack_w4(W)
     ref = O.gemv(O.pack_w4(W), x)
-    assert_close(_run(lbq, "w4", blob, 4096, 4096, 0, x), ref, what="cfg1 f32")
-    assert_close(_run(lbq, "w4", blob, 4096, 4096, 0, x, f32=False), ref, fp16_out=True, what="cfg1 f16")
+    assert_close(_run(lbq, "w4", blob, 4096, 4096, 0, x), ref, what="single 4096 f32")
+    assert_close(_run(lbq, "w4", blob, 4096, 4096, 0, x, f32=False), ref, fp16_out=True, what="single 4096 f16")
 
 
 def test_large_single_problem_elementwise(lbq):

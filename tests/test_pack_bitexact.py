@@ -19,11 +19,11 @@ def test_w2_pack_bitexact(lbq, N, K):
 
 
 def test_pack_with_outliers_bitexact(lbq):
-    W = synth.weights_heavy_cols(40, 1024, config_id=2, layer_id=99)
+    W = synth.weights_heavy_cols(40, 1024, workload=synth.WL_LLAMA8B_W4, layer_id=99)
     idx = O.select_outliers_w4(W)
     assert np.array_equal(lbq.select_outliers_w4(W), idx)
     assert np.array_equal(lbq.pack_w4(W, idx), O.pack_w4(W, idx))
-    X = synth.profile_vectors(1024, config_id=3, layer_id=99)
+    X = synth.profile_vectors(1024, workload=synth.WL_LLAMA8B_W2, layer_id=99)
     idx2 = O.select_outliers_impact(W, X)
     assert np.array_equal(lbq.select_outliers_impact(W, X), idx2)
     assert len(idx2) == int(0.035 * 1024)
@@ -58,7 +58,7 @@ def test_layouts_match_oracle(lbq):
 
 def test_llama8b_qproj_rows_bitexact(lbq):
     """A slice of the config-2 q_proj (full K = 4096) with the W4 outlier variant."""
-    W = synth.weights_heavy_cols(4096, 4096, config_id=2, layer_id=0)[:256]
+    W = synth.weights_heavy_cols(4096, 4096, workload=synth.WL_LLAMA8B_W4, layer_id=0)[:256]
     idx = lbq.select_outliers_w4(W)
     assert np.array_equal(idx, O.select_outliers_w4(W))
     assert np.array_equal(lbq.pack_w4(W, idx), O.pack_w4(W, idx))

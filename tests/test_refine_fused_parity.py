@@ -87,8 +87,8 @@ def test_fused_refinement_llama8b_layer_every_row(lbq):
     probs, refs, sel, checks, keep = [], [], [], [], []
     with oracle_rows.pool() as ex:
         for li, (name, N, K) in enumerate(synth.LLAMA3_8B_LINEARS):
-            W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li)
-            x = synth.activations(1, K, config_id=2, layer_id=li)[0]
+            W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)
+            x = synth.activations(1, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)[0]
             blob = lbq.pack_w4(W)
             rblob = lbq.pack_refine((W - lbq.dequant_host(blob)).astype(np.float32))
             fut = oracle_rows.submit(ex, "w4", W, np.zeros(0, np.int32), x[None, :])

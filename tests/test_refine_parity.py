@@ -76,8 +76,8 @@ def test_apply_elementwise(lbq, N, K, k, f32):
 def test_llama8b_gemv_then_refinement(lbq, li):
     """4-bit GEMV, then select + apply on the same stream: y' = W_hat x + sum x_i C[:, i]."""
     name, N, K = synth.LLAMA3_8B_LINEARS[li]
-    W = synth.weights_heavy_cols(N, K, config_id=2, layer_id=li)
-    x = synth.activations(1, K, config_id=2, layer_id=li)[0]
+    W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)
+    x = synth.activations(1, K, workload=synth.WL_LLAMA8B_W4, layer_id=li)[0]
     base = lbq.pack_w4(W)
     # the residual from the oracle's own 4-bit packing (identical bytes, pinned on CPU)
     R = (W.astype(np.float64) - O.dequant_eff(O.pack_w4(W))).astype(np.float32)

@@ -49,14 +49,14 @@ def test_leading_dimensions(lbq):
 
 @pytest.mark.parametrize("name,N,K", [("gate_proj", 14336, 4096), ("down_proj", 4096, 14336)])
 @pytest.mark.parametrize("M", synth.SMALL_M_VALUES)
-def test_cfg4_sampled(lbq, name, N, K, M):
+def test_gate_down_small_m_sampled(lbq, name, N, K, M):
     li = 4 if name == "gate_proj" else 6
-    W = synth.weights_heavy_cols(N, K, config_id=4, layer_id=li)
-    X = synth.activations(M, K, config_id=4, layer_id=li)
+    W = synth.weights_heavy_cols(N, K, workload=synth.WL_SMALL_M, layer_id=li)
+    X = synth.activations(M, K, workload=synth.WL_SMALL_M, layer_id=li)
     Y = _gemm(lbq, lbq.pack_w4(W), M, N, K, 0, X)
     rows = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(M).choice(N, size=128)]))
     ref = O.gemm(O.pack_w4(W[rows]), X)
-    assert_close(Y[:, rows], ref, what="cfg4 %s M=%d" % (name, M))
+    assert_close(Y[:, rows], ref, what="small M %s M=%d" % (name, M))
 
 
 def test_wide_k_falls_back_to_row_passes(lbq):

@@ -58,9 +58,9 @@ def test_leading_dimensions_and_no_outliers(lbq):
 @pytest.mark.parametrize("M", [4, 8])
 def test_llama8b_sampled(lbq, li, M):
     name, N, K = synth.LLAMA3_8B_LINEARS[li]
-    W = synth.weights_heavy_cols(N, K, config_id=3, layer_id=li)
-    idx = O.select_outliers_impact(W, synth.profile_vectors(K, config_id=3, layer_id=li))
-    X = synth.activations(M, K, config_id=3, layer_id=li)
+    W = synth.weights_heavy_cols(N, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
+    idx = O.select_outliers_impact(W, synth.profile_vectors(K, workload=synth.WL_LLAMA8B_W2, layer_id=li))
+    X = synth.activations(M, K, workload=synth.WL_LLAMA8B_W2, layer_id=li)
     Y = _gemm(lbq, lbq.pack_w2cb(W, idx), M, N, K, len(idx), X)
     rows = np.unique(np.concatenate([[0, 1, N - 2, N - 1], np.random.default_rng(M + li).choice(N, size=128)]))
     assert_close(Y[:, rows], O.gemm(O.pack_w2cb(W[rows], idx), X), what="w2 %s M=%d" % (name, M))
