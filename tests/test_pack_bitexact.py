@@ -5,6 +5,8 @@ import pytest
 from bit_weight_only_lbq_gb300 import synth
 from oracle import lbq_oracle as O
 
+from degenerate_inputs import degenerate_matrix
+
 
 @pytest.mark.parametrize("N,K", [(1, 64), (3, 128), (17, 192), (64, 1024), (33, 4160)])
 def test_w4_pack_bitexact(lbq, N, K):
@@ -114,34 +116,12 @@ def test_refine_host_argument_checks(lbq):
     assert L.lbq_dequant_host(bad.ctypes.data, bad.size, out.ctypes.data) == 6        # LBQ_ERR_FORMAT
 
 
-def _degenerate_groups() -> np.ndarray:
-    """4 x 384 FP32 (12 groups of 32 per row, a ragged last record): every group
-    one corner of the quantisers - zero, constant, one-sided, tiny, huge,
-    exact rounding ties, a lone spike, two-valued - then permuted and negated
-    across the rows, next to plain Gaussian groups."""
-    r = np.random.default_rng(11)
-    ramp = np.arange(32, dtype=np.float64)
-    groups = [
-        np.zeros(32),                                        # all zero: scale floor, q = z
-        np.full(32, 0.3),                                    # constant positive
-        np.full(32, -0.7),                                   # constant negative
-        np.linspace(1.0, 4.0, 32),                           # one-sided: z clamps to 0
-        np.linspace(-4.0, -1.0, 32),                         # one-sided: z clamps to 15
-        r.standard_normal(32) * 1e-7,                        # far below the FP16 normal range
-        r.uniform(-6.0e4, 6.0e4, 32),                        # near the FP16 maximum
-        np.concatenate([[0.0, 15.0], (ramp[:30] % 15) + 0.5]),   # s = 1: every other value a tie
-        np.where(ramp == 17, 0.5, 0.0),                      # a lone spike
-        np.where(ramp % 2 == 0, 0.1, -0.1),                  # two values: codes at the outer centroids
-        r.standard_normal(32) * 0.02,
-        np.full(32, 1e-30),                                  # FP32 tiny, constant
-    ]
-    row0 = np.concatenate(groups)
-    rows = [row0, -row0, np.concatenate(groups[::-1]), np.concatenate([g[::-1] for g in groups[6:] + groups[:6]])]
-    return np.stack(rows).astype(np.float32)
-
-
-def test_degenerate_groups_bitexact(lbq):
-    W = _degenerate_groups()
+@pytest.mark.parametrize("family", ["mixed", "tiny", "large"])
+def test_degenerate_groups_bitexact(lbq, family):
+    """Zero, constant, one-sided, exact-tie, lone-spike, two-valued, sub-FP16 and
+    large groups, a ragged last record: the C++ packers and the host dequantiser
+    byte-identical to the oracle."""
+    W = degenerate_matrix(6, 384, family)
     assert np.array_equal(lbq.pack_w4(W), O.pack_w4(W))
     assert np.array_equal(lbq.pack_w2cb(W), O.pack_w2cb(W))
     idx = np.array([0, 40, 200, 233, 383], np.int32)         # outlier columns inside degenerate groups
