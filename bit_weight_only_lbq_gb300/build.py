@@ -30,7 +30,7 @@ def sources():
     return cu, cpp
 
 
-def build(verbose: bool = False, debug: bool = False) -> str:
+def build(verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(OUT_DIR, exist_ok=True)
     obj_dir = os.path.join(OUT_DIR, "obj")
@@ -48,8 +48,6 @@ def build(verbose: bool = False, debug: bool = False) -> str:
         o = os.path.join(obj_dir, f + ".o")
         cmd = [nvcc, ARCH, "-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                *inc, "-c", os.path.join(CSRC, f), "-o", o]
-        if debug:
-            cmd.insert(1, "-DLBQ_DEBUG=1")
         jobs.append((cmd, o))
 
     def run(job):
