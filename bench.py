@@ -408,7 +408,8 @@ def main():
     ap.add_argument("--single", default=None,
                     help="kind:N:K:n_out:M - time one kernel configuration alone (profiling aid), "
                          "kind in w4, w2, w4m; sweep:KIND (one grouped launch of the step); "
-                         "kv:ROWS:WIDTH (KV cache read); refine:N:K:k (select + apply)")
+                         "kv:ROWS:WIDTH (KV cache read); refine:N:K:k (select + apply); "
+                         "embed:V:D:T (fused row gather of T token ids from a V x D 4-bit table)")
     args = ap.parse_args()
     if args.single:
         return run_single(args)
@@ -1065,7 +1066,7 @@ def run_single(args):
     from bit_weight_only_lbq_gb300 import lbq
     if args.single.startswith("sweep:"):
         return run_single_sweep(args, args.single.split(":")[1])
-    if args.single.startswith("kv:") or args.single.startswith("refine:"):
+    if args.single.split(":")[0] in ("kv", "refine", "embed"):
         return run_single_row(args)
     kind, N, K, n_out, M = args.single.split(":")
     N, K, n_out, M = int(N), int(K), int(n_out), int(M)
@@ -1099,9 +1100,10 @@ def run_single(args):
 
 
 def run_single_row(args):
-    """The KV cache read (kv:ROWS:WIDTH, after filling the cache) or the refinement
-    (refine:N:K:k, select + apply on a random residual), launched steps times after
-    warmup without graphs (for ncu captures)."""
+    """The KV cache read (kv:ROWS:WIDTH, after filling the cache), the refinement
+    (refine:N:K:k, select + apply on a random residual) or the embedding row gather
+    (embed:V:D:T, T random token ids of a random V x D 4-bit table, FP16 rows out),
+    launched steps times after warmup without graphs (for ncu captures)."""
     import torch
     from bit_weight_only_lbq_gb300 import lbq
     dev = torch.device("cuda", 0)
@@ -1115,6 +1117,13 @@ def run_single_row(args):
         out = torch.empty((rows, width), dtype=torch.float16, device=dev)
         fn = lambda: lbq.kv_dequant(cache, 0, rows, width, out)
         nbytes = rows * (lbq.kv_record_bytes(width) + 2 * width)
+    elif parts[0] == "embed":
+        V, D, T = int(parts[1]), int(parts[2]), int(parts[3])
+        table = torch.from_numpy(lbq.pack_w4(rng.standard_normal((V, D), dtype=np.float32) * np.float32(0.02))).to(dev)
+        ids = torch.from_numpy(rng.integers(0, V, size=T).astype(np.int32)).to(dev)
+        out = torch.empty((T, D), dtype=torch.float16, device=dev)
+        fn = lambda: lbq.embed_gather(lbq.LBQ_KIND_W4, table, V, D, 0, ids, out)
+        nbytes = int(T * D * (W4_BYTES_PER_WEIGHT + 2) + 4 * T)
     else:
         N, K, k = int(parts[1]), int(parts[2]), int(parts[3])
         blob = torch.from_numpy(lbq.pack_refine((rng.standard_normal((N, K)) * 1e-3).astype(np.float32))).to(dev)
