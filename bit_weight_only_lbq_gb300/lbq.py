@@ -239,9 +239,16 @@ def pack_refine(R) -> np.ndarray:
 
 def dequant_host(blob) -> np.ndarray:
     """The N x K FP32 matrix a resident blob applies (outlier columns exact)."""
-    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    blob = np.ascontiguousarray(blob, dtype=np.uint8).reshape(-1)
+    kinds = {b"LBQW4G32": LBQ_KIND_W4, b"LBQW2C32": LBQ_KIND_W2CB}
+    if blob.size < 40 or bytes(blob[:8]) not in kinds:
+        raise LbqError(6, "lbq_dequant_host")                    # LBQ_ERR_FORMAT, before sizing anything
     N = int(blob[16:24].view("<i8")[0])
     K = int(blob[24:32].view("<i8")[0])
+    n_out = int(blob[32:36].view("<i4")[0])
+    L = Layout()
+    if lib().lbq_blob_layout(kinds[bytes(blob[:8])], N, K, n_out, ctypes.byref(L)) != 0 or L.total_bytes > blob.size:
+        raise LbqError(6, "lbq_dequant_host")
     out = np.empty((N, K), np.float32)
     _check(lib().lbq_dequant_host(_ptr(blob), blob.size, _ptr(out)), "lbq_dequant_host")
     return out

@@ -131,3 +131,17 @@ def test_degenerate_groups_bitexact(lbq, family):
     for kind, pack in (("w4", O.pack_w4), ("w2", O.pack_w2cb)):
         blob = pack(W, idx)
         assert np.array_equal(lbq.dequant_host(blob), O.dequant_eff(blob).astype(np.float32)), kind
+
+
+def test_dequant_host_rejects_bad_blobs(lbq):
+    """A short, foreign, truncated or size-inflated blob is LBQ_ERR_FORMAT before
+    anything is sized from its header."""
+    W = synth.random_matrix(8, 128, seed=5, scale=0.02)
+    for pack in (lbq.pack_w4, lbq.pack_w2cb):
+        b = pack(W, np.array([3], np.int32))
+        huge = b.copy()
+        huge[16:24] = np.frombuffer(np.int64(10 ** 12).tobytes(), np.uint8)   # N far beyond the blob
+        for bad in (b[:20], b[:-16], huge, np.zeros(256, np.uint8)):
+            with pytest.raises(lbq.LbqError) as e:
+                lbq.dequant_host(bad)
+            assert e.value.status == 6
