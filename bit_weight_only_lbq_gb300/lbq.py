@@ -240,15 +240,22 @@ def pack_refine(R) -> np.ndarray:
 def dequant_host(blob) -> np.ndarray:
     """The N x K FP32 matrix a resident blob applies (outlier columns exact)."""
     blob = np.ascontiguousarray(blob, dtype=np.uint8).reshape(-1)
+    # the library's own checks, made before the output is sized from the header:
+    # shorter than the header or than the header says -> LBQ_ERR_BUFFER_TOO_SMALL,
+    # not a blob of this format -> LBQ_ERR_FORMAT
     kinds = {b"LBQW4G32": LBQ_KIND_W4, b"LBQW2C32": LBQ_KIND_W2CB}
-    if blob.size < 40 or bytes(blob[:8]) not in kinds:
-        raise LbqError(6, "lbq_dequant_host")                    # LBQ_ERR_FORMAT, before sizing anything
+    if blob.size < 128:
+        raise LbqError(5, "lbq_dequant_host")
+    if bytes(blob[:8]) not in kinds:
+        raise LbqError(6, "lbq_dequant_host")
     N = int(blob[16:24].view("<i8")[0])
     K = int(blob[24:32].view("<i8")[0])
     n_out = int(blob[32:36].view("<i4")[0])
     L = Layout()
-    if lib().lbq_blob_layout(kinds[bytes(blob[:8])], N, K, n_out, ctypes.byref(L)) != 0 or L.total_bytes > blob.size:
+    if lib().lbq_blob_layout(kinds[bytes(blob[:8])], N, K, n_out, ctypes.byref(L)) != 0:
         raise LbqError(6, "lbq_dequant_host")
+    if L.total_bytes > blob.size:
+        raise LbqError(5, "lbq_dequant_host")
     out = np.empty((N, K), np.float32)
     _check(lib().lbq_dequant_host(_ptr(blob), blob.size, _ptr(out)), "lbq_dequant_host")
     return out

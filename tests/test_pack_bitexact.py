@@ -134,14 +134,20 @@ def test_degenerate_groups_bitexact(lbq, family):
 
 
 def test_dequant_host_rejects_bad_blobs(lbq):
-    """A short, foreign, truncated or size-inflated blob is LBQ_ERR_FORMAT before
-    anything is sized from its header."""
+    """Bad blobs get the C call's statuses before anything is sized from the header:
+    shorter than the header, or than the header says (N inflated, truncated):
+    LBQ_ERR_BUFFER_TOO_SMALL; not this library's format: LBQ_ERR_FORMAT."""
     W = synth.random_matrix(8, 128, seed=5, scale=0.02)
     for pack in (lbq.pack_w4, lbq.pack_w2cb):
         b = pack(W, np.array([3], np.int32))
         huge = b.copy()
-        huge[16:24] = np.frombuffer(np.int64(10 ** 12).tobytes(), np.uint8)   # N far beyond the blob
-        for bad in (b[:20], b[:-16], huge, np.zeros(256, np.uint8)):
+        huge[16:24] = np.frombuffer(np.int64(10 ** 6).tobytes(), np.uint8)    # N far beyond the blob
+        for bad, status in ((b[:20], 5), (b[:-16], 5), (huge, 5), (np.zeros(256, np.uint8), 6)):
             with pytest.raises(lbq.LbqError) as e:
                 lbq.dequant_host(bad)
-            assert e.value.status == 6
+            assert e.value.status == status
+        # the C entry point itself answers the same, without writing (nothing to write into)
+        L = lbq.lib()
+        one = np.zeros(1, np.float32)
+        for bad, status in ((b[:20], 5), (b[:-16], 5), (huge, 5), (np.zeros(256, np.uint8), 6)):
+            assert L.lbq_dequant_host(bad.ctypes.data, bad.size, one.ctypes.data) == status
